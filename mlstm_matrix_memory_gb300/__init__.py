@@ -1,0 +1,18 @@
+"""GB300-native mLSTM matrix memory: stabilized parallel forward and recurrent step.
+
+The compute runs in hand-written CUDA kernels for sm_103a behind the C-ABI
+library ``libmlstm.so`` (declared in ``include/mlstm.h``).  This package is the
+thin Python binding: it validates tensors, passes device pointers and the
+current CUDA stream, and returns.  PyTorch supplies device memory and streams
+only.  The library is loaded on first use; if it is missing the calls raise.
+"""
+from .binding import (  # noqa: F401
+    MlstmError,
+    parallel_fwd,
+    parallel_fwd_workspace_bytes,
+    step,
+    last_device_status,
+    set_spin_limit,
+    library,
+    library_path,
+)

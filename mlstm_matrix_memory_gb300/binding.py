@@ -1,0 +1,197 @@
+"""ctypes binding to ``libmlstm.so`` (argument marshalling only).
+
+Every step of the mLSTM path runs in the library's CUDA kernels; this module
+checks tensor shapes, dtypes, devices and contiguity, hands raw device
+pointers plus the current CUDA stream to the C-ABI declared in
+``include/mlstm.h``, and turns non-zero status codes into ``MlstmError``.
+There is no fallback: if the library is missing or no GPU is present, the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libmlstm.so"
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+MLSTM_F32, MLSTM_BF16 = 0, 1
+ALGOS = {"auto": 0, "simt": 1, "tc": 2}
+_DTYPES = {torch.float32: MLSTM_F32, torch.bfloat16: MLSTM_BF16}
+
+
+class MlstmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_str(code)} ({code})")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def library() -> ctypes.CDLL:
+    """Load ``libmlstm.so`` (built by ``__graft_entry__.build()`` or
+    ``mlstm_matrix_memory_gb300.build``).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m mlstm_matrix_memory_gb300.build`")
+        lib = ctypes.CDLL(path)
+        vp, i, sz, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
+        lib.mlstm_parallel_fwd_workspace.argtypes = [i, i, i]
+        lib.mlstm_parallel_fwd_workspace.restype = sz
+        lib.mlstm_parallel_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
+        lib.mlstm_parallel_fwd.restype = i
+        lib.mlstm_parallel_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, i, vp]
+        lib.mlstm_parallel_fwd_ex.restype = i
+        lib.mlstm_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+        lib.mlstm_step.restype = i
+        lib.mlstm_last_device_status.argtypes = [vp]
+        lib.mlstm_last_device_status.restype = i
+        lib.mlstm_set_spin_limit.argtypes = [ll]
+        lib.mlstm_set_spin_limit.restype = ll
+        lib.mlstm_status_str.argtypes = [i]
+        lib.mlstm_status_str.restype = ctypes.c_char_p
+        lib.mlstm_version.argtypes = []
+        lib.mlstm_version.restype = i
+        _lib = lib
+        return lib
+
+
+def status_str(code: int) -> str:
+    try:
+        return library().mlstm_status_str(int(code)).decode()
+    except Exception:
+        return "unknown status"
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, shape, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def parallel_fwd_workspace_bytes(B: int, H: int, T: int) -> int:
+    return int(library().mlstm_parallel_fwd_workspace(B, H, T))
+
+
+def parallel_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: torch.Tensor,
+                 fgate_pre: torch.Tensor, *, h: Optional[torch.Tensor] = None,
+                 return_mn: bool = False, workspace: Optional[torch.Tensor] = None,
+                 algo: str = "auto"):
+    """Stabilized parallel mLSTM forward pass (H~, no output gate).
+
+    q, k [B,H,T,d_qk], v [B,H,T,d_v] (fp32 or bf16, same dtype, contiguous,
+    CUDA); igate_pre, fgate_pre [B,H,T] fp32.  Returns h [B,H,T,d_v] in the
+    input dtype, and with ``return_mn`` also the row stabilizer m and the
+    normalizer n, both [B,H,T] fp32.  Runs on the current stream.
+    """
+    lib = library()
+    if q.dim() != 4:
+        raise ValueError("q must be [B,H,T,d_qk]")
+    B, H, T, dqk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    _need(q, "q", (B, H, T, dqk), q.dtype, dev)
+    _need(k, "k", (B, H, T, dqk), q.dtype, dev)
+    _need(v, "v", (B, H, T, dv), q.dtype, dev)
+    _need(igate_pre, "igate_pre", (B, H, T), torch.float32, dev)
+    _need(fgate_pre, "fgate_pre", (B, H, T), torch.float32, dev)
+    if h is None:
+        h = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
+    _need(h, "h", (B, H, T, dv), q.dtype, dev)
+    m = n = None
+    if return_mn:
+        m = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        n = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    ws_bytes = int(lib.mlstm_parallel_fwd_workspace(B, H, T))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    if workspace.device != dev or workspace.numel() * workspace.element_size() < ws_bytes:
+        raise ValueError(f"workspace must hold {ws_bytes} bytes on {dev}")
+    rc = lib.mlstm_parallel_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(h),
+                                   _ptr(m), _ptr(n), B, H, T, dqk, dv, _DTYPES[q.dtype],
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   ALGOS[algo], _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_parallel_fwd")
+    return (h, m, n) if return_mn else h
+
+
+def step(C: torch.Tensor, n: torch.Tensor, m: torch.Tensor, q: torch.Tensor, k: torch.Tensor,
+         v: torch.Tensor, igate_pre: torch.Tensor, fgate_pre: torch.Tensor,
+         o: Optional[torch.Tensor] = None, *, h: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One stabilized recurrent mLSTM step; updates C [B,H,d_v,d_qk], n [B,H,d_qk],
+    m [B,H] (fp32) in place and returns h = sigma(o) * h~ [B,H,d_v] (o=None: no
+    output gate).  q, k [B,H,d_qk], v, o [B,H,d_v] share one dtype (fp32/bf16);
+    igate_pre, fgate_pre [B,H] fp32."""
+    lib = library()
+    if C.dim() != 4:
+        raise ValueError("C must be [B,H,d_v,d_qk]")
+    B, H, dv, dqk = C.shape
+    dev = C.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    _need(C, "C", (B, H, dv, dqk), torch.float32, dev)
+    _need(n, "n", (B, H, dqk), torch.float32, dev)
+    _need(m, "m", (B, H), torch.float32, dev)
+    _need(q, "q", (B, H, dqk), q.dtype, dev)
+    _need(k, "k", (B, H, dqk), q.dtype, dev)
+    _need(v, "v", (B, H, dv), q.dtype, dev)
+    if o is not None:
+        _need(o, "o", (B, H, dv), q.dtype, dev)
+    _need(igate_pre, "igate_pre", (B, H), torch.float32, dev)
+    _need(fgate_pre, "fgate_pre", (B, H), torch.float32, dev)
+    if h is None:
+        h = torch.empty((B, H, dv), dtype=q.dtype, device=dev)
+    _need(h, "h", (B, H, dv), q.dtype, dev)
+    rc = lib.mlstm_step(_ptr(C), _ptr(n), _ptr(m), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(igate_pre),
+                        _ptr(fgate_pre), _ptr(h), B, H, dqk, dv, _DTYPES[q.dtype], _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_step")
+    return h
+
+
+def last_device_status(stream: Optional[int] = None) -> int:
+    """Synchronize ``stream`` (default: current) and return, then clear, the
+    status word the kernels set when a bounded wait gives up."""
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    return int(library().mlstm_last_device_status(stream))
+
+
+def set_spin_limit(limit: int) -> int:
+    """Set the per-wait spin budget of the kernels' bounded waits (0 = default);
+    returns the previous value.  Small values make waits give up (fault injection)."""
+    return int(library().mlstm_set_spin_limit(int(limit)))

@@ -1,0 +1,430 @@
+/*
+ * fp64 CPU oracle for the mLSTM matrix-memory cell.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code, header, table or
+ * helper with the CUDA path.
+ *
+ * Source: "xLSTM: Extended Long Short-Term Memory".
+ *   part 28/30, "Parallel mLSTM Forward Pass": eqs (71)-(78);
+ *   part 28/30, "Parallel mLSTM Backward Pass", forward summary: eqs (79)-(86)
+ *     and the log forget matrix, eq (101);
+ *   part 28/30, recurrent mLSTM backward, eqs (59)-(70) (the recurrent
+ *     forward they differentiate is what oracle_recurrent_* evaluates);
+ *   part 17/30, section 2.3 tail: forget gate eq (26), output gate eq (27),
+ *     multiple heads equal multiple cells (no memory mixing), and the
+ *     mLSTM reuses the sLSTM stabilization.
+ *
+ * Readings of the pages taken here (the pages do not print them):
+ *  - The recurrent forward equations themselves are not on the pages; the
+ *    recurrence is the one the backward equations (59)-(70) differentiate:
+ *      C_t = f_t C_{t-1} + i_t v_t k_t^T,   n_t = f_t n_{t-1} + i_t k_t,
+ *      h~_t = C_t q_t / max(|n_t^T q_t|, 1),  h_t = o_t (.) h~_t,
+ *    with i_t = exp(i~_t) (eq 69 has dL/di~ proportional to exp(i~)), and the
+ *    forget activation f_t = sigma(f~_t), the one the parallel form fixes
+ *    (eq 71 builds F from sigma(f~)).
+ *  - k enters scaled by 1/sqrt(d_qk) (the 1/sqrt(d) factor is moved onto K
+ *    below eq 76); q is unscaled.
+ *  - Stabilizer (sLSTM eq 15 is not on the pages): a running log-space max
+ *    m_t = max(log f_t + m_{t-1}, i~_t) with gates rescaled by exp(-m_t), and
+ *    the normalizer floor 1 becoming exp(-m_t).  The state starts at C=0, n=0,
+ *    m=-inf.  The stored (C, n) is the true state times exp(-m), so h~ does
+ *    not depend on m in exact arithmetic; this m is the one that equals the
+ *    parallel form's row maximum (80) at every step and keeps every rescaled
+ *    gate at most 1.
+ *  - The max in (75) is the row-wise max of (80).
+ *
+ * All arithmetic is IEEE fp64; build without -ffast-math (-inf must flow).
+ * Layouts are row-major with the last index fastest:
+ *   q,k [B,H,T,dqk]  v [B,H,T,dv]  igate,fgate [B,H,T]  og [B,H,T,dv]
+ *   h   [B,H,T,dv]   C [B,H,dv,dqk]  n [B,H,dqk]  m [B,H]
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTATION
+#define ORACLE_MUTATION 0   /* >0 plants a known mistake (mutation tests only) */
+#endif
+
+int oracle_mutation(void) { return ORACLE_MUTATION; }
+
+static void set_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* log(sigma(x)) evaluated without overflow: min(x,0) - log1p(exp(-|x|)).
+ * Gives 0 at x=+inf and -inf at x=-inf. */
+static double log_sigmoid(double x)
+{
+#if ORACLE_MUTATION == 7
+    return x;                       /* mutation: exponential forget activation */
+#else
+    double mn = x < 0.0 ? x : 0.0;
+    return mn - log1p(exp(-fabs(x)));
+#endif
+}
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+static double key_scale(int dqk)
+{
+#if ORACLE_MUTATION == 1
+    (void)dqk;
+    return 1.0;                     /* mutation: 1/sqrt(d) dropped */
+#else
+    return 1.0 / sqrt((double)dqk);
+#endif
+}
+
+/* ---------------------------------------------------------------------------
+ * Stabilized parallel forward for one head, one query row i (0-based).
+ * part 28/30, eqs (79)-(86); eq (101) for log F; eq (78) for the output gate.
+ *   D~_ij = Fbar_ij + I~_ij,  Fbar_ij = sum_{k=j+1..i} log sigma(f~_k)  (j<=i)
+ *   m_i   = max_j D~_ij                                   (row-wise, eq 80)
+ *   D'_ij = exp(D~_ij - m_i)                              (eq 81)
+ *   C~'_ij = (q_i . k_j)/sqrt(d) * D'_ij                  (eq 82)
+ *   b_i   = sum_j C~'_ij                                  (eq 83)
+ *   n_i   = max(|b_i|, exp(-m_i))                         (eq 84)
+ *   H~_i  = sum_j (C~'_ij / n_i) v_j                      (eqs 85-86)
+ * Entries with j > i have Fbar = -inf, so D' = 0 there and they drop out of
+ * every sum over j (the pages sum over j = 1..T).
+ * `dt` and `cp` are scratch of length T.
+ */
+static void parallel_row(int T, int dqk, int dv, const double *q, const double *k,
+                         const double *v, const double *ig, const double *fg,
+                         const double *og, int i, double *h_row, double *m_row,
+                         double *n_row, double *dt, double *cp)
+{
+    (void)T;
+    const double s = key_scale(dqk);
+    /* eq (101), evaluated for this row by walking j down from i: the sum over
+     * k = j+1..i grows by one term log sigma(f~_{j+1}) per step. */
+    double fbar = 0.0;              /* Fbar_ii = 0 */
+    for (int j = i; j >= 0; --j) {
+        if (j < i) {
+#if ORACLE_MUTATION == 4
+            fbar += log_sigmoid(fg[j]);          /* mutation: sum starts at k=j */
+#else
+            fbar += log_sigmoid(fg[j + 1]);
+#endif
+        }
+        dt[j] = fbar + ig[j];       /* eq (79): D~ = Fbar + I~, I~_ij = i~_j (eq 72) */
+    }
+    double m = -INFINITY;           /* eq (80) */
+    for (int j = 0; j <= i; ++j) if (dt[j] > m) m = dt[j];
+    double b = 0.0;
+    const double *qi = q + (size_t)i * dqk;
+    for (int j = 0; j <= i; ++j) {
+        const double *kj = k + (size_t)j * dqk;
+        double qk = 0.0;
+#if ORACLE_MUTATION == 8
+        (void)kj;                   /* mutation: q_j . k_i instead of q_i . k_j */
+        for (int c = 0; c < dqk; ++c) qk += q[(size_t)j * dqk + c] * k[(size_t)i * dqk + c];
+#else
+        for (int c = 0; c < dqk; ++c) qk += qi[c] * kj[c];
+#endif
+        double dprime = exp(dt[j] - m);                     /* eq (81) */
+        cp[j] = qk * s * dprime;                            /* eq (82) */
+        b += cp[j];                                         /* eq (83) */
+    }
+#if ORACLE_MUTATION == 3
+    double nrm = fmax(fabs(b), 1.0);                        /* mutation: floor 1 */
+#elif ORACLE_MUTATION == 6
+    double nrm = fmax(b, exp(-m));                          /* mutation: no |.| */
+#else
+    double nrm = fmax(fabs(b), exp(-m));                    /* eq (84) */
+#endif
+    for (int c = 0; c < dv; ++c) h_row[c] = 0.0;
+    for (int j = 0; j <= i; ++j) {
+        double w = cp[j] / nrm;                             /* eq (85) */
+        const double *vj = v + (size_t)j * dv;
+        for (int c = 0; c < dv; ++c) h_row[c] += w * vj[c]; /* eq (86) */
+    }
+    if (og) {                                               /* eq (78) */
+        const double *oi = og + (size_t)i * dv;
+        for (int c = 0; c < dv; ++c) h_row[c] *= sigmoid(oi[c]);
+    }
+    if (m_row) *m_row = m;
+    if (n_row) *n_row = nrm;
+}
+
+/* Full stabilized parallel forward over all (b,h) and all rows. */
+int oracle_parallel_stabilized(int B, int H, int T, int dqk, int dv,
+                               const double *q, const double *k, const double *v,
+                               const double *ig, const double *fg, const double *og,
+                               double *h, double *m_out, double *n_out, int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
+    set_threads(nthreads);
+    const long BH = (long)B * H;
+#pragma omp parallel
+    {
+        double *dt = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
+        double *cp = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < BH; ++bh) {
+            const double *qh = q + (size_t)bh * T * dqk, *kh = k + (size_t)bh * T * dqk;
+            const double *vh = v + (size_t)bh * T * dv;
+            const double *igh = ig + (size_t)bh * T, *fgh = fg + (size_t)bh * T;
+            const double *ogh = og ? og + (size_t)bh * T * dv : NULL;
+            for (int i = 0; i < T; ++i)
+                parallel_row(T, dqk, dv, qh, kh, vh, igh, fgh, ogh, i,
+                             h + ((size_t)bh * T + i) * dv,
+                             m_out ? m_out + (size_t)bh * T + i : NULL,
+                             n_out ? n_out + (size_t)bh * T + i : NULL, dt, cp);
+        }
+        free(dt);
+        free(cp);
+    }
+    return 0;
+}
+
+/* Stabilized parallel forward for a list of sampled rows.  rows[r] holds a
+ * flat (bh, i) pair as bh*T + i; row r of h_out/m_out/n_out receives it. */
+int oracle_parallel_rows(int B, int H, int T, int dqk, int dv,
+                         const double *q, const double *k, const double *v,
+                         const double *ig, const double *fg, const double *og,
+                         const long *rows, int nrows,
+                         double *h_out, double *m_out, double *n_out, int nthreads)
+{
+    if (B < 0 || H < 0 || T <= 0 || dqk <= 0 || dv <= 0 || nrows < 0) return -1;
+    set_threads(nthreads);
+    const long BHT = (long)B * H * T;
+    for (int r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= BHT) return -1;
+#pragma omp parallel
+    {
+        double *dt = (double *)malloc(sizeof(double) * T);
+        double *cp = (double *)malloc(sizeof(double) * T);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < nrows; ++r) {
+            long bh = rows[r] / T;
+            int i = (int)(rows[r] % T);
+            parallel_row(T, dqk, dv, q + (size_t)bh * T * dqk, k + (size_t)bh * T * dqk,
+                         v + (size_t)bh * T * dv, ig + (size_t)bh * T, fg + (size_t)bh * T,
+                         og ? og + (size_t)bh * T * dv : NULL, i, h_out + (size_t)r * dv,
+                         m_out ? m_out + r : NULL, n_out ? n_out + r : NULL, dt, cp);
+        }
+        free(dt);
+        free(cp);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Unstabilized parallel forward, part 28/30 eqs (71)-(73) and (76):
+ *   F_ij = prod_{k=j+1..i} sigma(f~_k) (1 on the diagonal, 0 above),
+ *   D = F (.) exp(I~),  C~ = (Q K^T / sqrt(d)) (.) D,
+ *   H~ = C V,  C = C~ / max(|sum_j C~_ij|, 1).
+ * Overflows for large |i~| or long sequences; used on small inputs only.
+ */
+int oracle_parallel_unstabilized(int B, int H, int T, int dqk, int dv,
+                                 const double *q, const double *k, const double *v,
+                                 const double *ig, const double *fg, const double *og,
+                                 double *h, int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
+    set_threads(nthreads);
+    const long BH = (long)B * H;
+    const double s = key_scale(dqk);
+#pragma omp parallel
+    {
+        double *ct = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < BH; ++bh) {
+            const double *qh = q + (size_t)bh * T * dqk, *kh = k + (size_t)bh * T * dqk;
+            const double *vh = v + (size_t)bh * T * dv;
+            const double *igh = ig + (size_t)bh * T, *fgh = fg + (size_t)bh * T;
+            for (int i = 0; i < T; ++i) {
+                double rowsum = 0.0;
+                for (int j = 0; j <= i; ++j) {
+                    double F = 1.0;                             /* eq (71) */
+                    for (int kk = j + 1; kk <= i; ++kk) F *= exp(log_sigmoid(fgh[kk]));
+                    double D = F * exp(igh[j]);                 /* eq (73) */
+                    double qk = 0.0;
+                    for (int c = 0; c < dqk; ++c) qk += qh[(size_t)i * dqk + c] * kh[(size_t)j * dqk + c];
+                    ct[j] = qk * s * D;                         /* eq (76), C~ */
+                    rowsum += ct[j];
+                }
+                double nrm = fmax(fabs(rowsum), 1.0);
+                double *hr = h + ((size_t)bh * T + i) * dv;
+                for (int c = 0; c < dv; ++c) hr[c] = 0.0;
+                for (int j = 0; j <= i; ++j)
+                    for (int c = 0; c < dv; ++c) hr[c] += ct[j] / nrm * vh[(size_t)j * dv + c];
+                if (og) {
+                    const double *oi = og + ((size_t)bh * T + i) * dv;
+                    for (int c = 0; c < dv; ++c) hr[c] *= sigmoid(oi[c]);
+                }
+            }
+        }
+        free(ct);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * One stabilized recurrent step on a single head's state, in place.
+ * C [dv,dqk], n [dqk], *m scalar; q,k [dqk], v [dv]; og [dv] or NULL; h [dv].
+ *   m'  = max(log sigma(f~) + m, i~)
+ *   f'  = exp(log sigma(f~) + m - m'),  i' = exp(i~ - m')
+ *   C  <- f' C + i' v (k/sqrt(d))^T,    n <- f' n + i' k/sqrt(d)
+ *   h~  = C q / max(|n . q|, exp(-m')), h = sigma(o~) (.) h~   (eqs 27, 59)
+ * The stored state is the true state scaled by exp(-m).
+ */
+static void step_head(int dqk, int dv, double *C, double *n, double *m,
+                      const double *q, const double *k, const double *v,
+                      double igv, double fgv, const double *og, double *h)
+{
+    const double s = key_scale(dqk);
+    const double lf = log_sigmoid(fgv);
+    double m_prev = *m;
+#if ORACLE_MUTATION == 2
+    if (isinf(m_prev) && m_prev < 0) m_prev = 0.0;   /* mutation: m_0 = 0 */
+#endif
+    const double m_new = fmax(lf + m_prev, igv);
+    const double fp = exp(lf + m_prev - m_new);
+#if ORACLE_MUTATION == 5
+    const double ip = exp(igv);                      /* mutation: i' not rescaled */
+#else
+    const double ip = exp(igv - m_new);
+#endif
+    for (int r = 0; r < dv; ++r) {
+        double acc = 0.0;
+        for (int c = 0; c < dqk; ++c) {
+            double cv = fp * C[(size_t)r * dqk + c] + ip * v[r] * (k[c] * s);
+            C[(size_t)r * dqk + c] = cv;
+            acc += cv * q[c];
+        }
+        h[r] = acc;
+    }
+    double nq = 0.0;
+    for (int c = 0; c < dqk; ++c) {
+        n[c] = fp * n[c] + ip * (k[c] * s);
+        nq += n[c] * q[c];
+    }
+    const double nrm = fmax(fabs(nq), exp(-m_new));
+    for (int r = 0; r < dv; ++r) {
+        h[r] /= nrm;
+        if (og) h[r] *= sigmoid(og[r]);
+    }
+    *m = m_new;
+}
+
+/* One stabilized step for every head, state updated in place (the generation
+ * step).  q,k [B,H,dqk]; v,og,h [B,H,dv]; igate,fgate [B,H]. */
+int oracle_step(int B, int H, int dqk, int dv, double *C, double *n, double *m,
+                const double *q, const double *k, const double *v, const double *og,
+                const double *ig, const double *fg, double *h, int nthreads)
+{
+    if (B < 0 || H < 0 || dqk <= 0 || dv <= 0) return -1;
+    set_threads(nthreads);
+    const long BH = (long)B * H;
+#pragma omp parallel for schedule(static)
+    for (long bh = 0; bh < BH; ++bh)
+        step_head(dqk, dv, C + (size_t)bh * dv * dqk, n + (size_t)bh * dqk, m + bh,
+                  q + (size_t)bh * dqk, k + (size_t)bh * dqk, v + (size_t)bh * dv,
+                  ig[bh], fg[bh], og ? og + (size_t)bh * dv : NULL, h + (size_t)bh * dv);
+    return 0;
+}
+
+/* Stabilized recurrent forward over whole sequences from C=0, n=0, m=-inf.
+ * Writes h [B,H,T,dv] and, when non-NULL, the final state C, n, m. */
+int oracle_recurrent_stabilized(int B, int H, int T, int dqk, int dv,
+                                const double *q, const double *k, const double *v,
+                                const double *ig, const double *fg, const double *og,
+                                double *h, double *C_out, double *n_out, double *m_out,
+                                int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
+    set_threads(nthreads);
+    const long BH = (long)B * H;
+#pragma omp parallel
+    {
+        double *C = (double *)malloc(sizeof(double) * dv * dqk);
+        double *n = (double *)malloc(sizeof(double) * dqk);
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < BH; ++bh) {
+            memset(C, 0, sizeof(double) * dv * dqk);
+            memset(n, 0, sizeof(double) * dqk);
+            double m = -INFINITY;
+            for (int t = 0; t < T; ++t) {
+                size_t ti = (size_t)bh * T + t;
+                step_head(dqk, dv, C, n, &m, q + ti * dqk, k + ti * dqk, v + ti * dv,
+                          ig[ti], fg[ti], og ? og + ti * dv : NULL, h + ti * dv);
+            }
+            if (C_out) memcpy(C_out + (size_t)bh * dv * dqk, C, sizeof(double) * dv * dqk);
+            if (n_out) memcpy(n_out + (size_t)bh * dqk, n, sizeof(double) * dqk);
+            if (m_out) m_out[bh] = m;
+        }
+        free(C);
+        free(n);
+    }
+    return 0;
+}
+
+/* Unstabilized recurrent forward, the recurrence eqs (59)-(70) differentiate:
+ * f = sigma(f~), i = exp(i~), C = f C + i v (k/sqrt d)^T, n = f n + i k/sqrt d,
+ * h~ = C q / max(|n.q|, 1).  Small inputs only (exp(i~) is not bounded). */
+int oracle_recurrent_unstabilized(int B, int H, int T, int dqk, int dv,
+                                  const double *q, const double *k, const double *v,
+                                  const double *ig, const double *fg, const double *og,
+                                  double *h, int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
+    set_threads(nthreads);
+    const long BH = (long)B * H;
+    const double s = key_scale(dqk);
+#pragma omp parallel
+    {
+        double *C = (double *)malloc(sizeof(double) * dv * dqk);
+        double *n = (double *)malloc(sizeof(double) * dqk);
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < BH; ++bh) {
+            memset(C, 0, sizeof(double) * dv * dqk);
+            memset(n, 0, sizeof(double) * dqk);
+            for (int t = 0; t < T; ++t) {
+                size_t ti = (size_t)bh * T + t;
+                const double *qt = q + ti * dqk, *kt = k + ti * dqk, *vt = v + ti * dv;
+                const double f = exp(log_sigmoid(fg[ti])), i = exp(ig[ti]);
+                double nq = 0.0;
+                for (int c = 0; c < dqk; ++c) {
+                    n[c] = f * n[c] + i * kt[c] * s;
+                    nq += n[c] * qt[c];
+                }
+                const double nrm = fmax(fabs(nq), 1.0);
+                for (int r = 0; r < dv; ++r) {
+                    double acc = 0.0;
+                    for (int c = 0; c < dqk; ++c) {
+                        C[(size_t)r * dqk + c] = f * C[(size_t)r * dqk + c] + i * vt[r] * kt[c] * s;
+                        acc += C[(size_t)r * dqk + c] * qt[c];
+                    }
+                    double hv = acc / nrm;
+                    if (og) hv *= sigmoid(og[ti * dv + r]);
+                    h[ti * dv + r] = hv;
+                }
+            }
+        }
+        free(C);
+        free(n);
+    }
+    return 0;
+}

@@ -1,0 +1,24 @@
+"""Each planted mistake in the oracle (compiled with -DORACLE_MUTATION=k, on the
+CPU) must be caught by at least one pin; the unmutated oracle passes all.
+
+Mutations: 1 drops 1/sqrt(d); 2 starts the recurrence at m=0; 3 uses floor 1
+in the stabilized normalizer; 4 shifts the forget-sum index; 5 leaves the
+input gate unrescaled in the step; 6 drops |.| on the row sum; 7 uses an
+exponential forget activation; 8 transposes q and k.
+"""
+import pytest
+
+import oracle
+import pins
+
+
+@pytest.mark.parametrize("mutation", range(1, 9))
+def test_mutation_is_caught(mutation):
+    assert oracle._lib(mutation).oracle_mutation() == mutation
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(mutation)
+        except AssertionError as e:
+            caught.append(f"{pin.__name__}: {e}")
+    assert caught, f"mutation {mutation} passed every pin"
