@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark of the stabilized parallel mLSTM forward on GB300.
+
+One step = the whole parallel hot path over one batch: gate preprocessing
+(log-sigmoid prefix sums, prefix-max stabilizer) and the fused causal kernel
+(Q K^T, gating, signed row sum, C'V, normalization).  Workload at N=1: the
+125M-scale layer, B=8, H=4, T=2048, d_qk=d_v=384, bf16 q/k/v, fp32 gates,
+synthetic seeded inputs.  The recurrent generation step (B=256, H=4, d=512,
+fp32 state, in place) is timed in the same run and reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  Under torchrun (N > 1) every rank runs the
+same per-GPU workload on its own GPU (heads are independent: weak scaling, no
+collective on the data path); value = work of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mlstm_matrix_memory_gb300 import workloads as W  # noqa: E402
+
+METRIC = "mLSTM parallel fwd causal TFLOP/s + tokens/s at T=2048 (1×GB300, % of peak)"
+L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default=W.L125M.name, choices=sorted(W.PARALLEL_WORKLOADS))
+    p.add_argument("--algo", default="auto", choices=("auto", "tc", "simt"))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-step", action="store_true", help="skip the recurrent-step measurement")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    return p.parse_args()
+
+
+def dist_setup(n):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d["hbm_gbs"], "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampler of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def kernel_traffic(name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source that is built now (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[name]
+        src = os.path.join(ROOT, "mlstm_matrix_memory_gb300", "csrc", d["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return d["bytes_per_launch"] if sha == d["source_sha256_16"] else None
+    except Exception:
+        return None
+
+
+def oracle_rows(w, heads: int, stride: int = 8):
+    """A bounded sample of the workload for the CPU oracle: every `stride`-th
+    query row of `heads` (b,h) sequences.  Returns (inputs, rows, causal
+    flops of those rows: 2 (i+1) (d_qk + d_v) per row i)."""
+    x = W.parallel_inputs(w, 0, B=1, H=heads)
+    rows, flops = [], 0.0
+    for bh in range(heads):
+        for i in range(stride - 1, w.T, stride):
+            rows.append(bh * w.T + i)
+            flops += 2.0 * (i + 1) * (w.d_qk + w.d_v)
+    return x, rows, flops
+
+
+def oracle_time(x, rows, reps_or_seconds, by_time):
+    import oracle
+    a = (x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"])
+    f = [oracle.f64(t) for t in a]            # widen once, outside the timed region
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.parallel_rows(*f, rows)
+        n += 1
+        el = time.perf_counter() - t0
+        if (by_time and el >= reps_or_seconds) or (not by_time and n >= reps_or_seconds):
+            return n, el
+
+
+def cpu_baseline(w, seconds):
+    import oracle
+    cores = oracle.max_threads()
+    x, rows, flops = oracle_rows(w, heads=max(1, cores))
+    n, el = oracle_time(x, rows, seconds, by_time=True)
+    return {"value": n * flops / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"every 8th query row of {max(1, cores)} heads of {w.name} (fp64, OpenMP over rows), "
+                      f"{n} passes in {el:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    """The oracle, as it stands, timed on the host cores on a bounded sample of
+    the workload per step (rank 0 only)."""
+    w = W.PARALLEL_WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    import oracle
+    cores = oracle.max_threads()
+    x, rows, flops = oracle_rows(w, heads=max(1, cores))
+    oracle_time(x, rows[: max(1, len(rows) // 16)], args.warmup, by_time=False)
+    n, el = oracle_time(x, rows, args.steps, by_time=False)
+    ms = el * 1e3 / n
+    tflops = flops / (ms * 1e-3) / 1e12
+    sample = f"every 8th query row of {max(1, cores)} heads of {w.name} per step (fp64, OpenMP over rows)"
+    line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": sample, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def time_parallel(M, w, xd, algo, steps, warmup, flush):
+    """Per-step CUDA events on the launching stream; L2 flushed before each step."""
+    stream = torch.cuda.current_stream()
+    B, H, T = w.B, w.H, w.T
+    ws = torch.empty(M.parallel_fwd_workspace_bytes(B, H, T), dtype=torch.uint8, device="cuda")
+    h = torch.empty((B, H, T, w.d_v), dtype=w.dtype, device="cuda")
+
+    def one():
+        M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
+        M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=algo)
+
+    for _ in range(warmup):
+        one()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
+        ev[i][1].record(stream)
+        M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=algo)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    gate_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    if M.last_device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    return step_ms, fwd_ms, gate_ms
+
+
+def time_e2e(M, w, xh, algo, steps, warmup):
+    """Through the public API with host buffers: pinned H2D of the step's
+    inputs, both kernels, D2H of h, all inside the timed region."""
+    stream = torch.cuda.current_stream()
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in xh.items()}
+    h_host = torch.empty((w.B, w.H, w.T, w.d_v), dtype=w.dtype).pin_memory()
+    h = torch.empty_like(h_host, device="cuda")
+    ws = torch.empty(M.parallel_fwd_workspace_bytes(w.B, w.H, w.T), dtype=torch.uint8, device="cuda")
+
+    def one():
+        for k in dev:
+            dev[k].copy_(xh[k], non_blocking=True)
+        M.parallel_fwd(dev["q"], dev["k"], dev["v"], dev["igate_pre"], dev["fgate_pre"], h=h, workspace=ws,
+                       algo=algo)
+        h_host.copy_(h, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(v.numel() * v.element_size() for v in xh.values())
+    return e0.elapsed_time(e1) / steps, h2d, h_host.numel() * h_host.element_size()
+
+
+def time_step(M, steps, warmup):
+    """The recurrent generation step, B=256, H=4, d=512, state updated in place
+    (1 GiB of C read and written per step: larger than L2)."""
+    w = W.STEP
+    x = W.step_inputs(w, 0)
+    xd = {k: v.cuda() for k, v in x.items()}
+    stream = torch.cuda.current_stream()
+    h = torch.empty((w.B, w.H, w.d_v), dtype=w.dtype, device="cuda")
+
+    def one():
+        M.step(xd["C"], xd["n"], xd["m"], xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], xd["o"],
+               h=h)
+
+    for _ in range(warmup):
+        one()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        ev[i][0].record(stream)
+        one()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    BH = w.B * w.H
+    nbytes = (2 * BH * w.d_v * w.d_qk * 4 + 2 * BH * w.d_qk * 4 + 2 * BH * 4   # C, n, m read+write
+              + BH * (2 * w.d_qk + 3 * w.d_v) * 2 + 2 * BH * 4)                # q,k,v,o,h (bf16), gates
+    return ms, nbytes, w
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    from mlstm_matrix_memory_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(ws)
+    import mlstm_matrix_memory_gb300 as M
+
+    w = W.PARALLEL_WORKLOADS[args.workload]
+    algo = args.algo
+    if algo == "auto":
+        algo = "tc" if M.tc_supported(w.d_qk, w.d_v, w.dtype) else "simt"
+    xh = W.parallel_inputs(w, seed=rank)
+    xh = {k: v.pin_memory() for k, v in xh.items()}
+    xd = {k: v.cuda() for k, v in xh.items()}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
+
+    barrier(ws)
+    torch.cuda.synchronize()
+    step_ms, fwd_ms, gate_ms = time_parallel(M, w, xd, algo, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_step = max_over_ranks(statistics.mean(step_ms), ws)
+    t_fwd = max_over_ranks(statistics.mean(fwd_ms), ws)
+    e2e_ms, h2d, d2h = time_e2e(M, w, xh, algo, max(5, args.steps // 5), 2)
+    e2e_ms = max_over_ranks(e2e_ms, ws)
+    rec = None
+    if not args.no_step:
+        rec = time_step(M, max(10, args.steps // 2), 3)
+    clk = clocks.stop() if clocks else None
+
+    flops = w.causal_flops
+    value = ws * flops / (t_step * 1e-3) / 1e12
+    peak_tf, peak_bw, src = peaks()
+    achieved = flops / (t_fwd * 1e-3) / 1e12
+    traffic = kernel_traffic("fwd_tc_" + w.name) if algo == "tc" else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) q/k/v, N(0,1) input and N(3,1) forget pre-activations)",
+        "tokens_per_s": ws * w.tokens / (t_step * 1e-3),
+        "frac_of_peak": value / ws / peak_tf,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_qk": w.d_qk, "d_v": w.d_v,
+                   "kernel": algo, "l2": "flushed before every timed step (512 MB memset)",
+                   "parallelism": f"{ws} independent replica(s), heads independent, no collective"},
+        "gate_prep_ms": statistics.mean(gate_ms),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
+                     "traffic": traffic, "kernel": f"mlstm fwd_{algo}",
+                     "work": "causal flops T^2 (d_qk+d_v) per head per launch"},
+        "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+    }
+    if rec is not None:
+        ms, nbytes, sw = rec
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        line["recurrent_step"] = {"workload": sw.name, "ms": ms, "GB_per_s": gbs, "bytes": nbytes,
+                                  "tokens_per_s": sw.B / (ms * 1e-3),
+                                  "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_bw,
+                                               "unit": "GB/s", "frac": gbs / peak_bw,
+                                               "peak_source": f"{src} copy bandwidth",
+                                               "traffic": kernel_traffic("step_" + sw.name)}}
+    if clk:
+        line["clocks"] = clk
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

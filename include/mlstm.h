@@ -1,0 +1,164 @@
+/*
+ * mlstm.h - C ABI of libmlstm.so, the GB300 (sm_103a) mLSTM matrix-memory path.
+ *
+ * Method: "xLSTM: Extended Long Short-Term Memory".
+ *   part 28/30 "Parallel mLSTM Forward Pass", eqs (71)-(77), and its stabilized
+ *   summary eqs (79)-(86) with the log forget matrix eq (101);
+ *   the recurrent mLSTM whose backward pass is eqs (59)-(70) (part 28/30),
+ *   with the output gate eq (27) (part 17/30) for generation.
+ *
+ * Conventions shared by every entry point
+ *  - All tensors are dense, row-major, last index fastest, in DEVICE memory
+ *    owned by the caller.  The library never allocates, frees or retains them.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls only enqueue work on it; they do not synchronize.
+ *  - Every call returns an mlstm_status.  Argument errors are detected on the
+ *    host before anything is launched and leave all buffers untouched.  Calls
+ *    never abort the process.
+ *  - The kernels' internal waits are bounded.  A wait that runs out sets a
+ *    device-side status word and the kernel returns early (its outputs are then
+ *    undefined); mlstm_last_device_status() reads and clears that word.
+ *  - k enters scaled by 1/sqrt(d_qk) (the factor is moved onto K below eq 76);
+ *    q is not scaled.  Both entry points take the raw k.
+ *  - dtype: MLSTM_F32 or MLSTM_BF16 for q, k, v, o and the output h.  Gate
+ *    pre-activations, the stabilizer m, the normalizer n and the state (C, n,
+ *    m) are always fp32.  Arithmetic is fp32 (bf16 tensor-core products with
+ *    fp32 accumulation on the bf16 path).
+ */
+#ifndef MLSTM_H
+#define MLSTM_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLSTM_OK = 0,
+    MLSTM_EINVAL = -1,       /* a size, pointer or combination is invalid */
+    MLSTM_EALIGN = -2,       /* a pointer is not 16-byte aligned */
+    MLSTM_EDTYPE = -3,       /* unsupported dtype */
+    MLSTM_ECUDA = -4,        /* a CUDA runtime/driver call failed */
+    MLSTM_ETIMEOUT = -5,     /* a kernel's bounded wait ran out (device status) */
+    MLSTM_EUNSUPPORTED = -6, /* valid arguments this build or device cannot run */
+    MLSTM_EWORKSPACE = -7    /* workspace missing or smaller than required */
+} mlstm_status;
+
+typedef enum { MLSTM_F32 = 0, MLSTM_BF16 = 1 } mlstm_dtype;
+
+/* Kernel choice for mlstm_parallel_fwd_ex. */
+typedef enum {
+    MLSTM_ALGO_AUTO = 0, /* tensor-core kernel when the shape allows, else SIMT */
+    MLSTM_ALGO_SIMT = 1, /* fp32 CUDA-core kernel: any d_qk, d_v <= 512 (fp32 or bf16) */
+    MLSTM_ALGO_TC = 2    /* tcgen05/TMEM kernel: bf16, d_qk and d_v multiples of 64, <= 512 */
+} mlstm_algo;
+
+/* Bytes of device workspace mlstm_parallel_fwd needs for B*H sequences of
+ * length T: the per-token gate terms of eqs (79)-(80) and (101), 3 fp32 per
+ * token, rounded up to 256 bytes.  Returns 0 if any size is negative. */
+size_t mlstm_parallel_fwd_workspace(int B, int H, int T);
+
+/* Stabilized parallel mLSTM forward pass, part 28/30 eqs (79)-(86):
+ *   Fbar_ij = sum_{k=j+1..i} log sigmoid(fgate_pre_k)    (eq 101, j <= i)
+ *   D~_ij   = Fbar_ij + igate_pre_j,  m_i = max_{j<=i} D~_ij        (79)-(80)
+ *   C'_ij   = (q_i . k_j)/sqrt(d_qk) * exp(D~_ij - m_i)              (81)-(82)
+ *   b_i = sum_j C'_ij,  n_i = max(|b_i|, exp(-m_i))                   (83)-(84)
+ *   h_i = sum_j (C'_ij / n_i) v_j                                     (85)-(86)
+ * (H~ of eq 77; the output gate of eq 78 is not applied.)
+ *
+ *   q, k       [B,H,T,d_qk]  dtype
+ *   v          [B,H,T,d_v]   dtype
+ *   igate_pre  [B,H,T] fp32   input-gate pre-activations i~
+ *   fgate_pre  [B,H,T] fp32   forget-gate pre-activations f~
+ *   h          [B,H,T,d_v]   dtype, output
+ *   m_out      [B,H,T] fp32   output, may be NULL: row stabilizer m_i
+ *   n_out      [B,H,T] fp32   output, may be NULL: normalizer n_i
+ *   workspace  >= mlstm_parallel_fwd_workspace(B,H,T) bytes of device memory,
+ *              16-byte aligned; contents on entry are ignored.
+ * Requirements: B,H >= 0, T >= 0, 1 <= d_qk, d_v <= 512, d_qk and d_v
+ * multiples of 8 (fp32: multiples of 4); q, k, v, h 16-byte aligned.
+ * B*H*T == 0 is a no-op returning MLSTM_OK.  If a row's n_i is 0 (all its
+ * C'_ij are exactly 0 and exp(-m_i) underflows), its h_i is written as 0. */
+int mlstm_parallel_fwd(const void *q, const void *k, const void *v,
+                       const float *igate_pre, const float *fgate_pre,
+                       void *h, float *m_out, float *n_out,
+                       int B, int H, int T, int d_qk, int d_v, int dtype,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* mlstm_parallel_fwd with an explicit kernel choice (mlstm_algo).  Returns
+ * MLSTM_EUNSUPPORTED if the forced kernel cannot run this shape or dtype. */
+int mlstm_parallel_fwd_ex(const void *q, const void *k, const void *v,
+                          const float *igate_pre, const float *fgate_pre,
+                          void *h, float *m_out, float *n_out,
+                          int B, int H, int T, int d_qk, int d_v, int dtype,
+                          void *workspace, size_t workspace_bytes, int algo, void *stream);
+
+/* The two phases of mlstm_parallel_fwd_ex, for callers that time or reuse
+ * them separately.
+ *
+ * mlstm_gate_prep: the gate terms of eqs (79)-(81) and (101) for every token,
+ * written to `workspace` (>= mlstm_parallel_fwd_workspace(B,H,T) bytes):
+ *   cs_t = sum_{k<=t} log sigmoid(fgate_pre_k)     (fp64 accumulation)
+ *   a_t  = igate_pre_t - cs_t,  m_t = cs_t + max_{j<=t} a_j   (row max, eq 80)
+ * stored as three fp32 arrays of B*H*T entries, each starting on a 256-byte
+ * boundary: a_t*log2(e), max_{j<=t} a_j*log2(e), m_t.
+ *
+ * mlstm_parallel_fwd_gated: eqs (81)-(86) from those terms; same arguments and
+ * rules as mlstm_parallel_fwd_ex minus the gate pre-activations.  The
+ * workspace must hold the output of mlstm_gate_prep for the same B, H, T. */
+int mlstm_gate_prep(const float *igate_pre, const float *fgate_pre, int B, int H, int T,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+int mlstm_parallel_fwd_gated(const void *q, const void *k, const void *v,
+                             void *h, float *m_out, float *n_out,
+                             int B, int H, int T, int d_qk, int d_v, int dtype,
+                             const void *workspace, size_t workspace_bytes, int algo,
+                             void *stream);
+
+/* One stabilized recurrent mLSTM step for every head, the generation step
+ * (the recurrence differentiated by part 28/30 eqs 59-70, output gate eq 27):
+ *   m'  = max(log sigmoid(f~) + m, i~)
+ *   f'  = exp(log sigmoid(f~) + m - m'),   i' = exp(i~ - m')
+ *   C  <- f' C + i' v (k/sqrt(d_qk))^T,    n <- f' n + i' k/sqrt(d_qk)
+ *   h   = sigmoid(o) * (C q) / max(|n . q|, exp(-m'))
+ * The stored (C, n) is the true state times exp(-m).  A fresh sequence starts
+ * from C = 0, n = 0, m = -inf.
+ *
+ *   C          [B,H,d_v,d_qk] fp32  in/out (updated in place)
+ *   n          [B,H,d_qk]     fp32  in/out
+ *   m          [B,H]          fp32  in/out
+ *   q, k       [B,H,d_qk]     dtype
+ *   v          [B,H,d_v]      dtype
+ *   o          [B,H,d_v]      dtype output-gate pre-activations, or NULL for
+ *                             no output gate (h = h~)
+ *   igate_pre, fgate_pre [B,H] fp32
+ *   h          [B,H,d_v]      dtype output
+ * Requirements: B,H >= 0; 1 <= d_qk, d_v <= 512; d_qk a multiple of 8;
+ * C, n, q, k 16-byte aligned.  h may not alias any input. */
+int mlstm_step(float *C, float *n, float *m,
+               const void *q, const void *k, const void *v, const void *o,
+               const float *igate_pre, const float *fgate_pre, void *h,
+               int B, int H, int d_qk, int d_v, int dtype, void *stream);
+
+/* Synchronizes `stream`, then returns and clears the device status word of
+ * the current device: MLSTM_OK, or MLSTM_ETIMEOUT if a kernel's bounded wait
+ * ran out since the last call.  MLSTM_ECUDA if the synchronization failed. */
+int mlstm_last_device_status(void *stream);
+
+/* Spin budget of each bounded wait inside the kernels (iterations of a
+ * polling loop).  0 restores the default.  Returns the previous budget.
+ * Small budgets make waits give up early; used to test the timeout path. */
+long long mlstm_set_spin_limit(long long limit);
+
+/* Static, human-readable name of a status code. */
+const char *mlstm_status_str(int status);
+
+/* Library ABI version (major*100 + minor). */
+int mlstm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLSTM_H */

@@ -13,6 +13,9 @@ from .binding import (  # noqa: F401
     step,
     last_device_status,
     set_spin_limit,
+    gate_prep,
+    parallel_fwd_gated,
+    tc_supported,
     library,
     library_path,
 )

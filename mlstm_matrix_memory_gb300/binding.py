@@ -54,6 +54,10 @@ def library() -> ctypes.CDLL:
         lib.mlstm_parallel_fwd.restype = i
         lib.mlstm_parallel_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, i, vp]
         lib.mlstm_parallel_fwd_ex.restype = i
+        lib.mlstm_gate_prep.argtypes = [vp, vp, i, i, i, vp, sz, vp]
+        lib.mlstm_gate_prep.restype = i
+        lib.mlstm_parallel_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, i, vp]
+        lib.mlstm_parallel_fwd_gated.restype = i
         lib.mlstm_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
         lib.mlstm_step.restype = i
         lib.mlstm_last_device_status.argtypes = [vp]
@@ -195,3 +199,45 @@ def set_spin_limit(limit: int) -> int:
     """Set the per-wait spin budget of the kernels' bounded waits (0 = default);
     returns the previous value.  Small values make waits give up (fault injection)."""
     return int(library().mlstm_set_spin_limit(int(limit)))
+
+
+def gate_prep(igate_pre: torch.Tensor, fgate_pre: torch.Tensor, workspace: torch.Tensor) -> None:
+    """Gate phase of the parallel forward (log-sigmoid prefix sums and the
+    prefix-max stabilizer) into ``workspace``; [B,H,T] fp32 CUDA inputs."""
+    lib = library()
+    B, H, T = igate_pre.shape
+    dev = igate_pre.device
+    _need(igate_pre, "igate_pre", (B, H, T), torch.float32, dev)
+    _need(fgate_pre, "fgate_pre", (B, H, T), torch.float32, dev)
+    rc = lib.mlstm_gate_prep(_ptr(igate_pre), _ptr(fgate_pre), B, H, T, _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_gate_prep")
+
+
+def parallel_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, workspace: torch.Tensor,
+                       h: torch.Tensor, m: Optional[torch.Tensor] = None, n: Optional[torch.Tensor] = None,
+                       algo: str = "auto") -> torch.Tensor:
+    """Fused phase of the parallel forward, reading the gate terms that
+    ``gate_prep`` left in ``workspace``.  Writes ``h`` (and m, n if given)."""
+    lib = library()
+    B, H, T, dqk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    _need(q, "q", (B, H, T, dqk), q.dtype, dev)
+    _need(k, "k", (B, H, T, dqk), q.dtype, dev)
+    _need(v, "v", (B, H, T, dv), q.dtype, dev)
+    _need(h, "h", (B, H, T, dv), q.dtype, dev)
+    rc = lib.mlstm_parallel_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(h), _ptr(m), _ptr(n), B, H, T, dqk, dv,
+                                      _DTYPES[q.dtype], _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), ALGOS[algo], _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_parallel_fwd_gated")
+    return h
+
+
+def tc_supported(d_qk: int, d_v: int, dtype: torch.dtype) -> bool:
+    """Whether the tensor-core kernel tiles this head size and dtype."""
+    return dtype == torch.bfloat16 and d_qk % 64 == 0 and d_v % 64 == 0 and d_qk <= 512 and d_v <= 512

@@ -1,0 +1,61 @@
+// Host-side launch interfaces between the C-ABI layer (api.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace mlstm {
+
+// Per-token gate terms of one sequence set, produced by gate_prep, each
+// [B*H*T] fp32 (see gate_prep.cu):
+//   a2[t] = (i~_t - cs_t) * log2(e)                 column term of D~ - m
+//   p2[t] = max_{j<=t} a2[j]                        row term of D~ - m
+//   m[t]  = cs_t + max_{j<=t}(i~_j - cs_j)          row max of D~ (eq 80)
+// with cs_t = sum_{k<=t} log sigmoid(f~_k).  Then for j <= i:
+//   D~_ij - m_i = (a2[j] - p2[i]) / log2(e)  <= 0.
+struct GateTerms {
+  float* a2;
+  float* p2;
+  float* m;
+};
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* h;
+  float* m_out;   // may be null
+  float* n_out;   // may be null
+  GateTerms g;
+  int BH, T, dqk, dv;
+  int dtype;      // kF32 / kBF16
+  float scale;    // 1/sqrt(dqk)
+  DevStatus st;
+};
+
+struct StepArgs {
+  float* C;
+  float* n;
+  float* m;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;  // may be null
+  const float* ig;
+  const float* fg;
+  void* h;
+  int BH, dqk, dv;
+  int dtype;
+  float scale;
+};
+
+cudaError_t launch_gate_prep(const float* ig, const float* fg, GateTerms g, int BH, int T,
+                             cudaStream_t stream);
+cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream);
+bool fwd_tc_supported(int dqk, int dv, int dtype);
+int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);   // returns a Status
+cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
+
+}  // namespace mlstm
