@@ -141,6 +141,40 @@ int mlstm_step(float *C, float *n, float *m,
                const float *igate_pre, const float *fgate_pre, void *h,
                int B, int H, int d_qk, int d_v, int dtype, void *stream);
 
+/* Size of the scratch array built into the library for
+ * mlstm_parallel_fwd_noalloc: 4 MiB, enough for B*H*T up to 349,504 tokens. */
+#define MLSTM_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* mlstm_parallel_fwd for callers that cannot allocate device memory.  (The
+ * paper has no counterpart to this entry point; it is a library convenience.)
+ *
+ * Who needs it: code that must not call cudaMalloc or any allocating routine,
+ * for example a plug-in whose host application owns all device memory, a
+ * caller working inside a memory pool's own callbacks, or a job whose memory
+ * budget is fixed up front.  Such callers cannot provide the workspace that
+ * mlstm_parallel_fwd asks for.  This entry point instead uses a fixed scratch
+ * array of MLSTM_NOALLOC_SCRATCH_BYTES compiled into the library.  Every GPU
+ * that loads the library holds that array until the process exits.
+ *
+ * Same arguments, results and rules as mlstm_parallel_fwd, minus the
+ * workspace; the caller still passes all inputs and outputs.  It allocates
+ * nothing.
+ *  - Returns MLSTM_EWORKSPACE, and launches nothing, when the job needs more
+ *    scratch than the array holds: mlstm_parallel_fwd_workspace(B,H,T) >
+ *    MLSTM_NOALLOC_SCRATCH_BYTES.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *    first call before any stream capture begins.
+ *  - Every call on a device shares the one array.  Calls whose kernels
+ *    overlap on the GPU (other streams, other host threads) race on it and
+ *    give wrong results: serialize them.  Nothing in the array needs clearing
+ *    between calls; each call overwrites what it reads. */
+int mlstm_parallel_fwd_noalloc(const void *q, const void *k, const void *v,
+                               const float *igate_pre, const float *fgate_pre,
+                               void *h, float *m_out, float *n_out,
+                               int B, int H, int T, int d_qk, int d_v, int dtype,
+                               void *stream);
+
 /* Synchronizes `stream`, then returns and clears the device status word of
  * the current device: MLSTM_OK, or MLSTM_ETIMEOUT if a kernel's bounded wait
  * ran out since the last call.  MLSTM_ECUDA if the synchronization failed. */
