@@ -17,7 +17,7 @@ __device__ int g_status[2];
 
 namespace {
 
-constexpr long long kDefaultSpin = 1LL << 26;
+constexpr long long kDefaultSpin = 1LL << 22;
 std::atomic<long long> g_spin_limit{kDefaultSpin};
 
 constexpr int kMaxDevices = 64;

@@ -1,6 +1,487 @@
-// placeholder, replaced by the tcgen05 kernel
+// Fused causal mLSTM forward on the Blackwell tensor cores (tcgen05 + TMEM + TMA).
+//
+// "xLSTM: Extended Long Short-Term Memory", part 28/30, stabilized parallel
+// forward, eqs (79)-(86).  bf16 q, k, v; fp32 accumulation; fp32 gates.
+//
+// One CTA computes 128 query rows (one TMEM lane per row) of one head for a
+// slice of d_v.  Per causal key tile j (BN keys):
+//   S_j  = Q K_j^T                       tcgen05.mma, A = Q, B = K_j (both K-major,
+//                                        TMA-staged with 128-byte swizzle), D in TMEM
+//   P_j  = S_j * s * D'_j                gating warps: tcgen05.ld of S, the gate
+//                                        D'_ij = exp2(a2_j - p2_i) (eq 81; zero above
+//                                        the diagonal), signed row sum b_i in fp32
+//                                        (eq 83), bf16 P written to shared memory
+//   O   += P_j V_j                       tcgen05.mma, A = P (K-major), B = V_j (MN-major)
+// The row max m_i of eq (80) is known before the loop (prefix max from the gate
+// pass), so the online rescaling of O and b that softmax attention needs never
+// fires here and is not performed.  Off-diagonal tiles use the rank-one form
+// D'_ij = 2^(a2_j - A) * 2^(A - p2_i) with A the tile's max column term (both
+// factors <= 1): one exponential per row and per column instead of per entry.
+// The epilogue divides O by n_i = max(|b_i|, exp(-m_i)) (eq 84) and stores H~.
+//
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2
+// TMEM allocator, warps 4..11 gating + epilogue (two warps per TMEM lane
+// quarter, each owning half of the tile's columns).  S is double-buffered in
+// TMEM so the MMA of tile j+1 overlaps the gating of tile j.  Every wait is
+// bounded; a wait that runs out records its site, raises a CTA-wide abort flag,
+// drains in-flight copies and MMAs, frees TMEM and returns.
+#include <algorithm>
+#include <mutex>
+
 #include "internal.h"
+#include "tc_ptx.cuh"
+
 namespace mlstm {
-bool fwd_tc_supported(int, int, int) { return false; }
-int launch_fwd_tc(const FwdArgs&, cudaStream_t) { return kUnsupported; }
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;
+constexpr int kThreads = 384;
+constexpr int kStageBytes = 16384;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemLimit = 232448;      // opt-in shared memory per block on sm_100-family
+constexpr long long kDrainSpin = 1LL << 22;
+
+// barrier slots
+enum : int {
+  kBarQFull = 0,
+  kBarSFull = 1,    // 2 buffers
+  kBarSEmpty = 3,   // 2 buffers
+  kBarPFull = 5,
+  kBarPEmpty = 6,
+  kBarOFull = 7,
+  kBarDrain = 8,
+  kBarFull = 9,                   // kMaxStages
+  kBarEmpty = 9 + kMaxStages,     // kMaxStages
+  kNumBars = 9 + 2 * kMaxStages,
+};
+
+// wait-site codes recorded in the status word
+enum : int { kSiteProducer = 1, kSiteMma = 2, kSiteGate = 3, kSiteEpilogue = 4 };
+
+struct TcParams {
+  const float* a2;
+  const float* p2;
+  const float* mrow;
+  __nv_bfloat16* h;
+  float* m_out;
+  float* n_out;
+  int T, BH, dqk, dv;
+  int nsplit;      // CTAs per query tile along d_v (1 or 2)
+  int dv_slice;    // d_v columns of the first slice (the second gets the rest)
+  int nst;         // ring stages
+  int kd;          // d columns per K stage (64 or 128)
+  int vk;          // keys per V stage
+  int nqt;         // query tiles per head
+  float log2_scale;
+  DevStatus st;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+              const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
+  constexpr int HALF = BN / 2;           // columns of a tile owned by one gating warp
+  constexpr uint32_t SOFF = kTmemCols - 2 * BN;   // TMEM column of S buffer 0
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ uint32_t tmem_holder;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &abort_flag;
+
+  // ---- work item: longest query tiles of all heads first
+  const int per_rank = p.BH * p.nsplit;
+  const int qt = p.nqt - 1 - (int)(blockIdx.x / per_rank);
+  const int rem = (int)(blockIdx.x % per_rank);
+  const int bh = rem / p.nsplit, split = rem % p.nsplit;
+  const int i0 = qt * kBM;
+  const int dv_off = split * p.dv_slice;
+  const int dv_cta = split == 0 ? p.dv_slice : p.dv - p.dv_slice;
+  const int i_last = min(p.T, i0 + kBM) - 1;
+  const int nkv = i_last / BN + 1;
+  const int nkc = p.dqk / p.kd;          // K stages per key tile
+  const int nvc = BN / p.vk;             // V stages per key tile
+  const size_t hbase = (size_t)bh * p.T;
+
+  const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint32_t sQ = base;                                  // dqk/64 boxes of [128 x 64] bf16
+  const uint32_t sP = sQ + (uint32_t)p.dqk * kBM * 2;        // BN/64 boxes of [128 x 64] bf16
+  const uint32_t sRing = sP + (uint32_t)BN * kBM * 2;        // nst stages of 16 KB
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(kBarQFull), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kBarSFull + b), 1);
+      mbar_init(bar(kBarSEmpty + b), 8);
+    }
+    mbar_init(bar(kBarPFull), 8);
+    mbar_init(bar(kBarPEmpty), 1);
+    mbar_init(bar(kBarOFull), 1);
+    mbar_init(bar(kBarDrain), 1);
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(bar(kBarFull + s), 1);
+      mbar_init(bar(kBarEmpty + s), 1);
+    }
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  const long long spin = p.st.spin_limit;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int last_it[kMaxStages];
+    for (int s = 0; s < kMaxStages; ++s) last_it[s] = -1;
+    mbar_arrive_expect_tx(bar(kBarQFull), (uint32_t)p.dqk * kBM * 2);
+    for (int b = 0; b < p.dqk / 64; ++b)
+      tma_load_3d(sQ + b * 16384u, &tmap_q, bar(kBarQFull), b * 64, i0, bh);
+    int it = 0;
+    bool ok = true;
+    for (int j = 0; j <= nkv && ok; ++j) {
+      if (j < nkv) {
+        for (int c = 0; c < nkc && ok; ++c, ++it) {
+          const int st = it % p.nst;
+          ok = mbar_wait(bar(kBarEmpty + st), ((it / p.nst) & 1) ^ 1, spin, abort, p.st, kSiteProducer);
+          if (!ok) break;
+          const uint32_t dst = sRing + st * kStageBytes;
+          mbar_arrive_expect_tx(bar(kBarFull + st), (uint32_t)BN * p.kd * 2);
+          for (int b = 0; b < p.kd / 64; ++b)
+            tma_load_3d(dst + b * (BN * 128u), &tmap_k, bar(kBarFull + st), c * p.kd + b * 64, j * BN, bh);
+          last_it[st] = it;
+        }
+      }
+      if (j >= 1 && ok) {
+        for (int e = 0; e < nvc && ok; ++e, ++it) {
+          const int st = it % p.nst;
+          ok = mbar_wait(bar(kBarEmpty + st), ((it / p.nst) & 1) ^ 1, spin, abort, p.st, kSiteProducer);
+          if (!ok) break;
+          const uint32_t dst = sRing + st * kStageBytes;
+          mbar_arrive_expect_tx(bar(kBarFull + st), (uint32_t)p.vk * dv_cta * 2);
+          for (int s = 0; s < dv_cta / 64; ++s)
+            tma_load_3d(dst + s * (p.vk * 128u), &tmap_v, bar(kBarFull + st), dv_off + s * 64,
+                        (j - 1) * BN + e * p.vk, bh);
+          last_it[st] = it;
+        }
+      }
+    }
+    // make sure no copy is still writing this CTA's shared memory on exit
+    for (long long w = 0; w < kDrainSpin; ++w)
+      if (mbar_try_wait(bar(kBarQFull), 0)) break;
+    for (int s = 0; s < kMaxStages; ++s)
+      if (last_it[s] >= 0) {
+        for (long long w = 0; w < kDrainSpin; ++w)
+          if (mbar_try_wait(bar(kBarFull + s), (last_it[s] / p.nst) & 1)) break;
+      }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idS = idesc_bf16_f32(kBM, BN, 0, 0);
+    bool ok = mbar_wait(bar(kBarQFull), 0, spin, abort, p.st, kSiteMma);
+    tc_fence_after();
+    int it = 0;
+    for (int j = 0; j <= nkv && ok; ++j) {
+      if (j < nkv) {
+        const int buf = j & 1, u = j >> 1;
+        ok = mbar_wait(bar(kBarSEmpty + buf), (u & 1) ^ 1, spin, abort, p.st, kSiteMma);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_s = tmem + SOFF + buf * BN;
+        for (int c = 0; c < nkc && ok; ++c, ++it) {
+          const int st = it % p.nst;
+          ok = mbar_wait(bar(kBarFull + st), (it / p.nst) & 1, spin, abort, p.st, kSiteMma);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sk = sRing + st * kStageBytes;
+          for (int kk = 0; kk < p.kd / 16; ++kk) {
+            const int dd = c * p.kd + kk * 16, kb = kk * 16;
+            const uint64_t ad = smem_desc_sw128(sQ + (dd >> 6) * 16384u + (dd & 63) * 2, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(sk + (kb >> 6) * (BN * 128u) + (kb & 63) * 2, 16, 1024);
+            mma_bf16_ss(d_s, ad, bd, idS, (c | kk) != 0);
+          }
+          mma_commit(bar(kBarEmpty + st));
+        }
+        if (!ok) break;
+        mma_commit(bar(kBarSFull + buf));
+      }
+      if (j >= 1) {
+        const int jj = j - 1;
+        ok = mbar_wait(bar(kBarPFull), jj & 1, spin, abort, p.st, kSiteMma);
+        if (!ok) break;
+        tc_fence_after();
+        for (int e = 0; e < nvc && ok; ++e, ++it) {
+          const int st = it % p.nst;
+          ok = mbar_wait(bar(kBarFull + st), (it / p.nst) & 1, spin, abort, p.st, kSiteMma);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sv = sRing + st * kStageBytes;
+          for (int kk = 0; kk < p.vk / 16; ++kk) {
+            const int key = e * p.vk + kk * 16;
+            const uint64_t ad = smem_desc_sw128(sP + (key >> 6) * 16384u + (key & 63) * 2, 16, 1024);
+            int n_off = 0;
+            while (n_off < dv_cta) {
+              const int nw = min(256, dv_cta - n_off);
+              const uint64_t bd = smem_desc_sw128(sv + (n_off >> 6) * (p.vk * 128u) + kk * 2048u,
+                                                  p.vk * 128u, 1024);
+              mma_bf16_ss(tmem + n_off, ad, bd, idesc_bf16_f32(kBM, nw, 0, 1), (jj | e | kk) != 0);
+              n_off += nw;
+            }
+          }
+          mma_commit(bar(kBarEmpty + st));
+        }
+        if (!ok) break;
+        mma_commit(bar(kBarPEmpty));
+      }
+    }
+    if (ok) mma_commit(bar(kBarOFull));
+    // drain: every MMA issued above has completed before TMEM is released
+    mma_commit(bar(kBarDrain));
+    for (long long w = 0; w < kDrainSpin; ++w)
+      if (mbar_try_wait(bar(kBarDrain), 0)) break;
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ gating + epilogue
+    const int gw = warp - 4, qd = gw & 3, half = gw >> 2;
+    const int rl = 32 * qd + lane;                  // row within the tile = TMEM lane
+    const int i = i0 + rl;
+    const bool row_ok = i < p.T;
+    const float rr = row_ok ? p.p2[hbase + i] - p.log2_scale : 0.0f;   // P = S * 2^(a2_j - rr)
+    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    float bsum = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int j0 = j * BN, cbase = j0 + half * HALF;
+      const int buf = j & 1, u = j >> 1;
+      float av[HALF / 32];
+#pragma unroll
+      for (int t = 0; t < HALF / 32; ++t) {
+        const int col = cbase + lane + 32 * t;
+        av[t] = col < p.T ? p.a2[hbase + col] : -INFINITY;
+      }
+      const bool diag = j0 + BN - 1 > i0;
+      float A = -INFINITY;
+      if (!diag) {
+#pragma unroll
+        for (int t = 0; t < HALF / 32; ++t) A = fmaxf(A, av[t]);
+        A = warp_max(A);
+#pragma unroll
+        for (int t = 0; t < HALF / 32; ++t) av[t] = A == -INFINITY ? 0.0f : exp2f(av[t] - A);
+      }
+      ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[HALF];
+#pragma unroll
+      for (int t = 0; t < HALF / 32; ++t)
+        tmem_ld32(tmem + lane_addr + SOFF + buf * BN + half * HALF + 32 * t,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * t]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSEmpty + buf));
+
+      uint32_t pk[HALF / 2];
+      if (!diag) {
+        const float r = (A == -INFINITY || !row_ok) ? 0.0f : exp2f(A - rr);
+#pragma unroll
+        for (int c = 0; c < HALF; c += 2) {
+          const float c0 = __shfl_sync(0xffffffffu, av[c / 32], c & 31);
+          const float c1 = __shfl_sync(0xffffffffu, av[(c + 1) / 32], (c + 1) & 31);
+          const float x0 = __uint_as_float(sv[c]) * c0 * r;
+          const float x1 = __uint_as_float(sv[c + 1]) * c1 * r;
+          bsum += x0 + x1;
+          pk[c / 2] = pack_bf16x2(x0, x1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < HALF; c += 2) {
+          const float a0 = __shfl_sync(0xffffffffu, av[c / 32], c & 31);
+          const float a1 = __shfl_sync(0xffffffffu, av[(c + 1) / 32], (c + 1) & 31);
+          const int col = cbase + c;
+          const float e0 = (row_ok && col <= i) ? exp2f(a0 - rr) : 0.0f;
+          const float e1 = (row_ok && col + 1 <= i) ? exp2f(a1 - rr) : 0.0f;
+          const float x0 = __uint_as_float(sv[c]) * e0;
+          const float x1 = __uint_as_float(sv[c + 1]) * e1;
+          bsum += x0 + x1;
+          pk[c / 2] = pack_bf16x2(x0, x1);
+        }
+      }
+      // the previous tile's O MMA must be done reading P before it is overwritten
+      ok = mbar_wait(bar(kBarPEmpty), (j & 1) ^ 1, spin, abort, p.st, kSiteGate);
+      if (!ok) break;
+#pragma unroll
+      for (int g = 0; g < HALF / 8; ++g) {
+        const int c = half * HALF + 8 * g;           // column within the tile
+        const uint32_t addr = sP + (c >> 6) * 16384u + rl * 128u + ((((c & 63) >> 3) ^ (rl & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * g]),
+                     "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarPFull));
+    }
+
+    // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n
+    if (ok) ok = mbar_wait(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
+    tc_fence_after();
+    // after the last O MMA the P tile is free: reuse it to combine the two half sums
+    float* bpart = reinterpret_cast<float*>(dsmem + (sP - smem_u32(dsmem)));
+    if (ok) bpart[half * kBM + rl] = bsum;
+    named_bar_sync(1, 256);
+    if (ok) {
+      const float b = bpart[rl] + bpart[kBM + rl];
+      const float m = row_ok ? p.mrow[hbase + i] : 0.0f;
+      const float nrm = fmaxf(fabsf(b), expf(-m));
+      const float inv = nrm > 0.0f ? 1.0f / nrm : 0.0f;
+      const int cols = dv_cta / 2, c0 = half * cols;
+      __nv_bfloat16* hrow = p.h + (hbase + (row_ok ? i : 0)) * p.dv + dv_off + c0;
+      for (int ch = 0; ch < cols / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_addr + c0 + 32 * ch, o);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          w[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(hrow + 32 * ch);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        }
+      }
+      if (row_ok && split == 0 && half == 0) {
+        if (p.m_out) p.m_out[hbase + i] = m;
+        if (p.n_out) p.n_out[hbase + i] = nrm;
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static std::once_flag once;
+  static EncodeTiled fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  });
+  return fn;
+}
+
+// [BH, T, d] bf16 viewed as a 3-D tensor (d fastest); box = 64 x rows x 1 with
+// 128-byte swizzle.  Rows past T read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * T};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int bn, nsplit, dv_slice, kd, vk, nst;
+  size_t smem;
+};
+
+Plan plan_for(int dqk, int dv) {
+  Plan pl;
+  if (dv <= 256) {
+    pl.bn = 128; pl.nsplit = 1; pl.dv_slice = dv;
+  } else if (dv <= 384) {
+    pl.bn = 64; pl.nsplit = 1; pl.dv_slice = dv;
+  } else {
+    pl.bn = 128; pl.nsplit = 2; pl.dv_slice = 256;
+  }
+  pl.kd = (pl.bn == 64 && dqk % 128 == 0) ? 128 : 64;
+  const int widest = pl.dv_slice;   // the first slice is never narrower than the second
+  pl.vk = 16;
+  for (int v = 128; v >= 16; v >>= 1)
+    if (v <= pl.bn && v * widest * 2 <= kStageBytes) { pl.vk = v; break; }
+  const size_t fixed = 1024 + (size_t)dqk * kBM * 2 + (size_t)pl.bn * kBM * 2;
+  const size_t static_smem = 1024;  // barriers, TMEM address, abort flag (rounded up)
+  long long room = (long long)kSmemLimit - (long long)static_smem - (long long)fixed;
+  pl.nst = (int)std::min<long long>(kMaxStages, room / kStageBytes);
+  pl.smem = fixed + (size_t)pl.nst * kStageBytes;
+  return pl;
+}
+
+template <int BN>
+int launch_bn(const FwdArgs& a, const Plan& pl, const CUtensorMap& mq, const CUtensorMap& mk,
+              const CUtensorMap& mv, cudaStream_t stream) {
+  if (cudaFuncSetAttribute(fwd_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
+      cudaSuccess)
+    return kCuda;
+  TcParams p;
+  p.a2 = a.g.a2; p.p2 = a.g.p2; p.mrow = a.g.m;
+  p.h = (__nv_bfloat16*)a.h; p.m_out = a.m_out; p.n_out = a.n_out;
+  p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv;
+  p.nsplit = pl.nsplit; p.dv_slice = pl.dv_slice; p.nst = pl.nst; p.kd = pl.kd; p.vk = pl.vk;
+  p.nqt = (a.T + kBM - 1) / kBM;
+  p.log2_scale = log2f(a.scale);
+  p.st = a.st;
+  const long long grid = (long long)p.nqt * a.BH * pl.nsplit;
+  if (grid > 0x7fffffffLL) return kInval;
+  fwd_tc_kernel<BN><<<(unsigned)grid, kThreads, pl.smem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
+int device_is_sm100_family() {
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
+  return major == 10;
+}
+
+}  // namespace
+
+bool fwd_tc_supported(int dqk, int dv, int dtype) {
+  return dtype == kBF16 && dqk % 64 == 0 && dv % 64 == 0 && dqk >= 64 && dv >= 64 && dqk <= 512 &&
+         dv <= 512;
+}
+
+int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
+  if (a.BH <= 0 || a.T <= 0) return kOk;
+  if (!fwd_tc_supported(a.dqk, a.dv, a.dtype)) return kUnsupported;
+  if (!device_is_sm100_family()) return kUnsupported;
+  const Plan pl = plan_for(a.dqk, a.dv);
+  if (pl.nst < 2) return kUnsupported;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, pl.bn) ||
+      !make_map(&mv, a.v, a.dv, a.T, a.BH, pl.vk))
+    return kCuda;
+  return pl.bn == 64 ? launch_bn<64>(a, pl, mq, mk, mv, stream) : launch_bn<128>(a, pl, mq, mk, mv, stream);
+}
+
 }  // namespace mlstm
