@@ -19,13 +19,14 @@
 // factors <= 1): one exponential per row and per column instead of per entry.
 // The epilogue divides O by n_i = max(|b_i|, exp(-m_i)) (eq 84) and stores H~.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2
-// TMEM allocator, warps 4..11 gating + epilogue (two warps per TMEM lane
+// Warp roles (384 threads): warps 0, 2, 3 TMA producers (warp 2 also
+// allocates TMEM), warp 1 MMA issuer, warps 4..11 gating + epilogue (two warps per TMEM lane
 // quarter, each owning half of the tile's columns).  S is double-buffered in
 // TMEM so the MMA of tile j+1 overlaps the gating of tile j.  Every wait is
 // bounded; a wait that runs out records its site, raises a CTA-wide abort flag,
 // drains in-flight copies and MMAs, frees TMEM and returns.
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -36,13 +37,31 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBM = 128;
+constexpr int kBM = 128;           // query rows per CTA (TMEM lanes)
+constexpr int kBN = 128;           // keys per tile
 constexpr int kThreads = 384;
-constexpr int kStageBytes = 16384;
+constexpr int kStageBytes = 32768;   // one ring slot: a 128x128 K chunk or a VKxdv V chunk
 constexpr int kMaxStages = 8;
+constexpr int kProducers = 3;      // warps 0, 2, 3 issue the tensor loads
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemLimit = 232448;      // opt-in shared memory per block on sm_100-family
 constexpr long long kDrainSpin = 1LL << 22;
+
+#ifdef MLSTM_TRACE
+// Per-event clock64 stamps of one CTA (trace builds only): [event][tile].
+constexpr int kTraceTiles = 64;
+__device__ long long g_trace[24 * kTraceTiles];
+__device__ int g_trace_block;
+#define TRACE(ev, j)                                                                  \
+  do {                                                                                \
+    if ((int)blockIdx.x == g_trace_block && (j) < kTraceTiles)                        \
+      g_trace[(ev) * kTraceTiles + (j)] = clock64();                                  \
+  } while (0)
+#else
+#define TRACE(ev, j) \
+  do {               \
+  } while (0)
+#endif
 
 // barrier slots
 enum : int {
@@ -72,23 +91,24 @@ struct TcParams {
   int nsplit;      // CTAs per query tile along d_v (1 or 2)
   int dv_slice;    // d_v columns of the first slice (the second gets the rest)
   int nst;         // ring stages
-  int kd;          // d columns per K stage (64 or 128)
   int vk;          // keys per V stage
   int nqt;         // query tiles per head
   float log2_scale;
   DevStatus st;
 };
 
-template <int BN>
+template <int BN, int NSBUF, int VK>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
               const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
   constexpr int HALF = BN / 2;           // columns of a tile owned by one gating warp
-  constexpr uint32_t SOFF = kTmemCols - 2 * BN;   // TMEM column of S buffer 0
+  constexpr uint32_t SOFF = kTmemCols - NSBUF * BN;   // TMEM column of S buffer 0
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
+  __shared__ int last_it_s[kMaxStages];     // last ring iteration loaded into each slot
+  volatile int* last_it = last_it_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &abort_flag;
@@ -103,8 +123,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   const int dv_cta = split == 0 ? p.dv_slice : p.dv - p.dv_slice;
   const int i_last = min(p.T, i0 + kBM) - 1;
   const int nkv = i_last / BN + 1;
-  const int nkc = p.dqk / p.kd;          // K stages per key tile
-  const int nvc = BN / p.vk;             // V stages per key tile
+  const int nkc = (p.dqk + 127) / 128;   // K stages per key tile (128 d-columns each)
+  constexpr int nvc = BN / VK;           // V stages per key tile
   const size_t hbase = (size_t)bh * p.T;
 
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
@@ -113,12 +133,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   const uint32_t sRing = sP + (uint32_t)BN * kBM * 2;        // nst stages of 16 KB
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
+  if (threadIdx.x < kMaxStages) last_it_s[threadIdx.x] = -1;
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar(kBarQFull), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarSFull + b), 1);
-      mbar_init(bar(kBarSEmpty + b), 8);
+      mbar_init(bar(kBarSEmpty + b), 8);   // one arrival per gating warp
     }
     mbar_init(bar(kBarPFull), 8);
     mbar_init(bar(kBarPEmpty), 1);
@@ -142,108 +163,139 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
   const long long spin = p.st.spin_limit;
+  if (threadIdx.x == 0) TRACE(14, 0);
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ TMA producer
-    int last_it[kMaxStages];
-    for (int s = 0; s < kMaxStages; ++s) last_it[s] = -1;
-    mbar_arrive_expect_tx(bar(kBarQFull), (uint32_t)p.dqk * kBM * 2);
-    for (int b = 0; b < p.dqk / 64; ++b)
-      tma_load_3d(sQ + b * 16384u, &tmap_q, bar(kBarQFull), b * 64, i0, bh);
-    int it = 0;
+  if ((warp == 0 || warp == 2 || warp == 3) && lane == 0) {
+    // ------------------------------------------------------------ TMA producers
+    // Three producer warps share the ring.  Each slot has one owner, producer
+    // slot % kProducers, which handles every round of that slot in order, so
+    // no producer ever waits more than one phase ahead on a slot's barrier
+    // (parity waits cannot tell phase k from phase k+2).  Several issuing
+    // warps keep more tensor loads in flight than one.  Ring order per key
+    // tile j: K_j (nkc slots), then V_{j-1} (nvc slots).
+    const int pi = warp == 0 ? 0 : warp - 1;
+    if (pi == 0) mbar_arrive_expect_tx(bar(kBarQFull), (uint32_t)p.dqk * kBM * 2);
+    for (int b2 = pi; b2 < p.dqk / 64; b2 += kProducers)
+      tma_load_3d(sQ + b2 * 16384u, &tmap_q, bar(kBarQFull), b2 * 64, i0, bh);
+    int st = 0, it = 0;
+    uint32_t ph = 0;
     bool ok = true;
+    const uint32_t vbytes = (uint32_t)VK * dv_cta * 2;
     for (int j = 0; j <= nkv && ok; ++j) {
       if (j < nkv) {
-        for (int c = 0; c < nkc && ok; ++c, ++it) {
-          const int st = it % p.nst;
-          ok = mbar_wait(bar(kBarEmpty + st), ((it / p.nst) & 1) ^ 1, spin, abort, p.st, kSiteProducer);
-          if (!ok) break;
-          const uint32_t dst = sRing + st * kStageBytes;
-          mbar_arrive_expect_tx(bar(kBarFull + st), (uint32_t)BN * p.kd * 2);
-          for (int b = 0; b < p.kd / 64; ++b)
-            tma_load_3d(dst + b * (BN * 128u), &tmap_k, bar(kBarFull + st), c * p.kd + b * 64, j * BN, bh);
-          last_it[st] = it;
+        for (int c = 0; c < nkc; ++c, ++it) {
+          if (st % kProducers == pi) {
+            ok = mbar_wait(bar(kBarEmpty + st), ph ^ 1, spin, abort, p.st, kSiteProducer);
+            if (!ok) break;
+            if (c == 0) TRACE(4, j);
+            TRACE(16, it);
+            const int kb = min(2, (p.dqk - c * 128) / 64);     // 64-column boxes in this chunk
+            mbar_arrive_expect_tx(bar(kBarFull + st), (uint32_t)kb * BN * 128);
+            for (int b2 = 0; b2 < kb; ++b2)
+              tma_load_3d(sRing + st * kStageBytes + b2 * (BN * 128u), &tmap_k, bar(kBarFull + st),
+                          c * 128 + b2 * 64, j * BN, bh);
+            last_it[st] = it;
+          }
+          if (++st == p.nst) { st = 0; ph ^= 1; }
         }
       }
       if (j >= 1 && ok) {
-        for (int e = 0; e < nvc && ok; ++e, ++it) {
-          const int st = it % p.nst;
-          ok = mbar_wait(bar(kBarEmpty + st), ((it / p.nst) & 1) ^ 1, spin, abort, p.st, kSiteProducer);
-          if (!ok) break;
-          const uint32_t dst = sRing + st * kStageBytes;
-          mbar_arrive_expect_tx(bar(kBarFull + st), (uint32_t)p.vk * dv_cta * 2);
-          for (int s = 0; s < dv_cta / 64; ++s)
-            tma_load_3d(dst + s * (p.vk * 128u), &tmap_v, bar(kBarFull + st), dv_off + s * 64,
-                        (j - 1) * BN + e * p.vk, bh);
-          last_it[st] = it;
+        for (int e = 0; e < nvc; ++e, ++it) {
+          if (st % kProducers == pi) {
+            ok = mbar_wait(bar(kBarEmpty + st), ph ^ 1, spin, abort, p.st, kSiteProducer);
+            if (!ok) break;
+            if (e == 0) TRACE(5, j - 1);
+            TRACE(16, it);
+            const uint32_t dst = sRing + st * kStageBytes;
+            mbar_arrive_expect_tx(bar(kBarFull + st), vbytes);
+            for (int s2 = 0; s2 < dv_cta / 64; ++s2)
+              tma_load_3d(dst + s2 * (VK * 128u), &tmap_v, bar(kBarFull + st), dv_off + s2 * 64,
+                          (j - 1) * BN + e * VK, bh);
+            last_it[st] = it;
+          }
+          if (++st == p.nst) { st = 0; ph ^= 1; }
         }
       }
     }
-    // make sure no copy is still writing this CTA's shared memory on exit
-    for (long long w = 0; w < kDrainSpin; ++w)
-      if (mbar_try_wait(bar(kBarQFull), 0)) break;
-    for (int s = 0; s < kMaxStages; ++s)
-      if (last_it[s] >= 0) {
-        for (long long w = 0; w < kDrainSpin; ++w)
-          if (mbar_try_wait(bar(kBarFull + s), (last_it[s] / p.nst) & 1)) break;
-      }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
+    // Descriptors are built once; per MMA only the start-address field moves
+    // (16-byte units in the low bits, no carry: shared addresses < 256 KB).
     const uint32_t idS = idesc_bf16_f32(kBM, BN, 0, 0);
+    const uint64_t dQ = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dK = smem_desc_sw128(sRing, 16, 1024);
+    const uint64_t dP = smem_desc_sw128(sP, 16, 1024);
+    const uint64_t dV = smem_desc_sw128(sRing, VK * 128u, 1024);
+    const int npieces = (dv_cta + 255) / 256;
+    const int nw0 = dv_cta > 256 ? 256 : dv_cta, nw1 = dv_cta - nw0;   // O columns per MMA
+    const uint32_t idO0 = idesc_bf16_f32(kBM, nw0, 0, 1);
+    const uint32_t idO1 = idesc_bf16_f32(kBM, nw1 > 0 ? nw1 : 16, 0, 1);
+    const uint32_t vpiece1 = (uint32_t)(nw0 >> 6) * (VK * 128u) >> 4;   // 2nd piece's B offset (16 B units)
+    constexpr int vsteps = VK / 16;
     bool ok = mbar_wait(bar(kBarQFull), 0, spin, abort, p.st, kSiteMma);
     tc_fence_after();
-    int it = 0;
+    int st = 0, mit = 0;
+    uint32_t ph = 0;
     for (int j = 0; j <= nkv && ok; ++j) {
       if (j < nkv) {
-        const int buf = j & 1, u = j >> 1;
+        const int buf = j % NSBUF, u = j / NSBUF;
+        TRACE(0, j);
         ok = mbar_wait(bar(kBarSEmpty + buf), (u & 1) ^ 1, spin, abort, p.st, kSiteMma);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_s = tmem + SOFF + buf * BN;
-        for (int c = 0; c < nkc && ok; ++c, ++it) {
-          const int st = it % p.nst;
-          ok = mbar_wait(bar(kBarFull + st), (it / p.nst) & 1, spin, abort, p.st, kSiteMma);
+        for (int c = 0; c < nkc; ++c, ++mit) {
+          TRACE(17, mit);
+          ok = mbar_wait(bar(kBarFull + st), ph, spin, abort, p.st, kSiteMma);
           if (!ok) break;
-          tc_fence_after();
-          const uint32_t sk = sRing + st * kStageBytes;
-          for (int kk = 0; kk < p.kd / 16; ++kk) {
-            const int dd = c * p.kd + kk * 16, kb = kk * 16;
-            const uint64_t ad = smem_desc_sw128(sQ + (dd >> 6) * 16384u + (dd & 63) * 2, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(sk + (kb >> 6) * (BN * 128u) + (kb & 63) * 2, 16, 1024);
-            mma_bf16_ss(d_s, ad, bd, idS, (c | kk) != 0);
+          TRACE(18, mit);
+          if (c == 0) TRACE(13, j);
+          const uint64_t aq = dQ + (uint64_t)(c * 2048);            // Q boxes 2c, 2c+1 (16 KB each)
+          const uint64_t bk = dK + (uint64_t)(st * (kStageBytes >> 4));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d_s, aq + 2 * kk, bk + 2 * kk, idS, (c | kk) != 0);
+          if (p.dqk - c * 128 > 64) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ss(d_s, aq + 1024 + 2 * kk, bk + (BN * 128 >> 4) + 2 * kk, idS, 1);
           }
           mma_commit(bar(kBarEmpty + st));
+          TRACE(19, mit);
+          if (++st == p.nst) { st = 0; ph ^= 1; }
         }
         if (!ok) break;
         mma_commit(bar(kBarSFull + buf));
+        TRACE(1, j);
       }
       if (j >= 1) {
         const int jj = j - 1;
         ok = mbar_wait(bar(kBarPFull), jj & 1, spin, abort, p.st, kSiteMma);
         if (!ok) break;
         tc_fence_after();
-        for (int e = 0; e < nvc && ok; ++e, ++it) {
-          const int st = it % p.nst;
-          ok = mbar_wait(bar(kBarFull + st), (it / p.nst) & 1, spin, abort, p.st, kSiteMma);
+        TRACE(2, jj);
+        for (int e = 0; e < nvc; ++e, ++mit) {
+          TRACE(17, mit);
+          ok = mbar_wait(bar(kBarFull + st), ph, spin, abort, p.st, kSiteMma);
           if (!ok) break;
-          tc_fence_after();
-          const uint32_t sv = sRing + st * kStageBytes;
-          for (int kk = 0; kk < p.vk / 16; ++kk) {
-            const int key = e * p.vk + kk * 16;
-            const uint64_t ad = smem_desc_sw128(sP + (key >> 6) * 16384u + (key & 63) * 2, 16, 1024);
-            int n_off = 0;
-            while (n_off < dv_cta) {
-              const int nw = min(256, dv_cta - n_off);
-              const uint64_t bd = smem_desc_sw128(sv + (n_off >> 6) * (p.vk * 128u) + kk * 2048u,
-                                                  p.vk * 128u, 1024);
-              mma_bf16_ss(tmem + n_off, ad, bd, idesc_bf16_f32(kBM, nw, 0, 1), (jj | e | kk) != 0);
-              n_off += nw;
-            }
+          TRACE(18, mit);
+          if (e == 0) TRACE(15, jj);
+          const uint64_t bv = dV + (uint64_t)(st * (kStageBytes >> 4));
+#pragma unroll
+          for (int kk = 0; kk < vsteps; ++kk) {
+            const int key = e * VK + kk * 16;
+            const uint64_t ap = dP + (uint64_t)((key >> 6) * 1024 + (key & 63) * 2 / 16);
+            const uint32_t acc = (jj | e | kk) != 0;
+            mma_bf16_ss(tmem, ap, bv + kk * 128, idO0, acc);
+            if (npieces > 1) mma_bf16_ss(tmem + nw0, ap, bv + kk * 128 + vpiece1, idO1, acc);
           }
           mma_commit(bar(kBarEmpty + st));
+          TRACE(19, mit);
+          if (++st == p.nst) { st = 0; ph ^= 1; }
         }
         if (!ok) break;
         mma_commit(bar(kBarPEmpty));
+        TRACE(3, jj);
       }
     }
     if (ok) mma_commit(bar(kBarOFull));
@@ -261,14 +313,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
     float bsum = 0.0f;
     bool ok = true;
+    // column terms of the next tile are loaded one tile ahead (latency hiding)
+    float av_next[HALF / 32];
+#pragma unroll
+    for (int t = 0; t < HALF / 32; ++t) {
+      const int col = half * HALF + lane + 32 * t;
+      av_next[t] = col < p.T ? p.a2[hbase + col] : -INFINITY;
+    }
     for (int j = 0; j < nkv && ok; ++j) {
       const int j0 = j * BN, cbase = j0 + half * HALF;
-      const int buf = j & 1, u = j >> 1;
+      const int buf = j % NSBUF, u = j / NSBUF;
       float av[HALF / 32];
 #pragma unroll
       for (int t = 0; t < HALF / 32; ++t) {
-        const int col = cbase + lane + 32 * t;
-        av[t] = col < p.T ? p.a2[hbase + col] : -INFINITY;
+        av[t] = av_next[t];
+        const int col = cbase + BN + lane + 32 * t;
+        av_next[t] = (j + 1 < nkv && col < p.T) ? p.a2[hbase + col] : -INFINITY;
       }
       const bool diag = j0 + BN - 1 > i0;
       float A = -INFINITY;
@@ -282,6 +342,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
       if (!ok) break;
       tc_fence_after();
+      if (gw == 0 && lane == 0) TRACE(6, j);
       uint32_t sv[HALF];
 #pragma unroll
       for (int t = 0; t < HALF / 32; ++t)
@@ -291,6 +352,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSEmpty + buf));
+      if (gw == 0 && lane == 0) TRACE(7, j);
 
       uint32_t pk[HALF / 2];
       if (!diag) {
@@ -319,8 +381,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         }
       }
       // the previous tile's O MMA must be done reading P before it is overwritten
+      if (gw == 0 && lane == 0) TRACE(8, j);
       ok = mbar_wait(bar(kBarPEmpty), (j & 1) ^ 1, spin, abort, p.st, kSiteGate);
       if (!ok) break;
+      if (gw == 0 && lane == 0) TRACE(9, j);
 #pragma unroll
       for (int g = 0; g < HALF / 8; ++g) {
         const int c = half * HALF + 8 * g;           // column within the tile
@@ -332,11 +396,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPFull));
+      if (gw == 0 && lane == 0) TRACE(10, j);
     }
 
     // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n
     if (ok) ok = mbar_wait(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
     tc_fence_after();
+    if (gw == 0 && lane == 0) TRACE(11, 0);
     // after the last O MMA the P tile is free: reuse it to combine the two half sums
     float* bpart = reinterpret_cast<float*>(dsmem + (sP - smem_u32(dsmem)));
     if (ok) bpart[half * kBM + rl] = bsum;
@@ -368,12 +434,25 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       }
     }
     tc_fence_before();
+    if (gw == 0 && lane == 0) TRACE(12, 0);
   }
 
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  // After an abort some loads may never have been consumed: wait (bounded)
+  // until none of them can still write this CTA's shared memory.
+  if (threadIdx.x == 0 && abort_flag) {
+    for (long long w = 0; w < kDrainSpin; ++w)
+      if (mbar_try_wait(bar(kBarQFull), 0)) break;
+    for (int s2 = 0; s2 < p.nst; ++s2)
+      if (last_it[s2] >= 0) {
+        const uint32_t par = (uint32_t)(last_it[s2] / p.nst) & 1u;
+        for (long long w = 0; w < kDrainSpin; ++w)
+          if (mbar_try_wait(bar(kBarFull + s2), par)) break;
+      }
   }
 }
 
@@ -411,49 +490,53 @@ bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows) 
 }
 
 struct Plan {
-  int bn, nsplit, dv_slice, kd, vk, nst;
+  int nsbuf, nsplit, dv_slice, vk, nst;
   size_t smem;
 };
 
+// Tiling: 128 query rows x 128 keys.  TMEM (512 columns) holds O (dv_slice
+// columns) and NSBUF S buffers of 128 columns: dv <= 256 double-buffers S;
+// dv <= 384 single-buffers it (the gating warps release S as soon as they have
+// read it); larger dv is split over two CTAs of 256 + the rest.
 Plan plan_for(int dqk, int dv) {
   Plan pl;
   if (dv <= 256) {
-    pl.bn = 128; pl.nsplit = 1; pl.dv_slice = dv;
+    pl.nsbuf = 2; pl.nsplit = 1; pl.dv_slice = dv;
   } else if (dv <= 384) {
-    pl.bn = 64; pl.nsplit = 1; pl.dv_slice = dv;
+    pl.nsbuf = 1; pl.nsplit = 1; pl.dv_slice = dv;
   } else {
-    pl.bn = 128; pl.nsplit = 2; pl.dv_slice = 256;
+    pl.nsbuf = 2; pl.nsplit = 2; pl.dv_slice = 256;
   }
-  pl.kd = (pl.bn == 64 && dqk % 128 == 0) ? 128 : 64;
-  const int widest = pl.dv_slice;   // the first slice is never narrower than the second
-  pl.vk = 16;
-  for (int v = 128; v >= 16; v >>= 1)
-    if (v <= pl.bn && v * widest * 2 <= kStageBytes) { pl.vk = v; break; }
-  const size_t fixed = 1024 + (size_t)dqk * kBM * 2 + (size_t)pl.bn * kBM * 2;
+  pl.vk = 32;
+  for (int v = 128; v >= 32; v >>= 1)
+    if (v * pl.dv_slice * 2 <= kStageBytes) { pl.vk = v; break; }
+  const size_t fixed = 1024 + (size_t)dqk * kBM * 2 + (size_t)kBN * kBM * 2;
   const size_t static_smem = 1024;  // barriers, TMEM address, abort flag (rounded up)
   long long room = (long long)kSmemLimit - (long long)static_smem - (long long)fixed;
   pl.nst = (int)std::min<long long>(kMaxStages, room / kStageBytes);
+  static const char* force_st = getenv("MLSTM_TC_STAGES");   // tuning: fewer ring stages
+  if (force_st && atoi(force_st) >= 2 && atoi(force_st) < pl.nst) pl.nst = atoi(force_st);
   pl.smem = fixed + (size_t)pl.nst * kStageBytes;
   return pl;
 }
 
-template <int BN>
-int launch_bn(const FwdArgs& a, const Plan& pl, const CUtensorMap& mq, const CUtensorMap& mk,
+template <int NSBUF, int VK>
+int launch_ns(const FwdArgs& a, const Plan& pl, const CUtensorMap& mq, const CUtensorMap& mk,
               const CUtensorMap& mv, cudaStream_t stream) {
-  if (cudaFuncSetAttribute(fwd_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(fwd_tc_kernel<kBN, NSBUF, VK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)pl.smem) != cudaSuccess)
     return kCuda;
   TcParams p;
   p.a2 = a.g.a2; p.p2 = a.g.p2; p.mrow = a.g.m;
   p.h = (__nv_bfloat16*)a.h; p.m_out = a.m_out; p.n_out = a.n_out;
   p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv;
-  p.nsplit = pl.nsplit; p.dv_slice = pl.dv_slice; p.nst = pl.nst; p.kd = pl.kd; p.vk = pl.vk;
+  p.nsplit = pl.nsplit; p.dv_slice = pl.dv_slice; p.nst = pl.nst; p.vk = pl.vk;
   p.nqt = (a.T + kBM - 1) / kBM;
   p.log2_scale = log2f(a.scale);
   p.st = a.st;
   const long long grid = (long long)p.nqt * a.BH * pl.nsplit;
   if (grid > 0x7fffffffLL) return kInval;
-  fwd_tc_kernel<BN><<<(unsigned)grid, kThreads, pl.smem, stream>>>(mq, mk, mv, p);
+  fwd_tc_kernel<kBN, NSBUF, VK><<<(unsigned)grid, kThreads, pl.smem, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }
 
@@ -465,6 +548,15 @@ int device_is_sm100_family() {
 }
 
 }  // namespace
+
+#ifdef MLSTM_TRACE
+extern "C" int mlstm_trace_set_block(int b) {
+  return cudaMemcpyToSymbol(g_trace_block, &b, sizeof(int)) == cudaSuccess ? 0 : -4;
+}
+extern "C" int mlstm_trace_read(long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -4;
+}
+#endif
 
 bool fwd_tc_supported(int dqk, int dv, int dtype) {
   return dtype == kBF16 && dqk % 64 == 0 && dv % 64 == 0 && dqk >= 64 && dv >= 64 && dqk <= 512 &&
@@ -478,10 +570,12 @@ int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
   const Plan pl = plan_for(a.dqk, a.dv);
   if (pl.nst < 2) return kUnsupported;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, pl.bn) ||
+  if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, kBN) ||
       !make_map(&mv, a.v, a.dv, a.T, a.BH, pl.vk))
     return kCuda;
-  return pl.bn == 64 ? launch_bn<64>(a, pl, mq, mk, mv, stream) : launch_bn<128>(a, pl, mq, mk, mv, stream);
+  if (pl.nsbuf == 1) return launch_ns<1, 32>(a, pl, mq, mk, mv, stream);      // 256 < dv slice <= 384
+  if (pl.vk == 64) return launch_ns<2, 64>(a, pl, mq, mk, mv, stream);        // 128 < dv slice <= 256
+  return launch_ns<2, 128>(a, pl, mq, mk, mv, stream);                        // dv slice <= 128
 }
 
 }  // namespace mlstm

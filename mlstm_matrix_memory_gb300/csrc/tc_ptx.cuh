@@ -41,11 +41,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Gives up
 // after `limit` polls or as soon as *abort is set by another role; on giving
 // up it records the site in the device status word and raises *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit,
                                           volatile int* abort, const DevStatus& st, int site) {
+  if (mbar_test_wait(bar, parity)) return true;      // fast path: already complete
   for (long long it = 0; it < limit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
@@ -67,6 +81,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* desc, uint
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
+}
+
+// Bring a tile into L2 ahead of its TMA load (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* desc, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(desc)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
