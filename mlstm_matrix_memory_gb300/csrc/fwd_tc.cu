@@ -40,7 +40,7 @@ using namespace tc;
 constexpr int kBM = 128;           // query rows per CTA (TMEM lanes)
 constexpr int kBN = 128;           // keys per tile
 constexpr int kThreads = 384;
-constexpr int kStageBytes = 32768;   // one ring slot: a 128x128 K chunk or a VKxdv V chunk
+constexpr int kStageBytes = 32768;   // one ring slot: a [128 keys x 128 columns] K or V chunk
 constexpr int kMaxStages = 8;
 constexpr int kProducers = 3;      // warps 0, 2, 3 issue the tensor loads
 constexpr uint32_t kTmemCols = 512;
@@ -97,10 +97,11 @@ struct TcParams {
   DevStatus st;
 };
 
-template <int BN, int NSBUF, int VK>
+template <int BN, int NSBUF>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-              const __grid_constant__ CUtensorMap tmap_v, const TcParams p) {
+              const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_h,
+              const TcParams p) {
   constexpr int HALF = BN / 2;           // columns of a tile owned by one gating warp
   constexpr uint32_t SOFF = kTmemCols - NSBUF * BN;   // TMEM column of S buffer 0
   extern __shared__ uint8_t dsmem[];
@@ -124,7 +125,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   const int i_last = min(p.T, i0 + kBM) - 1;
   const int nkv = i_last / BN + 1;
   const int nkc = (p.dqk + 127) / 128;   // K stages per key tile (128 d-columns each)
-  constexpr int nvc = BN / VK;           // V stages per key tile
+  const int nvc = (dv_cta + 127) / 128;  // V stages per key tile (128 d_v columns each)
   const size_t hbase = (size_t)bh * p.T;
 
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
@@ -180,7 +181,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     int st = 0, it = 0;
     uint32_t ph = 0;
     bool ok = true;
-    const uint32_t vbytes = (uint32_t)VK * dv_cta * 2;
     for (int j = 0; j <= nkv && ok; ++j) {
       if (j < nkv) {
         for (int c = 0; c < nkc; ++c, ++it) {
@@ -207,10 +207,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
             if (e == 0) TRACE(5, j - 1);
             TRACE(16, it);
             const uint32_t dst = sRing + st * kStageBytes;
-            mbar_arrive_expect_tx(bar(kBarFull + st), vbytes);
-            for (int s2 = 0; s2 < dv_cta / 64; ++s2)
-              tma_load_3d(dst + s2 * (VK * 128u), &tmap_v, bar(kBarFull + st), dv_off + s2 * 64,
-                          (j - 1) * BN + e * VK, bh);
+            const int vb = min(2, (dv_cta - e * 128) / 64);   // 64-column boxes in this chunk
+            mbar_arrive_expect_tx(bar(kBarFull + st), (uint32_t)vb * BN * 128);
+            for (int s2 = 0; s2 < vb; ++s2)
+              tma_load_3d(dst + s2 * (BN * 128u), &tmap_v, bar(kBarFull + st), dv_off + e * 128 + s2 * 64,
+                          (j - 1) * BN, bh);
             last_it[st] = it;
           }
           if (++st == p.nst) { st = 0; ph ^= 1; }
@@ -225,13 +226,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const uint64_t dQ = smem_desc_sw128(sQ, 16, 1024);
     const uint64_t dK = smem_desc_sw128(sRing, 16, 1024);
     const uint64_t dP = smem_desc_sw128(sP, 16, 1024);
-    const uint64_t dV = smem_desc_sw128(sRing, VK * 128u, 1024);
-    const int npieces = (dv_cta + 255) / 256;
-    const int nw0 = dv_cta > 256 ? 256 : dv_cta, nw1 = dv_cta - nw0;   // O columns per MMA
-    const uint32_t idO0 = idesc_bf16_f32(kBM, nw0, 0, 1);
-    const uint32_t idO1 = idesc_bf16_f32(kBM, nw1 > 0 ? nw1 : 16, 0, 1);
-    const uint32_t vpiece1 = (uint32_t)(nw0 >> 6) * (VK * 128u) >> 4;   // 2nd piece's B offset (16 B units)
-    constexpr int vsteps = VK / 16;
+    // V chunk: [128 keys x 128 d_v] as two 64-column boxes (MN-major atoms
+    // BN*128 bytes apart); O[:, chunk] += P V_chunk over 8 k-steps of 16 keys.
+    const uint64_t dV = smem_desc_sw128(sRing, BN * 128u, 1024);
+    const uint32_t idO128 = idesc_bf16_f32(kBM, 128, 0, 1), idO64 = idesc_bf16_f32(kBM, 64, 0, 1);
     bool ok = mbar_wait(bar(kBarQFull), 0, spin, abort, p.st, kSiteMma);
     tc_fence_after();
     int st = 0, mit = 0;
@@ -281,13 +279,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           TRACE(18, mit);
           if (e == 0) TRACE(15, jj);
           const uint64_t bv = dV + (uint64_t)(st * (kStageBytes >> 4));
+          const uint32_t d_o = tmem + e * 128;
+          const uint32_t acc0 = jj != 0;
+          // keys 16kk..16kk+15: P box kk/4 at +32 B per step; V rows at +2 KB per 16 keys
+          if (dv_cta - e * 128 >= 128) {
 #pragma unroll
-          for (int kk = 0; kk < vsteps; ++kk) {
-            const int key = e * VK + kk * 16;
-            const uint64_t ap = dP + (uint64_t)((key >> 6) * 1024 + (key & 63) * 2 / 16);
-            const uint32_t acc = (jj | e | kk) != 0;
-            mma_bf16_ss(tmem, ap, bv + kk * 128, idO0, acc);
-            if (npieces > 1) mma_bf16_ss(tmem + nw0, ap, bv + kk * 128 + vpiece1, idO1, acc);
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_bf16_ss(d_o, dP + (kk >> 2) * 1024 + (kk & 3) * 2, bv + kk * 128, idO128, acc0 | (kk != 0));
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_bf16_ss(d_o, dP + (kk >> 2) * 1024 + (kk & 3) * 2, bv + kk * 128, idO64, acc0 | (kk != 0));
           }
           mma_commit(bar(kBarEmpty + st));
           TRACE(19, mit);
@@ -403,35 +405,52 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     if (ok) ok = mbar_wait(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
     tc_fence_after();
     if (gw == 0 && lane == 0) TRACE(11, 0);
-    // after the last O MMA the P tile is free: reuse it to combine the two half sums
+    // After the last O MMA no operand is read any more: the P tile combines the
+    // two half row sums, and Q/P/ring space stages the bf16 output tile (128
+    // rows x dv_cta in 64-column boxes with the 128-byte swizzle) for TMA stores.
     float* bpart = reinterpret_cast<float*>(dsmem + (sP - smem_u32(dsmem)));
     if (ok) bpart[half * kBM + rl] = bsum;
     named_bar_sync(1, 256);
+    float nrm = 0.0f, m = 0.0f;
     if (ok) {
       const float b = bpart[rl] + bpart[kBM + rl];
-      const float m = row_ok ? p.mrow[hbase + i] : 0.0f;
-      const float nrm = fmaxf(fabsf(b), expf(-m));
+      m = row_ok ? p.mrow[hbase + i] : 0.0f;
+      nrm = fmaxf(fabsf(b), expf(-m));
+    }
+    named_bar_sync(1, 256);              // bpart reads done before the tile overwrites P
+    if (ok) {
       const float inv = nrm > 0.0f ? 1.0f / nrm : 0.0f;
       const int cols = dv_cta / 2, c0 = half * cols;
-      __nv_bfloat16* hrow = p.h + (hbase + (row_ok ? i : 0)) * p.dv + dv_off + c0;
       for (int ch = 0; ch < cols / 32; ++ch) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_addr + c0 + 32 * ch, o);
         tmem_wait_ld();
-        uint32_t w[16];
+        const int col = c0 + 32 * ch;                    // first of this thread's 32 columns
+        const uint32_t box = sQ + (uint32_t)(col >> 6) * 16384u + rl * 128u;
 #pragma unroll
-        for (int t = 0; t < 16; ++t)
-          w[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(hrow + 32 * ch);
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+          for (int t = 0; t < 4; ++t)
+            w[t] = pack_bf16x2(__uint_as_float(o[8 * g + 2 * t]) * inv, __uint_as_float(o[8 * g + 2 * t + 1]) * inv);
+          const int chunk = ((col & 63) >> 3) + g;     // 16-byte chunk within the 128-byte row
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + ((chunk ^ (rl & 7)) << 4)), "r"(w[0]),
+                       "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
         }
       }
       if (row_ok && split == 0 && half == 0) {
         if (p.m_out) p.m_out[hbase + i] = m;
         if (p.n_out) p.n_out[hbase + i] = nrm;
       }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, 256);
+    if (ok && gw == 0 && lane == 0) {
+      for (int b2 = 0; b2 < dv_cta / 64; ++b2)
+        tma_store_3d(&tmap_h, sQ + b2 * 16384u, dv_off + b2 * 64, i0, bh);
+      tma_store_commit();
+      tma_store_wait_all();
     }
     tc_fence_before();
     if (gw == 0 && lane == 0) TRACE(12, 0);
@@ -507,9 +526,7 @@ Plan plan_for(int dqk, int dv) {
   } else {
     pl.nsbuf = 2; pl.nsplit = 2; pl.dv_slice = 256;
   }
-  pl.vk = 32;
-  for (int v = 128; v >= 32; v >>= 1)
-    if (v * pl.dv_slice * 2 <= kStageBytes) { pl.vk = v; break; }
+  pl.vk = kBN;   // V boxes cover a whole key tile
   const size_t fixed = 1024 + (size_t)dqk * kBM * 2 + (size_t)kBN * kBM * 2;
   const size_t static_smem = 1024;  // barriers, TMEM address, abort flag (rounded up)
   long long room = (long long)kSmemLimit - (long long)static_smem - (long long)fixed;
@@ -520,10 +537,10 @@ Plan plan_for(int dqk, int dv) {
   return pl;
 }
 
-template <int NSBUF, int VK>
+template <int NSBUF>
 int launch_ns(const FwdArgs& a, const Plan& pl, const CUtensorMap& mq, const CUtensorMap& mk,
-              const CUtensorMap& mv, cudaStream_t stream) {
-  if (cudaFuncSetAttribute(fwd_tc_kernel<kBN, NSBUF, VK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+              const CUtensorMap& mv, const CUtensorMap& mh, cudaStream_t stream) {
+  if (cudaFuncSetAttribute(fwd_tc_kernel<kBN, NSBUF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)pl.smem) != cudaSuccess)
     return kCuda;
   TcParams p;
@@ -536,7 +553,7 @@ int launch_ns(const FwdArgs& a, const Plan& pl, const CUtensorMap& mq, const CUt
   p.st = a.st;
   const long long grid = (long long)p.nqt * a.BH * pl.nsplit;
   if (grid > 0x7fffffffLL) return kInval;
-  fwd_tc_kernel<kBN, NSBUF, VK><<<(unsigned)grid, kThreads, pl.smem, stream>>>(mq, mk, mv, p);
+  fwd_tc_kernel<kBN, NSBUF><<<(unsigned)grid, kThreads, pl.smem, stream>>>(mq, mk, mv, mh, p);
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }
 
@@ -569,13 +586,12 @@ int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
   if (!device_is_sm100_family()) return kUnsupported;
   const Plan pl = plan_for(a.dqk, a.dv);
   if (pl.nst < 2) return kUnsupported;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mh;
   if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, kBN) ||
-      !make_map(&mv, a.v, a.dv, a.T, a.BH, pl.vk))
+      !make_map(&mv, a.v, a.dv, a.T, a.BH, pl.vk) || !make_map(&mh, a.h, a.dv, a.T, a.BH, kBM))
     return kCuda;
-  if (pl.nsbuf == 1) return launch_ns<1, 32>(a, pl, mq, mk, mv, stream);      // 256 < dv slice <= 384
-  if (pl.vk == 64) return launch_ns<2, 64>(a, pl, mq, mk, mv, stream);        // 128 < dv slice <= 256
-  return launch_ns<2, 128>(a, pl, mq, mk, mv, stream);                        // dv slice <= 128
+  return pl.nsbuf == 1 ? launch_ns<1>(a, pl, mq, mk, mv, mh, stream)
+                       : launch_ns<2>(a, pl, mq, mk, mv, mh, stream);
 }
 
 }  // namespace mlstm
