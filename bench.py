@@ -212,31 +212,34 @@ def run_reference(args, ws, rank):
 
 
 def time_parallel(M, w, xd, algo, steps, warmup, flush):
-    """Per-step CUDA events on the launching stream; L2 flushed before each step."""
+    """The step (gate pass + fused kernel through the public call) timed with
+    CUDA events on the launching stream, L2 flushed before every step; then
+    the fused kernel alone (gate terms already in the workspace), same way,
+    for its roofline."""
     stream = torch.cuda.current_stream()
     B, H, T = w.B, w.H, w.T
     ws = torch.empty(M.parallel_fwd_workspace_bytes(B, H, T), dtype=torch.uint8, device="cuda")
     h = torch.empty((B, H, T, w.d_v), dtype=w.dtype, device="cuda")
 
-    def one():
-        M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
-        M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=algo)
+    def step():
+        M.parallel_fwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], h=h, workspace=ws, algo=algo)
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
 
     for _ in range(warmup):
-        one()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    torch.cuda.synchronize()
-    for i in range(steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
-        ev[i][1].record(stream)
-        M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=algo)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    fwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    gate_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        step()
+    step_ms = timed(step)
+    fwd_ms = timed(lambda: M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=algo))
+    gate_ms = timed(lambda: M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws))
     if M.last_device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
     return step_ms, fwd_ms, gate_ms
@@ -353,11 +356,13 @@ def main():
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_qk": w.d_qk, "d_v": w.d_v,
                    "kernel": algo, "l2": "flushed before every timed step (512 MB memset)",
                    "parallelism": f"{ws} independent replica(s), heads independent, no collective"},
-        "gate_prep_ms": statistics.mean(gate_ms),
+        "gate_prep_ms_alone": statistics.mean(gate_ms),
+        "fused_kernel_ms_alone": statistics.mean(fwd_ms),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
                      "traffic": traffic, "kernel": f"mlstm fwd_{algo}",
-                     "work": "causal flops T^2 (d_qk+d_v) per head per launch"},
+                     "work": "causal flops T^2 (d_qk+d_v) per head per launch",
+                     "timing": "fused kernel alone, CUDA events per launch, L2 flushed before each"},
         "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,

@@ -108,9 +108,11 @@ int mlstm_gate_prep(const float* igate_pre, const float* fgate_pre, int B, int H
                           static_cast<cudaStream_t>(stream)) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
 }
 
-int mlstm_parallel_fwd_gated(const void* q, const void* k, const void* v, void* h, float* m_out, float* n_out,
-                             int B, int H, int T, int d_qk, int d_v, int dtype, const void* workspace,
-                             size_t workspace_bytes, int algo, void* stream) {
+namespace {
+
+int fwd_gated(const void* q, const void* k, const void* v, void* h, float* m_out, float* n_out, int B, int H,
+              int T, int d_qk, int d_v, int dtype, const void* workspace, size_t workspace_bytes, int algo,
+              bool after_gate_prep, void* stream) {
   int rc = check_sizes(B, H, T);
   if (rc != MLSTM_OK) return rc;
   if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
@@ -141,9 +143,19 @@ int mlstm_parallel_fwd_gated(const void* q, const void* k, const void* v, void* 
   a.scale = (float)(1.0 / sqrt((double)d_qk));
   a.st.word = status;
   a.st.spin_limit = g_spin_limit.load();
+  a.after_gate_prep = after_gate_prep;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (use_tc) return launch_fwd_tc(a, s);
   return launch_fwd_simt(a, s) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
+}
+
+}  // namespace
+
+int mlstm_parallel_fwd_gated(const void* q, const void* k, const void* v, void* h, float* m_out, float* n_out,
+                             int B, int H, int T, int d_qk, int d_v, int dtype, const void* workspace,
+                             size_t workspace_bytes, int algo, void* stream) {
+  return fwd_gated(q, k, v, h, m_out, n_out, B, H, T, d_qk, d_v, dtype, workspace, workspace_bytes, algo, false,
+                   stream);
 }
 
 int mlstm_parallel_fwd_ex(const void* q, const void* k, const void* v, const float* igate_pre,
@@ -165,8 +177,8 @@ int mlstm_parallel_fwd_ex(const void* q, const void* k, const void* v, const flo
   if (algo == MLSTM_ALGO_TC && !fwd_tc_supported(d_qk, d_v, dtype)) return MLSTM_EUNSUPPORTED;
   rc = mlstm_gate_prep(igate_pre, fgate_pre, B, H, T, workspace, workspace_bytes, stream);
   if (rc != MLSTM_OK) return rc;
-  return mlstm_parallel_fwd_gated(q, k, v, h, m_out, n_out, B, H, T, d_qk, d_v, dtype, workspace,
-                                  workspace_bytes, algo, stream);
+  return fwd_gated(q, k, v, h, m_out, n_out, B, H, T, d_qk, d_v, dtype, workspace, workspace_bytes, algo, true,
+                   stream);
 }
 
 int mlstm_parallel_fwd(const void* q, const void* k, const void* v, const float* igate_pre,

@@ -308,6 +308,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   } else if (warp >= 4) {
     // ------------------------------------------------------------ gating + epilogue
     const int gw = warp - 4, qd = gw & 3, half = gw >> 2;
+    // gate terms come from the preceding gate pass: wait for that grid (a no-op
+    // unless this kernel was launched as its programmatic dependent)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int rl = 32 * qd + lane;                  // row within the tile = TMEM lane
     const int i = i0 + rl;
     const bool row_ok = i < p.T;
@@ -553,7 +556,17 @@ int launch_ns(const FwdArgs& a, const Plan& pl, const CUtensorMap& mq, const CUt
   p.st = a.st;
   const long long grid = (long long)p.nqt * a.BH * pl.nsplit;
   if (grid > 0x7fffffffLL) return kInval;
-  fwd_tc_kernel<kBN, NSBUF><<<(unsigned)grid, kThreads, pl.smem, stream>>>(mq, mk, mv, mh, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.after_gate_prep ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, fwd_tc_kernel<kBN, NSBUF>, mq, mk, mv, mh, p) != cudaSuccess) return kCuda;
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }
 

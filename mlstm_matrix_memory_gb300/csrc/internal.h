@@ -33,6 +33,9 @@ struct FwdArgs {
   int dtype;      // kF32 / kBF16
   float scale;    // 1/sqrt(dqk)
   DevStatus st;
+  bool after_gate_prep = false;   // launched right after gate_prep on the same stream:
+                                  // may overlap its prologue with it (programmatic
+                                  // dependent launch; gate terms are read after the wait)
 };
 
 struct StepArgs {
