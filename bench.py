@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-step", action="store_true", help="skip the recurrent-step measurement")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--profile-kernel", choices=("fwd", "step"), default=None,
+                   help="no timing: one warm-up and one launch of the fused forward kernel (on --workload) "
+                        "or of the recurrent step (B=64, H=4, d=512: 256 MB of state), for ncu captures")
     return p.parse_args()
 
 
@@ -303,9 +306,33 @@ def time_step(M, steps, warmup):
     return ms, nbytes, w
 
 
+def profile_once(args):
+    """One warm-up and one profiled launch of a single kernel (small, L2-exceeding case)."""
+    import mlstm_matrix_memory_gb300 as M
+    if args.profile_kernel == "fwd":
+        w = W.PARALLEL_WORKLOADS[args.workload]
+        xd = {k: v.cuda() for k, v in W.parallel_inputs(w, 0).items()}
+        ws = torch.empty(M.parallel_fwd_workspace_bytes(w.B, w.H, w.T), dtype=torch.uint8, device="cuda")
+        h = torch.empty((w.B, w.H, w.T, w.d_v), dtype=w.dtype, device="cuda")
+        M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
+        for _ in range(2):
+            M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=args.algo)
+    else:
+        xd = {k: v.cuda() for k, v in W.step_inputs(W.STEP, 0, B=64).items()}
+        for _ in range(2):
+            M.step(xd["C"], xd["n"], xd["m"], xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], xd["o"])
+    torch.cuda.synchronize()
+    if M.last_device_status() != 0:
+        raise RuntimeError("device status word set")
+    print("profile run done")
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup(args.gpus)
+    if args.profile_kernel:
+        profile_once(args)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank)
         return
