@@ -479,38 +479,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-  static std::once_flag once;
-  static EncodeTiled fn = nullptr;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(ptr);
-  });
-  return fn;
-}
-
-// [BH, T, d] bf16 viewed as a 3-D tensor (d fastest); box = 64 x rows x 1 with
-// 128-byte swizzle.  Rows past T read as zeros.
-bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows) {
-  EncodeTiled enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * T};
-  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct Plan {
   int nsbuf, nsplit, dv_slice, vk, nst;
   size_t smem;
@@ -579,6 +547,38 @@ int device_is_sm100_family() {
 
 }  // namespace
 
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static std::once_flag once;
+  static EncodeTiled fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  });
+  return fn;
+}
+
+// [BH, T, d] bf16 viewed as a 3-D tensor (d fastest); box = 64 x rows x 1 with
+// 128-byte swizzle.  Rows past T read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * T};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 #ifdef MLSTM_TRACE
 extern "C" int mlstm_trace_set_block(int b) {
   return cudaMemcpyToSymbol(g_trace_block, &b, sizeof(int)) == cudaSuccess ? 0 : -4;
@@ -597,6 +597,17 @@ int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
   if (a.BH <= 0 || a.T <= 0) return kOk;
   if (!fwd_tc_supported(a.dqk, a.dv, a.dtype)) return kUnsupported;
   if (!device_is_sm100_family()) return kUnsupported;
+  // CTA-pair kernel when the shape allows it; MLSTM_TC_VARIANT=single or
+  // =pair in the environment forces one variant (tuning and tests).
+  const char* var = getenv("MLSTM_TC_VARIANT");
+  const bool force_single = var && var[0] == 's', force_pair = var && var[0] == 'p';
+  // The pair halves each SM's K/V traffic, which pays off once query tiles see
+  // many key tiles (long sequences) or when d_v is split over two CTAs anyway;
+  // at T <= 2048 with d_v <= 384 the single-CTA kernel is faster (measured).
+  const bool pair_pays = a.T > 2048 || a.dv > 384;
+  if (!force_single && fwd_tc2_supported(a.dqk, a.dv) && (pair_pays || force_pair))
+    return launch_fwd_tc2(a, stream);
+  if (force_pair) return kUnsupported;
   const Plan pl = plan_for(a.dqk, a.dv);
   if (pl.nst < 2) return kUnsupported;
   CUtensorMap mq, mk, mv, mh;

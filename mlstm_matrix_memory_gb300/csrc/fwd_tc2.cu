@@ -1,0 +1,535 @@
+// Fused causal mLSTM forward on a pair of SMs (tcgen05 cta_group::2).
+//
+// "xLSTM: Extended Long Short-Term Memory", part 28/30, stabilized parallel
+// forward, eqs (79)-(86); same arithmetic as fwd_tc.cu (see there), different
+// decomposition.  A cluster of two CTAs owns 256 consecutive query rows of one
+// head (CTA rank r: rows 128r..128r+127 of the pair) and a slice of d_v.  The
+// leader (rank 0) issues M=256 MMAs: each CTA holds its own 128 rows of Q, P,
+// S and O, and one half of every K and V tile (K: 64 of the 128 keys; V: 64 of
+// each 128 d_v columns).  Each SM therefore loads half of the K/V bytes a
+// single-CTA tile needs, and a ring slot covers twice the MMA work.
+//
+// Synchronisation: every tensor load of both CTAs completes on the leader's
+// `full` barrier; the leader's MMA commits are multicast to both CTAs'
+// `empty`, `s_full`, `p_empty` and `o_full` barriers; the gating warps of
+// both CTAs arrive on the leader's `s_empty` and `p_full`.  Waits are bounded
+// as in fwd_tc.cu.
+#include <algorithm>
+#include <cstdlib>
+#include <mutex>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace mlstm {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;                 // query rows per CTA (256 per pair)
+constexpr int kBN = 128;                 // keys per tile
+constexpr int kThreads = 384;
+constexpr int kSlotBytes = 32768;        // ring slot per CTA: 4 K boxes [64 keys x 64 d] or 2 V boxes [128 keys x 64 d_v]
+constexpr int kMaxSlots = 8;
+constexpr int kProducers = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemLimit = 232448;
+constexpr long long kDrainSpin = 1LL << 22;
+
+enum : int {
+  kBarQFull = 0,
+  kBarSFull = 1,
+  kBarSEmpty = 3,
+  kBarPFull = 5,
+  kBarPEmpty = 6,
+  kBarOFull = 7,
+  kBarDrain = 8,
+  kBarFull = 9,
+  kBarEmpty = 9 + kMaxSlots,
+  kNumBars = 9 + 2 * kMaxSlots,
+};
+enum : int { kSiteProducer = 11, kSiteMma = 12, kSiteGate = 13, kSiteEpilogue = 14 };
+
+#ifdef MLSTM_TRACE
+// clock64 stamps of both CTAs of one cluster (trace builds only): [cta][event][tile]
+__device__ long long g_trace2[2 * 16 * 64];
+__device__ int g_trace2_cluster;
+#define TRACE2(ev, j)                                                                             \
+  do {                                                                                            \
+    if ((int)(blockIdx.x >> 1) == g_trace2_cluster && (j) < 64)                                   \
+      g_trace2[((int)cluster_ctarank() * 16 + (ev)) * 64 + (j)] = clock64();                      \
+  } while (0)
+#else
+#define TRACE2(ev, j) \
+  do {                \
+  } while (0)
+#endif
+
+struct Tc2Params {
+  const float* a2;
+  const float* p2;
+  const float* mrow;
+  float* m_out;
+  float* n_out;
+  int T, BH, dqk, dv;
+  int nsplit, dv_slice, nst, npairs;
+  float log2_scale;
+  DevStatus st;
+};
+
+// MMA bursts with compile-time trip counts: every descriptor is the slot base
+// plus a constant, so the issuing thread sends the MMAs back to back.
+// S += Q K^T over KB boxes of 64 d-columns (4 k-steps each).
+template <int KB>
+__device__ __forceinline__ void issue_s(uint32_t d_s, uint64_t aq, uint64_t bk, uint32_t idS, bool first) {
+#pragma unroll
+  for (int b2 = 0; b2 < KB; ++b2)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16_ss_pair(d_s, aq + b2 * 1024 + 2 * kk, bk + b2 * 512 + 2 * kk, idS, first ? ((b2 | kk) != 0) : 1u);
+}
+// O[:, chunk] += P V_chunk for VB chunks of 128 d_v columns (8 k-steps of 16 keys each).
+template <int VB>
+__device__ __forceinline__ void issue_o(uint32_t d_o, uint64_t dP, uint64_t bv, uint32_t idO, bool first) {
+#pragma unroll
+  for (int b2 = 0; b2 < VB; ++b2)
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk)
+      mma_bf16_ss_pair(d_o + b2 * 128, dP + (kk >> 2) * 1024 + (kk & 3) * 2, bv + b2 * 1024 + kk * 128, idO,
+                       first ? (kk != 0) : 1u);
+}
+
+template <int NSBUF>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+               const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_h,
+               const Tc2Params p) {
+  constexpr int HALF = kBN / 2;
+  constexpr uint32_t SOFF = kTmemCols - NSBUF * kBN;
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ uint32_t tmem_holder;
+  __shared__ int abort_flag;
+  __shared__ int last_it_s[kMaxSlots];
+  volatile int* abort = &abort_flag;
+  volatile int* last_it = last_it_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  // ---- work item: longest query-row pairs of all heads first
+  const int cid = (int)(blockIdx.x >> 1);
+  const int per_rank = p.BH * p.nsplit;
+  const int pair = p.npairs - 1 - cid / per_rank;
+  const int rem = cid % per_rank;
+  const int bh = rem / p.nsplit, split = rem % p.nsplit;
+  const int i0 = (2 * pair + (int)rank) * kBM;               // this CTA's first query row
+  const int dv_off = split * p.dv_slice;
+  const int dv_cta = split == 0 ? p.dv_slice : p.dv - p.dv_slice;
+  const int pair_last = min(p.T, (2 * pair + 2) * kBM) - 1;
+  const int nkv = pair_last / kBN + 1;                       // key tiles, same in both CTAs
+  const int nkc = (p.dqk + 255) / 256;                       // K slots per key tile
+  const int nch = dv_cta / 128;                              // 128-column O chunks
+  const int nvc = (nch + 1) / 2;                             // V slots per key tile
+  const size_t hbase = (size_t)bh * p.T;
+
+  const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint32_t sQ = base;
+  const uint32_t sP = sQ + (uint32_t)p.dqk * kBM * 2;
+  const uint32_t sRing = sP + (uint32_t)kBN * kBM * 2;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto lbar = [&](int i) { return mapa_shared(smem_u32(&bars[i]), 0); };   // leader's barrier
+
+  if (threadIdx.x < kMaxSlots) last_it_s[threadIdx.x] = -1;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(bar(kBarQFull), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kBarSFull + b), 1);
+      mbar_init(bar(kBarSEmpty + b), 16);    // gating warps of both CTAs
+    }
+    mbar_init(bar(kBarPFull), 16);
+    mbar_init(bar(kBarPEmpty), 1);
+    mbar_init(bar(kBarOFull), 1);
+    mbar_init(bar(kBarDrain), 1);
+    for (int s = 0; s < kMaxSlots; ++s) {
+      mbar_init(bar(kBarFull + s), 1);
+      mbar_init(bar(kBarEmpty + s), 1);
+    }
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(smem_u32(&tmem_holder), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();                       // peer barriers initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  const long long spin = p.st.spin_limit;
+  if (threadIdx.x == 0) TRACE2(0, 0);
+
+  if ((warp == 0 || warp == 2 || warp == 3) && lane == 0) {
+    // ------------------------------------------------------------ TMA producers (both CTAs)
+    // Slot st is owned by producer st % kProducers in every round.  Each CTA
+    // loads its own halves into its own slots; completion is counted on the
+    // leader's full barrier, whose expected byte count (both halves) only the
+    // leader's producer posts.
+    const int pi = warp == 0 ? 0 : warp - 1;
+    if (leader && pi == 0) mbar_arrive_expect_tx(bar(kBarQFull), 2u * (uint32_t)p.dqk * kBM * 2);
+    for (int b2 = pi; b2 < p.dqk / 64; b2 += kProducers)
+      tma_load_3d_pair(sQ + b2 * 16384u, &tmap_q, lbar(kBarQFull), b2 * 64, i0, bh);
+    int st = 0, it = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int j = 0; j <= nkv && ok; ++j) {
+      if (j < nkv) {
+        for (int c = 0; c < nkc; ++c, ++it) {
+          if (st % kProducers == pi) {
+            ok = mbar_wait(bar(kBarEmpty + st), ph ^ 1, spin, abort, p.st, kSiteProducer);
+            if (!ok) break;
+            const int kb = min(4, (p.dqk - c * 256) / 64);   // [64 keys x 64 d] boxes in this slot
+            TRACE2(12, it);
+            if (leader) mbar_arrive_expect_tx(bar(kBarFull + st), 2u * (uint32_t)kb * 8192u);
+            for (int b2 = 0; b2 < kb; ++b2)
+              tma_load_3d_pair(sRing + st * kSlotBytes + b2 * 8192u, &tmap_k, lbar(kBarFull + st),
+                               c * 256 + b2 * 64, j * kBN + (int)rank * 64, bh);
+            last_it[st] = it;
+          }
+          if (++st == p.nst) { st = 0; ph ^= 1; }
+        }
+      }
+      if (j >= 1 && ok) {
+        for (int e = 0; e < nvc; ++e, ++it) {
+          if (st % kProducers == pi) {
+            ok = mbar_wait(bar(kBarEmpty + st), ph ^ 1, spin, abort, p.st, kSiteProducer);
+            if (!ok) break;
+            const int vb = min(2, nch - 2 * e);                // 128-column chunks in this slot
+            TRACE2(12, it);
+            if (leader) mbar_arrive_expect_tx(bar(kBarFull + st), 2u * (uint32_t)vb * 16384u);
+            for (int b2 = 0; b2 < vb; ++b2)
+              tma_load_3d_pair(sRing + st * kSlotBytes + b2 * 16384u, &tmap_v, lbar(kBarFull + st),
+                               dv_off + (2 * e + b2) * 128 + (int)rank * 64, (j - 1) * kBN, bh);
+            last_it[st] = it;
+          }
+          if (++st == p.nst) { st = 0; ph ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    const uint32_t idS = idesc_bf16_f32(2 * kBM, kBN, 0, 0);       // M=256 rows over the pair, N=128 keys
+    const uint32_t idO = idesc_bf16_f32(2 * kBM, 128, 0, 1);       // N=128 d_v columns, V MN-major
+    const uint64_t dQ = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dK = smem_desc_sw128(sRing, 16, 1024);
+    const uint64_t dP = smem_desc_sw128(sP, 16, 1024);
+    const uint64_t dV = smem_desc_sw128(sRing, 16384, 1024);
+    bool ok = mbar_wait(bar(kBarQFull), 0, spin, abort, p.st, kSiteMma);
+    tc_fence_after();
+    int st = 0, mit = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j <= nkv && ok; ++j) {
+      if (j < nkv) {
+        const int buf = j % NSBUF, u = j / NSBUF;
+        TRACE2(1, j);
+        ok = mbar_wait(bar(kBarSEmpty + buf), (u & 1) ^ 1, spin, abort, p.st, kSiteMma);
+        if (!ok) break;
+        tc_fence_after();
+        TRACE2(2, j);
+        const uint32_t d_s = tmem + SOFF + buf * kBN;
+        for (int c = 0; c < nkc; ++c, ++mit) {
+          TRACE2(14, mit);
+          ok = mbar_wait(bar(kBarFull + st), ph, spin, abort, p.st, kSiteMma);
+          if (!ok) break;
+          TRACE2(15, mit);
+          const int kb = min(4, (p.dqk - c * 256) / 64);
+          const uint64_t bk = dK + (uint64_t)(st * (kSlotBytes >> 4));
+          const uint64_t aq = dQ + (uint64_t)(4 * c * 1024);           // Q boxes 4c.. (16 KB each)
+          if (kb == 4) issue_s<4>(d_s, aq, bk, idS, c == 0);
+          else issue_s<2>(d_s, aq, bk, idS, c == 0);                   // d_qk is a multiple of 128
+          mma_commit_pair_mc(bar(kBarEmpty + st), 0x3);
+          if (++st == p.nst) { st = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(bar(kBarSFull + buf), 0x3);
+        TRACE2(3, j);
+      }
+      if (j >= 1) {
+        const int jj = j - 1;
+        ok = mbar_wait(bar(kBarPFull), jj & 1, spin, abort, p.st, kSiteMma);
+        if (!ok) break;
+        tc_fence_after();
+        TRACE2(4, jj);
+        for (int e = 0; e < nvc; ++e, ++mit) {
+          TRACE2(14, mit);
+          ok = mbar_wait(bar(kBarFull + st), ph, spin, abort, p.st, kSiteMma);
+          if (!ok) break;
+          TRACE2(15, mit);
+          const int vb = min(2, nch - 2 * e);
+          const uint64_t bv = dV + (uint64_t)(st * (kSlotBytes >> 4));
+          if (vb == 2) issue_o<2>(tmem + 2 * e * 128, dP, bv, idO, jj == 0);
+          else issue_o<1>(tmem + 2 * e * 128, dP, bv, idO, jj == 0);
+          mma_commit_pair_mc(bar(kBarEmpty + st), 0x3);
+          if (++st == p.nst) { st = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(bar(kBarPEmpty), 0x3);
+        TRACE2(5, jj);
+      }
+    }
+    if (ok) mma_commit_pair_mc(bar(kBarOFull), 0x3);
+    mma_commit_pair(bar(kBarDrain));
+    for (long long w = 0; w < kDrainSpin; ++w)
+      if (mbar_try_wait(bar(kBarDrain), 0)) break;
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ gating + epilogue (both CTAs)
+    const int gw = warp - 4, qd = gw & 3, half = gw >> 2;
+    asm volatile("griddepcontrol.wait;" ::: "memory");        // gate terms from the preceding gate pass
+    const int rl = 32 * qd + lane;
+    const int i = i0 + rl;
+    const bool row_ok = i < p.T;
+    const float rr = row_ok ? p.p2[hbase + i] - p.log2_scale : 0.0f;
+    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    const uint32_t l_sempty0 = lbar(kBarSEmpty), l_sempty1 = lbar(kBarSEmpty + 1), l_pfull = lbar(kBarPFull);
+    float bsum = 0.0f;
+    bool ok = true;
+    float av_next[HALF / 32];
+#pragma unroll
+    for (int t = 0; t < HALF / 32; ++t) {
+      const int col = half * HALF + lane + 32 * t;
+      av_next[t] = col < p.T ? p.a2[hbase + col] : -INFINITY;
+    }
+    for (int j = 0; j < nkv && ok; ++j) {
+      const int j0 = j * kBN, cbase = j0 + half * HALF;
+      const int buf = j % NSBUF, u = j / NSBUF;
+      float av[HALF / 32];
+#pragma unroll
+      for (int t = 0; t < HALF / 32; ++t) {
+        av[t] = av_next[t];
+        const int col = cbase + kBN + lane + 32 * t;
+        av_next[t] = (j + 1 < nkv && col < p.T) ? p.a2[hbase + col] : -INFINITY;
+      }
+      const bool diag = j0 + kBN - 1 > i0;                    // some column of the tile lies above a row
+      float A = -INFINITY;
+      if (!diag) {
+#pragma unroll
+        for (int t = 0; t < HALF / 32; ++t) A = fmaxf(A, av[t]);
+        A = warp_max(A);
+#pragma unroll
+        for (int t = 0; t < HALF / 32; ++t) av[t] = A == -INFINITY ? 0.0f : exp2f(av[t] - A);
+      }
+      ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
+      if (!ok) break;
+      tc_fence_after();
+      if (gw == 0 && lane == 0) TRACE2(6, j);
+      uint32_t sv[HALF];
+#pragma unroll
+      for (int t = 0; t < HALF / 32; ++t)
+        tmem_ld32(tmem + lane_addr + SOFF + buf * kBN + half * HALF + 32 * t,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * t]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf == 0 ? l_sempty0 : l_sempty1);
+
+      uint32_t pk[HALF / 2];
+      if (!diag) {
+        const float r = (A == -INFINITY || !row_ok) ? 0.0f : exp2f(A - rr);
+#pragma unroll
+        for (int c = 0; c < HALF; c += 2) {
+          const float c0 = __shfl_sync(0xffffffffu, av[c / 32], c & 31);
+          const float c1 = __shfl_sync(0xffffffffu, av[(c + 1) / 32], (c + 1) & 31);
+          const float x0 = __uint_as_float(sv[c]) * c0 * r;
+          const float x1 = __uint_as_float(sv[c + 1]) * c1 * r;
+          bsum += x0 + x1;
+          pk[c / 2] = pack_bf16x2(x0, x1);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < HALF; c += 2) {
+          const float a0 = __shfl_sync(0xffffffffu, av[c / 32], c & 31);
+          const float a1 = __shfl_sync(0xffffffffu, av[(c + 1) / 32], (c + 1) & 31);
+          const int col = cbase + c;
+          const float e0 = (row_ok && col <= i) ? exp2f(a0 - rr) : 0.0f;
+          const float e1 = (row_ok && col + 1 <= i) ? exp2f(a1 - rr) : 0.0f;
+          const float x0 = __uint_as_float(sv[c]) * e0;
+          const float x1 = __uint_as_float(sv[c + 1]) * e1;
+          bsum += x0 + x1;
+          pk[c / 2] = pack_bf16x2(x0, x1);
+        }
+      }
+      if (gw == 0 && lane == 0) TRACE2(7, j);
+      ok = mbar_wait(bar(kBarPEmpty), (j & 1) ^ 1, spin, abort, p.st, kSiteGate);
+      if (!ok) break;
+      if (gw == 0 && lane == 0) TRACE2(8, j);
+#pragma unroll
+      for (int g = 0; g < HALF / 8; ++g) {
+        const int c = half * HALF + 8 * g;
+        const uint32_t addr = sP + (c >> 6) * 16384u + rl * 128u + ((((c & 63) >> 3) ^ (rl & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * g]),
+                     "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(l_pfull);
+      if (gw == 0 && lane == 0) TRACE2(9, j);
+    }
+
+    // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n, staged for TMA stores
+    if (ok) ok = mbar_wait(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
+    tc_fence_after();
+    if (gw == 0 && lane == 0) TRACE2(10, 0);
+    float* bpart = reinterpret_cast<float*>(dsmem + (sP - smem_u32(dsmem)));
+    if (ok) bpart[half * kBM + rl] = bsum;
+    named_bar_sync(1, 256);
+    float nrm = 0.0f, m = 0.0f;
+    if (ok) {
+      const float b = bpart[rl] + bpart[kBM + rl];
+      m = row_ok ? p.mrow[hbase + i] : 0.0f;
+      nrm = fmaxf(fabsf(b), expf(-m));
+    }
+    named_bar_sync(1, 256);
+    if (ok) {
+      const float inv = nrm > 0.0f ? 1.0f / nrm : 0.0f;
+      const int cols = dv_cta / 2, c0 = half * cols;
+      for (int ch = 0; ch < cols / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_addr + c0 + 32 * ch, o);
+        tmem_wait_ld();
+        const int col = c0 + 32 * ch;
+        const uint32_t box = sQ + (uint32_t)(col >> 6) * 16384u + rl * 128u;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            w[t] = pack_bf16x2(__uint_as_float(o[8 * g + 2 * t]) * inv, __uint_as_float(o[8 * g + 2 * t + 1]) * inv);
+          const int chunk = ((col & 63) >> 3) + g;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + ((chunk ^ (rl & 7)) << 4)), "r"(w[0]),
+                       "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
+        }
+      }
+      if (row_ok && split == 0 && half == 0) {
+        if (p.m_out) p.m_out[hbase + i] = m;
+        if (p.n_out) p.n_out[hbase + i] = nrm;
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, 256);
+    if (ok && gw == 0 && lane == 0 && i0 < p.T) {
+      for (int b2 = 0; b2 < dv_cta / 64; ++b2)
+        tma_store_3d(&tmap_h, sQ + b2 * 16384u, dv_off + b2 * 64, i0, bh);
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+    if (gw == 0 && lane == 0) TRACE2(11, 0);
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    // after an abort, loads of this pair may never have been consumed: the
+    // leader waits (bounded) for the last phase of every slot it loaded
+    if (lane == 0 && leader && abort_flag) {
+      for (long long w = 0; w < kDrainSpin; ++w)
+        if (mbar_try_wait(bar(kBarQFull), 0)) break;
+      for (int s2 = 0; s2 < p.nst; ++s2)
+        if (last_it[s2] >= 0) {
+          const uint32_t par = (uint32_t)(last_it[s2] / p.nst) & 1u;
+          for (long long w = 0; w < kDrainSpin; ++w)
+            if (mbar_try_wait(bar(kBarFull + s2), par)) break;
+        }
+    }
+    __syncwarp();
+  }
+  // both CTAs are done with TMEM and with each other's shared memory
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0) TRACE2(13, 0);
+}
+
+#ifdef MLSTM_TRACE
+}  // namespace
+extern "C" int mlstm_trace2_set_cluster(int c) {
+  return cudaMemcpyToSymbol(g_trace2_cluster, &c, sizeof(int)) == cudaSuccess ? 0 : -4;
+}
+extern "C" int mlstm_trace2_read(long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace2, sizeof(g_trace2)) == cudaSuccess ? 0 : -4;
+}
+namespace {
+#endif
+
+template <int NSBUF>
+int launch_pair(const FwdArgs& a, const Tc2Params& p, size_t smem, const CUtensorMap& mq, const CUtensorMap& mk,
+                const CUtensorMap& mv, const CUtensorMap& mh, cudaStream_t stream) {
+  if (cudaFuncSetAttribute(fwd_tc2_kernel<NSBUF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return kCuda;
+  const long long grid = 2LL * p.npairs * a.BH * p.nsplit;
+  if (grid > 0x7fffffffLL) return kInval;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.after_gate_prep ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, fwd_tc2_kernel<NSBUF>, mq, mk, mv, mh, p) != cudaSuccess) return kCuda;
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
+}  // namespace
+
+// The pair splits each 128-column V chunk and each 128-key K tile in halves
+// of 64 (one swizzle atom), so d_qk and every d_v slice are multiples of 128.
+bool fwd_tc2_supported(int dqk, int dv) {
+  if (dqk % 128 != 0 || dqk > 512) return false;
+  if (dv <= 384) return dv % 128 == 0;
+  return dv == 512;
+}
+
+int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
+  Tc2Params p;
+  p.a2 = a.g.a2; p.p2 = a.g.p2; p.mrow = a.g.m;
+  p.m_out = a.m_out; p.n_out = a.n_out;
+  p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv;
+  int nsbuf;
+  if (a.dv <= 256) { nsbuf = 2; p.nsplit = 1; p.dv_slice = a.dv; }
+  else if (a.dv <= 384) { nsbuf = 1; p.nsplit = 1; p.dv_slice = a.dv; }
+  else { nsbuf = 2; p.nsplit = 2; p.dv_slice = 256; }
+  const int nqt = (a.T + kBM - 1) / kBM;
+  p.npairs = (nqt + 1) / 2;
+  p.log2_scale = log2f(a.scale);
+  p.st = a.st;
+  const size_t fixed = 1024 + (size_t)a.dqk * kBM * 2 + (size_t)kBN * kBM * 2;
+  const long long room = (long long)kSmemLimit - 1024 - (long long)fixed;
+  p.nst = (int)std::min<long long>(kMaxSlots, room / kSlotBytes);
+  if (p.nst < 2) return kUnsupported;
+  const size_t smem = fixed + (size_t)p.nst * kSlotBytes;
+  CUtensorMap mq, mk, mv, mh;
+  if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, 64) ||
+      !make_map(&mv, a.v, a.dv, a.T, a.BH, kBN) || !make_map(&mh, a.h, a.dv, a.T, a.BH, kBM))
+    return kCuda;
+  return nsbuf == 1 ? launch_pair<1>(a, p, smem, mq, mk, mv, mh, stream)
+                    : launch_pair<2>(a, p, smem, mq, mk, mv, mh, stream);
+}
+
+}  // namespace mlstm

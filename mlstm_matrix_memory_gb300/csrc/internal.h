@@ -2,6 +2,7 @@
 // kernels.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -60,5 +61,13 @@ cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream);
 bool fwd_tc_supported(int dqk, int dv, int dtype);
 int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);   // returns a Status
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
+
+// CTA-pair (cta_group::2) variant of the tensor-core forward (fwd_tc2.cu).
+bool fwd_tc2_supported(int dqk, int dv);
+int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream);
+
+// 3-D TMA map over a [BH, T, d] bf16 tensor, box 64 x rows x 1, 128-byte
+// swizzle; rows past T read as zeros and are clipped on stores (fwd_tc.cu).
+bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows);
 
 }  // namespace mlstm

@@ -35,6 +35,8 @@ def args(x):
 
 SHAPES = [
     (1, 1, 128, 64, 64),      # one tile
+    (1, 2, 384, 128, 128),    # three query tiles: a CTA pair plus a pair whose second CTA is past T
+    (2, 1, 600, 384, 384),
     (1, 2, 300, 64, 64),      # ragged tail, 128-key tiles
     (2, 1, 257, 128, 128),
     (1, 1, 520, 256, 256),
@@ -46,9 +48,26 @@ SHAPES = [
 ]
 
 
+@pytest.fixture(params=["auto", "single", "pair"])
+def variant(request, monkeypatch):
+    """auto: the library's choice; single: the one-CTA kernel; pair: the CTA-pair
+    kernel (cta_group::2), skipped for shapes it does not tile."""
+    if request.param == "auto":
+        monkeypatch.delenv("MLSTM_TC_VARIANT", raising=False)
+    else:
+        monkeypatch.setenv("MLSTM_TC_VARIANT", request.param)
+    return request.param
+
+
+def pair_tiles(dqk, dv):
+    return dqk % 128 == 0 and dqk <= 512 and ((dv <= 384 and dv % 128 == 0) or dv == 512)
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_tc_vs_oracle(M, shape):
+def test_tc_vs_oracle(M, shape, variant):
     B, H, T, dqk, dv = shape
+    if variant == "pair" and not pair_tiles(dqk, dv):
+        pytest.skip("the pair kernel tiles d_qk and each d_v slice in multiples of 128")
     x = W.sequence_inputs(B, H, T, dqk, dv, torch.bfloat16, seed=T + dqk)
     h, m, n = run(M, x)
     wh, wm, wn = oracle.parallel_stabilized(*args(x))
@@ -81,7 +100,7 @@ def test_tc_gate_regimes(M, gates):
 
 
 @pytest.mark.parametrize("w", [W.L125M, W.L350M, W.LONG], ids=lambda w: w.name)
-def test_full_size_sampled_rows(M, w):
+def test_full_size_sampled_rows(M, w, variant):
     """Full B, H, T, d as benchmarked; the oracle evaluates sampled rows one by one."""
     x = W.parallel_inputs(w, 0)
     h, m, n = run(M, x)
