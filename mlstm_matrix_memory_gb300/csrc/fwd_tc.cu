@@ -54,8 +54,7 @@ __device__ long long g_trace[24 * kTraceTiles];
 __device__ int g_trace_block;
 #define TRACE(ev, j)                                                                  \
   do {                                                                                \
-    if ((int)blockIdx.x == g_trace_block && (j) < kTraceTiles)                        \
-      g_trace[(ev) * kTraceTiles + (j)] = clock64();                                  \
+    if (trace_on && (j) < kTraceTiles) g_trace[(ev) * kTraceTiles + (j)] = clock64(); \
   } while (0)
 #else
 #define TRACE(ev, j) \
@@ -113,6 +112,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &abort_flag;
+#ifdef MLSTM_TRACE
+  const bool trace_on = (int)blockIdx.x == g_trace_block;   // read once
+#endif
 
   // ---- work item: longest query tiles of all heads first
   const int per_rank = p.BH * p.nsplit;
@@ -240,7 +242,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         TRACE(0, j);
         ok = mbar_wait(bar(kBarSEmpty + buf), (u & 1) ^ 1, spin, abort, p.st, kSiteMma);
         if (!ok) break;
-        tc_fence_after();
+        // no tcgen05 fence: the gating warps finished their TMEM reads (wait::ld)
+        // and made P visible to the async proxy before arriving
         const uint32_t d_s = tmem + SOFF + buf * BN;
         for (int c = 0; c < nkc; ++c, ++mit) {
           TRACE(17, mit);
@@ -251,12 +254,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           const uint64_t aq = dQ + (uint64_t)(c * 2048);            // Q boxes 2c, 2c+1 (16 KB each)
           const uint64_t bk = dK + (uint64_t)(st * (kStageBytes >> 4));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < 4; ++kk) {
+            if (j == 5) TRACE(20, c * 8 + kk);
             mma_bf16_ss(d_s, aq + 2 * kk, bk + 2 * kk, idS, (c | kk) != 0);
+          }
           if (p.dqk - c * 128 > 64) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
+            for (int kk = 0; kk < 4; ++kk) {
+              if (j == 5) TRACE(20, c * 8 + 4 + kk);
               mma_bf16_ss(d_s, aq + 1024 + 2 * kk, bk + (BN * 128 >> 4) + 2 * kk, idS, 1);
+            }
           }
           mma_commit(bar(kBarEmpty + st));
           TRACE(19, mit);
@@ -270,7 +277,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         const int jj = j - 1;
         ok = mbar_wait(bar(kBarPFull), jj & 1, spin, abort, p.st, kSiteMma);
         if (!ok) break;
-        tc_fence_after();
+        // no tcgen05 fence: the gating warps finished their TMEM reads (wait::ld)
+        // and made P visible to the async proxy before arriving
         TRACE(2, jj);
         for (int e = 0; e < nvc; ++e, ++mit) {
           TRACE(17, mit);
@@ -284,8 +292,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           // keys 16kk..16kk+15: P box kk/4 at +32 B per step; V rows at +2 KB per 16 keys
           if (dv_cta - e * 128 >= 128) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              if (jj == 5) TRACE(21, e * 8 + kk);
               mma_bf16_ss(d_o, dP + (kk >> 2) * 1024 + (kk & 3) * 2, bv + kk * 128, idO128, acc0 | (kk != 0));
+            }
           } else {
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
@@ -293,6 +303,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           }
           mma_commit(bar(kBarEmpty + st));
           TRACE(19, mit);
+          if (jj == 5) TRACE(22, e);
           if (++st == p.nst) { st = 0; ph ^= 1; }
         }
         if (!ok) break;
@@ -453,7 +464,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       for (int b2 = 0; b2 < dv_cta / 64; ++b2)
         tma_store_3d(&tmap_h, sQ + b2 * 16384u, dv_off + b2 * 64, i0, bh);
       tma_store_commit();
-      tma_store_wait_all();
+      tma_store_wait_read();
     }
     tc_fence_before();
     if (gw == 0 && lane == 0) TRACE(12, 0);
@@ -603,8 +614,8 @@ int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
   const bool force_single = var && var[0] == 's', force_pair = var && var[0] == 'p';
   // The pair halves each SM's K/V traffic, which pays off once query tiles see
   // many key tiles (long sequences) or when d_v is split over two CTAs anyway;
-  // at T <= 2048 with d_v <= 384 the single-CTA kernel is faster (measured).
-  const bool pair_pays = a.T > 2048 || a.dv > 384;
+  // for short sequences with d_v <= 384 the single-CTA kernel is faster (measured).
+  const bool pair_pays = a.T >= 2048 || a.dv > 384;
   if (!force_single && fwd_tc2_supported(a.dqk, a.dv) && (pair_pays || force_pair))
     return launch_fwd_tc2(a, stream);
   if (force_pair) return kUnsupported;

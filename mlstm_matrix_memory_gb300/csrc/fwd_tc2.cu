@@ -56,8 +56,7 @@ __device__ long long g_trace2[2 * 16 * 64];
 __device__ int g_trace2_cluster;
 #define TRACE2(ev, j)                                                                             \
   do {                                                                                            \
-    if ((int)(blockIdx.x >> 1) == g_trace2_cluster && (j) < 64)                                   \
-      g_trace2[((int)cluster_ctarank() * 16 + (ev)) * 64 + (j)] = clock64();                      \
+    if (trace_on && (j) < 64) g_trace2[(trace_rank * 16 + (ev)) * 64 + (j)] = clock64();          \
   } while (0)
 #else
 #define TRACE2(ev, j) \
@@ -88,15 +87,13 @@ __device__ __forceinline__ void issue_s(uint32_t d_s, uint64_t aq, uint64_t bk, 
     for (int kk = 0; kk < 4; ++kk)
       mma_bf16_ss_pair(d_s, aq + b2 * 1024 + 2 * kk, bk + b2 * 512 + 2 * kk, idS, first ? ((b2 | kk) != 0) : 1u);
 }
-// O[:, chunk] += P V_chunk for VB chunks of 128 d_v columns (8 k-steps of 16 keys each).
-template <int VB>
+// O[:, cols] += P V[:, cols] over the 128 keys of a tile (8 k-steps of 16 keys):
+// N = 256 columns (each CTA holds one whole 128-column chunk: two MN atoms
+// 16 KB apart) or N = 128 (each CTA holds 64 columns: one atom).
 __device__ __forceinline__ void issue_o(uint32_t d_o, uint64_t dP, uint64_t bv, uint32_t idO, bool first) {
 #pragma unroll
-  for (int b2 = 0; b2 < VB; ++b2)
-#pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk)
-      mma_bf16_ss_pair(d_o + b2 * 128, dP + (kk >> 2) * 1024 + (kk & 3) * 2, bv + b2 * 1024 + kk * 128, idO,
-                       first ? (kk != 0) : 1u);
+  for (int kk = 0; kk < kBN / 16; ++kk)
+    mma_bf16_ss_pair(d_o, dP + (kk >> 2) * 1024 + (kk & 3) * 2, bv + kk * 128, idO, first ? (kk != 0) : 1u);
 }
 
 template <int NSBUF>
@@ -117,6 +114,10 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
+#ifdef MLSTM_TRACE
+  const bool trace_on = (int)(blockIdx.x >> 1) == g_trace2_cluster;   // read once
+  const int trace_rank = (int)rank;
+#endif
 
   // ---- work item: longest query-row pairs of all heads first
   const int cid = (int)(blockIdx.x >> 1);
@@ -209,12 +210,15 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
           if (st % kProducers == pi) {
             ok = mbar_wait(bar(kBarEmpty + st), ph ^ 1, spin, abort, p.st, kSiteProducer);
             if (!ok) break;
-            const int vb = min(2, nch - 2 * e);                // 128-column chunks in this slot
+            // slot e covers chunks 2e, 2e+1 (N=256: this CTA loads chunk 2e+rank whole)
+            // or the last odd chunk 2e alone (N=128: this CTA loads its 64-column half)
+            const bool wide = 2 * e + 1 < nch;
             TRACE2(12, it);
-            if (leader) mbar_arrive_expect_tx(bar(kBarFull + st), 2u * (uint32_t)vb * 16384u);
-            for (int b2 = 0; b2 < vb; ++b2)
-              tma_load_3d_pair(sRing + st * kSlotBytes + b2 * 16384u, &tmap_v, lbar(kBarFull + st),
-                               dv_off + (2 * e + b2) * 128 + (int)rank * 64, (j - 1) * kBN, bh);
+            if (leader) mbar_arrive_expect_tx(bar(kBarFull + st), (wide ? 4u : 2u) * 16384u);
+            const int col0 = wide ? dv_off + (2 * e + (int)rank) * 128 : dv_off + 2 * e * 128 + (int)rank * 64;
+            for (int b2 = 0; b2 < (wide ? 2 : 1); ++b2)
+              tma_load_3d_pair(sRing + st * kSlotBytes + b2 * 16384u, &tmap_v, lbar(kBarFull + st), col0 + b2 * 64,
+                               (j - 1) * kBN, bh);
             last_it[st] = it;
           }
           if (++st == p.nst) { st = 0; ph ^= 1; }
@@ -225,6 +229,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     // ------------------------------------------------------------ MMA issuer (leader only)
     const uint32_t idS = idesc_bf16_f32(2 * kBM, kBN, 0, 0);       // M=256 rows over the pair, N=128 keys
     const uint32_t idO = idesc_bf16_f32(2 * kBM, 128, 0, 1);       // N=128 d_v columns, V MN-major
+    const uint32_t idO2 = idesc_bf16_f32(2 * kBM, 256, 0, 1);      // N=256: two chunks
     const uint64_t dQ = smem_desc_sw128(sQ, 16, 1024);
     const uint64_t dK = smem_desc_sw128(sRing, 16, 1024);
     const uint64_t dP = smem_desc_sw128(sP, 16, 1024);
@@ -239,7 +244,8 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         TRACE2(1, j);
         ok = mbar_wait(bar(kBarSEmpty + buf), (u & 1) ^ 1, spin, abort, p.st, kSiteMma);
         if (!ok) break;
-        tc_fence_after();
+        // no tcgen05 fence: the gating warps finished their TMEM reads (wait::ld)
+        // and made P visible to the async proxy before arriving
         TRACE2(2, j);
         const uint32_t d_s = tmem + SOFF + buf * kBN;
         for (int c = 0; c < nkc; ++c, ++mit) {
@@ -263,17 +269,17 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         const int jj = j - 1;
         ok = mbar_wait(bar(kBarPFull), jj & 1, spin, abort, p.st, kSiteMma);
         if (!ok) break;
-        tc_fence_after();
+        // no tcgen05 fence: the gating warps finished their TMEM reads (wait::ld)
+        // and made P visible to the async proxy before arriving
         TRACE2(4, jj);
         for (int e = 0; e < nvc; ++e, ++mit) {
           TRACE2(14, mit);
           ok = mbar_wait(bar(kBarFull + st), ph, spin, abort, p.st, kSiteMma);
           if (!ok) break;
           TRACE2(15, mit);
-          const int vb = min(2, nch - 2 * e);
+          const bool wide = 2 * e + 1 < nch;
           const uint64_t bv = dV + (uint64_t)(st * (kSlotBytes >> 4));
-          if (vb == 2) issue_o<2>(tmem + 2 * e * 128, dP, bv, idO, jj == 0);
-          else issue_o<1>(tmem + 2 * e * 128, dP, bv, idO, jj == 0);
+          issue_o(tmem + 2 * e * 128, dP, bv, wide ? idO2 : idO, jj == 0);
           mma_commit_pair_mc(bar(kBarEmpty + st), 0x3);
           if (++st == p.nst) { st = 0; ph ^= 1; }
         }
@@ -427,7 +433,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       for (int b2 = 0; b2 < dv_cta / 64; ++b2)
         tma_store_3d(&tmap_h, sQ + b2 * 16384u, dv_off + b2 * 64, i0, bh);
       tma_store_commit();
-      tma_store_wait_all();
+      tma_store_wait_read();
     }
     if (gw == 0 && lane == 0) TRACE2(11, 0);
     tc_fence_before();

@@ -94,6 +94,11 @@ __device__ __forceinline__ void tma_store_3d(const void* desc, uint32_t src, int
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until all committed bulk stores have completed.
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until all committed bulk stores have read their shared-memory source
+// (the global writes complete asynchronously, before the grid completes).
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Bring a tile into L2 ahead of its TMA load (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const void* desc, int c0, int c1, int c2) {
