@@ -5,9 +5,15 @@
 // decomposition.  A cluster of two CTAs owns 256 consecutive query rows of one
 // head (CTA rank r: rows 128r..128r+127 of the pair) and a slice of d_v.  The
 // leader (rank 0) issues M=256 MMAs: each CTA holds its own 128 rows of Q, P,
-// S and O, and one half of every K and V tile (K: 64 of the 128 keys; V: 64 of
-// each 128 d_v columns).  Each SM therefore loads half of the K/V bytes a
-// single-CTA tile needs, and a ring slot covers twice the MMA work.
+// S and O, and one half of every K and V tile (K: 64 of the 128 keys; V: half
+// of the d_v columns).  Each SM therefore loads half of the K/V bytes a
+// single-CTA tile needs.
+//
+// K and V stream through two rings of 16 KB granules, every granule full: a K
+// granule is [64 keys x 128 d] (one 8-MMA burst of the S product), a V
+// granule [128 keys x 64 d_v].  One producer thread fills each ring and one
+// MMA thread drains it: warp 1 issues S = Q K^T, warp 2 issues O += P V, so
+// the tensor pipe stays fed while either thread waits on a barrier.
 //
 // Synchronisation: every tensor load of both CTAs completes on the leader's
 // `full` barrier; the leader's MMA commits are multicast to both CTAs'
@@ -29,9 +35,9 @@ using namespace tc;
 constexpr int kBM = 128;                 // query rows per CTA (256 per pair)
 constexpr int kBN = 128;                 // keys per tile
 constexpr int kThreads = 384;
-constexpr int kSlotBytes = 32768;        // ring slot per CTA: 4 K boxes [64 keys x 64 d] or 2 V boxes [128 keys x 64 d_v]
-constexpr int kMaxSlots = 8;
-constexpr int kProducers = 3;
+constexpr int kSlotBytes = 16384;        // ring granule per CTA: 2 K boxes [64 keys x 64 d] or 1 V box [128 keys x 64 d_v]
+constexpr int kMaxSlots = 16;
+constexpr int kProducers = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemLimit = 232448;
 constexpr long long kDrainSpin = 1LL << 22;
@@ -43,10 +49,10 @@ enum : int {
   kBarPFull = 5,
   kBarPEmpty = 6,
   kBarOFull = 7,
-  kBarDrain = 8,
-  kBarFull = 9,
-  kBarEmpty = 9 + kMaxSlots,
-  kNumBars = 9 + 2 * kMaxSlots,
+  kBarDrain = 8,                          // two: S issuer, O issuer
+  kBarFull = 10,
+  kBarEmpty = 10 + kMaxSlots,
+  kNumBars = 10 + 2 * kMaxSlots,
 };
 enum : int { kSiteProducer = 11, kSiteMma = 12, kSiteGate = 13, kSiteEpilogue = 14 };
 
@@ -71,7 +77,7 @@ struct Tc2Params {
   float* m_out;
   float* n_out;
   int T, BH, dqk, dv;
-  int nsplit, dv_slice, nst, npairs;
+  int nsplit, dv_slice, nk, nv, npairs;   // nk + nv ring granules (K ring, then V ring)
   float log2_scale;
   DevStatus st;
 };
@@ -107,9 +113,9 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
-  __shared__ int last_it_s[kMaxSlots];
+  __shared__ int last_par_s[kMaxSlots];
   volatile int* abort = &abort_flag;
-  volatile int* last_it = last_it_s;
+  volatile int* last_par = last_par_s;      // parity of each granule's last fill, -1 if never filled
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -130,9 +136,9 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   const int dv_cta = split == 0 ? p.dv_slice : p.dv - p.dv_slice;
   const int pair_last = min(p.T, (2 * pair + 2) * kBM) - 1;
   const int nkv = pair_last / kBN + 1;                       // key tiles, same in both CTAs
-  const int nkc = (p.dqk + 255) / 256;                       // K slots per key tile
-  const int nch = dv_cta / 128;                              // 128-column O chunks
-  const int nvc = (nch + 1) / 2;                             // V slots per key tile
+  const int nkg = p.dqk / 128;                               // K granules per key tile
+  const int nch = dv_cta / 128;                              // 128-column O chunks (one V granule each)
+  const int nvc = (nch + 1) / 2;                             // chunk pairs
   const size_t hbase = (size_t)bh * p.T;
 
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
@@ -142,7 +148,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   auto lbar = [&](int i) { return mapa_shared(smem_u32(&bars[i]), 0); };   // leader's barrier
 
-  if (threadIdx.x < kMaxSlots) last_it_s[threadIdx.x] = -1;
+  if (threadIdx.x < kMaxSlots) last_par_s[threadIdx.x] = -1;
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(bar(kBarQFull), 1);
@@ -154,6 +160,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarOFull), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain + 1), 1);
     for (int s = 0; s < kMaxSlots; ++s) {
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
@@ -175,123 +182,131 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   const long long spin = p.st.spin_limit;
   if (threadIdx.x == 0) TRACE2(0, 0);
 
-  if ((warp == 0 || warp == 2 || warp == 3) && lane == 0) {
+  if ((warp == 0 || warp == 3) && lane == 0) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
-    // Slot st is owned by producer st % kProducers in every round.  Each CTA
-    // loads its own halves into its own slots; completion is counted on the
-    // leader's full barrier, whose expected byte count (both halves) only the
-    // leader's producer posts.
-    const int pi = warp == 0 ? 0 : warp - 1;
+    // Warp 0 fills the K ring, warp 3 the V ring.  Each CTA loads its own
+    // halves into its own granules; completion is counted on the leader's full
+    // barrier, whose expected byte count (both halves) only the leader posts.
+    const int pi = warp == 0 ? 0 : 1;
     if (leader && pi == 0) mbar_arrive_expect_tx(bar(kBarQFull), 2u * (uint32_t)p.dqk * kBM * 2);
     for (int b2 = pi; b2 < p.dqk / 64; b2 += kProducers)
       tma_load_3d_pair(sQ + b2 * 16384u, &tmap_q, lbar(kBarQFull), b2 * 64, i0, bh);
-    int st = 0, it = 0;
+    const int base_slot = pi == 0 ? 0 : p.nk, n = pi == 0 ? p.nk : p.nv;
+    int st = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int j = 0; j <= nkv && ok; ++j) {
-      if (j < nkv) {
-        for (int c = 0; c < nkc; ++c, ++it) {
-          if (st % kProducers == pi) {
-            ok = mbar_wait(bar(kBarEmpty + st), ph ^ 1, spin, abort, p.st, kSiteProducer);
-            if (!ok) break;
-            const int kb = min(4, (p.dqk - c * 256) / 64);   // [64 keys x 64 d] boxes in this slot
-            TRACE2(12, it);
-            if (leader) mbar_arrive_expect_tx(bar(kBarFull + st), 2u * (uint32_t)kb * 8192u);
-            for (int b2 = 0; b2 < kb; ++b2)
-              tma_load_3d_pair(sRing + st * kSlotBytes + b2 * 8192u, &tmap_k, lbar(kBarFull + st),
-                               c * 256 + b2 * 64, j * kBN + (int)rank * 64, bh);
-            last_it[st] = it;
+    // loads the ring's next granule
+    auto load = [&](const CUtensorMap* map, int nbox, uint32_t box_bytes, int x0, int dx, int y) {
+      if (!ok) return;
+      const int g = base_slot + st;
+      ok = mbar_wait(bar(kBarEmpty + g), ph ^ 1, spin, abort, p.st, kSiteProducer);
+      if (!ok) return;
+      if (leader) mbar_arrive_expect_tx(bar(kBarFull + g), 2u * kSlotBytes);
+      for (int b2 = 0; b2 < nbox; ++b2)
+        tma_load_3d_pair(sRing + g * kSlotBytes + b2 * box_bytes, map, lbar(kBarFull + g), x0 + b2 * dx, y, bh);
+      last_par[g] = (int)ph;
+      if (++st == n) { st = 0; ph ^= 1; }
+    };
+    if (pi == 0) {
+      for (int j = 0; j < nkv && ok; ++j)
+        for (int c = 0; c < nkg; ++c) load(&tmap_k, 2, 8192u, c * 128, 64, j * kBN + (int)rank * 64);
+    } else {
+      for (int j = 0; j < nkv && ok; ++j)
+        for (int e = 0; e < nvc; ++e) {
+          // a pair of 128-column chunks in two adjacent granules takes one N=256
+          // MMA burst (this CTA holds chunk 2e+rank whole); otherwise each chunk
+          // is its own N=128 burst over one granule (this CTA holds 64 columns)
+          if (2 * e + 1 < nch && st + 1 < n) {
+            const int col = dv_off + (2 * e + (int)rank) * 128;
+            load(&tmap_v, 1, 0u, col, 0, j * kBN);
+            load(&tmap_v, 1, 0u, col + 64, 0, j * kBN);
+          } else {
+            for (int q = 2 * e; q < min(2 * e + 2, nch); ++q)
+              load(&tmap_v, 1, 0u, dv_off + q * 128 + (int)rank * 64, 0, j * kBN);
           }
-          if (++st == p.nst) { st = 0; ph ^= 1; }
         }
-      }
-      if (j >= 1 && ok) {
-        for (int e = 0; e < nvc; ++e, ++it) {
-          if (st % kProducers == pi) {
-            ok = mbar_wait(bar(kBarEmpty + st), ph ^ 1, spin, abort, p.st, kSiteProducer);
-            if (!ok) break;
-            // slot e covers chunks 2e, 2e+1 (N=256: this CTA loads chunk 2e+rank whole)
-            // or the last odd chunk 2e alone (N=128: this CTA loads its 64-column half)
-            const bool wide = 2 * e + 1 < nch;
-            TRACE2(12, it);
-            if (leader) mbar_arrive_expect_tx(bar(kBarFull + st), (wide ? 4u : 2u) * 16384u);
-            const int col0 = wide ? dv_off + (2 * e + (int)rank) * 128 : dv_off + 2 * e * 128 + (int)rank * 64;
-            for (int b2 = 0; b2 < (wide ? 2 : 1); ++b2)
-              tma_load_3d_pair(sRing + st * kSlotBytes + b2 * 16384u, &tmap_v, lbar(kBarFull + st), col0 + b2 * 64,
-                               (j - 1) * kBN, bh);
-            last_it[st] = it;
-          }
-          if (++st == p.nst) { st = 0; ph ^= 1; }
-        }
-      }
     }
-  } else if (warp == 1 && lane == 0 && leader) {
-    // ------------------------------------------------------------ MMA issuer (leader only)
+  } else if ((warp == 1 || warp == 2) && lane == 0 && leader) {
+    // ------------------------------------------------------------ MMA issuers (leader only)
+    // S and O use disjoint TMEM columns and rings, so the two threads need no
+    // ordering between them beyond the gating handshake.
+    const bool s_role = warp == 1;
     const uint32_t idS = idesc_bf16_f32(2 * kBM, kBN, 0, 0);       // M=256 rows over the pair, N=128 keys
     const uint32_t idO = idesc_bf16_f32(2 * kBM, 128, 0, 1);       // N=128 d_v columns, V MN-major
     const uint32_t idO2 = idesc_bf16_f32(2 * kBM, 256, 0, 1);      // N=256: two chunks
     const uint64_t dQ = smem_desc_sw128(sQ, 16, 1024);
     const uint64_t dK = smem_desc_sw128(sRing, 16, 1024);
     const uint64_t dP = smem_desc_sw128(sP, 16, 1024);
-    const uint64_t dV = smem_desc_sw128(sRing, 16384, 1024);
-    bool ok = mbar_wait(bar(kBarQFull), 0, spin, abort, p.st, kSiteMma);
+    const uint64_t dV = smem_desc_sw128(sRing + (uint32_t)p.nk * kSlotBytes, 16384, 1024);
+    bool ok = s_role ? mbar_wait(bar(kBarQFull), 0, spin, abort, p.st, kSiteMma) : true;
     tc_fence_after();
-    int st = 0, mit = 0;
+    const int base_slot = s_role ? 0 : p.nk, n = s_role ? p.nk : p.nv;
+    int st = 0;
     uint32_t ph = 0;
-    for (int j = 0; j <= nkv && ok; ++j) {
-      if (j < nkv) {
+    auto full = [&](int s2) { return mbar_wait(bar(kBarFull + base_slot + s2), ph, spin, abort, p.st, kSiteMma); };
+    auto release = [&](int s2) { mma_commit_pair_mc(bar(kBarEmpty + base_slot + s2), 0x3); };
+    auto next = [&]() { if (++st == n) { st = 0; ph ^= 1; } };
+    if (s_role) {
+      for (int j = 0; j < nkv && ok; ++j) {
         const int buf = j % NSBUF, u = j / NSBUF;
         TRACE2(1, j);
         ok = mbar_wait(bar(kBarSEmpty + buf), (u & 1) ^ 1, spin, abort, p.st, kSiteMma);
         if (!ok) break;
         // no tcgen05 fence: the gating warps finished their TMEM reads (wait::ld)
-        // and made P visible to the async proxy before arriving
+        // before arriving
         TRACE2(2, j);
         const uint32_t d_s = tmem + SOFF + buf * kBN;
-        for (int c = 0; c < nkc; ++c, ++mit) {
-          TRACE2(14, mit);
-          ok = mbar_wait(bar(kBarFull + st), ph, spin, abort, p.st, kSiteMma);
+        for (int c = 0; c < nkg; ++c) {
+          ok = full(st);
           if (!ok) break;
-          TRACE2(15, mit);
-          const int kb = min(4, (p.dqk - c * 256) / 64);
-          const uint64_t bk = dK + (uint64_t)(st * (kSlotBytes >> 4));
-          const uint64_t aq = dQ + (uint64_t)(4 * c * 1024);           // Q boxes 4c.. (16 KB each)
-          if (kb == 4) issue_s<4>(d_s, aq, bk, idS, c == 0);
-          else issue_s<2>(d_s, aq, bk, idS, c == 0);                   // d_qk is a multiple of 128
-          mma_commit_pair_mc(bar(kBarEmpty + st), 0x3);
-          if (++st == p.nst) { st = 0; ph ^= 1; }
+          issue_s<2>(d_s, dQ + (uint64_t)(2 * c * 1024), dK + (uint64_t)(st * (kSlotBytes >> 4)), idS, c == 0);
+          release(st);
+          next();
         }
         if (!ok) break;
         mma_commit_pair_mc(bar(kBarSFull + buf), 0x3);
         TRACE2(3, j);
       }
-      if (j >= 1) {
-        const int jj = j - 1;
-        ok = mbar_wait(bar(kBarPFull), jj & 1, spin, abort, p.st, kSiteMma);
+    } else {
+      for (int j = 0; j < nkv && ok; ++j) {
+        ok = mbar_wait(bar(kBarPFull), j & 1, spin, abort, p.st, kSiteMma);
         if (!ok) break;
-        // no tcgen05 fence: the gating warps finished their TMEM reads (wait::ld)
-        // and made P visible to the async proxy before arriving
-        TRACE2(4, jj);
-        for (int e = 0; e < nvc; ++e, ++mit) {
-          TRACE2(14, mit);
-          ok = mbar_wait(bar(kBarFull + st), ph, spin, abort, p.st, kSiteMma);
-          if (!ok) break;
-          TRACE2(15, mit);
-          const bool wide = 2 * e + 1 < nch;
-          const uint64_t bv = dV + (uint64_t)(st * (kSlotBytes >> 4));
-          issue_o(tmem + 2 * e * 128, dP, bv, wide ? idO2 : idO, jj == 0);
-          mma_commit_pair_mc(bar(kBarEmpty + st), 0x3);
-          if (++st == p.nst) { st = 0; ph ^= 1; }
+        // no tcgen05 fence: P is in shared memory, made visible to the async
+        // proxy by the gating warps before they arrived
+        TRACE2(4, j);
+        for (int e = 0; e < nvc && ok; ++e) {
+          if (2 * e + 1 < nch && st + 1 < n) {
+            // granules st, st+1: this CTA's two MN atoms 16 KB apart, N=256
+            const int s0 = st;
+            ok = full(s0);
+            next();
+            ok = ok && full(st);
+            if (!ok) break;
+            issue_o(tmem + 256 * e, dP, dV + (uint64_t)(s0 * (kSlotBytes >> 4)), idO2, j == 0);
+            release(s0);
+            release(st);
+            next();
+          } else {
+            for (int q = 2 * e; q < min(2 * e + 2, nch); ++q) {
+              ok = full(st);
+              if (!ok) break;
+              issue_o(tmem + 128 * q, dP, dV + (uint64_t)(st * (kSlotBytes >> 4)), idO, j == 0);
+              release(st);
+              next();
+            }
+          }
         }
         if (!ok) break;
         mma_commit_pair_mc(bar(kBarPEmpty), 0x3);
-        TRACE2(5, jj);
+        TRACE2(5, j);
       }
+      if (ok) mma_commit_pair_mc(bar(kBarOFull), 0x3);
     }
-    if (ok) mma_commit_pair_mc(bar(kBarOFull), 0x3);
-    mma_commit_pair(bar(kBarDrain));
+    // every MMA this thread issued has completed before TMEM is released
+    const int drain = kBarDrain + (s_role ? 0 : 1);
+    mma_commit_pair(bar(drain));
     for (long long w = 0; w < kDrainSpin; ++w)
-      if (mbar_try_wait(bar(kBarDrain), 0)) break;
+      if (mbar_try_wait(bar(drain), 0)) break;
   } else if (warp >= 4) {
     // ------------------------------------------------------------ gating + epilogue (both CTAs)
     const int gw = warp - 4, qd = gw & 3, half = gw >> 2;
@@ -446,11 +461,10 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     if (lane == 0 && leader && abort_flag) {
       for (long long w = 0; w < kDrainSpin; ++w)
         if (mbar_try_wait(bar(kBarQFull), 0)) break;
-      for (int s2 = 0; s2 < p.nst; ++s2)
-        if (last_it[s2] >= 0) {
-          const uint32_t par = (uint32_t)(last_it[s2] / p.nst) & 1u;
+      for (int s2 = 0; s2 < p.nk + p.nv; ++s2)
+        if (last_par[s2] >= 0) {
           for (long long w = 0; w < kDrainSpin; ++w)
-            if (mbar_try_wait(bar(kBarFull + s2), par)) break;
+            if (mbar_try_wait(bar(kBarFull + s2), (uint32_t)last_par[s2])) break;
         }
     }
     __syncwarp();
@@ -527,9 +541,16 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   p.st = a.st;
   const size_t fixed = 1024 + (size_t)a.dqk * kBM * 2 + (size_t)kBN * kBM * 2;
   const long long room = (long long)kSmemLimit - 1024 - (long long)fixed;
-  p.nst = (int)std::min<long long>(kMaxSlots, room / kSlotBytes);
-  if (p.nst < 2) return kUnsupported;
-  const size_t smem = fixed + (size_t)p.nst * kSlotBytes;
+  const int total = (int)std::min<long long>(kMaxSlots, room / kSlotBytes);
+  if (total < 2) return kUnsupported;
+  // split the granules between the rings in proportion to the bytes a key
+  // tile needs from each; two V granules at least when chunks pair up (N=256)
+  const int nkg = a.dqk / 128, nch = p.dv_slice / 128;
+  p.nv = (int)lround((double)total * nch / (nkg + nch));
+  if (nch >= 2 && total >= 4) p.nv = std::max(p.nv, 2);
+  p.nv = std::min(std::max(p.nv, 1), total - 1);
+  p.nk = total - p.nv;
+  const size_t smem = fixed + (size_t)total * kSlotBytes;
   CUtensorMap mq, mk, mv, mh;
   if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, 64) ||
       !make_map(&mv, a.v, a.dv, a.T, a.BH, kBN) || !make_map(&mh, a.h, a.dv, a.T, a.BH, kBM))
