@@ -147,9 +147,11 @@ def kernel_traffic(name: str):
     try:
         with open(path) as f:
             d = json.load(f)[name]
-        src = os.path.join(ROOT, "mlstm_matrix_memory_gb300", "csrc", d["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return d["bytes_per_launch"] if sha == d["source_sha256_16"] else None
+        srcs = d["source"] if isinstance(d["source"], list) else [d["source"]]
+        h = hashlib.sha256()
+        for name_ in srcs:
+            h.update(open(os.path.join(ROOT, "mlstm_matrix_memory_gb300", "csrc", name_), "rb").read())
+        return d["bytes_per_launch"] if h.hexdigest()[:16] == d["source_sha256_16"] else None
     except Exception:
         return None
 
