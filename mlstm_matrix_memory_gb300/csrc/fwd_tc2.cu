@@ -315,6 +315,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     const int i = i0 + rl;
     const bool row_ok = i < p.T;
     const float rr = row_ok ? p.p2[hbase + i] - p.log2_scale : 0.0f;
+    const float m = row_ok ? p.mrow[hbase + i] : 0.0f;        // for the epilogue
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
     const uint32_t l_sempty0 = lbar(kBarSEmpty), l_sempty1 = lbar(kBarSEmpty + 1), l_pfull = lbar(kBarPFull);
     float bsum = 0.0f;
@@ -409,47 +410,51 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     float* bpart = reinterpret_cast<float*>(dsmem + (sP - smem_u32(dsmem)));
     if (ok) bpart[half * kBM + rl] = bsum;
     named_bar_sync(1, 256);
-    float nrm = 0.0f, m = 0.0f;
+    if (gw == 0 && lane == 0) TRACE2(12, 0);
+    float nrm = 0.0f;
     if (ok) {
       const float b = bpart[rl] + bpart[kBM + rl];
-      m = row_ok ? p.mrow[hbase + i] : 0.0f;
       nrm = fmaxf(fabsf(b), expf(-m));
     }
     named_bar_sync(1, 256);
     if (ok) {
       const float inv = nrm > 0.0f ? 1.0f / nrm : 0.0f;
       const int cols = dv_cta / 2, c0 = half * cols;
-      for (int ch = 0; ch < cols / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_addr + c0 + 32 * ch, o);
+      // 64 columns (one staging box) per TMEM wait; cols is a multiple of 64
+      for (int ch = 0; ch < cols / 64; ++ch) {
+        uint32_t o[64];
+        tmem_ld32(tmem + lane_addr + c0 + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tmem_ld32(tmem + lane_addr + c0 + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
         tmem_wait_ld();
-        const int col = c0 + 32 * ch;
+        const int col = c0 + 64 * ch;
         const uint32_t box = sQ + (uint32_t)(col >> 6) * 16384u + rl * 128u;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 8; ++g) {
           uint32_t w[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t)
             w[t] = pack_bf16x2(__uint_as_float(o[8 * g + 2 * t]) * inv, __uint_as_float(o[8 * g + 2 * t + 1]) * inv);
-          const int chunk = ((col & 63) >> 3) + g;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + ((chunk ^ (rl & 7)) << 4)), "r"(w[0]),
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + ((g ^ (rl & 7)) << 4)), "r"(w[0]),
                        "r"(w[1]), "r"(w[2]), "r"(w[3])
                        : "memory");
+        }
+        // the box is complete once the half's four warps wrote their rows: store
+        // it while the next box is formed (the store out of the SM is the slow part)
+        fence_proxy_async_smem();
+        named_bar_sync(2 + half, 128);
+        if (qd == 0 && lane == 0 && i0 < p.T) {
+          tma_store_3d(&tmap_h, box - rl * 128u, dv_off + col, i0, bh);
+          tma_store_commit();
         }
       }
       if (row_ok && split == 0 && half == 0) {
         if (p.m_out) p.m_out[hbase + i] = m;
         if (p.n_out) p.n_out[hbase + i] = nrm;
       }
-      fence_proxy_async_smem();
     }
-    named_bar_sync(1, 256);
-    if (ok && gw == 0 && lane == 0 && i0 < p.T) {
-      for (int b2 = 0; b2 < dv_cta / 64; ++b2)
-        tma_store_3d(&tmap_h, sQ + b2 * 16384u, dv_off + b2 * 64, i0, bh);
-      tma_store_commit();
-      tma_store_wait_read();
-    }
+    if (gw == 0 && lane == 0) TRACE2(14, 0);
+    if (ok && qd == 0 && lane == 0) tma_store_wait_read();
+    if (gw == 0 && lane == 0) TRACE2(15, 0);
     if (gw == 0 && lane == 0) TRACE2(11, 0);
     tc_fence_before();
   }
