@@ -612,10 +612,9 @@ int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
   // =pair in the environment forces one variant (tuning and tests).
   const char* var = getenv("MLSTM_TC_VARIANT");
   const bool force_single = var && var[0] == 's', force_pair = var && var[0] == 'p';
-  // The pair halves each SM's K/V traffic, which pays off once query tiles see
-  // many key tiles (long sequences) or when d_v is split over two CTAs anyway;
-  // for short sequences with d_v <= 384 the single-CTA kernel is faster (measured).
-  const bool pair_pays = a.T >= 2048 || a.dv > 384;
+  // The pair halves each SM's K/V traffic and runs persistently; it is as fast
+  // or faster from T = 512 on (measured), and the only choice for d_v = 512.
+  const bool pair_pays = a.T > 256 || a.dv > 384;
   if (!force_single && fwd_tc2_supported(a.dqk, a.dv) && (pair_pays || force_pair))
     return launch_fwd_tc2(a, stream);
   if (force_pair) return kUnsupported;

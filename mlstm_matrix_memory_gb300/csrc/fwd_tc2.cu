@@ -50,9 +50,10 @@ enum : int {
   kBarPEmpty = 6,
   kBarOFull = 7,
   kBarDrain = 8,                          // two: S issuer, O issuer
-  kBarFull = 10,
-  kBarEmpty = 10 + kMaxSlots,
-  kNumBars = 10 + 2 * kMaxSlots,
+  kBarQEmpty = 10,                        // Q of the current item read by its last S product
+  kBarFull = 11,
+  kBarEmpty = 11 + kMaxSlots,
+  kNumBars = 11 + 2 * kMaxSlots,
 };
 enum : int { kSiteProducer = 11, kSiteMma = 12, kSiteGate = 13, kSiteEpilogue = 14 };
 
@@ -78,6 +79,7 @@ struct Tc2Params {
   float* n_out;
   int T, BH, dqk, dv;
   int nsplit, dv_slice, nk, nv, npairs;   // nk + nv ring granules (K ring, then V ring)
+  int n_items, nclusters;                 // work items (query-row pairs x d_v splits); clusters launched
   float log2_scale;
   DevStatus st;
 };
@@ -102,6 +104,31 @@ __device__ __forceinline__ void issue_o(uint32_t d_o, uint64_t dP, uint64_t bv, 
     mma_bf16_ss_pair(d_o, dP + (kk >> 2) * 1024 + (kk & 3) * 2, bv + kk * 128, idO, first ? (kk != 0) : 1u);
 }
 
+// One work item: a pair of 128-row query blocks of one head and one d_v slice.
+struct Item {
+  int bh, split, i0, dv_off, dv_cta, nkv;
+};
+
+// Items in longest-first order over all heads; cluster c takes, in round r,
+// item r*G + c (r even) or r*G + G-1-c (r odd).  This serpentine order
+// balances the clusters as well as greedy list scheduling does here, and
+// every role of both CTAs derives the same sequence without communicating.
+__device__ __forceinline__ bool item_at(const Tc2Params& p, int r, int c, uint32_t rank, Item& it) {
+  const int G = p.nclusters;
+  const int w = r * G + ((r & 1) ? G - 1 - c : c);
+  if (w >= p.n_items) return false;
+  const int per_rank = p.BH * p.nsplit;
+  const int pair = p.npairs - 1 - w / per_rank;
+  const int rem = w % per_rank;
+  it.bh = rem / p.nsplit;
+  it.split = rem % p.nsplit;
+  it.i0 = (2 * pair + (int)rank) * kBM;
+  it.dv_off = it.split * p.dv_slice;
+  it.dv_cta = it.split == 0 ? p.dv_slice : p.dv - p.dv_slice;
+  it.nkv = (min(p.T, (2 * pair + 2) * kBM) - 1) / kBN + 1;       // key tiles, same in both CTAs
+  return true;
+}
+
 template <int NSBUF>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -114,33 +141,26 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
   __shared__ int last_par_s[kMaxSlots];
+  __shared__ int q_par_s;
+  __shared__ float bpart[2 * kBM];
   volatile int* abort = &abort_flag;
   volatile int* last_par = last_par_s;      // parity of each granule's last fill, -1 if never filled
+  volatile int* q_par = &q_par_s;           // parity of the last Q fill, -1 if none
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
+  const int cid = (int)(blockIdx.x >> 1);
 #ifdef MLSTM_TRACE
-  const bool trace_on = (int)(blockIdx.x >> 1) == g_trace2_cluster;   // read once
+  const bool trace_cluster = cid == g_trace2_cluster;   // read once; the first item is traced
+  bool trace_on = trace_cluster;
   const int trace_rank = (int)rank;
+#define TRACE_ITEM(q) (trace_on = trace_cluster && (q) == 0)
+#else
+#define TRACE_ITEM(q) ((void)0)
 #endif
 
-  // ---- work item: longest query-row pairs of all heads first
-  const int cid = (int)(blockIdx.x >> 1);
-  const int per_rank = p.BH * p.nsplit;
-  const int pair = p.npairs - 1 - cid / per_rank;
-  const int rem = cid % per_rank;
-  const int bh = rem / p.nsplit, split = rem % p.nsplit;
-  const int i0 = (2 * pair + (int)rank) * kBM;               // this CTA's first query row
-  const int dv_off = split * p.dv_slice;
-  const int dv_cta = split == 0 ? p.dv_slice : p.dv - p.dv_slice;
-  const int pair_last = min(p.T, (2 * pair + 2) * kBM) - 1;
-  const int nkv = pair_last / kBN + 1;                       // key tiles, same in both CTAs
   const int nkg = p.dqk / 128;                               // K granules per key tile
-  const int nch = dv_cta / 128;                              // 128-column O chunks (one V granule each)
-  const int nvc = (nch + 1) / 2;                             // chunk pairs
-  const size_t hbase = (size_t)bh * p.T;
-
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sQ = base;
   const uint32_t sP = sQ + (uint32_t)p.dqk * kBM * 2;
@@ -151,7 +171,9 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   if (threadIdx.x < kMaxSlots) last_par_s[threadIdx.x] = -1;
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    q_par_s = -1;
     mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarSFull + b), 1);
       mbar_init(bar(kBarSEmpty + b), 16);    // gating warps of both CTAs
@@ -169,6 +191,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
+    tma_prefetch_desc(&tmap_h);
   }
   if (warp == 2) {
     tmem_alloc_pair(smem_u32(&tmem_holder), kTmemCols);
@@ -181,16 +204,16 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   const uint32_t tmem = tmem_holder;
   const long long spin = p.st.spin_limit;
   if (threadIdx.x == 0) TRACE2(0, 0);
+  Item it;
 
   if ((warp == 0 || warp == 3) && lane == 0) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
-    // Warp 0 fills the K ring, warp 3 the V ring.  Each CTA loads its own
-    // halves into its own granules; completion is counted on the leader's full
-    // barrier, whose expected byte count (both halves) only the leader posts.
+    // Warp 0 fills the K ring, warp 3 the V ring; both load half of each
+    // item's Q once the previous item's S products have read the old Q.  Each
+    // CTA loads its own halves into its own buffers; completion is counted on
+    // the leader's full barriers, whose expected bytes (both halves) only the
+    // leader posts.
     const int pi = warp == 0 ? 0 : 1;
-    if (leader && pi == 0) mbar_arrive_expect_tx(bar(kBarQFull), 2u * (uint32_t)p.dqk * kBM * 2);
-    for (int b2 = pi; b2 < p.dqk / 64; b2 += kProducers)
-      tma_load_3d_pair(sQ + b2 * 16384u, &tmap_q, lbar(kBarQFull), b2 * 64, i0, bh);
     const int base_slot = pi == 0 ? 0 : p.nk, n = pi == 0 ? p.nk : p.nv;
     int st = 0;
     uint32_t ph = 0;
@@ -203,33 +226,49 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       if (!ok) return;
       if (leader) mbar_arrive_expect_tx(bar(kBarFull + g), 2u * kSlotBytes);
       for (int b2 = 0; b2 < nbox; ++b2)
-        tma_load_3d_pair(sRing + g * kSlotBytes + b2 * box_bytes, map, lbar(kBarFull + g), x0 + b2 * dx, y, bh);
+        tma_load_3d_pair(sRing + g * kSlotBytes + b2 * box_bytes, map, lbar(kBarFull + g), x0 + b2 * dx, y, it.bh);
       last_par[g] = (int)ph;
       if (++st == n) { st = 0; ph ^= 1; }
     };
-    if (pi == 0) {
-      for (int j = 0; j < nkv && ok; ++j)
-        for (int c = 0; c < nkg; ++c) load(&tmap_k, 2, 8192u, c * 128, 64, j * kBN + (int)rank * 64);
-    } else {
-      for (int j = 0; j < nkv && ok; ++j)
-        for (int e = 0; e < nvc; ++e) {
-          // a pair of 128-column chunks in two adjacent granules takes one N=256
-          // MMA burst (this CTA holds chunk 2e+rank whole); otherwise each chunk
-          // is its own N=128 burst over one granule (this CTA holds 64 columns)
-          if (2 * e + 1 < nch && st + 1 < n) {
-            const int col = dv_off + (2 * e + (int)rank) * 128;
-            load(&tmap_v, 1, 0u, col, 0, j * kBN);
-            load(&tmap_v, 1, 0u, col + 64, 0, j * kBN);
-          } else {
-            for (int q = 2 * e; q < min(2 * e + 2, nch); ++q)
-              load(&tmap_v, 1, 0u, dv_off + q * 128 + (int)rank * 64, 0, j * kBN);
+    int qi = 0;
+    for (int r = 0; r * p.nclusters < p.n_items && ok; ++r) {
+      if (!item_at(p, r, cid, rank, it)) continue;
+      if (qi > 0) ok = mbar_wait(bar(kBarQEmpty), (uint32_t)(qi - 1) & 1u, spin, abort, p.st, kSiteProducer);
+      if (!ok) break;
+      if (leader && pi == 0) {
+        mbar_arrive_expect_tx(bar(kBarQFull), 2u * (uint32_t)p.dqk * kBM * 2);
+        *q_par = qi & 1;
+      }
+      for (int b2 = pi; b2 < p.dqk / 64; b2 += kProducers)
+        tma_load_3d_pair(sQ + b2 * 16384u, &tmap_q, lbar(kBarQFull), b2 * 64, it.i0, it.bh);
+      ++qi;
+      const int nch = it.dv_cta / 128, nvc = (nch + 1) / 2;
+      if (pi == 0) {
+        for (int j = 0; j < it.nkv && ok; ++j)
+          for (int c = 0; c < nkg; ++c) load(&tmap_k, 2, 8192u, c * 128, 64, j * kBN + (int)rank * 64);
+      } else {
+        for (int j = 0; j < it.nkv && ok; ++j)
+          for (int e = 0; e < nvc; ++e) {
+            // a pair of 128-column chunks in two adjacent granules takes one N=256
+            // MMA burst (this CTA holds chunk 2e+rank whole); otherwise each chunk
+            // is its own N=128 burst over one granule (this CTA holds 64 columns)
+            if (2 * e + 1 < nch && st + 1 < n) {
+              const int col = it.dv_off + (2 * e + (int)rank) * 128;
+              load(&tmap_v, 1, 0u, col, 0, j * kBN);
+              load(&tmap_v, 1, 0u, col + 64, 0, j * kBN);
+            } else {
+              for (int q = 2 * e; q < min(2 * e + 2, nch); ++q)
+                load(&tmap_v, 1, 0u, it.dv_off + q * 128 + (int)rank * 64, 0, j * kBN);
+            }
           }
-        }
+      }
     }
   } else if ((warp == 1 || warp == 2) && lane == 0 && leader) {
     // ------------------------------------------------------------ MMA issuers (leader only)
-    // S and O use disjoint TMEM columns and rings, so the two threads need no
-    // ordering between them beyond the gating handshake.
+    // Warp 1 issues S = Q K^T, warp 2 issues O += P V.  The two products use
+    // disjoint TMEM columns and rings, so the threads need no ordering between
+    // them beyond the gating handshake; with two issuing threads the tensor
+    // pipe stays fed while either one waits on a barrier.
     const bool s_role = warp == 1;
     const uint32_t idS = idesc_bf16_f32(2 * kBM, kBN, 0, 0);       // M=256 rows over the pair, N=128 keys
     const uint32_t idO = idesc_bf16_f32(2 * kBM, 128, 0, 1);       // N=128 d_v columns, V MN-major
@@ -238,69 +277,81 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     const uint64_t dK = smem_desc_sw128(sRing, 16, 1024);
     const uint64_t dP = smem_desc_sw128(sP, 16, 1024);
     const uint64_t dV = smem_desc_sw128(sRing + (uint32_t)p.nk * kSlotBytes, 16384, 1024);
-    bool ok = s_role ? mbar_wait(bar(kBarQFull), 0, spin, abort, p.st, kSiteMma) : true;
-    tc_fence_after();
     const int base_slot = s_role ? 0 : p.nk, n = s_role ? p.nk : p.nv;
     int st = 0;
     uint32_t ph = 0;
+    bool ok = true;
     auto full = [&](int s2) { return mbar_wait(bar(kBarFull + base_slot + s2), ph, spin, abort, p.st, kSiteMma); };
     auto release = [&](int s2) { mma_commit_pair_mc(bar(kBarEmpty + base_slot + s2), 0x3); };
     auto next = [&]() { if (++st == n) { st = 0; ph ^= 1; } };
-    if (s_role) {
-      for (int j = 0; j < nkv && ok; ++j) {
-        const int buf = j % NSBUF, u = j / NSBUF;
-        TRACE2(1, j);
-        ok = mbar_wait(bar(kBarSEmpty + buf), (u & 1) ^ 1, spin, abort, p.st, kSiteMma);
-        if (!ok) break;
-        // no tcgen05 fence: the gating warps finished their TMEM reads (wait::ld)
-        // before arriving
-        TRACE2(2, j);
-        const uint32_t d_s = tmem + SOFF + buf * kBN;
-        for (int c = 0; c < nkg; ++c) {
-          ok = full(st);
+    int qi = 0, gt = 0;                    // items and key tiles so far
+    for (int r = 0; r * p.nclusters < p.n_items && ok; ++r) {
+      if (!item_at(p, r, cid, rank, it)) continue;
+      TRACE_ITEM(qi);
+      if (s_role) {
+        ok = mbar_wait(bar(kBarQFull), (uint32_t)qi & 1u, spin, abort, p.st, kSiteMma);
+        for (int j = 0; j < it.nkv && ok; ++j, ++gt) {
+          const int buf = gt % NSBUF, u = gt / NSBUF;
+          TRACE2(1, j);
+          ok = mbar_wait(bar(kBarSEmpty + buf), (u & 1) ^ 1, spin, abort, p.st, kSiteMma);
           if (!ok) break;
-          issue_s<2>(d_s, dQ + (uint64_t)(2 * c * 1024), dK + (uint64_t)(st * (kSlotBytes >> 4)), idS, c == 0);
-          release(st);
-          next();
-        }
-        if (!ok) break;
-        mma_commit_pair_mc(bar(kBarSFull + buf), 0x3);
-        TRACE2(3, j);
-      }
-    } else {
-      for (int j = 0; j < nkv && ok; ++j) {
-        ok = mbar_wait(bar(kBarPFull), j & 1, spin, abort, p.st, kSiteMma);
-        if (!ok) break;
-        // no tcgen05 fence: P is in shared memory, made visible to the async
-        // proxy by the gating warps before they arrived
-        TRACE2(4, j);
-        for (int e = 0; e < nvc && ok; ++e) {
-          if (2 * e + 1 < nch && st + 1 < n) {
-            // granules st, st+1: this CTA's two MN atoms 16 KB apart, N=256
-            const int s0 = st;
-            ok = full(s0);
-            next();
-            ok = ok && full(st);
+          // no tcgen05 fence: the gating warps finished their TMEM reads (wait::ld)
+          // before arriving
+          TRACE2(2, j);
+          const uint32_t d_s = tmem + SOFF + buf * kBN;
+          for (int c = 0; c < nkg; ++c) {
+            ok = full(st);
             if (!ok) break;
-            issue_o(tmem + 256 * e, dP, dV + (uint64_t)(s0 * (kSlotBytes >> 4)), idO2, j == 0);
-            release(s0);
+            issue_s<2>(d_s, dQ + (uint64_t)(2 * c * 1024), dK + (uint64_t)(st * (kSlotBytes >> 4)), idS, c == 0);
             release(st);
             next();
-          } else {
-            for (int q = 2 * e; q < min(2 * e + 2, nch); ++q) {
-              ok = full(st);
+          }
+          if (!ok) break;
+          mma_commit_pair_mc(bar(kBarSFull + buf), 0x3);
+          TRACE2(3, j);
+        }
+        // this item's Q may be replaced once its S products complete
+        if (ok) mma_commit_pair_mc(bar(kBarQEmpty), 0x3);
+      } else {
+        const int nch = it.dv_cta / 128, nvc = (nch + 1) / 2;
+        for (int j = 0; j < it.nkv && ok; ++j, ++gt) {
+          ok = mbar_wait(bar(kBarPFull), (uint32_t)gt & 1u, spin, abort, p.st, kSiteMma);
+          if (!ok) break;
+          // P is in shared memory, made visible to the async proxy before the
+          // gating warps arrived.  Before the first tile of an item they also
+          // finished reading the previous item's O (wait::ld), which these
+          // MMAs overwrite.
+          if (j == 0) tc_fence_after();
+          TRACE2(4, j);
+          for (int e = 0; e < nvc && ok; ++e) {
+            if (2 * e + 1 < nch && st + 1 < n) {
+              // granules st, st+1: this CTA's two MN atoms 16 KB apart, N=256
+              const int s0 = st;
+              ok = full(s0);
+              next();
+              ok = ok && full(st);
               if (!ok) break;
-              issue_o(tmem + 128 * q, dP, dV + (uint64_t)(st * (kSlotBytes >> 4)), idO, j == 0);
+              issue_o(tmem + 256 * e, dP, dV + (uint64_t)(s0 * (kSlotBytes >> 4)), idO2, j == 0);
+              release(s0);
               release(st);
               next();
+            } else {
+              for (int q = 2 * e; q < min(2 * e + 2, nch); ++q) {
+                ok = full(st);
+                if (!ok) break;
+                issue_o(tmem + 128 * q, dP, dV + (uint64_t)(st * (kSlotBytes >> 4)), idO, j == 0);
+                release(st);
+                next();
+              }
             }
           }
+          if (!ok) break;
+          mma_commit_pair_mc(bar(kBarPEmpty), 0x3);
+          TRACE2(5, j);
         }
-        if (!ok) break;
-        mma_commit_pair_mc(bar(kBarPEmpty), 0x3);
-        TRACE2(5, j);
+        if (ok) mma_commit_pair_mc(bar(kBarOFull), 0x3);
       }
-      if (ok) mma_commit_pair_mc(bar(kBarOFull), 0x3);
+      ++qi;
     }
     // every MMA this thread issued has completed before TMEM is released
     const int drain = kBarDrain + (s_role ? 0 : 1);
@@ -312,160 +363,171 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     const int gw = warp - 4, qd = gw & 3, half = gw >> 2;
     asm volatile("griddepcontrol.wait;" ::: "memory");        // gate terms from the preceding gate pass
     const int rl = 32 * qd + lane;
-    const int i = i0 + rl;
-    const bool row_ok = i < p.T;
-    const float rr = row_ok ? p.p2[hbase + i] - p.log2_scale : 0.0f;
-    const float m = row_ok ? p.mrow[hbase + i] : 0.0f;        // for the epilogue
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
     const uint32_t l_sempty0 = lbar(kBarSEmpty), l_sempty1 = lbar(kBarSEmpty + 1), l_pfull = lbar(kBarPFull);
-    float bsum = 0.0f;
     bool ok = true;
-    float av_next[HALF / 32];
-#pragma unroll
-    for (int t = 0; t < HALF / 32; ++t) {
-      const int col = half * HALF + lane + 32 * t;
-      av_next[t] = col < p.T ? p.a2[hbase + col] : -INFINITY;
-    }
-    for (int j = 0; j < nkv && ok; ++j) {
-      const int j0 = j * kBN, cbase = j0 + half * HALF;
-      const int buf = j % NSBUF, u = j / NSBUF;
-      float av[HALF / 32];
+    int qi = 0, gt = 0;
+    for (int r = 0; r * p.nclusters < p.n_items && ok; ++r) {
+      if (!item_at(p, r, cid, rank, it)) continue;
+      TRACE_ITEM(qi);
+      const int i = it.i0 + rl;
+      const bool row_ok = i < p.T;
+      const size_t hbase = (size_t)it.bh * p.T;
+      const float rr = row_ok ? p.p2[hbase + i] - p.log2_scale : 0.0f;
+      const float m = row_ok ? p.mrow[hbase + i] : 0.0f;      // for the epilogue
+      float bsum = 0.0f;
+      float av_next[HALF / 32];
 #pragma unroll
       for (int t = 0; t < HALF / 32; ++t) {
-        av[t] = av_next[t];
-        const int col = cbase + kBN + lane + 32 * t;
-        av_next[t] = (j + 1 < nkv && col < p.T) ? p.a2[hbase + col] : -INFINITY;
+        const int col = half * HALF + lane + 32 * t;
+        av_next[t] = col < p.T ? p.a2[hbase + col] : -INFINITY;
       }
-      const bool diag = j0 + kBN - 1 > i0;                    // some column of the tile lies above a row
-      float A = -INFINITY;
-      if (!diag) {
+      for (int j = 0; j < it.nkv && ok; ++j, ++gt) {
+        const int j0 = j * kBN, cbase = j0 + half * HALF;
+        const int buf = gt % NSBUF, u = gt / NSBUF;
+        float av[HALF / 32];
 #pragma unroll
-        for (int t = 0; t < HALF / 32; ++t) A = fmaxf(A, av[t]);
-        A = warp_max(A);
+        for (int t = 0; t < HALF / 32; ++t) {
+          av[t] = av_next[t];
+          const int col = cbase + kBN + lane + 32 * t;
+          av_next[t] = (j + 1 < it.nkv && col < p.T) ? p.a2[hbase + col] : -INFINITY;
+        }
+        const bool diag = j0 + kBN - 1 > it.i0;                 // some column of the tile lies above a row
+        float A = -INFINITY;
+        if (!diag) {
 #pragma unroll
-        for (int t = 0; t < HALF / 32; ++t) av[t] = A == -INFINITY ? 0.0f : exp2f(av[t] - A);
+          for (int t = 0; t < HALF / 32; ++t) A = fmaxf(A, av[t]);
+          A = warp_max(A);
+#pragma unroll
+          for (int t = 0; t < HALF / 32; ++t) av[t] = A == -INFINITY ? 0.0f : exp2f(av[t] - A);
+        }
+        ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
+        if (!ok) break;
+        tc_fence_after();
+        if (gw == 0 && lane == 0) TRACE2(6, j);
+        uint32_t sv[HALF];
+#pragma unroll
+        for (int t = 0; t < HALF / 32; ++t)
+          tmem_ld32(tmem + lane_addr + SOFF + buf * kBN + half * HALF + 32 * t,
+                    *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * t]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(buf == 0 ? l_sempty0 : l_sempty1);
+
+        uint32_t pk[HALF / 2];
+        if (!diag) {
+          const float rfac = (A == -INFINITY || !row_ok) ? 0.0f : exp2f(A - rr);
+#pragma unroll
+          for (int c = 0; c < HALF; c += 2) {
+            const float c0 = __shfl_sync(0xffffffffu, av[c / 32], c & 31);
+            const float c1 = __shfl_sync(0xffffffffu, av[(c + 1) / 32], (c + 1) & 31);
+            const float x0 = __uint_as_float(sv[c]) * c0 * rfac;
+            const float x1 = __uint_as_float(sv[c + 1]) * c1 * rfac;
+            bsum += x0 + x1;
+            pk[c / 2] = pack_bf16x2(x0, x1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < HALF; c += 2) {
+            const float a0 = __shfl_sync(0xffffffffu, av[c / 32], c & 31);
+            const float a1 = __shfl_sync(0xffffffffu, av[(c + 1) / 32], (c + 1) & 31);
+            const int col = cbase + c;
+            const float e0 = (row_ok && col <= i) ? exp2f(a0 - rr) : 0.0f;
+            const float e1 = (row_ok && col + 1 <= i) ? exp2f(a1 - rr) : 0.0f;
+            const float x0 = __uint_as_float(sv[c]) * e0;
+            const float x1 = __uint_as_float(sv[c + 1]) * e1;
+            bsum += x0 + x1;
+            pk[c / 2] = pack_bf16x2(x0, x1);
+          }
+        }
+        if (gw == 0 && lane == 0) TRACE2(7, j);
+        ok = mbar_wait(bar(kBarPEmpty), ((uint32_t)gt & 1u) ^ 1u, spin, abort, p.st, kSiteGate);
+        if (!ok) break;
+        if (gw == 0 && lane == 0) TRACE2(8, j);
+#pragma unroll
+        for (int g = 0; g < HALF / 8; ++g) {
+          const int c = half * HALF + 8 * g;
+          const uint32_t addr = sP + (c >> 6) * 16384u + rl * 128u + ((((c & 63) >> 3) ^ (rl & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * g]),
+                       "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        // also orders this warp's earlier TMEM reads of O before the next
+        // item's first O product (which waits on this arrival)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(l_pfull);
+        if (gw == 0 && lane == 0) TRACE2(9, j);
       }
-      ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
+      if (!ok) break;
+
+      // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n.  Each half stages its
+      // 64-column boxes one at a time in its 16 KB of the P buffer (free until
+      // the next item's first P) and stores each by TMA as soon as it is written.
+      ok = mbar_wait(bar(kBarOFull), (uint32_t)qi & 1u, spin, abort, p.st, kSiteEpilogue);
       if (!ok) break;
       tc_fence_after();
-      if (gw == 0 && lane == 0) TRACE2(6, j);
-      uint32_t sv[HALF];
-#pragma unroll
-      for (int t = 0; t < HALF / 32; ++t)
-        tmem_ld32(tmem + lane_addr + SOFF + buf * kBN + half * HALF + 32 * t,
-                  *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * t]));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(buf == 0 ? l_sempty0 : l_sempty1);
-
-      uint32_t pk[HALF / 2];
-      if (!diag) {
-        const float r = (A == -INFINITY || !row_ok) ? 0.0f : exp2f(A - rr);
-#pragma unroll
-        for (int c = 0; c < HALF; c += 2) {
-          const float c0 = __shfl_sync(0xffffffffu, av[c / 32], c & 31);
-          const float c1 = __shfl_sync(0xffffffffu, av[(c + 1) / 32], (c + 1) & 31);
-          const float x0 = __uint_as_float(sv[c]) * c0 * r;
-          const float x1 = __uint_as_float(sv[c + 1]) * c1 * r;
-          bsum += x0 + x1;
-          pk[c / 2] = pack_bf16x2(x0, x1);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < HALF; c += 2) {
-          const float a0 = __shfl_sync(0xffffffffu, av[c / 32], c & 31);
-          const float a1 = __shfl_sync(0xffffffffu, av[(c + 1) / 32], (c + 1) & 31);
-          const int col = cbase + c;
-          const float e0 = (row_ok && col <= i) ? exp2f(a0 - rr) : 0.0f;
-          const float e1 = (row_ok && col + 1 <= i) ? exp2f(a1 - rr) : 0.0f;
-          const float x0 = __uint_as_float(sv[c]) * e0;
-          const float x1 = __uint_as_float(sv[c + 1]) * e1;
-          bsum += x0 + x1;
-          pk[c / 2] = pack_bf16x2(x0, x1);
-        }
-      }
-      if (gw == 0 && lane == 0) TRACE2(7, j);
-      ok = mbar_wait(bar(kBarPEmpty), (j & 1) ^ 1, spin, abort, p.st, kSiteGate);
-      if (!ok) break;
-      if (gw == 0 && lane == 0) TRACE2(8, j);
-#pragma unroll
-      for (int g = 0; g < HALF / 8; ++g) {
-        const int c = half * HALF + 8 * g;
-        const uint32_t addr = sP + (c >> 6) * 16384u + rl * 128u + ((((c & 63) >> 3) ^ (rl & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * g]),
-                     "r"(pk[4 * g + 1]), "r"(pk[4 * g + 2]), "r"(pk[4 * g + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(l_pfull);
-      if (gw == 0 && lane == 0) TRACE2(9, j);
-    }
-
-    // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n, staged for TMA stores
-    if (ok) ok = mbar_wait(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
-    tc_fence_after();
-    if (gw == 0 && lane == 0) TRACE2(10, 0);
-    float* bpart = reinterpret_cast<float*>(dsmem + (sP - smem_u32(dsmem)));
-    if (ok) bpart[half * kBM + rl] = bsum;
-    named_bar_sync(1, 256);
-    if (gw == 0 && lane == 0) TRACE2(12, 0);
-    float nrm = 0.0f;
-    if (ok) {
+      if (gw == 0 && lane == 0) TRACE2(10, 0);
+      bpart[half * kBM + rl] = bsum;
+      named_bar_sync(1, 256);
       const float b = bpart[rl] + bpart[kBM + rl];
-      nrm = fmaxf(fabsf(b), expf(-m));
-    }
-    named_bar_sync(1, 256);
-    if (ok) {
+      const float nrm = fmaxf(fabsf(b), expf(-m));
       const float inv = nrm > 0.0f ? 1.0f / nrm : 0.0f;
-      const int cols = dv_cta / 2, c0 = half * cols;
-      // 64 columns (one staging box) per TMEM wait; cols is a multiple of 64
+      if (row_ok && it.split == 0 && half == 0) {
+        if (p.m_out) p.m_out[hbase + i] = m;
+        if (p.n_out) p.n_out[hbase + i] = nrm;
+      }
+      if (gw == 0 && lane == 0) TRACE2(12, 0);
+      const int cols = it.dv_cta / 2, c0 = half * cols;      // a multiple of 64
+      const uint32_t stage = sP + (uint32_t)half * 16384u;
+      const bool issuer = qd == 0 && lane == 0 && it.i0 < p.T;
       for (int ch = 0; ch < cols / 64; ++ch) {
         uint32_t o[64];
         tmem_ld32(tmem + lane_addr + c0 + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
         tmem_ld32(tmem + lane_addr + c0 + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
         tmem_wait_ld();
-        const int col = c0 + 64 * ch;
-        const uint32_t box = sQ + (uint32_t)(col >> 6) * 16384u + rl * 128u;
+        // the half's previous box must have been read out by its store (and
+        // bpart read by everyone, for the first box)
+        if (issuer) tma_store_wait_read();
+        named_bar_sync(2 + half, 128);
+        const uint32_t row = stage + rl * 128u;
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           uint32_t w[4];
 #pragma unroll
           for (int t = 0; t < 4; ++t)
             w[t] = pack_bf16x2(__uint_as_float(o[8 * g + 2 * t]) * inv, __uint_as_float(o[8 * g + 2 * t + 1]) * inv);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + ((g ^ (rl & 7)) << 4)), "r"(w[0]),
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((g ^ (rl & 7)) << 4)), "r"(w[0]),
                        "r"(w[1]), "r"(w[2]), "r"(w[3])
                        : "memory");
         }
-        // the box is complete once the half's four warps wrote their rows: store
-        // it while the next box is formed (the store out of the SM is the slow part)
         fence_proxy_async_smem();
         named_bar_sync(2 + half, 128);
-        if (qd == 0 && lane == 0 && i0 < p.T) {
-          tma_store_3d(&tmap_h, box - rl * 128u, dv_off + col, i0, bh);
+        if (issuer) {
+          tma_store_3d(&tmap_h, stage, it.dv_off + c0 + 64 * ch, it.i0, it.bh);
           tma_store_commit();
         }
       }
-      if (row_ok && split == 0 && half == 0) {
-        if (p.m_out) p.m_out[hbase + i] = m;
-        if (p.n_out) p.n_out[hbase + i] = nrm;
-      }
+      if (gw == 0 && lane == 0) TRACE2(14, 0);
+      // the P buffer is free again once both halves' last stores read it out
+      if (issuer) tma_store_wait_read();
+      named_bar_sync(1, 256);
+      if (gw == 0 && lane == 0) TRACE2(11, 0);
+      ++qi;
     }
-    if (gw == 0 && lane == 0) TRACE2(14, 0);
-    if (ok && qd == 0 && lane == 0) tma_store_wait_read();
-    if (gw == 0 && lane == 0) TRACE2(15, 0);
-    if (gw == 0 && lane == 0) TRACE2(11, 0);
     tc_fence_before();
   }
 
   __syncthreads();
   if (warp == 0) {
     // after an abort, loads of this pair may never have been consumed: the
-    // leader waits (bounded) for the last phase of every slot it loaded
+    // leader waits (bounded) for the last phase of Q and of every granule
     if (lane == 0 && leader && abort_flag) {
-      for (long long w = 0; w < kDrainSpin; ++w)
-        if (mbar_try_wait(bar(kBarQFull), 0)) break;
+      if (*q_par >= 0)
+        for (long long w = 0; w < kDrainSpin; ++w)
+          if (mbar_try_wait(bar(kBarQFull), (uint32_t)*q_par)) break;
       for (int s2 = 0; s2 < p.nk + p.nv; ++s2)
         if (last_par[s2] >= 0) {
           for (long long w = 0; w < kDrainSpin; ++w)
@@ -495,14 +557,46 @@ extern "C" int mlstm_trace2_read(long long* host) {
 namespace {
 #endif
 
+// Clusters of two that fit on the device at once with this shared-memory size
+// (queried once per size; half the SM count if the query fails).
+int resident_pairs(size_t smem) {
+  static std::mutex mu;
+  static size_t last_smem = 0;
+  static int last_dev = -1, last = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int dev = 0, sms = 0, n = 0;
+  cudaGetDevice(&dev);
+  if (last_smem == smem && last_dev == dev && last > 0) return last;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaFuncSetAttribute(fwd_tc2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, fwd_tc2_kernel<1>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = std::max(1, sms / 2);
+  }
+  last_smem = smem;
+  last_dev = dev;
+  last = n;
+  return n;
+}
+
 template <int NSBUF>
 int launch_pair(const FwdArgs& a, const Tc2Params& p, size_t smem, const CUtensorMap& mq, const CUtensorMap& mk,
                 const CUtensorMap& mv, const CUtensorMap& mh, cudaStream_t stream) {
   if (cudaFuncSetAttribute(fwd_tc2_kernel<NSBUF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return kCuda;
-  const long long grid = 2LL * p.npairs * a.BH * p.nsplit;
-  if (grid > 0x7fffffffLL) return kInval;
+  const long long grid = 2LL * p.nclusters;      // persistent: each cluster loops over its items
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
@@ -545,7 +639,7 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   p.log2_scale = log2f(a.scale);
   p.st = a.st;
   const size_t fixed = 1024 + (size_t)a.dqk * kBM * 2 + (size_t)kBN * kBM * 2;
-  const long long room = (long long)kSmemLimit - 1024 - (long long)fixed;
+  const long long room = (long long)kSmemLimit - 2048 - (long long)fixed;   // 2 KB for static shared
   const int total = (int)std::min<long long>(kMaxSlots, room / kSlotBytes);
   if (total < 2) return kUnsupported;
   // split the granules between the rings in proportion to the bytes a key
@@ -556,6 +650,10 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   p.nv = std::min(std::max(p.nv, 1), total - 1);
   p.nk = total - p.nv;
   const size_t smem = fixed + (size_t)total * kSlotBytes;
+  const long long items = (long long)p.npairs * a.BH * p.nsplit;
+  if (items > 0x7fffffffLL) return kInval;
+  p.n_items = (int)items;
+  p.nclusters = std::min(p.n_items, resident_pairs(smem));
   CUtensorMap mq, mk, mv, mh;
   if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, 64) ||
       !make_map(&mv, a.v, a.dv, a.T, a.BH, kBN) || !make_map(&mh, a.h, a.dv, a.T, a.BH, kBM))
