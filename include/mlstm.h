@@ -99,7 +99,7 @@ int mlstm_parallel_fwd_ex(const void *q, const void *k, const void *v,
  *
  * mlstm_gate_prep: the gate terms of eqs (79)-(81) and (101) for every token,
  * written to `workspace` (>= mlstm_parallel_fwd_workspace(B,H,T) bytes):
- *   cs_t = sum_{k<=t} log sigmoid(fgate_pre_k)     (fp64 accumulation)
+ *   cs_t = sum_{k<=t} log sigmoid(fgate_pre_k)     (fp32 two-sum accumulation)
  *   a_t  = igate_pre_t - cs_t,  m_t = cs_t + max_{j<=t} a_j   (row max, eq 80)
  * stored as three fp32 arrays of B*H*T entries, each starting on a 256-byte
  * boundary: a_t*log2(e), max_{j<=t} a_j*log2(e), m_t.
@@ -140,6 +140,29 @@ int mlstm_step(float *C, float *n, float *m,
                const void *q, const void *k, const void *v, const void *o,
                const float *igate_pre, const float *fgate_pre, void *h,
                int B, int H, int d_qk, int d_v, int dtype, void *stream);
+
+/* L consecutive recurrent steps for every head in one call: recurrent
+ * prefill of a prompt, or several generated tokens at once.  The result is
+ * exactly that of mlstm_step applied for t = 0, 1, ..., L-1 in order (same
+ * recurrence, same state convention, same output gate), but the state is
+ * read from and written to memory once instead of L times: each head's C
+ * stays on chip for the whole run.
+ *
+ *   C, n, m    as in mlstm_step: the state before token 0 on entry, the state
+ *              after token L-1 on return (updated in place)
+ *   q, k       [B,H,L,d_qk]  dtype
+ *   v          [B,H,L,d_v]   dtype
+ *   o          [B,H,L,d_v]   dtype, or NULL for no output gate
+ *   igate_pre, fgate_pre [B,H,L] fp32
+ *   h          [B,H,L,d_v]   dtype output, token t of head (b,h) at
+ *              ((b*H + h)*L + t)*d_v
+ * Requirements: B,H,L >= 0; 1 <= d_qk, d_v <= 512; d_qk a multiple of 8;
+ * C, n, q, k 16-byte aligned.  h may not alias any input.  L = 0 leaves the
+ * state unchanged and launches nothing. */
+int mlstm_step_seq(float *C, float *n, float *m,
+                   const void *q, const void *k, const void *v, const void *o,
+                   const float *igate_pre, const float *fgate_pre, void *h,
+                   int B, int H, int L, int d_qk, int d_v, int dtype, void *stream);
 
 /* Size of the scratch array built into the library for
  * mlstm_parallel_fwd_noalloc: 4 MiB, enough for B*H*T up to 349,504 tokens. */

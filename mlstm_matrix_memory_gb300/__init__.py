@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     parallel_fwd,
     parallel_fwd_workspace_bytes,
     step,
+    step_seq,
     last_device_status,
     set_spin_limit,
     gate_prep,

@@ -60,6 +60,8 @@ def library() -> ctypes.CDLL:
         lib.mlstm_parallel_fwd_gated.restype = i
         lib.mlstm_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
         lib.mlstm_step.restype = i
+        lib.mlstm_step_seq.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.mlstm_step_seq.restype = i
         lib.mlstm_last_device_status.argtypes = [vp]
         lib.mlstm_last_device_status.restype = i
         lib.mlstm_set_spin_limit.argtypes = [ll]
@@ -184,6 +186,43 @@ def step(C: torch.Tensor, n: torch.Tensor, m: torch.Tensor, q: torch.Tensor, k: 
                         _ptr(fgate_pre), _ptr(h), B, H, dqk, dv, _DTYPES[q.dtype], _stream(dev))
     if rc != 0:
         raise MlstmError(rc, "mlstm_step")
+    return h
+
+
+def step_seq(C: torch.Tensor, n: torch.Tensor, m: torch.Tensor, q: torch.Tensor, k: torch.Tensor,
+             v: torch.Tensor, igate_pre: torch.Tensor, fgate_pre: torch.Tensor,
+             o: Optional[torch.Tensor] = None, *, h: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """L recurrent steps per head in one call (``mlstm_step_seq``).  The state
+    C [B,H,d_v,d_qk], n [B,H,d_qk], m [B,H] (fp32) is updated in place; q, k
+    [B,H,L,d_qk], v, o [B,H,L,d_v] share one dtype; igate_pre, fgate_pre
+    [B,H,L] fp32.  Returns h [B,H,L,d_v]."""
+    lib = library()
+    if C.dim() != 4 or q.dim() != 4:
+        raise ValueError("C must be [B,H,d_v,d_qk] and q [B,H,L,d_qk]")
+    B, H, dv, dqk = C.shape
+    L = q.shape[2]
+    dev = C.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    _need(C, "C", (B, H, dv, dqk), torch.float32, dev)
+    _need(n, "n", (B, H, dqk), torch.float32, dev)
+    _need(m, "m", (B, H), torch.float32, dev)
+    _need(q, "q", (B, H, L, dqk), q.dtype, dev)
+    _need(k, "k", (B, H, L, dqk), q.dtype, dev)
+    _need(v, "v", (B, H, L, dv), q.dtype, dev)
+    if o is not None:
+        _need(o, "o", (B, H, L, dv), q.dtype, dev)
+    _need(igate_pre, "igate_pre", (B, H, L), torch.float32, dev)
+    _need(fgate_pre, "fgate_pre", (B, H, L), torch.float32, dev)
+    if h is None:
+        h = torch.empty((B, H, L, dv), dtype=q.dtype, device=dev)
+    _need(h, "h", (B, H, L, dv), q.dtype, dev)
+    rc = lib.mlstm_step_seq(_ptr(C), _ptr(n), _ptr(m), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(igate_pre),
+                            _ptr(fgate_pre), _ptr(h), B, H, L, dqk, dv, _DTYPES[q.dtype], _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_step_seq")
     return h
 
 

@@ -207,6 +207,24 @@ int mlstm_step(float* C, float* n, float* m, const void* q, const void* k, const
   return launch_step(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
 }
 
+int mlstm_step_seq(float* C, float* n, float* m, const void* q, const void* k, const void* v, const void* o,
+                   const float* igate_pre, const float* fgate_pre, void* h, int B, int H, int L, int d_qk,
+                   int d_v, int dtype, void* stream) {
+  if (B < 0 || H < 0 || L < 0) return MLSTM_EINVAL;
+  if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512 || d_qk % 8 != 0) return MLSTM_EINVAL;
+  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
+  const long long BH = (long long)B * H;
+  if (BH > (1LL << 28) || BH * (long long)L > (1LL << 40)) return MLSTM_EINVAL;
+  if (BH == 0 || L == 0) return MLSTM_OK;
+  if (!C || !n || !m || !q || !k || !v || !igate_pre || !fgate_pre || !h) return MLSTM_EINVAL;
+  if (!aligned16(C) || !aligned16(n) || !aligned16(q) || !aligned16(k)) return MLSTM_EALIGN;
+  StepArgs a;
+  a.C = C; a.n = n; a.m = m; a.q = q; a.k = k; a.v = v; a.o = o; a.ig = igate_pre; a.fg = fgate_pre;
+  a.h = h; a.BH = (int)BH; a.dqk = d_qk; a.dv = d_v; a.dtype = dtype;
+  a.scale = (float)(1.0 / sqrt((double)d_qk));
+  return launch_step_seq(a, L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
+}
+
 int mlstm_last_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLSTM_ECUDA;
   int* status = nullptr;

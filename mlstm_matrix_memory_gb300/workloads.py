@@ -130,6 +130,26 @@ def step_inputs(w: StepWorkload, seed: int = 0, *, B: Optional[int] = None,
     return dict(C=C, n=n, m=m, q=q, k=k, v=v, o=o, igate_pre=ig, fgate_pre=fg)
 
 
+def step_seq_inputs(w: StepWorkload, L: int, seed: int = 0, *, B: Optional[int] = None,
+                    H: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Like ``step_inputs`` with a token axis of length L: state C, n, m as
+    there; q, k [B,H,L,d_qk], v, o [B,H,L,d_v] in ``w.dtype`` ~ N(0,1);
+    igate_pre, fgate_pre [B,H,L] fp32."""
+    B = w.B if B is None else B
+    H = w.H if H is None else H
+    g = torch.Generator().manual_seed(seed)
+    C = _normal(g, (B, H, w.d_v, w.d_qk), 0.0, w.state_std)
+    n = _normal(g, (B, H, w.d_qk), 0.0, w.state_std)
+    m = _normal(g, (B, H), 0.0, w.state_std)
+    q = _normal(g, (B, H, L, w.d_qk), 0.0, 1.0).to(w.dtype)
+    k = _normal(g, (B, H, L, w.d_qk), 0.0, 1.0).to(w.dtype)
+    v = _normal(g, (B, H, L, w.d_v), 0.0, 1.0).to(w.dtype)
+    o = _normal(g, (B, H, L, w.d_v), 0.0, 1.0).to(w.dtype)
+    ig = _normal(g, (B, H, L), w.ig_mean, w.ig_std)
+    fg = _normal(g, (B, H, L), w.fg_mean, w.fg_std)
+    return dict(C=C, n=n, m=m, q=q, k=k, v=v, o=o, igate_pre=ig, fgate_pre=fg)
+
+
 def sequence_inputs(B: int, H: int, T: int, d_qk: int, d_v: int, dtype: torch.dtype,
                     seed: int = 0, ig=(0.0, 1.0), fg=(3.0, 1.0), qkv_std: float = 1.0,
                     with_ogate: bool = False) -> Dict[str, torch.Tensor]:

@@ -136,6 +136,20 @@ def recurrent_unstabilized(q, k, v, ig, fg, og=None, *, nthreads: int = 0, mutat
     return h
 
 
+def step_seq(C, n, m, q, k, v, ig, fg, o=None, *, nthreads: int = 0, mutation: int = 0):
+    """L consecutive stabilized steps on copies of the given state: ``step``
+    applied to tokens t = 0..L-1 in order (q, k [B,H,L,d_qk], v, o [B,H,L,d_v],
+    ig, fg [B,H,L]).  Returns (h [B,H,L,d_v], C, n, m) after the last token."""
+    C, n, m = f64(C).copy(), f64(n).copy(), f64(m).copy()
+    q, k, v, ig, fg, o = map(f64, (q, k, v, ig, fg, o))
+    B, H, L, _ = q.shape
+    h = np.empty((B, H, L, v.shape[-1]))
+    for t in range(L):
+        h[:, :, t], C, n, m = step(C, n, m, q[:, :, t], k[:, :, t], v[:, :, t], ig[:, :, t], fg[:, :, t],
+                                   None if o is None else o[:, :, t], nthreads=nthreads, mutation=mutation)
+    return h, C, n, m
+
+
 def step(C, n, m, q, k, v, ig, fg, o=None, *, nthreads: int = 0, mutation: int = 0):
     """One stabilized recurrent step on copies of the given state.
     Returns (h, C_new, n_new, m_new); the inputs are not modified."""
