@@ -116,6 +116,26 @@ int mlstm_parallel_fwd_gated(const void *q, const void *k, const void *v,
                              const void *workspace, size_t workspace_bytes, int algo,
                              void *stream);
 
+/* The recurrent state after the last token of each sequence, from the gate
+ * terms of the parallel pass: the hand-off from a parallel prefill to
+ * mlstm_step / mlstm_step_seq.  Unrolling the stabilized recurrence (part
+ * 28/30 eqs 59-70) from C = 0, n = 0, m = -inf over t = 1..T gives
+ *   m = m_T (the last row's max of eq 80),
+ *   C = sum_j D'_Tj v_j (k_j/sqrt(d_qk))^T,   n = sum_j D'_Tj k_j/sqrt(d_qk),
+ * where D'_Tj = exp(D~_Tj - m_T) is the last row of the stabilized gate
+ * matrix of eq (81); (C, n) are stored times exp(-m) as mlstm_step expects.
+ *
+ *   k          [B,H,T,d_qk] dtype,  v [B,H,T,d_v] dtype (the same as passed
+ *              to the parallel forward)
+ *   workspace  the gate terms of the same B, H, T, as left by
+ *              mlstm_gate_prep, mlstm_parallel_fwd or mlstm_parallel_fwd_ex
+ *   C          [B,H,d_v,d_qk] fp32 out,  n [B,H,d_qk] fp32 out,  m [B,H] fp32 out
+ * Requirements as for mlstm_parallel_fwd_gated (T >= 1).  The outputs are
+ * overwritten; they may not alias k, v or the workspace. */
+int mlstm_parallel_final_state(const void *k, const void *v, const void *workspace, size_t workspace_bytes,
+                               float *C, float *n, float *m, int B, int H, int T, int d_qk, int d_v,
+                               int dtype, void *stream);
+
 /* One stabilized recurrent mLSTM step for every head, the generation step
  * (the recurrence differentiated by part 28/30 eqs 59-70, output gate eq 27):
  *   m'  = max(log sigmoid(f~) + m, i~)

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     parallel_fwd_workspace_bytes,
     step,
     step_seq,
+    parallel_final_state,
     last_device_status,
     set_spin_limit,
     gate_prep,

@@ -62,6 +62,8 @@ def library() -> ctypes.CDLL:
         lib.mlstm_step.restype = i
         lib.mlstm_step_seq.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.mlstm_step_seq.restype = i
+        lib.mlstm_parallel_final_state.argtypes = [vp, vp, vp, sz, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.mlstm_parallel_final_state.restype = i
         lib.mlstm_last_device_status.argtypes = [vp]
         lib.mlstm_last_device_status.restype = i
         lib.mlstm_set_spin_limit.argtypes = [ll]
@@ -187,6 +189,33 @@ def step(C: torch.Tensor, n: torch.Tensor, m: torch.Tensor, q: torch.Tensor, k: 
     if rc != 0:
         raise MlstmError(rc, "mlstm_step")
     return h
+
+
+def parallel_final_state(k: torch.Tensor, v: torch.Tensor, workspace: torch.Tensor):
+    """The recurrent state (C [B,H,d_v,d_qk], n [B,H,d_qk], m [B,H], fp32) after
+    the last token of k [B,H,T,d_qk], v [B,H,T,d_v], from the gate terms that
+    ``gate_prep`` or ``parallel_fwd(..., workspace=...)`` left in ``workspace``:
+    the hand-off from a parallel prefill to ``step`` / ``step_seq``."""
+    lib = library()
+    if k.dim() != 4 or v.dim() != 4:
+        raise ValueError("k and v must be [B,H,T,d]")
+    B, H, T, dqk = k.shape
+    dv = v.shape[-1]
+    dev = k.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if k.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {k.dtype}")
+    _need(k, "k", (B, H, T, dqk), k.dtype, dev)
+    _need(v, "v", (B, H, T, dv), k.dtype, dev)
+    C = torch.empty((B, H, dv, dqk), dtype=torch.float32, device=dev)
+    n = torch.empty((B, H, dqk), dtype=torch.float32, device=dev)
+    m = torch.empty((B, H), dtype=torch.float32, device=dev)
+    rc = lib.mlstm_parallel_final_state(_ptr(k), _ptr(v), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _ptr(C), _ptr(n), _ptr(m), B, H, T, dqk, dv, _DTYPES[k.dtype], _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_parallel_final_state")
+    return C, n, m
 
 
 def step_seq(C: torch.Tensor, n: torch.Tensor, m: torch.Tensor, q: torch.Tensor, k: torch.Tensor,

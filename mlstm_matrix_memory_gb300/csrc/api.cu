@@ -189,6 +189,25 @@ int mlstm_parallel_fwd(const void* q, const void* k, const void* v, const float*
                                workspace, workspace_bytes, MLSTM_ALGO_AUTO, stream);
 }
 
+int mlstm_parallel_final_state(const void* k, const void* v, const void* workspace, size_t workspace_bytes,
+                               float* C, float* n, float* m, int B, int H, int T, int d_qk, int d_v, int dtype,
+                               void* stream) {
+  int rc = check_sizes(B, H, T);
+  if (rc != MLSTM_OK) return rc;
+  if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
+  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
+  const long long BH = (long long)B * H, BHT = BH * T;
+  if (BH == 0) return MLSTM_OK;
+  if (T < 1) return MLSTM_EINVAL;
+  if (!k || !v || !C || !n || !m) return MLSTM_EINVAL;
+  if (!workspace || workspace_bytes < mlstm_parallel_fwd_workspace(B, H, T)) return MLSTM_EWORKSPACE;
+  if (!aligned16(workspace)) return MLSTM_EALIGN;
+  return launch_final_state(k, v, carve(workspace, BHT), C, n, m, (int)BH, T, d_qk, d_v, dtype,
+                            (float)(1.0 / sqrt((double)d_qk)), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLSTM_OK
+             : MLSTM_ECUDA;
+}
+
 int mlstm_step(float* C, float* n, float* m, const void* q, const void* k, const void* v, const void* o,
                const float* igate_pre, const float* fgate_pre, void* h, int B, int H, int d_qk, int d_v,
                int dtype, void* stream) {

@@ -63,6 +63,9 @@ int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream);   // returns a Status
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
 // L steps per head; q/k/v/o/gates/h carry a token axis of length L.
 cudaError_t launch_step_seq(const StepArgs& a, int L, cudaStream_t stream);
+// (C, n, m) after the last token, from the gate terms of the whole sequence.
+cudaError_t launch_final_state(const void* k, const void* v, GateTerms g, float* C, float* n, float* m, int BH,
+                               int T, int dqk, int dv, int dtype, float scale, cudaStream_t stream);
 
 // CTA-pair (cta_group::2) variant of the tensor-core forward (fwd_tc2.cu).
 bool fwd_tc2_supported(int dqk, int dv);
