@@ -130,8 +130,9 @@ int mlstm_parallel_fwd_gated(const void *q, const void *k, const void *v,
  *   workspace  the gate terms of the same B, H, T, as left by
  *              mlstm_gate_prep, mlstm_parallel_fwd or mlstm_parallel_fwd_ex
  *   C          [B,H,d_v,d_qk] fp32 out,  n [B,H,d_qk] fp32 out,  m [B,H] fp32 out
- * Requirements as for mlstm_parallel_fwd_gated (T >= 1).  The outputs are
- * overwritten; they may not alias k, v or the workspace. */
+ * Requirements as for mlstm_parallel_fwd_gated (T >= 1), and C, n 16-byte
+ * aligned.  The outputs are overwritten; they may not alias k, v or the
+ * workspace. */
 int mlstm_parallel_final_state(const void *k, const void *v, const void *workspace, size_t workspace_bytes,
                                float *C, float *n, float *m, int B, int H, int T, int d_qk, int d_v,
                                int dtype, void *stream);

@@ -200,10 +200,16 @@ int mlstm_parallel_final_state(const void* k, const void* v, const void* workspa
   if (BH == 0) return MLSTM_OK;
   if (T < 1) return MLSTM_EINVAL;
   if (!k || !v || !C || !n || !m) return MLSTM_EINVAL;
+  if (!aligned16(C) || !aligned16(n) || !aligned16(k) || !aligned16(v)) return MLSTM_EALIGN;
   if (!workspace || workspace_bytes < mlstm_parallel_fwd_workspace(B, H, T)) return MLSTM_EWORKSPACE;
   if (!aligned16(workspace)) return MLSTM_EALIGN;
+  int* status = nullptr;
+  if (status_ptr(&status) != kOk) return MLSTM_ECUDA;
+  DevStatus st;
+  st.word = status;
+  st.spin_limit = g_spin_limit.load();
   return launch_final_state(k, v, carve(workspace, BHT), C, n, m, (int)BH, T, d_qk, d_v, dtype,
-                            (float)(1.0 / sqrt((double)d_qk)), static_cast<cudaStream_t>(stream)) == cudaSuccess
+                            (float)(1.0 / sqrt((double)d_qk)), st, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLSTM_OK
              : MLSTM_ECUDA;
 }

@@ -549,14 +549,14 @@ int launch_ns(const FwdArgs& a, const Plan& pl, const CUtensorMap& mq, const CUt
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }
 
+}  // namespace
+
 int device_is_sm100_family() {
   int dev = 0, major = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
   return major == 10;
 }
-
-}  // namespace
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

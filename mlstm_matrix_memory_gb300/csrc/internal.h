@@ -65,7 +65,9 @@ cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_step_seq(const StepArgs& a, int L, cudaStream_t stream);
 // (C, n, m) after the last token, from the gate terms of the whole sequence.
 cudaError_t launch_final_state(const void* k, const void* v, GateTerms g, float* C, float* n, float* m, int BH,
-                               int T, int dqk, int dv, int dtype, float scale, cudaStream_t stream);
+                               int T, int dqk, int dv, int dtype, float scale, DevStatus st, cudaStream_t stream);
+// 1 when the current device runs tcgen05 code (sm_100 family).
+int device_is_sm100_family();
 
 // CTA-pair (cta_group::2) variant of the tensor-core forward (fwd_tc2.cu).
 bool fwd_tc2_supported(int dqk, int dv);
