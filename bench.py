@@ -308,6 +308,64 @@ def time_step(M, steps, warmup):
     return ms, nbytes, w
 
 
+def time_step_seq(M, reps, L=64):
+    """L recurrent steps per head in one call (recurrent prefill), B=256, H=4,
+    d=512: the state is read and written once per call."""
+    w = W.STEP
+    xd = {k: v.cuda() for k, v in W.step_seq_inputs(w, L, 0).items()}
+    h = torch.empty((w.B, w.H, L, w.d_v), dtype=w.dtype, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one():
+        M.step_seq(xd["C"], xd["n"], xd["m"], xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"],
+                   xd["o"], h=h)
+
+    for _ in range(2):
+        one()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for i in range(reps):
+        ev[i][0].record(stream)
+        one()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    flops = 4.0 * w.B * w.H * L * w.d_v * w.d_qk          # rank-one update + C q per token
+    return ms, flops, w, L
+
+
+def time_final_state(M, w, xd, reps):
+    """The parallel-to-recurrent hand-off on the parallel workload: (C, n, m)
+    after the last token from the gate terms; 2 T d_qk d_v flops per head."""
+    ws_buf = torch.empty(M.parallel_fwd_workspace_bytes(w.B, w.H, w.T), dtype=torch.uint8, device="cuda")
+    M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws_buf)
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        M.parallel_final_state(xd["k"], xd["v"], ws_buf)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for i in range(reps):
+        ev[i][0].record(stream)
+        M.parallel_final_state(xd["k"], xd["v"], ws_buf)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return ms, 2.0 * w.B * w.H * w.T * w.d_qk * w.d_v
+
+
+def fp32_alu_peak_tflops():
+    """FP32 FMA peak of the CUDA cores: SMs x 128 lanes x 2 flops x the
+    maximum SM clock from MEASURED_PEAKS.json (else 2070 MHz)."""
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except Exception:
+        pass
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, sms, mhz
+
+
 def profile_once(args):
     """One warm-up and one profiled launch of a single kernel (small, L2-exceeding case)."""
     import mlstm_matrix_memory_gb300 as M
@@ -365,9 +423,12 @@ def main():
     t_fwd = max_over_ranks(statistics.mean(fwd_ms), ws)
     e2e_ms, h2d, d2h = time_e2e(M, w, xh, algo, max(5, args.steps // 5), 2)
     e2e_ms = max_over_ranks(e2e_ms, ws)
-    rec = None
+    rec = seq = fs = None
     if not args.no_step:
         rec = time_step(M, max(10, args.steps // 2), 3)
+        seq = time_step_seq(M, 5)
+    if algo == "tc":
+        fs = time_final_state(M, w, xd, 10)
     clk = clocks.stop() if clocks else None
 
     flops = w.causal_flops
@@ -405,6 +466,23 @@ def main():
                                                "unit": "GB/s", "frac": gbs / peak_bw,
                                                "peak_source": f"{src} copy bandwidth",
                                                "traffic": kernel_traffic("step_" + sw.name)}}
+    if seq is not None:
+        ms, fl, sw, L = seq
+        tf = fl / (ms * 1e-3) / 1e12
+        alu_peak, sms, mhz = fp32_alu_peak_tflops()
+        line["recurrent_prefill"] = {"workload": f"{sw.name}_L{L}", "tokens_per_call": L, "ms": ms,
+                                     "tokens_per_s": sw.B * L / (ms * 1e-3),
+                                     "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak,
+                                                  "unit": "TFLOP/s", "frac": tf / alu_peak,
+                                                  "peak_source": f"FP32 FMA: {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz",
+                                                  "traffic": None}}
+    if fs is not None:
+        ms, fl = fs
+        tf = fl / (ms * 1e-3) / 1e12
+        line["final_state"] = {"workload": w.name, "ms": ms,
+                               "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+                                            "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
+                                            "traffic": None}}
     if clk:
         line["clocks"] = clk
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
