@@ -140,10 +140,12 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
+  __shared__ int s_issued_s;                // global key tile of the last fully issued S product
   __shared__ int last_par_s[kMaxSlots];
   __shared__ int q_par_s;
   __shared__ float bpart[2 * kBM];
   volatile int* abort = &abort_flag;
+  volatile int* s_issued = &s_issued_s;
   volatile int* last_par = last_par_s;      // parity of each granule's last fill, -1 if never filled
   volatile int* q_par = &q_par_s;           // parity of the last Q fill, -1 if none
 
@@ -172,6 +174,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   if (threadIdx.x == 0) {
     abort_flag = 0;
     q_par_s = -1;
+    s_issued_s = -1;
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
     for (int b = 0; b < 2; ++b) {
@@ -308,6 +311,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
           }
           if (!ok) break;
           mma_commit_pair_mc(bar(kBarSFull + buf), 0x3);
+          *s_issued = gt;
           TRACE2(3, j);
         }
         // this item's Q may be replaced once its S products complete
@@ -337,6 +341,12 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
               next();
             } else {
               for (int q = 2 * e; q < min(2 * e + 2, nch); ++q) {
+                // within an item, the tile's last (narrow) chunk waits until the
+                // next S product is issued: queued behind it, it keeps the pipe
+                // busy while the gating warps hand the S buffer back (bounded)
+                if (q == nch - 1 && nch > 1 && j + 1 < it.nkv)
+                  for (long long w2 = 0; *s_issued < gt + 1 && w2 < spin && !*abort; ++w2) {
+                  }
                 ok = full(st);
                 if (!ok) break;
                 issue_o(tmem + 128 * q, dP, dV + (uint64_t)(st * (kSlotBytes >> 4)), idO, j == 0);
@@ -353,6 +363,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       }
       ++qi;
     }
+    if (s_role) *s_issued = 0x7fffffff;     // no further S products
     // every MMA this thread issued has completed before TMEM is released
     const int drain = kBarDrain + (s_role ? 0 : 1);
     mma_commit_pair(bar(drain));
