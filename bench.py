@@ -251,20 +251,18 @@ def time_parallel(M, w, xd, algo, steps, warmup, flush):
 
 
 def time_e2e(M, w, xh, algo, steps, warmup):
-    """Through the public API with host buffers: pinned H2D of the step's
-    inputs, both kernels, D2H of h, all inside the timed region."""
+    """Through the public host-buffer call (``mlstm_parallel_fwd_host``): the
+    step's inputs in pinned host memory, h returned to pinned host memory,
+    uploads, compute and downloads overlapped by chunks of heads inside the
+    call, all inside the timed region."""
     stream = torch.cuda.current_stream()
-    dev = {k: torch.empty_like(v, device="cuda") for k, v in xh.items()}
+    xp = {k: v.pin_memory() for k, v in xh.items()}
     h_host = torch.empty((w.B, w.H, w.T, w.d_v), dtype=w.dtype).pin_memory()
-    h = torch.empty_like(h_host, device="cuda")
-    ws = torch.empty(M.parallel_fwd_workspace_bytes(w.B, w.H, w.T), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(M.parallel_fwd_host_workspace_bytes(w.B, w.H, w.T, w.d_qk, w.d_v, w.dtype),
+                     dtype=torch.uint8, device="cuda")
 
     def one():
-        for k in dev:
-            dev[k].copy_(xh[k], non_blocking=True)
-        M.parallel_fwd(dev["q"], dev["k"], dev["v"], dev["igate_pre"], dev["fgate_pre"], h=h, workspace=ws,
-                       algo=algo)
-        h_host.copy_(h, non_blocking=True)
+        M.parallel_fwd_host(xp["q"], xp["k"], xp["v"], xp["igate_pre"], xp["fgate_pre"], h=h_host, workspace=ws)
 
     for _ in range(warmup):
         one()

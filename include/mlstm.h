@@ -137,6 +137,31 @@ int mlstm_parallel_final_state(const void *k, const void *v, const void *workspa
                                float *C, float *n, float *m, int B, int H, int T, int d_qk, int d_v,
                                int dtype, void *stream);
 
+/* mlstm_parallel_fwd on inputs and an output in host memory: the call a
+ * caller makes whose tensors live on the CPU side.  The heads are processed
+ * in up to 8 chunks; each chunk's upload, its forward pass and its download
+ * overlap with those of its neighbours (two library-owned copy streams plus
+ * `stream` for the compute, two device buffers per operand in `workspace`).
+ * Results are identical to mlstm_parallel_fwd on the same data.
+ *
+ *   q, k, v, igate_pre, fgate_pre, h   as in mlstm_parallel_fwd, but host
+ *              pointers.  Page-locked memory (cudaHostAlloc, cudaHostRegister)
+ *              lets the copies run asynchronously and overlap; pageable
+ *              memory is correct but serialises them.
+ *   workspace  device memory of mlstm_parallel_fwd_host_workspace(...) bytes,
+ *              256-byte aligned, owned by the caller; no two calls that may
+ *              run at the same time may share it.
+ * The call returns once everything is queued; `stream` completes when h is
+ * in host memory (synchronise `stream` before reading h).  The library's copy
+ * streams and events are created on the first call on each device and kept;
+ * calls from several host threads are serialised while they queue work. */
+size_t mlstm_parallel_fwd_host_workspace(int B, int H, int T, int d_qk, int d_v, int dtype);
+
+int mlstm_parallel_fwd_host(const void *q, const void *k, const void *v,
+                            const float *igate_pre, const float *fgate_pre, void *h,
+                            int B, int H, int T, int d_qk, int d_v, int dtype,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
 /* One stabilized recurrent mLSTM step for every head, the generation step
  * (the recurrence differentiated by part 28/30 eqs 59-70, output gate eq 27):
  *   m'  = max(log sigmoid(f~) + m, i~)

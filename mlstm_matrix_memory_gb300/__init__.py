@@ -13,6 +13,8 @@ from .binding import (  # noqa: F401
     step,
     step_seq,
     parallel_final_state,
+    parallel_fwd_host,
+    parallel_fwd_host_workspace_bytes,
     last_device_status,
     set_spin_limit,
     gate_prep,

@@ -64,6 +64,10 @@ def library() -> ctypes.CDLL:
         lib.mlstm_step_seq.restype = i
         lib.mlstm_parallel_final_state.argtypes = [vp, vp, vp, sz, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.mlstm_parallel_final_state.restype = i
+        lib.mlstm_parallel_fwd_host_workspace.argtypes = [i, i, i, i, i, i]
+        lib.mlstm_parallel_fwd_host_workspace.restype = sz
+        lib.mlstm_parallel_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
+        lib.mlstm_parallel_fwd_host.restype = i
         lib.mlstm_last_device_status.argtypes = [vp]
         lib.mlstm_last_device_status.restype = i
         lib.mlstm_set_spin_limit.argtypes = [ll]
@@ -188,6 +192,47 @@ def step(C: torch.Tensor, n: torch.Tensor, m: torch.Tensor, q: torch.Tensor, k: 
                         _ptr(fgate_pre), _ptr(h), B, H, dqk, dv, _DTYPES[q.dtype], _stream(dev))
     if rc != 0:
         raise MlstmError(rc, "mlstm_step")
+    return h
+
+
+def parallel_fwd_host_workspace_bytes(B: int, H: int, T: int, d_qk: int, d_v: int, dtype: torch.dtype) -> int:
+    return int(library().mlstm_parallel_fwd_host_workspace(B, H, T, d_qk, d_v, _DTYPES[dtype]))
+
+
+def parallel_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: torch.Tensor,
+                      fgate_pre: torch.Tensor, *, h: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, device=None) -> torch.Tensor:
+    """``mlstm_parallel_fwd_host``: the parallel forward on CPU tensors (pin
+    them for overlapped copies), computed on ``device`` (default: current CUDA
+    device) in chunks of heads whose uploads, compute and downloads overlap.
+    Returns h on the CPU; the current stream completes when h is written."""
+    lib = library()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (igate_pre, "igate_pre"), (fgate_pre, "fgate_pre")):
+        if t.device.type != "cpu":
+            raise ValueError(f"{name} must be a CPU tensor")
+    B, H, T, dqk = q.shape
+    dv = v.shape[-1]
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    cpu = torch.device("cpu")
+    _need(q, "q", (B, H, T, dqk), q.dtype, cpu)
+    _need(k, "k", (B, H, T, dqk), q.dtype, cpu)
+    _need(v, "v", (B, H, T, dv), q.dtype, cpu)
+    _need(igate_pre, "igate_pre", (B, H, T), torch.float32, cpu)
+    _need(fgate_pre, "fgate_pre", (B, H, T), torch.float32, cpu)
+    if h is None:
+        h = torch.empty((B, H, T, dv), dtype=q.dtype, pin_memory=q.is_pinned())
+    _need(h, "h", (B, H, T, dv), q.dtype, cpu)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    need = parallel_fwd_host_workspace_bytes(B, H, T, dqk, dv, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError("workspace too small")
+    rc = lib.mlstm_parallel_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(h),
+                                     B, H, T, dqk, dv, _DTYPES[q.dtype], _ptr(workspace), need, _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_parallel_fwd_host")
     return h
 
 
