@@ -92,3 +92,45 @@ def test_spin_limit_roundtrip(lib):
     old = lib.mlstm_set_spin_limit(5)
     assert lib.mlstm_set_spin_limit(0) == 5
     lib.mlstm_set_spin_limit(old)
+
+
+def test_step_seq_validation(lib):
+    def seq(C=A, n=A, m=A, q=A, k=A, v=A, o=None, ig=A, fg=A, h=A, B=2, H=2, L=4, dqk=64, dv=64, dt=1):
+        return lib.mlstm_step_seq(C, n, m, q, k, v, o, ig, fg, h, B, H, L, dqk, dv, dt, None)
+    assert seq(L=-1) == -1
+    assert seq(dqk=20) == -1
+    assert seq(dv=0) == -1
+    assert seq(dt=5) == -3
+    assert seq(n=A + 4) == -2
+    assert seq(k=0) == -1
+    assert seq(L=0) == 0                      # an empty run leaves the state as it is
+    assert seq(B=0) == 0
+
+
+def test_final_state_validation(lib):
+    def fs(k=A, v=A, ws=A, wsb=1 << 20, C=A, n=A, m=A, B=1, H=2, T=16, dqk=64, dv=64, dt=1):
+        return lib.mlstm_parallel_final_state(k, v, ws, wsb, C, n, m, B, H, T, dqk, dv, dt, None)
+    assert fs(dqk=0) == -1
+    assert fs(dt=2) == -3
+    assert fs(T=0) == -1                      # a state after no tokens is not defined here
+    assert fs(C=A + 4) == -2
+    assert fs(ws=0) == -7
+    assert fs(wsb=64) == -7
+    assert fs(m=0) == -1
+    assert fs(B=0) == 0
+
+
+def test_host_call_validation(lib):
+    assert lib.mlstm_parallel_fwd_host_workspace(0, 1, 8, 64, 64, 1) == 0
+    assert lib.mlstm_parallel_fwd_host_workspace(1, 1, 8, 64, 64, 9) == 0
+    need = lib.mlstm_parallel_fwd_host_workspace(2, 3, 100, 64, 64, 1)
+    assert need >= 2 * 100 * (4 * 64 * 2)     # two slots of one head's q, k, v and h at least (6 chunks of 1 head)
+
+    def host(ws=A, wsb=need, B=2, H=3, T=100, dqk=64, dv=64, dt=1, q=A):
+        return lib.mlstm_parallel_fwd_host(q, A, A, A, A, A, B, H, T, dqk, dv, dt, ws, wsb, None)
+    assert host(dqk=600) == -1
+    assert host(dt=4) == -3
+    assert host(wsb=need - 1) == -7
+    assert host(ws=A + 16) == -2              # the workspace must be 256-byte aligned
+    assert host(q=0) == -1
+    assert host(T=0) == 0
