@@ -34,7 +34,8 @@ def _lib(mutation: int = 0) -> ctypes.CDLL:
         lib.oracle_step.argtypes = [i, i, i, i, p, p, p, p, p, p, p, p, p, p, i]
         lib.oracle_recurrent_stabilized.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, i]
         lib.oracle_recurrent_unstabilized.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, i]
-        for f in ("oracle_parallel_stabilized", "oracle_parallel_rows",
+        lib.oracle_parallel_backward.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, p, i]
+        for f in ("oracle_parallel_stabilized", "oracle_parallel_rows", "oracle_parallel_backward",
                   "oracle_parallel_unstabilized", "oracle_step",
                   "oracle_recurrent_stabilized", "oracle_recurrent_unstabilized",
                   "oracle_mutation", "oracle_max_threads"):
@@ -134,6 +135,24 @@ def recurrent_unstabilized(q, k, v, ig, fg, og=None, *, nthreads: int = 0, mutat
                                                         _p(fg), _p(og), _p(h), nthreads),
            "recurrent_unstabilized")
     return h
+
+
+def parallel_backward(q, k, v, ig, fg, dh, *, nthreads: int = 0, mutation: int = 0):
+    """Gradients of the stabilized parallel forward (no output gate) for the
+    output gradient dh = dL/dH~ [B,H,T,d_v]: returns (dq, dk, dv, d_igate,
+    d_fgate) in fp64, following part 28/30 eqs (87)-(105)."""
+    q, k, v, ig, fg, dh = map(f64, (q, k, v, ig, fg, dh))
+    B, H, T, dqk = q.shape
+    dv = v.shape[-1]
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dvv = np.empty_like(v)
+    dig = np.empty((B, H, T))
+    dfg = np.empty((B, H, T))
+    _check(_lib(mutation).oracle_parallel_backward(B, H, T, dqk, dv, _p(q), _p(k), _p(v), _p(ig), _p(fg), _p(dh),
+                                                   _p(dq), _p(dk), _p(dvv), _p(dig), _p(dfg), nthreads),
+           "parallel_backward")
+    return dq, dk, dvv, dig, dfg
 
 
 def step_seq(C, n, m, q, k, v, ig, fg, o=None, *, nthreads: int = 0, mutation: int = 0):

@@ -428,3 +428,154 @@ int oracle_recurrent_unstabilized(int B, int H, int T, int dqk, int dv,
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Stabilized parallel BACKWARD for one head, part 28/30 "Parallel mLSTM
+ * Backward Pass", eqs (87)-(105), evaluated literally with dense T x T
+ * matrices (the forward quantities of eqs (79)-(84) are recomputed first).
+ * Given dH~ = dL/dH~ [T, dv], it returns dQ, dK [T, dqk], dV [T, dv] and the
+ * pre-activation gradients d i~, d f~ [T].  The pages treat the stabilizer m
+ * as a constant (its gradients cancel), and so does this routine.
+ * Readings (the printed equations are garbled in places):
+ *  - eq (90) prints sign(n); the derivative of n = max(|b|, e^-m) with
+ *    respect to b is sign(b) where |b| exceeds the floor, so sign(b) is used;
+ *  - eq (93): delta_{C~',B} is the delta_{C~',b} of eq (92);
+ *  - eq (100): C is the normalised matrix C~' (.) (n^-1 1^T) of eq (85);
+ *  - eq (105): the vector is d i~ = [d i~_1 .. d i~_T] (printed "S").
+ * Matrix entries above the diagonal are zero (D' = 0 there) and are skipped.
+ * Scratch: 5 T*T doubles + 4 T.
+ */
+static void backward_head(int T, int dqk, int dv, const double *q, const double *k,
+                          const double *v, const double *ig, const double *fg, const double *dh,
+                          double *dq, double *dk, double *dvv, double *dig, double *dfg,
+                          double *S, double *Dp, double *Ct, double *dC, double *dDt,
+                          double *m, double *b, double *n, double *rs)
+{
+    const double s = key_scale(dqk);
+    /* forward recompute: D~ (eqs 79, 101), m (80), D' (81), C~' (82), b (83), n (84) */
+    for (int i = 0; i < T; ++i) {
+        double fbar = 0.0, mi = -INFINITY;
+        for (int j = i; j >= 0; --j) {
+            if (j < i) fbar += log_sigmoid(fg[j + 1]);
+            Dp[(size_t)i * T + j] = fbar + ig[j];                 /* D~ for now */
+            if (Dp[(size_t)i * T + j] > mi) mi = Dp[(size_t)i * T + j];
+        }
+        m[i] = mi;
+        double bi = 0.0;
+        for (int j = 0; j <= i; ++j) {
+            double qk = 0.0;
+            for (int c = 0; c < dqk; ++c) qk += q[(size_t)i * dqk + c] * k[(size_t)j * dqk + c];
+            S[(size_t)i * T + j] = qk * s;                        /* Q K^T / sqrt(d) */
+            Dp[(size_t)i * T + j] = exp(Dp[(size_t)i * T + j] - mi);
+            Ct[(size_t)i * T + j] = S[(size_t)i * T + j] * Dp[(size_t)i * T + j];
+            bi += Ct[(size_t)i * T + j];
+        }
+        b[i] = bi;
+        n[i] = fmax(fabs(bi), exp(-mi));
+    }
+    for (int i = 0; i < T; ++i) {
+        /* eq (87): dC = dH~ V^T */
+        for (int j = 0; j <= i; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < dv; ++c) acc += dh[(size_t)i * dv + c] * v[(size_t)j * dv + c];
+            dC[(size_t)i * T + j] = acc;
+        }
+        /* eq (89): dn = -((C~' (.) dC) 1) (.) n^-2 */
+        double r = 0.0;
+        for (int j = 0; j <= i; ++j) r += Ct[(size_t)i * T + j] * dC[(size_t)i * T + j];
+        const double dn = -r / (n[i] * n[i]);
+        /* eq (90): db = sign(b) (.) dn where |b| > exp(-m) */
+#if ORACLE_MUTATION == 9
+        const double db = fabs(b[i]) > exp(-m[i]) ? dn : 0.0;   /* mutation: sign(n) taken literally */
+#else
+        const double db = fabs(b[i]) > exp(-m[i]) ? (b[i] > 0 ? dn : (b[i] < 0 ? -dn : 0.0)) : 0.0;
+#endif
+        for (int j = 0; j <= i; ++j) {
+            /* eqs (91)-(93): dC~' = dC / n + db, both broadcast along the row */
+#if ORACLE_MUTATION == 10
+            const double dct = dC[(size_t)i * T + j] / n[i];         /* mutation: eq (92) term dropped */
+#else
+            const double dct = dC[(size_t)i * T + j] / n[i] + db;
+#endif
+            const double ddp = S[(size_t)i * T + j] * dct;        /* eq (94) */
+            dDt[(size_t)i * T + j] = Dp[(size_t)i * T + j] * ddp; /* eq (95) */
+            dC[(size_t)i * T + j] = Dp[(size_t)i * T + j] * dct;  /* D' (.) dC~', kept for (98)-(99) */
+        }
+    }
+    /* eq (98): dQ = (D' (.) dC~') K / sqrt(d) */
+    for (int i = 0; i < T; ++i)
+        for (int c = 0; c < dqk; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j <= i; ++j) acc += dC[(size_t)i * T + j] * k[(size_t)j * dqk + c];
+            dq[(size_t)i * dqk + c] = acc * s;
+        }
+    /* eq (99): dK = (D' (.) dC~')^T Q / sqrt(d) */
+    for (int j = 0; j < T; ++j)
+        for (int c = 0; c < dqk; ++c) {
+            double acc = 0.0;
+#if ORACLE_MUTATION == 12
+            for (int i = j; i < T; ++i) acc += dC[(size_t)i * T + j] * k[(size_t)i * dqk + c];  /* mutation: K for Q */
+#else
+            for (int i = j; i < T; ++i) acc += dC[(size_t)i * T + j] * q[(size_t)i * dqk + c];
+#endif
+            dk[(size_t)j * dqk + c] = acc * s;
+        }
+    /* eq (100): dV = C^T dH~ with C = C~' (.) (n^-1 1^T) */
+    for (int j = 0; j < T; ++j)
+        for (int c = 0; c < dv; ++c) {
+            double acc = 0.0;
+            for (int i = j; i < T; ++i) acc += Ct[(size_t)i * T + j] / n[i] * dh[(size_t)i * dv + c];
+            dvv[(size_t)j * dv + c] = acc;
+        }
+    /* eqs (96), (102)-(103): dFbar = dD~; d fbar_k = sum_{j<k} sum_{i>=k} dFbar_ij;
+     * d f~_k = sigma(-f~_k) d fbar_k */
+    for (int kk = 0; kk < T; ++kk) {
+        double acc = 0.0;
+        for (int i = kk; i < T; ++i)
+#if ORACLE_MUTATION == 11
+            for (int j = 0; j <= kk && j <= i; ++j) acc += dDt[(size_t)i * T + j];   /* mutation: j <= k */
+#else
+            for (int j = 0; j < kk; ++j) acc += dDt[(size_t)i * T + j];
+#endif
+        rs[kk] = acc;
+        dfg[kk] = sigmoid(-fg[kk]) * acc;
+    }
+    /* eqs (97), (105): dI = dD~; d i~_k = sum_{i>=k} dI_ik */
+    for (int kk = 0; kk < T; ++kk) {
+        double acc = 0.0;
+        for (int i = kk; i < T; ++i) acc += dDt[(size_t)i * T + kk];
+        dig[kk] = acc;
+    }
+}
+
+int oracle_parallel_backward(int B, int H, int T, int dqk, int dv,
+                             const double *q, const double *k, const double *v,
+                             const double *ig, const double *fg, const double *dh,
+                             double *dq, double *dk, double *dvv, double *dig, double *dfg, int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
+    set_threads(nthreads);
+    const long BH = (long)B * H;
+    const size_t TT = (size_t)(T > 0 ? T : 1) * (size_t)(T > 0 ? T : 1);
+    int fail = 0;
+#pragma omp parallel
+    {
+        double *buf = (double *)malloc(sizeof(double) * (5 * TT + 4 * (size_t)(T > 0 ? T : 1)));
+        if (!buf) {
+#pragma omp atomic write
+            fail = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < BH; ++bh) {
+            if (!buf) continue;
+            double *S = buf, *Dp = S + TT, *Ct = Dp + TT, *dC = Ct + TT, *dDt = dC + TT;
+            double *m = dDt + TT, *b = m + T, *n = b + T, *rs = n + T;
+            backward_head(T, dqk, dv, q + (size_t)bh * T * dqk, k + (size_t)bh * T * dqk, v + (size_t)bh * T * dv,
+                          ig + (size_t)bh * T, fg + (size_t)bh * T, dh + (size_t)bh * T * dv,
+                          dq + (size_t)bh * T * dqk, dk + (size_t)bh * T * dqk, dvv + (size_t)bh * T * dv,
+                          dig + (size_t)bh * T, dfg + (size_t)bh * T, S, Dp, Ct, dC, dDt, m, b, n, rs);
+        }
+        free(buf);
+    }
+    return fail ? -2 : 0;
+}

@@ -236,4 +236,26 @@ def pin_brute_force_dense(mutation=0):
     _close(h[0, 0], want, TOL, "dense brute force")
 
 
+def pin_backward_finite_differences(mutation=0):
+    """Every gradient of eqs (87)-(105) equals the central finite difference of
+    the (unmutated) forward, for L = sum(dH (.) H~), on a case with negative
+    row sums and floored rows."""
+    # seed 9: three rows with b < 0 above the floor and four rows on the floor
+    x = W.sequence_inputs(1, 1, 8, 3, 4, torch.float64, seed=9, ig=(-2.0, 1.5), fg=(0.5, 1.0))
+    dh = np.random.default_rng(9).standard_normal((1, 1, 8, 4))
+    got = dict(zip(("q", "k", "v", "igate_pre", "fgate_pre"),
+                   oracle.parallel_backward(*_args(x), dh, mutation=mutation)))
+    base = {k: oracle.f64(v) for k, v in x.items()}
+    eps = 1e-6
+    for name, g in got.items():
+        num = np.zeros_like(base[name])
+        for idx in range(num.size):
+            for sgn in (1.0, -1.0):
+                y = {k: v.copy() for k, v in base.items()}
+                y[name].reshape(-1)[idx] += sgn * eps
+                hh, _, _ = oracle.parallel_stabilized(*_args(y))
+                num.reshape(-1)[idx] += sgn * float(np.sum(hh * dh)) / (2 * eps)
+        _close(g, num, 1e-6, f"backward d{name} vs finite differences")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

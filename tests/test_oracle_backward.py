@@ -1,0 +1,65 @@
+"""Pins of the oracle's parallel backward (part 28/30 eqs 87-105).
+
+The backward is checked against central finite differences of the oracle's
+own stabilized forward, in fp64, on small random inputs: for the scalar
+L = sum(dH (.) H~(q, k, v, i~, f~)), every printed gradient must equal the
+numerical derivative of L.  A dropped term, a wrong sign or index, or a
+transposed operand anywhere in eqs (87)-(105) fails this.  The floor case
+(|b| below exp(-m), where eq (90) zeroes db) is covered by the second case.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mlstm_matrix_memory_gb300 import workloads as W
+
+
+def loss(x, dh):
+    h, _, _ = oracle.parallel_stabilized(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"])
+    return float(np.sum(h * dh))
+
+
+def numeric_grad(x, dh, name, eps=1e-6):
+    base = {k: oracle.f64(v) for k, v in x.items()}
+    g = np.zeros_like(base[name])
+    flat = g.reshape(-1)
+    for idx in range(flat.size):
+        for sgn in (1.0, -1.0):
+            y = {k: v.copy() for k, v in base.items()}
+            y[name].reshape(-1)[idx] += sgn * eps
+            flat[idx] += sgn * loss(y, dh) / (2 * eps)
+    return g
+
+
+@pytest.mark.parametrize("case", [
+    dict(T=7, d=4, ig=(0.0, 1.0), fg=(3.0, 1.0), seed=1),       # |b| above the floor almost everywhere
+    dict(T=9, d=3, ig=(-4.0, 0.5), fg=(0.0, 1.0), seed=2),      # small input gates: the floor engages on some rows
+])
+def test_backward_equals_finite_differences(case):
+    x = W.sequence_inputs(1, 1, case["T"], case["d"], case["d"] + 1, torch.float64, seed=case["seed"],
+                          ig=case["ig"], fg=case["fg"])
+    dh = np.random.default_rng(case["seed"]).standard_normal((1, 1, case["T"], case["d"] + 1))
+    dq, dk, dv, dig, dfg = oracle.parallel_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh)
+    got = {"q": dq, "k": dk, "v": dv, "igate_pre": dig, "fgate_pre": dfg}
+    for name, g in got.items():
+        num = numeric_grad(x, dh, name)
+        scale = max(1e-12, float(np.max(np.abs(num))))
+        assert np.max(np.abs(g - num)) <= 1e-6 * scale, name
+
+
+def test_backward_floor_case_reaches_the_floor():
+    """The second case above really has rows on the floor (|b| < exp(-m))."""
+    x = W.sequence_inputs(1, 1, 9, 3, 4, torch.float64, seed=2, ig=(-4.0, 0.5), fg=(0.0, 1.0))
+    h, m, n = oracle.parallel_stabilized(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"])
+    assert np.any(np.isclose(n, np.exp(-m), rtol=0, atol=0))
+
+
+def test_backward_heads_are_independent():
+    x = W.sequence_inputs(2, 2, 6, 4, 5, torch.float64, seed=4)
+    dh = np.random.default_rng(4).standard_normal((2, 2, 6, 5))
+    full = oracle.parallel_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh)
+    one = oracle.parallel_backward(*(t[1:2, 0:1] for t in (x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"])),
+                                   dh[1:2, 0:1])
+    for a, b in zip(full, one):
+        assert np.array_equal(a[1:2, 0:1], b)
