@@ -162,6 +162,29 @@ int mlstm_parallel_fwd_host(const void *q, const void *k, const void *v,
                             int B, int H, int T, int d_qk, int d_v, int dtype,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/* Backward pass of mlstm_parallel_fwd (part 28/30 eqs 87-105): given the
+ * output gradient dh = dL/dH~, the gradients of q, k, v and of the gate
+ * pre-activations.  The stabilizer m is held constant, as on the pages (its
+ * gradients cancel); eq (90) is read with sign(b), the derivative of |b|.
+ *
+ *   q, k, v, igate_pre, fgate_pre   the forward's inputs (layouts as there)
+ *   dh         [B,H,T,d_v]  dtype: dL/dH~
+ *   dq, dk     [B,H,T,d_qk] dtype out,   dv [B,H,T,d_v] dtype out
+ *   d_igate, d_fgate  [B,H,T] fp32 out
+ *   workspace  mlstm_parallel_bwd_workspace(B,H,T,dtype) bytes of device
+ *              memory, 256-byte aligned: it holds four T x T matrices per head
+ *              (fp32 S and dL/dC, the dtype's G and P), so it grows as B*H*T^2
+ *              (about 1.6 GB for B=8, H=4, T=2048, bf16).
+ * Requirements: 1 <= T <= 16384; 1 <= d_qk, d_v <= 512; no output may alias
+ * an input.  The five T x T products run as batched GEMMs (cuBLAS). */
+size_t mlstm_parallel_bwd_workspace(int B, int H, int T, int dtype);
+
+int mlstm_parallel_bwd(const void *q, const void *k, const void *v,
+                       const float *igate_pre, const float *fgate_pre, const void *dh,
+                       void *dq, void *dk, void *dv, float *d_igate, float *d_fgate,
+                       int B, int H, int T, int d_qk, int d_v, int dtype,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
 /* One stabilized recurrent mLSTM step for every head, the generation step
  * (the recurrence differentiated by part 28/30 eqs 59-70, output gate eq 27):
  *   m'  = max(log sigmoid(f~) + m, i~)

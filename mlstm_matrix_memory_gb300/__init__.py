@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     step,
     step_seq,
     parallel_final_state,
+    parallel_bwd,
     parallel_fwd_host,
     parallel_fwd_host_workspace_bytes,
     last_device_status,

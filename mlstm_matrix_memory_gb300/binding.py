@@ -68,6 +68,10 @@ def library() -> ctypes.CDLL:
         lib.mlstm_parallel_fwd_host_workspace.restype = sz
         lib.mlstm_parallel_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
         lib.mlstm_parallel_fwd_host.restype = i
+        lib.mlstm_parallel_bwd_workspace.argtypes = [i, i, i, i]
+        lib.mlstm_parallel_bwd_workspace.restype = sz
+        lib.mlstm_parallel_bwd.argtypes = [vp] * 11 + [i] * 6 + [vp, sz, vp]
+        lib.mlstm_parallel_bwd.restype = i
         lib.mlstm_last_device_status.argtypes = [vp]
         lib.mlstm_last_device_status.restype = i
         lib.mlstm_set_spin_limit.argtypes = [ll]
@@ -234,6 +238,37 @@ def parallel_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_p
     if rc != 0:
         raise MlstmError(rc, "mlstm_parallel_fwd_host")
     return h
+
+
+def parallel_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: torch.Tensor,
+                 fgate_pre: torch.Tensor, dh: torch.Tensor, *, workspace: Optional[torch.Tensor] = None):
+    """``mlstm_parallel_bwd``: gradients (dq, dk, dv, d_igate, d_fgate) of the
+    parallel forward for the output gradient dh = dL/dH~ (CUDA tensors)."""
+    lib = library()
+    B, H, T, dqk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    _need(q, "q", (B, H, T, dqk), q.dtype, dev)
+    _need(k, "k", (B, H, T, dqk), q.dtype, dev)
+    _need(v, "v", (B, H, T, dv), q.dtype, dev)
+    _need(igate_pre, "igate_pre", (B, H, T), torch.float32, dev)
+    _need(fgate_pre, "fgate_pre", (B, H, T), torch.float32, dev)
+    _need(dh, "dh", (B, H, T, dv), q.dtype, dev)
+    need = int(lib.mlstm_parallel_bwd_workspace(B, H, T, _DTYPES[q.dtype]))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dig, dfg = torch.empty_like(igate_pre), torch.empty_like(fgate_pre)
+    rc = lib.mlstm_parallel_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh), _ptr(dq),
+                                _ptr(dk), _ptr(dvv), _ptr(dig), _ptr(dfg), B, H, T, dqk, dv, _DTYPES[q.dtype],
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_parallel_bwd")
+    return dq, dk, dvv, dig, dfg
 
 
 def parallel_final_state(k: torch.Tensor, v: torch.Tensor, workspace: torch.Tensor):

@@ -1,0 +1,44 @@
+"""GPU parity of the parallel backward (mlstm_parallel_bwd) against the fp64
+oracle's eqs (87)-(105), each gradient within the forward's tolerances
+(relative to its own largest entry)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TOL_BF16, TOL_F32, rel_err
+from mlstm_matrix_memory_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    import mlstm_matrix_memory_gb300 as M
+    M.library()
+    return M
+
+
+# (B, H, T, d_qk, d_v, dtype, input-gate, forget-gate distributions)
+CASES = [
+    (1, 1, 64, 16, 16, torch.float32, (0.0, 1.0), (3.0, 1.0)),
+    (2, 2, 130, 64, 48, torch.float32, (-2.0, 1.5), (0.5, 1.0)),     # floored rows and negative row sums
+    (1, 2, 300, 64, 64, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),
+    (1, 1, 777, 128, 96, torch.bfloat16, (0.0, 2.0), (5.0, 1.0)),     # long-memory gates
+    (1, 1, 2048, 384, 384, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),   # one head of the 125M-scale layer
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(str(v) for v in c[:5]) + f"-{c[5]}")
+def test_bwd_matches_oracle(M, case):
+    B, H, T, dqk, dv, dtype, ig, fg = case
+    x = W.sequence_inputs(B, H, T, dqk, dv, dtype, seed=T + dv, ig=ig, fg=fg)
+    dh = torch.randn((B, H, T, dv), generator=torch.Generator().manual_seed(T)).to(dtype)
+    xd = {k: v.cuda() for k, v in x.items()}
+    got = M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh.cuda())
+    torch.cuda.synchronize()
+    assert M.last_device_status() == 0
+    want = oracle.parallel_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    for name, g, w in zip(("dq", "dk", "dv", "d_igate", "d_fgate"), got, want):
+        assert rel_err(g, w) <= tol, name
