@@ -351,6 +351,32 @@ def time_final_state(M, w, xd, reps):
     return ms, 2.0 * w.B * w.H * w.T * w.d_qk * w.d_v
 
 
+def time_backward(M, w, xd, reps):
+    """The parallel backward on the parallel workload for a seeded output
+    gradient: algorithmic work T^2 (3 d_qk + 2 d_v) flops per head (the five
+    causal products S, dC, dQ, dK, dV)."""
+    lib = M.library()
+    dh = torch.randn((w.B, w.H, w.T, w.d_v), generator=torch.Generator().manual_seed(1)).to(w.dtype).cuda()
+    ws_buf = torch.empty(int(lib.mlstm_parallel_bwd_workspace(w.B, w.H, w.T, 1 if w.dtype == torch.bfloat16 else 0)),
+                         dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one():
+        M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh, workspace=ws_buf)
+
+    for _ in range(2):
+        one()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for i in range(reps):
+        ev[i][0].record(stream)
+        one()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return ms, float(w.B * w.H * w.T * w.T * (3 * w.d_qk + 2 * w.d_v)), ws_buf.numel()
+
+
 def fp32_alu_peak_tflops():
     """FP32 FMA peak of the CUDA cores: SMs x 128 lanes x 2 flops x the
     maximum SM clock from MEASURED_PEAKS.json (else 2070 MHz)."""
@@ -425,8 +451,10 @@ def main():
     if not args.no_step:
         rec = time_step(M, max(10, args.steps // 2), 3)
         seq = time_step_seq(M, 5)
+    bwd = None
     if algo == "tc":
         fs = time_final_state(M, w, xd, 10)
+        bwd = time_backward(M, w, xd, 5)
     clk = clocks.stop() if clocks else None
 
     flops = w.causal_flops
@@ -481,6 +509,13 @@ def main():
                                "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
                                             "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
                                             "traffic": None}}
+    if bwd is not None:
+        ms, fl, wsb = bwd
+        tf = fl / (ms * 1e-3) / 1e12
+        line["backward"] = {"workload": w.name, "ms": ms, "workspace_bytes": wsb,
+                            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+                                         "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
+                                         "work": "causal T^2 (3 d_qk + 2 d_v) per head", "traffic": None}}
     if clk:
         line["clocks"] = clk
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
