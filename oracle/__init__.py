@@ -35,6 +35,8 @@ def _lib(mutation: int = 0) -> ctypes.CDLL:
         lib.oracle_recurrent_stabilized.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, i]
         lib.oracle_recurrent_unstabilized.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, i]
         lib.oracle_parallel_backward.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, p, i]
+        lib.oracle_set_forget_exp.argtypes = [i]
+        lib.oracle_set_forget_exp.restype = None
         for f in ("oracle_parallel_stabilized", "oracle_parallel_rows", "oracle_parallel_backward",
                   "oracle_parallel_unstabilized", "oracle_step",
                   "oracle_recurrent_stabilized", "oracle_recurrent_unstabilized",
@@ -135,6 +137,23 @@ def recurrent_unstabilized(q, k, v, ig, fg, og=None, *, nthreads: int = 0, mutat
                                                         _p(fg), _p(og), _p(h), nthreads),
            "recurrent_unstabilized")
     return h
+
+
+class forget_exp:
+    """Within the block, every oracle routine (of the given mutation build)
+    uses the exponential forget activation log f = f~ instead of
+    log sigma(f~) ("xLSTM", part 28/30: gamma is sigma or exp)."""
+
+    def __init__(self, mutation: int = 0):
+        self.lib = _lib(mutation)
+
+    def __enter__(self):
+        self.lib.oracle_set_forget_exp(1)
+        return self
+
+    def __exit__(self, *exc):
+        self.lib.oracle_set_forget_exp(0)
+        return False
 
 
 def parallel_backward(q, k, v, ig, fg, dh, *, nthreads: int = 0, mutation: int = 0):

@@ -85,6 +85,14 @@ static double log_sigmoid(double x)
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
+/* The forget-gate activation: sigma (log f = log sigma(f~), the default the
+ * parallel form fixes in eqs 71 and 101) or exp (log f = f~; part 28/30 eq 70
+ * allows gamma = exp).  Selected for the whole library by
+ * oracle_set_forget_exp; the tests set it around a call. */
+static int g_forget_exp = 0;
+void oracle_set_forget_exp(int on) { g_forget_exp = on ? 1 : 0; }
+static double log_forget(double x) { return g_forget_exp ? x : log_sigmoid(x); }
+
 static double key_scale(int dqk)
 {
 #if ORACLE_MUTATION == 1
@@ -122,9 +130,9 @@ static void parallel_row(int T, int dqk, int dv, const double *q, const double *
     for (int j = i; j >= 0; --j) {
         if (j < i) {
 #if ORACLE_MUTATION == 4
-            fbar += log_sigmoid(fg[j]);          /* mutation: sum starts at k=j */
+            fbar += log_forget(fg[j]);           /* mutation: sum starts at k=j */
 #else
-            fbar += log_sigmoid(fg[j + 1]);
+            fbar += log_forget(fg[j + 1]);
 #endif
         }
         dt[j] = fbar + ig[j];       /* eq (79): D~ = Fbar + I~, I~_ij = i~_j (eq 72) */
@@ -258,7 +266,7 @@ int oracle_parallel_unstabilized(int B, int H, int T, int dqk, int dv,
                 double rowsum = 0.0;
                 for (int j = 0; j <= i; ++j) {
                     double F = 1.0;                             /* eq (71) */
-                    for (int kk = j + 1; kk <= i; ++kk) F *= exp(log_sigmoid(fgh[kk]));
+                    for (int kk = j + 1; kk <= i; ++kk) F *= exp(log_forget(fgh[kk]));
                     double D = F * exp(igh[j]);                 /* eq (73) */
                     double qk = 0.0;
                     for (int c = 0; c < dqk; ++c) qk += qh[(size_t)i * dqk + c] * kh[(size_t)j * dqk + c];
@@ -295,7 +303,7 @@ static void step_head(int dqk, int dv, double *C, double *n, double *m,
                       double igv, double fgv, const double *og, double *h)
 {
     const double s = key_scale(dqk);
-    const double lf = log_sigmoid(fgv);
+    const double lf = log_forget(fgv);
     double m_prev = *m;
 #if ORACLE_MUTATION == 2
     if (isinf(m_prev) && m_prev < 0) m_prev = 0.0;   /* mutation: m_0 = 0 */
@@ -404,7 +412,7 @@ int oracle_recurrent_unstabilized(int B, int H, int T, int dqk, int dv,
             for (int t = 0; t < T; ++t) {
                 size_t ti = (size_t)bh * T + t;
                 const double *qt = q + ti * dqk, *kt = k + ti * dqk, *vt = v + ti * dv;
-                const double f = exp(log_sigmoid(fg[ti])), i = exp(ig[ti]);
+                const double f = exp(log_forget(fg[ti])), i = exp(ig[ti]);
                 double nq = 0.0;
                 for (int c = 0; c < dqk; ++c) {
                     n[c] = f * n[c] + i * kt[c] * s;
@@ -456,7 +464,7 @@ static void backward_head(int T, int dqk, int dv, const double *q, const double 
     for (int i = 0; i < T; ++i) {
         double fbar = 0.0, mi = -INFINITY;
         for (int j = i; j >= 0; --j) {
-            if (j < i) fbar += log_sigmoid(fg[j + 1]);
+            if (j < i) fbar += log_forget(fg[j + 1]);
             Dp[(size_t)i * T + j] = fbar + ig[j];                 /* D~ for now */
             if (Dp[(size_t)i * T + j] > mi) mi = Dp[(size_t)i * T + j];
         }
@@ -538,7 +546,8 @@ static void backward_head(int T, int dqk, int dv, const double *q, const double 
             for (int j = 0; j < kk; ++j) acc += dDt[(size_t)i * T + j];
 #endif
         rs[kk] = acc;
-        dfg[kk] = sigmoid(-fg[kk]) * acc;
+        /* eq (103) for sigma; d f~/d fbar = 1 for the exp activation */
+        dfg[kk] = (g_forget_exp ? 1.0 : sigmoid(-fg[kk])) * acc;
     }
     /* eqs (97), (105): dI = dD~; d i~_k = sum_{i>=k} dI_ik */
     for (int kk = 0; kk < T; ++kk) {

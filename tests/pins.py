@@ -258,4 +258,25 @@ def pin_backward_finite_differences(mutation=0):
         _close(g, num, 1e-6, f"backward d{name} vs finite differences")
 
 
+def pin_forget_exp_variant(mutation=0):
+    """The exponential forget activation: with f~ = 0 it gives f = 1 exactly,
+    the same cell as the sigma activation with f~ = +inf; and its parallel and
+    recurrent forms agree (part 28/30: gamma is sigma or exp)."""
+    x = _seq(21, T=24, fg=(0.0, 1.0))
+    x0 = dict(x, fgate_pre=torch.zeros_like(x["fgate_pre"]))
+    xinf = dict(x, fgate_pre=torch.full_like(x["fgate_pre"], math.inf))
+    with oracle.forget_exp(mutation):
+        h_exp, _, _ = oracle.parallel_stabilized(*_args(x0), mutation=mutation)
+        hp, _, _ = oracle.parallel_stabilized(*_args(x), mutation=mutation)
+        hr, _, _, _ = oracle.recurrent_stabilized(*_args(x), mutation=mutation)
+        hu = oracle.parallel_unstabilized(*_args(x), mutation=mutation)
+    h_sig, _, _ = oracle.parallel_stabilized(*_args(xinf), mutation=mutation)
+    _close(h_exp, h_sig, TOL, "exp forget with f~=0 equals sigma forget with f~=+inf")
+    _close(hp, hr, 1e-10, "exp forget: parallel equals recurrent")
+    _close(hp, hu, 1e-10, "exp forget: stabilized equals unstabilized")
+    # the exp variant really differs from sigma on generic f~
+    h_sig_x, _, _ = oracle.parallel_stabilized(*_args(x), mutation=mutation)
+    assert _rel(hp, h_sig_x) > 1e-3, "exp forget indistinguishable from sigma forget"
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -63,3 +63,14 @@ def test_backward_heads_are_independent():
                                    dh[1:2, 0:1])
     for a, b in zip(full, one):
         assert np.array_equal(a[1:2, 0:1], b)
+
+
+def test_backward_exp_forget_equals_finite_differences():
+    """With the exponential forget activation, d f~ = d fbar (eq 103 without the sigma factor)."""
+    x = W.sequence_inputs(1, 1, 7, 3, 4, torch.float64, seed=11, ig=(0.0, 1.0), fg=(0.0, 0.5))
+    dh = np.random.default_rng(11).standard_normal((1, 1, 7, 4))
+    with oracle.forget_exp():
+        got = oracle.parallel_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh)
+        for name, g in zip(("q", "k", "v", "igate_pre", "fgate_pre"), got):
+            num = numeric_grad(x, dh, name)
+            assert np.max(np.abs(g - num)) <= 1e-6 * max(1e-12, float(np.max(np.abs(num)))), name
