@@ -162,6 +162,44 @@ int mlstm_parallel_fwd_host(const void *q, const void *k, const void *v,
                             int B, int H, int T, int d_qk, int d_v, int dtype,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/* Options of the *_opt entry points; a zero-initialised struct (or a NULL
+ * pointer) gives the behaviour of the plain entry points.
+ *   algo        MLSTM_ALGO_* (the parallel forward; ignored elsewhere)
+ *   forget_exp  0: forget gate f = sigmoid(f~), log f = log sigmoid(f~) (the
+ *               form the parallel equations fix, part 28/30 eqs 71, 101);
+ *               1: f = exp(f~), log f = f~ (part 28/30 eq 70: the activation
+ *               may be sigma or exp).
+ *   ogate_pre   the parallel forward only: [B,H,T,d_v] dtype output-gate
+ *               pre-activations, 16-byte aligned, or NULL.  When given, h =
+ *               sigmoid(ogate_pre) (.) H~ (eq 78) instead of H~ (eq 77); the
+ *               CTA-pair kernel applies it in its epilogue, the other kernels
+ *               in a separate elementwise pass. */
+typedef struct {
+    int algo;
+    int forget_exp;
+    const void *ogate_pre;
+} mlstm_options;
+
+int mlstm_parallel_fwd_opt(const void *q, const void *k, const void *v,
+                           const float *igate_pre, const float *fgate_pre,
+                           void *h, float *m_out, float *n_out,
+                           int B, int H, int T, int d_qk, int d_v, int dtype,
+                           void *workspace, size_t workspace_bytes,
+                           const mlstm_options *opt, void *stream);
+
+/* mlstm_gate_prep with options (forget_exp); the gate terms then serve
+ * mlstm_parallel_fwd_gated and mlstm_parallel_final_state as usual. */
+int mlstm_gate_prep_opt(const float *igate_pre, const float *fgate_pre, int B, int H, int T,
+                        void *workspace, size_t workspace_bytes, const mlstm_options *opt,
+                        void *stream);
+
+/* mlstm_step_seq with options (forget_exp); L = 1 is one mlstm_step. */
+int mlstm_step_seq_opt(float *C, float *n, float *m,
+                       const void *q, const void *k, const void *v, const void *o,
+                       const float *igate_pre, const float *fgate_pre, void *h,
+                       int B, int H, int L, int d_qk, int d_v, int dtype,
+                       const mlstm_options *opt, void *stream);
+
 /* Backward pass of mlstm_parallel_fwd (part 28/30 eqs 87-105): given the
  * output gradient dh = dL/dH~, the gradients of q, k, v and of the gate
  * pre-activations.  The stabilizer m is held constant, as on the pages (its

@@ -72,6 +72,13 @@ def library() -> ctypes.CDLL:
         lib.mlstm_parallel_bwd_workspace.restype = sz
         lib.mlstm_parallel_bwd.argtypes = [vp] * 11 + [i] * 6 + [vp, sz, vp]
         lib.mlstm_parallel_bwd.restype = i
+        op = ctypes.POINTER(_Options)
+        lib.mlstm_parallel_fwd_opt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, op, vp]
+        lib.mlstm_parallel_fwd_opt.restype = i
+        lib.mlstm_gate_prep_opt.argtypes = [vp, vp, i, i, i, vp, sz, op, vp]
+        lib.mlstm_gate_prep_opt.restype = i
+        lib.mlstm_step_seq_opt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, op, vp]
+        lib.mlstm_step_seq_opt.restype = i
         lib.mlstm_last_device_status.argtypes = [vp]
         lib.mlstm_last_device_status.restype = i
         lib.mlstm_set_spin_limit.argtypes = [ll]
@@ -89,6 +96,20 @@ def status_str(code: int) -> str:
         return library().mlstm_status_str(int(code)).decode()
     except Exception:
         return "unknown status"
+
+
+class _Options(ctypes.Structure):
+    """``mlstm_options`` of include/mlstm.h."""
+    _fields_ = [("algo", ctypes.c_int), ("forget_exp", ctypes.c_int), ("ogate_pre", ctypes.c_void_p)]
+
+
+FORGET = {"sigmoid": 0, "exp": 1}
+
+
+def _options(algo: str = "auto", forget: str = "sigmoid", ogate: Optional[torch.Tensor] = None) -> _Options:
+    if forget not in FORGET:
+        raise ValueError(f"forget must be one of {sorted(FORGET)}")
+    return _Options(ALGOS[algo], FORGET[forget], None if ogate is None else ogate.data_ptr())
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -119,13 +140,16 @@ def parallel_fwd_workspace_bytes(B: int, H: int, T: int) -> int:
 def parallel_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: torch.Tensor,
                  fgate_pre: torch.Tensor, *, h: Optional[torch.Tensor] = None,
                  return_mn: bool = False, workspace: Optional[torch.Tensor] = None,
-                 algo: str = "auto"):
-    """Stabilized parallel mLSTM forward pass (H~, no output gate).
+                 algo: str = "auto", ogate: Optional[torch.Tensor] = None, forget: str = "sigmoid"):
+    """Stabilized parallel mLSTM forward pass.
 
     q, k [B,H,T,d_qk], v [B,H,T,d_v] (fp32 or bf16, same dtype, contiguous,
     CUDA); igate_pre, fgate_pre [B,H,T] fp32.  Returns h [B,H,T,d_v] in the
-    input dtype, and with ``return_mn`` also the row stabilizer m and the
-    normalizer n, both [B,H,T] fp32.  Runs on the current stream.
+    input dtype: H~, or sigmoid(ogate) * H~ when the output-gate
+    pre-activations ``ogate`` [B,H,T,d_v] are given; ``forget`` selects the
+    forget activation ("sigmoid" or "exp").  With ``return_mn`` also the row
+    stabilizer m and the normalizer n, both [B,H,T] fp32.  Runs on the
+    current stream.
     """
     lib = library()
     if q.dim() != 4:
@@ -154,10 +178,13 @@ def parallel_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: t
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     if workspace.device != dev or workspace.numel() * workspace.element_size() < ws_bytes:
         raise ValueError(f"workspace must hold {ws_bytes} bytes on {dev}")
-    rc = lib.mlstm_parallel_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(h),
-                                   _ptr(m), _ptr(n), B, H, T, dqk, dv, _DTYPES[q.dtype],
-                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                   ALGOS[algo], _stream(dev))
+    if ogate is not None:
+        _need(ogate, "ogate", (B, H, T, dv), q.dtype, dev)
+    opt = _options(algo, forget, ogate)
+    rc = lib.mlstm_parallel_fwd_opt(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(h),
+                                    _ptr(m), _ptr(n), B, H, T, dqk, dv, _DTYPES[q.dtype],
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    ctypes.byref(opt), _stream(dev))
     if rc != 0:
         raise MlstmError(rc, "mlstm_parallel_fwd")
     return (h, m, n) if return_mn else h
@@ -300,7 +327,8 @@ def parallel_final_state(k: torch.Tensor, v: torch.Tensor, workspace: torch.Tens
 
 def step_seq(C: torch.Tensor, n: torch.Tensor, m: torch.Tensor, q: torch.Tensor, k: torch.Tensor,
              v: torch.Tensor, igate_pre: torch.Tensor, fgate_pre: torch.Tensor,
-             o: Optional[torch.Tensor] = None, *, h: Optional[torch.Tensor] = None) -> torch.Tensor:
+             o: Optional[torch.Tensor] = None, *, h: Optional[torch.Tensor] = None,
+             forget: str = "sigmoid") -> torch.Tensor:
     """L recurrent steps per head in one call (``mlstm_step_seq``).  The state
     C [B,H,d_v,d_qk], n [B,H,d_qk], m [B,H] (fp32) is updated in place; q, k
     [B,H,L,d_qk], v, o [B,H,L,d_v] share one dtype; igate_pre, fgate_pre
@@ -328,8 +356,10 @@ def step_seq(C: torch.Tensor, n: torch.Tensor, m: torch.Tensor, q: torch.Tensor,
     if h is None:
         h = torch.empty((B, H, L, dv), dtype=q.dtype, device=dev)
     _need(h, "h", (B, H, L, dv), q.dtype, dev)
-    rc = lib.mlstm_step_seq(_ptr(C), _ptr(n), _ptr(m), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(igate_pre),
-                            _ptr(fgate_pre), _ptr(h), B, H, L, dqk, dv, _DTYPES[q.dtype], _stream(dev))
+    opt = _options(forget=forget)
+    rc = lib.mlstm_step_seq_opt(_ptr(C), _ptr(n), _ptr(m), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(igate_pre),
+                                _ptr(fgate_pre), _ptr(h), B, H, L, dqk, dv, _DTYPES[q.dtype], ctypes.byref(opt),
+                                _stream(dev))
     if rc != 0:
         raise MlstmError(rc, "mlstm_step_seq")
     return h
@@ -349,16 +379,18 @@ def set_spin_limit(limit: int) -> int:
     return int(library().mlstm_set_spin_limit(int(limit)))
 
 
-def gate_prep(igate_pre: torch.Tensor, fgate_pre: torch.Tensor, workspace: torch.Tensor) -> None:
-    """Gate phase of the parallel forward (log-sigmoid prefix sums and the
+def gate_prep(igate_pre: torch.Tensor, fgate_pre: torch.Tensor, workspace: torch.Tensor,
+              forget: str = "sigmoid") -> None:
+    """Gate phase of the parallel forward (log forget-gate prefix sums and the
     prefix-max stabilizer) into ``workspace``; [B,H,T] fp32 CUDA inputs."""
     lib = library()
     B, H, T = igate_pre.shape
     dev = igate_pre.device
     _need(igate_pre, "igate_pre", (B, H, T), torch.float32, dev)
     _need(fgate_pre, "fgate_pre", (B, H, T), torch.float32, dev)
-    rc = lib.mlstm_gate_prep(_ptr(igate_pre), _ptr(fgate_pre), B, H, T, _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _stream(dev))
+    opt = _options(forget=forget)
+    rc = lib.mlstm_gate_prep_opt(_ptr(igate_pre), _ptr(fgate_pre), B, H, T, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), ctypes.byref(opt), _stream(dev))
     if rc != 0:
         raise MlstmError(rc, "mlstm_gate_prep")
 

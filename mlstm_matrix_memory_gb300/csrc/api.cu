@@ -95,8 +95,8 @@ GateTerms carve(const void* workspace, long long BHT) {
 
 }  // namespace
 
-int mlstm_gate_prep(const float* igate_pre, const float* fgate_pre, int B, int H, int T, void* workspace,
-                    size_t workspace_bytes, void* stream) {
+int mlstm_gate_prep_opt(const float* igate_pre, const float* fgate_pre, int B, int H, int T, void* workspace,
+                        size_t workspace_bytes, const mlstm_options* opt, void* stream) {
   int rc = check_sizes(B, H, T);
   if (rc != MLSTM_OK) return rc;
   const long long BH = (long long)B * H, BHT = BH * T;
@@ -104,15 +104,20 @@ int mlstm_gate_prep(const float* igate_pre, const float* fgate_pre, int B, int H
   if (!igate_pre || !fgate_pre) return MLSTM_EINVAL;
   if (!workspace || workspace_bytes < mlstm_parallel_fwd_workspace(B, H, T)) return MLSTM_EWORKSPACE;
   if (!aligned16(workspace)) return MLSTM_EALIGN;
-  return launch_gate_prep(igate_pre, fgate_pre, carve(workspace, BHT), (int)BH, T,
+  return launch_gate_prep(igate_pre, fgate_pre, carve(workspace, BHT), (int)BH, T, opt ? opt->forget_exp : 0,
                           static_cast<cudaStream_t>(stream)) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
+}
+
+int mlstm_gate_prep(const float* igate_pre, const float* fgate_pre, int B, int H, int T, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  return mlstm_gate_prep_opt(igate_pre, fgate_pre, B, H, T, workspace, workspace_bytes, nullptr, stream);
 }
 
 namespace {
 
 int fwd_gated(const void* q, const void* k, const void* v, void* h, float* m_out, float* n_out, int B, int H,
               int T, int d_qk, int d_v, int dtype, const void* workspace, size_t workspace_bytes, int algo,
-              bool after_gate_prep, void* stream) {
+              bool after_gate_prep, const void* og, void* stream) {
   int rc = check_sizes(B, H, T);
   if (rc != MLSTM_OK) return rc;
   if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
@@ -124,6 +129,7 @@ int fwd_gated(const void* q, const void* k, const void* v, void* h, float* m_out
   if (BHT == 0) return MLSTM_OK;
   if (!q || !k || !v || !h) return MLSTM_EINVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(h)) return MLSTM_EALIGN;
+  if (og && !aligned16(og)) return MLSTM_EALIGN;
   if (!workspace || workspace_bytes < mlstm_parallel_fwd_workspace(B, H, T)) return MLSTM_EWORKSPACE;
   if (!aligned16(workspace)) return MLSTM_EALIGN;
 
@@ -144,9 +150,12 @@ int fwd_gated(const void* q, const void* k, const void* v, void* h, float* m_out
   a.st.word = status;
   a.st.spin_limit = g_spin_limit.load();
   a.after_gate_prep = after_gate_prep;
+  a.og = og;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (use_tc) return launch_fwd_tc(a, s);
-  return launch_fwd_simt(a, s) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
+  if (launch_fwd_simt(a, s) != cudaSuccess) return MLSTM_ECUDA;
+  // the CUDA-core kernel does not fuse the output gate
+  return launch_apply_ogate(h, og, BHT * d_v, dtype, s) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
 }
 
 }  // namespace
@@ -155,13 +164,15 @@ int mlstm_parallel_fwd_gated(const void* q, const void* k, const void* v, void* 
                              int B, int H, int T, int d_qk, int d_v, int dtype, const void* workspace,
                              size_t workspace_bytes, int algo, void* stream) {
   return fwd_gated(q, k, v, h, m_out, n_out, B, H, T, d_qk, d_v, dtype, workspace, workspace_bytes, algo, false,
-                   stream);
+                   nullptr, stream);
 }
 
-int mlstm_parallel_fwd_ex(const void* q, const void* k, const void* v, const float* igate_pre,
-                          const float* fgate_pre, void* h, float* m_out, float* n_out, int B, int H, int T,
-                          int d_qk, int d_v, int dtype, void* workspace, size_t workspace_bytes, int algo,
-                          void* stream) {
+int mlstm_parallel_fwd_opt(const void* q, const void* k, const void* v, const float* igate_pre,
+                           const float* fgate_pre, void* h, float* m_out, float* n_out, int B, int H, int T,
+                           int d_qk, int d_v, int dtype, void* workspace, size_t workspace_bytes,
+                           const mlstm_options* opt, void* stream) {
+  const int algo = opt ? opt->algo : MLSTM_ALGO_AUTO;
+  const void* og = opt ? opt->ogate_pre : nullptr;
   int rc = check_sizes(B, H, T);
   if (rc != MLSTM_OK) return rc;
   if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
@@ -175,10 +186,20 @@ int mlstm_parallel_fwd_ex(const void* q, const void* k, const void* v, const flo
   if (!workspace || workspace_bytes < mlstm_parallel_fwd_workspace(B, H, T)) return MLSTM_EWORKSPACE;
   if (!aligned16(workspace)) return MLSTM_EALIGN;
   if (algo == MLSTM_ALGO_TC && !fwd_tc_supported(d_qk, d_v, dtype)) return MLSTM_EUNSUPPORTED;
-  rc = mlstm_gate_prep(igate_pre, fgate_pre, B, H, T, workspace, workspace_bytes, stream);
+  rc = mlstm_gate_prep_opt(igate_pre, fgate_pre, B, H, T, workspace, workspace_bytes, opt, stream);
   if (rc != MLSTM_OK) return rc;
   return fwd_gated(q, k, v, h, m_out, n_out, B, H, T, d_qk, d_v, dtype, workspace, workspace_bytes, algo, true,
-                   stream);
+                   og, stream);
+}
+
+int mlstm_parallel_fwd_ex(const void* q, const void* k, const void* v, const float* igate_pre,
+                          const float* fgate_pre, void* h, float* m_out, float* n_out, int B, int H, int T,
+                          int d_qk, int d_v, int dtype, void* workspace, size_t workspace_bytes, int algo,
+                          void* stream) {
+  mlstm_options o = {};
+  o.algo = algo;
+  return mlstm_parallel_fwd_opt(q, k, v, igate_pre, fgate_pre, h, m_out, n_out, B, H, T, d_qk, d_v, dtype,
+                                workspace, workspace_bytes, &o, stream);
 }
 
 int mlstm_parallel_fwd(const void* q, const void* k, const void* v, const float* igate_pre,
@@ -232,9 +253,9 @@ int mlstm_step(float* C, float* n, float* m, const void* q, const void* k, const
   return launch_step(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
 }
 
-int mlstm_step_seq(float* C, float* n, float* m, const void* q, const void* k, const void* v, const void* o,
-                   const float* igate_pre, const float* fgate_pre, void* h, int B, int H, int L, int d_qk,
-                   int d_v, int dtype, void* stream) {
+int mlstm_step_seq_opt(float* C, float* n, float* m, const void* q, const void* k, const void* v, const void* o,
+                       const float* igate_pre, const float* fgate_pre, void* h, int B, int H, int L, int d_qk,
+                       int d_v, int dtype, const mlstm_options* opt, void* stream) {
   if (B < 0 || H < 0 || L < 0) return MLSTM_EINVAL;
   if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512 || d_qk % 8 != 0) return MLSTM_EINVAL;
   if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
@@ -247,7 +268,15 @@ int mlstm_step_seq(float* C, float* n, float* m, const void* q, const void* k, c
   a.C = C; a.n = n; a.m = m; a.q = q; a.k = k; a.v = v; a.o = o; a.ig = igate_pre; a.fg = fgate_pre;
   a.h = h; a.BH = (int)BH; a.dqk = d_qk; a.dv = d_v; a.dtype = dtype;
   a.scale = (float)(1.0 / sqrt((double)d_qk));
+  a.forget_exp = opt ? opt->forget_exp : 0;
   return launch_step_seq(a, L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
+}
+
+int mlstm_step_seq(float* C, float* n, float* m, const void* q, const void* k, const void* v, const void* o,
+                   const float* igate_pre, const float* fgate_pre, void* h, int B, int H, int L, int d_qk,
+                   int d_v, int dtype, void* stream) {
+  return mlstm_step_seq_opt(C, n, m, q, k, v, o, igate_pre, fgate_pre, h, B, H, L, d_qk, d_v, dtype, nullptr,
+                            stream);
 }
 
 int mlstm_last_device_status(void* stream) {

@@ -624,8 +624,13 @@ int launch_fwd_tc(const FwdArgs& a, cudaStream_t stream) {
   if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, kBN) ||
       !make_map(&mv, a.v, a.dv, a.T, a.BH, pl.vk) || !make_map(&mh, a.h, a.dv, a.T, a.BH, kBM))
     return kCuda;
-  return pl.nsbuf == 1 ? launch_ns<1>(a, pl, mq, mk, mv, mh, stream)
-                       : launch_ns<2>(a, pl, mq, mk, mv, mh, stream);
+  const int rc = pl.nsbuf == 1 ? launch_ns<1>(a, pl, mq, mk, mv, mh, stream)
+                               : launch_ns<2>(a, pl, mq, mk, mv, mh, stream);
+  // this kernel does not fuse the output gate: apply it in a separate pass
+  if (rc == kOk && a.og &&
+      launch_apply_ogate(a.h, a.og, (long long)a.BH * a.T * a.dv, a.dtype, stream) != cudaSuccess)
+    return kCuda;
+  return rc;
 }
 
 }  // namespace mlstm

@@ -77,6 +77,7 @@ struct Tc2Params {
   const float* mrow;
   float* m_out;
   float* n_out;
+  const __nv_bfloat16* og;                // output-gate pre-activations (eq 78), or null
   int T, BH, dqk, dv;
   int nsplit, dv_slice, nk, nv, npairs;   // nk + nv ring granules (K ring, then V ring)
   int n_items, nclusters;                 // work items (query-row pairs x d_v splits); clusters launched
@@ -129,7 +130,9 @@ __device__ __forceinline__ bool item_at(const Tc2Params& p, int r, int c, uint32
   return true;
 }
 
-template <int NSBUF>
+// OG: the output gate is applied in the epilogue (a separate instantiation,
+// so that the kernel without it keeps its register allocation).
+template <int NSBUF, bool OG>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_h,
@@ -494,7 +497,16 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       const int cols = it.dv_cta / 2, c0 = half * cols;      // a multiple of 64
       const uint32_t stage = sP + (uint32_t)half * 16384u;
       const bool issuer = qd == 0 && lane == 0 && it.i0 < p.T;
+      const bool use_og = OG && row_ok;
       for (int ch = 0; ch < cols / 64; ++ch) {
+        // the output gate's 64 values of this row and box (eq 78), loaded
+        // while the accumulator comes out of TMEM
+        uint4 og4[OG ? 8 : 1];
+        if (OG && use_og) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.og + (hbase + i) * (size_t)p.dv + it.dv_off + c0 + 64 * ch);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) og4[g] = __ldg(src + g);
+        }
         uint32_t o[64];
         tmem_ld32(tmem + lane_addr + c0 + 64 * ch, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
         tmem_ld32(tmem + lane_addr + c0 + 64 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
@@ -507,9 +519,17 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           uint32_t w[4];
+          const uint32_t* ow = reinterpret_cast<const uint32_t*>(&og4[OG ? g : 0]);
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            w[t] = pack_bf16x2(__uint_as_float(o[8 * g + 2 * t]) * inv, __uint_as_float(o[8 * g + 2 * t + 1]) * inv);
+          for (int t = 0; t < 4; ++t) {
+            float x0 = __uint_as_float(o[8 * g + 2 * t]) * inv, x1 = __uint_as_float(o[8 * g + 2 * t + 1]) * inv;
+            if (OG && use_og) {
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[t]));
+              x0 *= sigmoid(f.x);
+              x1 *= sigmoid(f.y);
+            }
+            w[t] = pack_bf16x2(x0, x1);
+          }
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((g ^ (rl & 7)) << 4)), "r"(w[0]),
                        "r"(w[1]), "r"(w[2]), "r"(w[3])
                        : "memory");
@@ -579,7 +599,7 @@ int resident_pairs(size_t smem) {
   cudaGetDevice(&dev);
   if (last_smem == smem && last_dev == dev && last > 0) return last;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaFuncSetAttribute(fwd_tc2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaFuncSetAttribute(fwd_tc2_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
   cfg.blockDim = dim3(kThreads);
@@ -591,7 +611,7 @@ int resident_pairs(size_t smem) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&n, fwd_tc2_kernel<1>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, fwd_tc2_kernel<1, false>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = std::max(1, sms / 2);
   }
@@ -601,10 +621,10 @@ int resident_pairs(size_t smem) {
   return n;
 }
 
-template <int NSBUF>
+template <int NSBUF, bool OG>
 int launch_pair(const FwdArgs& a, const Tc2Params& p, size_t smem, const CUtensorMap& mq, const CUtensorMap& mk,
                 const CUtensorMap& mv, const CUtensorMap& mh, cudaStream_t stream) {
-  if (cudaFuncSetAttribute(fwd_tc2_kernel<NSBUF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+  if (cudaFuncSetAttribute(fwd_tc2_kernel<NSBUF, OG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return kCuda;
   const long long grid = 2LL * p.nclusters;      // persistent: each cluster loops over its items
@@ -622,7 +642,7 @@ int launch_pair(const FwdArgs& a, const Tc2Params& p, size_t smem, const CUtenso
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.after_gate_prep ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, fwd_tc2_kernel<NSBUF>, mq, mk, mv, mh, p) != cudaSuccess) return kCuda;
+  if (cudaLaunchKernelEx(&cfg, fwd_tc2_kernel<NSBUF, OG>, mq, mk, mv, mh, p) != cudaSuccess) return kCuda;
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
 }
 
@@ -640,6 +660,7 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   Tc2Params p;
   p.a2 = a.g.a2; p.p2 = a.g.p2; p.mrow = a.g.m;
   p.m_out = a.m_out; p.n_out = a.n_out;
+  p.og = static_cast<const __nv_bfloat16*>(a.og);
   p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv;
   int nsbuf;
   if (a.dv <= 256) { nsbuf = 2; p.nsplit = 1; p.dv_slice = a.dv; }
@@ -669,8 +690,11 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, 64) ||
       !make_map(&mv, a.v, a.dv, a.T, a.BH, kBN) || !make_map(&mh, a.h, a.dv, a.T, a.BH, kBM))
     return kCuda;
-  return nsbuf == 1 ? launch_pair<1>(a, p, smem, mq, mk, mv, mh, stream)
-                    : launch_pair<2>(a, p, smem, mq, mk, mv, mh, stream);
+  if (p.og)
+    return nsbuf == 1 ? launch_pair<1, true>(a, p, smem, mq, mk, mv, mh, stream)
+                      : launch_pair<2, true>(a, p, smem, mq, mk, mv, mh, stream);
+  return nsbuf == 1 ? launch_pair<1, false>(a, p, smem, mq, mk, mv, mh, stream)
+                    : launch_pair<2, false>(a, p, smem, mq, mk, mv, mh, stream);
 }
 
 }  // namespace mlstm

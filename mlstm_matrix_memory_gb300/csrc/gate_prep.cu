@@ -108,10 +108,13 @@ __device__ __forceinline__ void emit(float* a2, float* p2, float* mrow, size_t i
   mrow[idx] = pm.ig + (d.hi + d.lo);
 }
 
+// log of the forget gate: log sigmoid(f~) (default) or f~ (exponential activation)
+__device__ __forceinline__ float log_forget(float x, int forget_exp) { return forget_exp ? x : log_sigmoid(x); }
+
 template <int SEG>
 __global__ void __launch_bounds__(kThreads)
 gate_prep_kernel(const float* __restrict__ ig, const float* __restrict__ fg, float* __restrict__ a2,
-                 float* __restrict__ p2, float* __restrict__ mrow, int T) {
+                 float* __restrict__ p2, float* __restrict__ mrow, int T, int forget_exp) {
   __shared__ F2 shs[kWarps];
   __shared__ MaxRec shm[kWarps];
   // the fused kernel that follows may start its prologue (it waits for this
@@ -124,7 +127,7 @@ gate_prep_kernel(const float* __restrict__ ig, const float* __restrict__ fg, flo
 #pragma unroll
   for (int s = 0; s < SEG; ++s) {
     const int t = t0 + s;
-    lf[s] = t < T ? log_sigmoid(fg[base + t]) : 0.0f;
+    lf[s] = t < T ? log_forget(fg[base + t], forget_exp) : 0.0f;
     iv[s] = t < T ? ig[base + t] : 0.0f;
     local = add2(local, lf[s]);
   }
@@ -152,7 +155,7 @@ gate_prep_kernel(const float* __restrict__ ig, const float* __restrict__ fg, flo
 // passes over global memory.
 __global__ void __launch_bounds__(kThreads)
 gate_prep_long_kernel(const float* __restrict__ ig, const float* __restrict__ fg, float* __restrict__ a2,
-                      float* __restrict__ p2, float* __restrict__ mrow, int T) {
+                      float* __restrict__ p2, float* __restrict__ mrow, int T, int forget_exp) {
   __shared__ F2 shs[kWarps];
   __shared__ MaxRec shm[kWarps];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -160,20 +163,20 @@ gate_prep_long_kernel(const float* __restrict__ ig, const float* __restrict__ fg
   const int seg = (T + kThreads - 1) / kThreads;
   const int t0 = min(T, (int)threadIdx.x * seg), t1 = min(T, t0 + seg);
   F2 local = {0.0f, 0.0f};
-  for (int t = t0; t < t1; ++t) local = add2(local, log_sigmoid(fg[base + t]));
+  for (int t = t0; t < t1; ++t) local = add2(local, log_forget(fg[base + t], forget_exp));
   const F2 cs0 = block_exclusive(local, F2{0.0f, 0.0f}, AddF2(), shs);
   const MaxRec none = {-INFINITY, 0.0f, {0.0f, 0.0f}};
   F2 cs = cs0;
   MaxRec segmax = none;
   for (int t = t0; t < t1; ++t) {
-    cs = add2(cs, log_sigmoid(fg[base + t]));
+    cs = add2(cs, log_forget(fg[base + t], forget_exp));
     const float iv = ig[base + t];
     segmax = MaxR()(segmax, rec((iv - cs.hi) - cs.lo, iv, cs));
   }
   MaxRec pm = block_exclusive(segmax, none, MaxR(), shm);
   cs = cs0;
   for (int t = t0; t < t1; ++t) {
-    cs = add2(cs, log_sigmoid(fg[base + t]));
+    cs = add2(cs, log_forget(fg[base + t], forget_exp));
     const float iv = ig[base + t];
     const float a = (iv - cs.hi) - cs.lo;
     pm = MaxR()(pm, rec(a, iv, cs));
@@ -183,18 +186,18 @@ gate_prep_long_kernel(const float* __restrict__ ig, const float* __restrict__ fg
 
 }  // namespace
 
-cudaError_t launch_gate_prep(const float* ig, const float* fg, GateTerms g, int BH, int T,
+cudaError_t launch_gate_prep(const float* ig, const float* fg, GateTerms g, int BH, int T, int forget_exp,
                              cudaStream_t stream) {
   if (BH <= 0 || T <= 0) return cudaSuccess;
   const int seg = (T + kThreads - 1) / kThreads;
   if (seg <= 2)
-    gate_prep_kernel<2><<<BH, kThreads, 0, stream>>>(ig, fg, g.a2, g.p2, g.m, T);
+    gate_prep_kernel<2><<<BH, kThreads, 0, stream>>>(ig, fg, g.a2, g.p2, g.m, T, forget_exp);
   else if (seg <= 4)
-    gate_prep_kernel<4><<<BH, kThreads, 0, stream>>>(ig, fg, g.a2, g.p2, g.m, T);
+    gate_prep_kernel<4><<<BH, kThreads, 0, stream>>>(ig, fg, g.a2, g.p2, g.m, T, forget_exp);
   else if (seg <= kMaxSeg)
-    gate_prep_kernel<kMaxSeg><<<BH, kThreads, 0, stream>>>(ig, fg, g.a2, g.p2, g.m, T);
+    gate_prep_kernel<kMaxSeg><<<BH, kThreads, 0, stream>>>(ig, fg, g.a2, g.p2, g.m, T, forget_exp);
   else
-    gate_prep_long_kernel<<<BH, kThreads, 0, stream>>>(ig, fg, g.a2, g.p2, g.m, T);
+    gate_prep_long_kernel<<<BH, kThreads, 0, stream>>>(ig, fg, g.a2, g.p2, g.m, T, forget_exp);
   return cudaGetLastError();
 }
 

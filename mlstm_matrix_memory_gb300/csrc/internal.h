@@ -34,6 +34,7 @@ struct FwdArgs {
   int dtype;      // kF32 / kBF16
   float scale;    // 1/sqrt(dqk)
   DevStatus st;
+  const void* og = nullptr;       // output-gate pre-activations [BH,T,dv] (dtype), or null
   bool after_gate_prep = false;   // launched right after gate_prep on the same stream:
                                   // may overlap its prologue with it (programmatic
                                   // dependent launch; gate terms are read after the wait)
@@ -53,9 +54,10 @@ struct StepArgs {
   int BH, dqk, dv;
   int dtype;
   float scale;
+  int forget_exp = 0;   // 1: log f = f~ (exponential forget activation)
 };
 
-cudaError_t launch_gate_prep(const float* ig, const float* fg, GateTerms g, int BH, int T,
+cudaError_t launch_gate_prep(const float* ig, const float* fg, GateTerms g, int BH, int T, int forget_exp,
                              cudaStream_t stream);
 cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t stream);
 bool fwd_tc_supported(int dqk, int dv, int dtype);
@@ -66,6 +68,9 @@ cudaError_t launch_step_seq(const StepArgs& a, int L, cudaStream_t stream);
 // (C, n, m) after the last token, from the gate terms of the whole sequence.
 cudaError_t launch_final_state(const void* k, const void* v, GateTerms g, float* C, float* n, float* m, int BH,
                                int T, int dqk, int dv, int dtype, float scale, DevStatus st, cudaStream_t stream);
+// h *= sigmoid(o) elementwise (the output gate, eq 78), for the kernels that
+// do not apply it in their epilogue.
+cudaError_t launch_apply_ogate(void* h, const void* og, long long n, int dtype, cudaStream_t stream);
 // 1 when the current device runs tcgen05 code (sm_100 family).
 int device_is_sm100_family();
 

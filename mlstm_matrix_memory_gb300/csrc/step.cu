@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kThreads)
 step_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict__ m,
             const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
             const T* __restrict__ o, const float* __restrict__ ig, const float* __restrict__ fg,
-            T* __restrict__ h, int dqk, int dv, int R, float scale) {
+            T* __restrict__ h, int dqk, int dv, int R, float scale, int forget_exp) {
   __shared__ __align__(16) float ks[kMaxD];   // s * k
   __shared__ __align__(16) float qs[kMaxD];
   __shared__ float hs[kMaxD];                 // numerators (C_new q) of this CTA's rows
@@ -57,7 +57,7 @@ step_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict__ m,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // gate scalars (every CTA of the cluster reads the old m before the barrier)
-  const float lf = log_sigmoid(fg[bh]);
+  const float lf = forget_exp ? fg[bh] : log_sigmoid(fg[bh]);    // exponential or sigmoid forget
   const float igv = ig[bh];
   const float m_old = m[bh];
   const float m_new = fmaxf(lf + m_old, igv);
@@ -152,7 +152,8 @@ cudaError_t launch_nv(const StepArgs& a, int R, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, step_kernel<T, NV>, a.C, a.n, a.m, (const T*)a.q, (const T*)a.k,
-                            (const T*)a.v, (const T*)a.o, a.ig, a.fg, (T*)a.h, a.dqk, a.dv, R, a.scale);
+                            (const T*)a.v, (const T*)a.o, a.ig, a.fg, (T*)a.h, a.dqk, a.dv, R, a.scale,
+                            a.forget_exp);
 }
 
 template <typename T>

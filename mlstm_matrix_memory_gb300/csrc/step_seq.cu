@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict__ m,
                 const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 const T* __restrict__ o, const float* __restrict__ ig, const float* __restrict__ fg,
-                T* __restrict__ h, int L, int dqk, int dv, int R, float scale) {
+                T* __restrict__ h, int L, int dqk, int dv, int R, float scale, int forget_exp) {
   constexpr int NP = NC / 2;
   extern __shared__ __align__(16) uint8_t smem[];
   const unsigned rank = cluster_rank();
@@ -199,7 +199,7 @@ step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict_
       }
       const float vv = (lane < kRW && wrow + lane < nrows)
                            ? Elem<T>::load(b.v, (size_t)tt * kRowsPerCta + wrow + lane) : 0.0f;
-      const float lf = log_sigmoid(b.fg[tt]);
+      const float lf = forget_exp ? b.fg[tt] : log_sigmoid(b.fg[tt]);   // exponential or sigmoid forget
       const float igv = b.ig[tt];
       const float m_new = fmaxf(lf + mm, igv);
       const float fp = expf(lf + mm - m_new);
@@ -286,7 +286,8 @@ cudaError_t launch_nc(const StepArgs& a, int L, int R, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, step_seq_kernel<T, NC>, a.C, a.n, a.m, (const T*)a.q, (const T*)a.k,
-                            (const T*)a.v, (const T*)a.o, a.ig, a.fg, (T*)a.h, L, a.dqk, a.dv, R, a.scale);
+                            (const T*)a.v, (const T*)a.o, a.ig, a.fg, (T*)a.h, L, a.dqk, a.dv, R, a.scale,
+                            a.forget_exp);
 }
 
 template <typename T>
