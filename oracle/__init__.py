@@ -35,6 +35,8 @@ def _lib(mutation: int = 0) -> ctypes.CDLL:
         lib.oracle_recurrent_stabilized.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, i]
         lib.oracle_recurrent_unstabilized.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, i]
         lib.oracle_parallel_backward.argtypes = [i, i, i, i, i, p, p, p, p, p, p, p, p, p, p, p, i]
+        lib.oracle_recurrent_backward.argtypes = [i, i, i, i, i] + [p] * 13 + [i]
+        lib.oracle_recurrent_backward.restype = ctypes.c_int
         lib.oracle_set_forget_exp.argtypes = [i]
         lib.oracle_set_forget_exp.restype = None
         for f in ("oracle_parallel_stabilized", "oracle_parallel_rows", "oracle_parallel_backward",
@@ -172,6 +174,22 @@ def parallel_backward(q, k, v, ig, fg, dh, *, nthreads: int = 0, mutation: int =
                                                    _p(dq), _p(dk), _p(dvv), _p(dig), _p(dfg), nthreads),
            "parallel_backward")
     return dq, dk, dvv, dig, dfg
+
+
+def recurrent_backward(q, k, v, ig, fg, dh, og=None, *, nthreads: int = 0, mutation: int = 0):
+    """Backpropagation through time of the unstabilized recurrence (part 28/30
+    eqs 59-70) for dh = dL/dh [B,H,T,d_v]: returns (dq, dk, dv, d_igate,
+    d_fgate, d_ogate) in fp64 (d_ogate None without an output gate)."""
+    q, k, v, ig, fg, dh, og = map(f64, (q, k, v, ig, fg, dh, og))
+    B, H, T, dqk = q.shape
+    dv = v.shape[-1]
+    dq, dk, dvv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    dig, dfg = np.empty((B, H, T)), np.empty((B, H, T))
+    dog = np.empty_like(dh) if og is not None else None
+    _check(_lib(mutation).oracle_recurrent_backward(B, H, T, dqk, dv, _p(q), _p(k), _p(v), _p(ig), _p(fg), _p(og),
+                                                    _p(dh), _p(dq), _p(dk), _p(dvv), _p(dig), _p(dfg), _p(dog),
+                                                    nthreads), "recurrent_backward")
+    return dq, dk, dvv, dig, dfg, dog
 
 
 def step_seq(C, n, m, q, k, v, ig, fg, o=None, *, nthreads: int = 0, mutation: int = 0):

@@ -588,3 +588,147 @@ int oracle_parallel_backward(int B, int H, int T, int dqk, int dv,
     }
     return fail ? -2 : 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Recurrent BACKWARD (backpropagation through time) of the unstabilized
+ * recurrence, part 28/30 eqs (59)-(70):
+ *   dh~_t = o_t (.) dh_t                                              (59)
+ *   dC_{t-1}^T = f_t dC_t^T + q_{t-1} dh~_{t-1}^T / N_{t-1}             (60)
+ *   dn_{t-1} = f_t dn_t - (q_{t-1}^T C_{t-1}^T dh~_{t-1}) / N_{t-1}^2
+ *              Omega(n_{t-1}^T q_{t-1}) q_{t-1}                         (61)
+ *   dv_t^T = i_t k_t^T dC_t^T,   dk_t^T = i_t (v_t^T dC_t + dn_t^T)      (62)-(63)
+ *   dq_t = C_t^T dh~_t / N_t - (q_t^T C_t^T dh~_t) / N_t^2 Omega(n_t^T q_t) n_t   (64)
+ *   d f~_t = (1^T (C_{t-1} (.) dC_t) 1 + 1^T (n_{t-1} (.) dn_t)) gamma(f~_t)   (68)
+ *   d i~_t = (1^T ((v_t k_t^T) (.) dC_t) 1 + 1^T (k_t (.) dn_t)) exp(i~_t)     (69)
+ *   d o~_t = h~_t (.) sigma'(o~_t) (.) dh_t                               (70)
+ * with N_t = max(|n_t^T q_t|, 1), Omega(z) = Theta(z-1) - Theta(-z-1), and
+ * gamma = sigma' or exp for the sigma or exp forget activation.  Readings:
+ *  - the key enters as s k (s = 1/sqrt(d_qk), as in the forward), so the raw
+ *    key's gradient is s times the k of eq (63);
+ *  - dC_t and dn_t above are the totals flowing into step t (the eq 60/61
+ *    recursion evaluated one step later), i.e. each includes step t's own
+ *    output term.
+ * The forward states C_t, n_t of every step are kept (small cases only).
+ * og may be NULL (o_t = 1, d o~ not written).
+ */
+int oracle_recurrent_backward(int B, int H, int T, int dqk, int dv,
+                              const double *q, const double *k, const double *v,
+                              const double *ig, const double *fg, const double *og, const double *dh,
+                              double *dq, double *dk, double *dvv, double *dig, double *dfg, double *dog,
+                              int nthreads)
+{
+    if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
+    set_threads(nthreads);
+    const long BH = (long)B * H;
+    const double s = key_scale(dqk);
+    const size_t CS = (size_t)dv * dqk;
+    int fail = 0;
+#pragma omp parallel
+    {
+        /* C_t, n_t for t = -1..T-1 (index t+1), plus dC, dn, dh~, h~ */
+        double *Cs = (double *)malloc(sizeof(double) * CS * (size_t)(T + 1));
+        double *ns = (double *)malloc(sizeof(double) * (size_t)dqk * (T + 1));
+        double *dC = (double *)malloc(sizeof(double) * CS);
+        double *dn = (double *)malloc(sizeof(double) * dqk);
+        double *dht = (double *)malloc(sizeof(double) * dv);
+        double *ht = (double *)malloc(sizeof(double) * dv);
+        if (!Cs || !ns || !dC || !dn || !dht || !ht) {
+#pragma omp atomic write
+            fail = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long bh = 0; bh < BH; ++bh) {
+            if (fail) continue;
+            memset(Cs, 0, sizeof(double) * CS);          /* C_{-1} = 0 */
+            memset(ns, 0, sizeof(double) * dqk);         /* n_{-1} = 0 */
+            for (int t = 0; t < T; ++t) {                /* forward, keeping every state */
+                const size_t ti = (size_t)bh * T + t;
+                const double f = exp(log_forget(fg[ti])), i = exp(ig[ti]);
+                const double *Cp = Cs + CS * t, *np = ns + (size_t)dqk * t;
+                double *Cn = Cs + CS * (t + 1), *nn = ns + (size_t)dqk * (t + 1);
+                for (int c = 0; c < dqk; ++c) nn[c] = f * np[c] + i * s * k[ti * dqk + c];
+                for (int r = 0; r < dv; ++r)
+                    for (int c = 0; c < dqk; ++c)
+                        Cn[(size_t)r * dqk + c] = f * Cp[(size_t)r * dqk + c] + i * v[ti * dv + r] * s * k[ti * dqk + c];
+            }
+            memset(dC, 0, sizeof(double) * CS);
+            memset(dn, 0, sizeof(double) * dqk);
+            for (int t = T - 1; t >= 0; --t) {
+                const size_t ti = (size_t)bh * T + t;
+                const double *Ct = Cs + CS * (t + 1), *nt = ns + (size_t)dqk * (t + 1);
+                const double *Cp = Cs + CS * t, *np = ns + (size_t)dqk * t;
+                const double i = exp(ig[ti]);
+                double nq = 0.0;
+                for (int c = 0; c < dqk; ++c) nq += nt[c] * q[ti * dqk + c];
+                const double N = fmax(fabs(nq), 1.0);
+#if ORACLE_MUTATION == 13
+                const double omega = nq > 1.0 ? 1.0 : 0.0;      /* mutation: Omega's negative branch dropped */
+#else
+                const double omega = (nq > 1.0 ? 1.0 : 0.0) - (-nq > 1.0 ? 1.0 : 0.0);
+#endif
+                for (int r = 0; r < dv; ++r) {
+                    double acc = 0.0;
+                    for (int c = 0; c < dqk; ++c) acc += Ct[(size_t)r * dqk + c] * q[ti * dqk + c];
+                    ht[r] = acc / N;                                               /* h~_t */
+                    const double o = og ? sigmoid(og[ti * dv + r]) : 1.0;
+                    dht[r] = o * dh[ti * dv + r];                                  /* (59) */
+                    if (og) dog[ti * dv + r] = ht[r] * o * (1.0 - o) * dh[ti * dv + r];   /* (70) */
+                }
+                /* q^T C_t^T dh~_t = (C_t q)^T dh~_t */
+                double qCdh = 0.0;
+                for (int r = 0; r < dv; ++r) qCdh += ht[r] * N * dht[r];
+                /* step t's own output terms join the totals (60)-(61) */
+                for (int r = 0; r < dv; ++r)
+                    for (int c = 0; c < dqk; ++c) dC[(size_t)r * dqk + c] += dht[r] * q[ti * dqk + c] / N;
+                for (int c = 0; c < dqk; ++c) dn[c] -= qCdh / (N * N) * omega * q[ti * dqk + c];
+                /* (64) */
+                for (int c = 0; c < dqk; ++c) {
+                    double acc = 0.0;
+                    for (int r = 0; r < dv; ++r) acc += Ct[(size_t)r * dqk + c] * dht[r];
+                    dq[ti * dqk + c] = acc / N - qCdh / (N * N) * omega * nt[c];
+                }
+                /* (62), (63) with the s of the key */
+                for (int r = 0; r < dv; ++r) {
+                    double acc = 0.0;
+                    for (int c = 0; c < dqk; ++c) acc += dC[(size_t)r * dqk + c] * s * k[ti * dqk + c];
+                    dvv[ti * dv + r] = i * acc;
+                }
+                for (int c = 0; c < dqk; ++c) {
+                    double acc = 0.0;
+                    for (int r = 0; r < dv; ++r) acc += v[ti * dv + r] * dC[(size_t)r * dqk + c];
+                    dk[ti * dqk + c] = s * i * (acc + dn[c]);
+                }
+                /* (68), (69) */
+                double sf = 0.0, si = 0.0;
+                for (int r = 0; r < dv; ++r)
+                    for (int c = 0; c < dqk; ++c) {
+                        sf += Cp[(size_t)r * dqk + c] * dC[(size_t)r * dqk + c];
+                        si += v[ti * dv + r] * s * k[ti * dqk + c] * dC[(size_t)r * dqk + c];
+                    }
+                for (int c = 0; c < dqk; ++c) {
+                    sf += np[c] * dn[c];
+                    si += s * k[ti * dqk + c] * dn[c];
+                }
+                const double x = fg[ti];
+#if ORACLE_MUTATION == 14
+                const double gamma = g_forget_exp ? exp(x) : sigmoid(x);   /* mutation: sigma for sigma' */
+#else
+                const double gamma = g_forget_exp ? exp(x) : sigmoid(x) * (1.0 - sigmoid(x));
+#endif
+                dfg[ti] = sf * gamma;
+                dig[ti] = si * i;
+                /* carry to step t-1: multiply by f_t (60)-(61) */
+                const double f = exp(log_forget(fg[ti]));
+                for (size_t e = 0; e < CS; ++e) dC[e] *= f;
+                for (int c = 0; c < dqk; ++c) dn[c] *= f;
+            }
+        }
+        free(Cs);
+        free(ns);
+        free(dC);
+        free(dn);
+        free(dht);
+        free(ht);
+    }
+    return fail ? -2 : 0;
+}

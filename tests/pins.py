@@ -258,6 +258,47 @@ def pin_backward_finite_differences(mutation=0):
         _close(g, num, 1e-6, f"backward d{name} vs finite differences")
 
 
+def _recurrent_fd(x, dh, got, tol, what):
+    base = {k: oracle.f64(v) for k, v in x.items()}
+    eps = 1e-6
+    for name, g in zip(("q", "k", "v", "igate_pre", "fgate_pre", "ogate_pre"), got):
+        num = np.zeros_like(base[name])
+        for idx in range(num.size):
+            for sgn in (1.0, -1.0):
+                y = {k: v.copy() for k, v in base.items()}
+                y[name].reshape(-1)[idx] += sgn * eps
+                hh = oracle.recurrent_unstabilized(y["q"], y["k"], y["v"], y["igate_pre"], y["fgate_pre"],
+                                                   y["ogate_pre"])
+                num.reshape(-1)[idx] += sgn * float(np.sum(hh * dh)) / (2 * eps)
+        _close(g, num, tol, f"{what} d{name} vs finite differences")
+
+
+def pin_recurrent_backward_finite_differences(mutation=0):
+    """Every gradient of the recurrent backward, eqs (59)-(70), equals the
+    central finite difference of the (unmutated) unstabilized recurrence for
+    L = sum(dh (.) h), output gate included, on a case whose n^T q takes both
+    signs above 1 in magnitude and stays below 1 on one step (all three
+    branches of the normalizer max(|n^T q|, 1))."""
+    x = W.sequence_inputs(1, 1, 7, 3, 4, torch.float64, seed=32, ig=(0.5, 1.0), fg=(1.0, 1.0), with_ogate=True)
+    dh = np.random.default_rng(32).standard_normal((1, 1, 7, 4))
+    got = oracle.recurrent_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh, x["ogate_pre"],
+                                    mutation=mutation)
+    _recurrent_fd(x, dh, got, 1e-6, "recurrent backward")
+
+
+def pin_recurrent_backward_equals_parallel(mutation=0):
+    """The recurrent (eqs 59-70) and parallel (eqs 87-105) backward passes
+    give the same gradients where the two forwards are the same function: no
+    output gate, sigma forget gate."""
+    x = W.sequence_inputs(2, 1, 20, 8, 6, torch.float64, seed=17, ig=(0.0, 1.0), fg=(3.0, 1.0))
+    dh = np.random.default_rng(17).standard_normal((2, 1, 20, 6))
+    rec = oracle.recurrent_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh,
+                                    mutation=mutation)[:5]
+    par = oracle.parallel_backward(*_args(x), dh, mutation=mutation)
+    for name, a, b in zip(("dq", "dk", "dv", "d_igate", "d_fgate"), rec, par):
+        _close(a, b, 1e-9, f"recurrent vs parallel backward {name}")
+
+
 def pin_forget_exp_variant(mutation=0):
     """The exponential forget activation: with f~ = 0 it gives f = 1 exactly,
     the same cell as the sigma activation with f~ = +inf; and its parallel and

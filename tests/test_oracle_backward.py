@@ -74,3 +74,15 @@ def test_backward_exp_forget_equals_finite_differences():
         for name, g in zip(("q", "k", "v", "igate_pre", "fgate_pre"), got):
             num = numeric_grad(x, dh, name)
             assert np.max(np.abs(g - num)) <= 1e-6 * max(1e-12, float(np.max(np.abs(num)))), name
+
+
+
+def test_recurrent_backward_exp_forget_finite_differences():
+    """Eqs (59)-(70) with the exponential forget activation (gamma = exp)
+    against central differences of the unstabilized recurrence."""
+    import pins
+    x = W.sequence_inputs(1, 1, 6, 3, 4, torch.float64, seed=13, ig=(-0.5, 1.0), fg=(0.0, 0.3), with_ogate=True)
+    dh = np.random.default_rng(13).standard_normal((1, 1, 6, 4))
+    with oracle.forget_exp():
+        got = oracle.recurrent_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh, x["ogate_pre"])
+        pins._recurrent_fd(x, dh, got, 1e-6, "exp forget recurrent backward")

@@ -7,6 +7,8 @@ input gate unrescaled in the step; 6 drops |.| on the row sum; 7 uses an
 exponential forget activation; 8 transposes q and k.  In the backward: 9
 takes eq (90)'s printed sign(n) literally; 10 drops the db term of eq (92);
 11 lets eq (102)'s inner sum include j = k; 12 uses K instead of Q in eq (99).
+In the recurrent backward: 13 drops Omega's negative branch; 14 takes
+sigma for sigma' in eq (68).
 """
 import pytest
 
@@ -14,7 +16,7 @@ import oracle
 import pins
 
 
-@pytest.mark.parametrize("mutation", range(1, 13))
+@pytest.mark.parametrize("mutation", range(1, 15))
 def test_mutation_is_caught(mutation):
     assert oracle._lib(mutation).oracle_mutation() == mutation
     caught = []
