@@ -223,6 +223,45 @@ int mlstm_parallel_bwd(const void *q, const void *k, const void *v,
                        int B, int H, int T, int d_qk, int d_v, int dtype,
                        void *workspace, size_t workspace_bytes, void *stream);
 
+/* Backward pass of the recurrent form (backpropagation through time, part
+ * 28/30 eqs 59-70) of the cell the recurrent step and mlstm_step_seq compute
+ * from a fresh state, for the output gradient dh = dL/dh:
+ *   C_t = f_t C_{t-1} + i_t v_t (s k_t)^T,  n_t = f_t n_{t-1} + i_t s k_t,
+ *   h_t = sigmoid(o~_t) (.) C_t q_t / max(|n_t . q_t|, 1),
+ * i_t = exp(i~_t), f_t = sigmoid(f~_t) (exp(f~_t) with forget_exp),
+ * s = 1/sqrt(d_qk), C_{-1} = 0, n_{-1} = 0.  Evaluated with the stabilized
+ * states (the result is that of the unstabilized recurrence); the gradient of
+ * the forget pre-activation uses the exact identity dL/dlog f_t =
+ * sum_{u>=t} (q_u . dq_u - k_u . dk_u), equal to eq (68).
+ *
+ *   q, k       [B,H,T,d_qk] dtype, 16-byte aligned;  v [B,H,T,d_v] dtype
+ *   igate_pre, fgate_pre   [B,H,T] fp32
+ *   dh         [B,H,T,d_v] dtype: dL/dh (dL/dH~ without an output gate)
+ *   dq, dk     [B,H,T,d_qk] dtype out,  dv [B,H,T,d_v] dtype out
+ *   d_igate, d_fgate       [B,H,T] fp32 out
+ *   d_ogate    [B,H,T,d_v] dtype out, required when opt->ogate_pre is set
+ *              (eq 70), else ignored
+ *   opt        NULL or: forget_exp (exponential forget activation) and
+ *              ogate_pre ([B,H,T,d_v] dtype output-gate pre-activations, or
+ *              NULL); algo is ignored
+ *   workspace  mlstm_recurrent_bwd_workspace(B,H,T,d_qk,d_v) bytes of device
+ *              memory, 256-byte aligned: per-CTA shares of dq and dk
+ *              (2 ceil(d_v/64) fp32 rows of d_qk per token) and three fp32
+ *              values per token, so it grows as B*H*T (about 1.2 GB for B=8,
+ *              H=4, T=2048, d=384).
+ * Requirements: 1 <= d_qk, d_v <= 512, d_qk a multiple of 8; no output may
+ * alias an input.  B*H*T = 0 returns MLSTM_OK without work.  Four kernels on
+ * `stream`: the forward and backward sweeps (state in registers, 64 rows of
+ * one head per CTA), the per-token combination, the per-head suffix sums. */
+size_t mlstm_recurrent_bwd_workspace(int B, int H, int T, int d_qk, int d_v);
+
+int mlstm_recurrent_bwd(const void *q, const void *k, const void *v,
+                        const float *igate_pre, const float *fgate_pre, const void *dh,
+                        void *dq, void *dk, void *dv, float *d_igate, float *d_fgate, void *d_ogate,
+                        int B, int H, int T, int d_qk, int d_v, int dtype,
+                        void *workspace, size_t workspace_bytes,
+                        const mlstm_options *opt, void *stream);
+
 /* One stabilized recurrent mLSTM step for every head, the generation step
  * (the recurrence differentiated by part 28/30 eqs 59-70, output gate eq 27):
  *   m'  = max(log sigmoid(f~) + m, i~)

@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     step_seq,
     parallel_final_state,
     parallel_bwd,
+    recurrent_bwd,
     parallel_fwd_host,
     parallel_fwd_host_workspace_bytes,
     last_device_status,

@@ -79,6 +79,10 @@ def library() -> ctypes.CDLL:
         lib.mlstm_gate_prep_opt.restype = i
         lib.mlstm_step_seq_opt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, op, vp]
         lib.mlstm_step_seq_opt.restype = i
+        lib.mlstm_recurrent_bwd_workspace.argtypes = [i, i, i, i, i]
+        lib.mlstm_recurrent_bwd_workspace.restype = sz
+        lib.mlstm_recurrent_bwd.argtypes = [vp] * 12 + [i] * 6 + [vp, sz, op, vp]
+        lib.mlstm_recurrent_bwd.restype = i
         lib.mlstm_last_device_status.argtypes = [vp]
         lib.mlstm_last_device_status.restype = i
         lib.mlstm_set_spin_limit.argtypes = [ll]
@@ -296,6 +300,44 @@ def parallel_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: t
     if rc != 0:
         raise MlstmError(rc, "mlstm_parallel_bwd")
     return dq, dk, dvv, dig, dfg
+
+
+def recurrent_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: torch.Tensor,
+                  fgate_pre: torch.Tensor, dh: torch.Tensor, *, ogate: Optional[torch.Tensor] = None,
+                  forget: str = "sigmoid", workspace: Optional[torch.Tensor] = None):
+    """``mlstm_recurrent_bwd``: gradients (dq, dk, dv, d_igate, d_fgate, d_ogate)
+    of the recurrent form from a fresh state, for dh = dL/dh (CUDA tensors);
+    d_ogate is None without an output gate."""
+    lib = library()
+    B, H, T, dqk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    _need(q, "q", (B, H, T, dqk), q.dtype, dev)
+    _need(k, "k", (B, H, T, dqk), q.dtype, dev)
+    _need(v, "v", (B, H, T, dv), q.dtype, dev)
+    _need(igate_pre, "igate_pre", (B, H, T), torch.float32, dev)
+    _need(fgate_pre, "fgate_pre", (B, H, T), torch.float32, dev)
+    _need(dh, "dh", (B, H, T, dv), q.dtype, dev)
+    if ogate is not None:
+        _need(ogate, "ogate", (B, H, T, dv), q.dtype, dev)
+    need = int(lib.mlstm_recurrent_bwd_workspace(B, H, T, dqk, dv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dig, dfg = torch.empty_like(igate_pre), torch.empty_like(fgate_pre)
+    dog = torch.empty_like(ogate) if ogate is not None else None
+    opt = _options("auto", forget, ogate)
+    rc = lib.mlstm_recurrent_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh), _ptr(dq),
+                                 _ptr(dk), _ptr(dvv), _ptr(dig), _ptr(dfg), None if dog is None else _ptr(dog),
+                                 B, H, T, dqk, dv, _DTYPES[q.dtype], _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), ctypes.byref(opt), _stream(dev))
+    if rc != 0:
+        raise MlstmError(rc, "mlstm_recurrent_bwd")
+    return dq, dk, dvv, dig, dfg, dog
 
 
 def parallel_final_state(k: torch.Tensor, v: torch.Tensor, workspace: torch.Tensor):

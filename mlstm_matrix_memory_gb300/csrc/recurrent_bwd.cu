@@ -1,0 +1,788 @@
+// Backward pass of the recurrent mLSTM form (backpropagation through time),
+// "xLSTM: Extended Long Short-Term Memory", part 28/30 eqs (59)-(70), with
+// the output gate of part 17/30 eq (27) and the gate activations of the
+// recurrent step:
+//   C_t = f_t C_{t-1} + i_t v_t (s k_t)^T,  n_t = f_t n_{t-1} + i_t s k_t,
+//   h~_t = C_t q_t / N_t,  N_t = max(|n_t^T q_t|, 1),  h_t = sigma(o~_t) (.) h~_t,
+// i_t = exp(i~_t), f_t = sigma(f~_t) (or exp(f~_t)), s = 1/sqrt(d_qk).
+//
+// Four passes, each state-carrying pass holding its matrix in registers the
+// way step_seq.cu does (a CTA owns 64 rows of one head, a warp 8 rows, a lane
+// every 32nd column pair):
+//
+// 1. forward sweep (stabilized: running max m, states C' = e^-m C, n' = e^-m n,
+//    so C/N = C'/N' with N' = max(|n'.q|, e^-m)).  Per token it forms h~, the
+//    output-gate gradient (eq 70), and this CTA's share of
+//        dq_t = (C'_t^T dh~_t - (h~_t . dh~_t) Omega_t n'_t) / N'_t        (eq 64)
+//    (the share of h~.dh~ over its rows goes into the second term, so the
+//    shares add up), and of h~.dh~ Omega, and log N_t.
+// 2. backward sweep over t = T-1..0 of dC_t, dn_t, eqs (60)-(61), kept as
+//    dC^ = e^-nu dC, dn^ = e^-nu dn with nu_t = max(log f_{t+1} + nu_{t+1},
+//    -log N_t): both recurrence coefficients are then at most 1.  Per token
+//        dv_t = i_t dC_t (s k_t),  dk_t = s i_t (dC_t^T v_t + dn_t)        (eqs 62-63)
+//    (dv rows are complete in the CTA; dk is a per-CTA share).
+// 3. per token: the shares summed into dq, dk; d i~_t = k_t . dk_t, which is
+//    eq (69) (i_t scales k_t wherever k_t enters), and r_t = q_t.dq_t - k_t.dk_t.
+// 4. per head: d f~_t = act'(f~_t) sum_{u >= t} r_u.  This is eq (68): adding a
+//    to log f_t changes the cell exactly as scaling q_u by e^a and k_u by e^-a
+//    for every u >= t does (the normalizer included, since n_u.q_u scales with
+//    C_u q_u), so dL/dlog f_t is that suffix sum; act' = dlog f/df~ is
+//    sigma(-f~) (eq 104) or 1 for the exponential activation.
+//
+// Work per token and head: 3 d_v d_qk fused multiply-adds in each sweep.
+#include <cmath>
+
+#include "internal.h"
+#include "mlstm.h"
+
+namespace mlstm {
+namespace {
+
+constexpr int kRW = 8;                      // rows per warp
+constexpr int kChunk = 16;                  // tokens staged in shared memory at a time
+constexpr int kGroup = 4;                   // tokens per cross-warp reduction
+constexpr int kMaxR = 8;                    // CTAs per head (d_v <= 512, 64 rows a CTA at least)
+constexpr float kRenorm = 1.0f / 16777216.0f;   // 2^-24: fold the scale into the state below this
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 ld2(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+// One chunk of tokens in shared memory; the row arrays hold the CTA's RPC
+// rows.  Sweep 2 also stages every CTA's share of h~.dh~ Omega and log N.
+template <typename T>
+struct Chunk {
+  T* q;        // [kChunk][dqk]
+  T* k;        // [kChunk][dqk]
+  T* v;        // [kChunk][RPC]
+  T* o;        // [kChunk][RPC]
+  T* dh;       // [kChunk][RPC]
+  float* ig;   // [kChunk]
+  float* fg;   // [kChunk]
+  float* lnN;  // [kChunk]
+  float* sp;   // [kMaxR][kChunk]
+};
+
+template <typename T>
+__host__ __device__ constexpr size_t chunk_bytes(int dqk, int rpc) {
+  return (size_t)kChunk * (2 * dqk + 3 * rpc) * sizeof(T) + (size_t)kChunk * (3 + kMaxR) * sizeof(float);
+}
+
+template <typename T>
+__device__ __forceinline__ Chunk<T> chunk_at(uint8_t* base, int dqk, int rpc) {
+  Chunk<T> b;
+  b.q = reinterpret_cast<T*>(base);
+  b.k = b.q + kChunk * dqk;
+  b.v = b.k + kChunk * dqk;
+  b.o = b.v + kChunk * rpc;
+  b.dh = b.o + kChunk * rpc;
+  b.ig = reinterpret_cast<float*>(b.dh + kChunk * rpc);
+  b.fg = b.ig + kChunk;
+  b.lnN = b.fg + kChunk;
+  b.sp = b.lnN + kChunk;
+  return b;
+}
+
+struct Inputs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;       // may be null
+  const void* dh;
+  const float* ig;
+  const float* fg;
+};
+
+// Shared scratch besides the two chunk buffers:
+//  tsc  per-token scalars of the chunk in process, four arrays of kChunk
+//       (sweep 1: f', i', e^-m, m; sweep 2: alpha, beta, i e^nu, h~.dh~ Omega);
+//  col  per token of a reduction group, every warp's column share;
+//  vec  per token, n' (sweep 1) or dn^ (sweep 2) in the warps' scaled form;
+//  sw   per token, every warp's share of h~.dh~ (sweep 1);
+//  sc   per token, four scalars for the combination; tok  its token index.
+struct Scratch {
+  float* tsc;
+  float* col;
+  float* vec;
+  float* sw;
+  float* sc;
+  int* tok;
+};
+
+__host__ __device__ constexpr size_t scratch_bytes(int dqk, int nw) {
+  return (size_t)4 * kChunk * sizeof(float) + (size_t)kGroup * (nw + 1) * dqk * sizeof(float) +
+         (size_t)kGroup * (nw + 4) * sizeof(float) + kGroup * sizeof(int);
+}
+
+__device__ __forceinline__ Scratch scratch_at(uint8_t* base, int dqk, int nw) {
+  Scratch r;
+  r.tsc = reinterpret_cast<float*>(base);
+  r.col = r.tsc + 4 * kChunk;
+  r.vec = r.col + kGroup * nw * dqk;
+  r.sw = r.vec + kGroup * dqk;
+  r.sc = r.sw + kGroup * nw;
+  r.tok = reinterpret_cast<int*>(r.sc + kGroup * 4);
+  return r;
+}
+
+// Copies of tokens [tok, tok+cnt) into `b` (all nthreads threads).  `sweep2`
+// also fetches the R CTAs' shares of h~.dh~ Omega and log N.
+template <typename T>
+__device__ __forceinline__ void stage(const Chunk<T>& b, const Inputs& in, size_t tok, int cnt, int dqk, int dv,
+                                      int rpc, int r0, int nrows, bool vec_rows, bool sweep2, const float* sp,
+                                      const float* lnN, int R, long long BHT) {
+  constexpr int E = 16 / sizeof(T);
+  const int nthreads = blockDim.x;
+  const T* q = static_cast<const T*>(in.q);
+  const T* k = static_cast<const T*>(in.k);
+  const T* v = static_cast<const T*>(in.v);
+  const T* o = static_cast<const T*>(in.o);
+  const T* dh = static_cast<const T*>(in.dh);
+  const int nq = cnt * dqk / E;
+  for (int p = threadIdx.x; p < nq; p += nthreads) {
+    cp_async16(b.q + p * E, q + tok * dqk + (size_t)p * E);
+    cp_async16(b.k + p * E, k + tok * dqk + (size_t)p * E);
+  }
+  if (vec_rows) {
+    const int per = nrows / E;
+    for (int p = threadIdx.x; p < cnt * per; p += nthreads) {
+      const int t = p / per, e = (p % per) * E;
+      cp_async16(b.v + t * rpc + e, v + (tok + t) * dv + r0 + e);
+      cp_async16(b.dh + t * rpc + e, dh + (tok + t) * dv + r0 + e);
+      if (o) cp_async16(b.o + t * rpc + e, o + (tok + t) * dv + r0 + e);
+    }
+  } else {
+    for (int p = threadIdx.x; p < cnt * nrows; p += nthreads) {
+      const int t = p / nrows, e = p % nrows;
+      b.v[t * rpc + e] = v[(tok + t) * dv + r0 + e];
+      b.dh[t * rpc + e] = dh[(tok + t) * dv + r0 + e];
+      if (o) b.o[t * rpc + e] = o[(tok + t) * dv + r0 + e];
+    }
+  }
+  for (int t = threadIdx.x; t < cnt; t += nthreads) {
+    cp_async4(b.ig + t, in.ig + tok + t);
+    cp_async4(b.fg + t, in.fg + tok + t);
+    if (sweep2) cp_async4(b.lnN + t, lnN + tok + t);
+  }
+  if (sweep2)
+    for (int p = threadIdx.x; p < R * cnt; p += nthreads) {
+      const int r = p / cnt, t = p % cnt;
+      cp_async4(b.sp + r * kChunk + t, sp + (size_t)r * BHT + tok + t);
+    }
+}
+
+// The eight per-lane row partial sums of a warp reduced in halving steps:
+// afterwards lane l (l % 4 == 0) holds the full sum of row myrow(l).
+__device__ __forceinline__ float reduce_rows(const float (&dot)[kRW], int lane) {
+  float e[4], f2[2], g;
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    e[j] = (b4 ? dot[j + 4] : dot[j]) + __shfl_xor_sync(0xffffffffu, b4 ? dot[j] : dot[j + 4], 16);
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    f2[j] = (b3 ? e[j + 2] : e[j]) + __shfl_xor_sync(0xffffffffu, b3 ? e[j] : e[j + 2], 8);
+  g = (b2 ? f2[1] : f2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? f2[0] : f2[1], 4);
+  g += __shfl_xor_sync(0xffffffffu, g, 2);
+  g += __shfl_xor_sync(0xffffffffu, g, 1);
+  return g;
+}
+
+// Inclusive scans over the 32 lanes.
+__device__ __forceinline__ float scan_add(float x, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  return x;
+}
+__device__ __forceinline__ float scan_max(float x, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x = fmaxf(x, y);
+  }
+  return x;
+}
+
+// x_t = max(g_t + x_{t-1}, h_t) over the lanes, from x_{-1} = x0, in closed
+// form: x_t = cs_t + max(x0, max_{j<=t}(h_j - cs_j)), cs the prefix sum of g.
+// Returns x_t; *xprev gets x_{t-1}.
+__device__ __forceinline__ float maxplus_scan(float g, float h, float x0, int lane, float* xprev) {
+  const float cs = scan_add(g, lane);
+  const float x = cs + fmaxf(x0, scan_max(h - cs, lane));
+  const float up = __shfl_up_sync(0xffffffffu, x, 1);
+  *xprev = lane == 0 ? x0 : up;
+  return x;
+}
+
+// The state of a warp is S * c^ with one scale S for all its entries, so a
+// decay multiplies S alone and the rank-one term is one fused multiply-add
+// per entry; when S falls below 2^-24 it is folded into the entries.
+template <int NC>
+__device__ __forceinline__ void fold_scale(float (&c)[kRW][NC], float (&vecs)[NC], float& S, float decay) {
+  const float s2 = S * decay;
+  if (s2 < kRenorm) {
+#pragma unroll
+    for (int i = 0; i < kRW; ++i)
+#pragma unroll
+      for (int u = 0; u < NC; ++u) c[i][u] *= s2;
+#pragma unroll
+    for (int u = 0; u < NC; ++u) vecs[u] *= s2;
+    S = 1.0f;
+  } else {
+    S = s2;
+  }
+}
+
+// Sweep 1 (forward in time).  Grid: BH * R CTAs of NW warps; CTA (bh, r)
+// owns rows [r RPC, (r+1) RPC) of head bh, RPC = 8 NW.
+template <typename T, int NC, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
+rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, float* __restrict__ spart,
+                    float* __restrict__ lnN, int Tn, int dqk, int dv, int R, float scale, int forget_exp,
+                    long long BHT) {
+  constexpr int NP = NC / 2, RPC = NW * kRW;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int bh = (int)(blockIdx.x / R), rank = (int)(blockIdx.x % R);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r0 = rank * RPC;
+  const int nrows = max(0, min(RPC, dv - r0));
+  const int wrow = warp * kRW;
+  const bool has_o = in.o != nullptr;
+  const bool vec_rows = (dv * (int)sizeof(T)) % 16 == 0 && (nrows * (int)sizeof(T)) % 16 == 0 &&
+                        (reinterpret_cast<uintptr_t>(in.v) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(in.o) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(in.dh) & 15) == 0;
+  const size_t tok0 = (size_t)bh * Tn;
+  const size_t cb = chunk_bytes<T>(dqk, RPC);
+  const Scratch sx = scratch_at(smem + 2 * cb, dqk, NW);
+  const int nchunks = (Tn + kChunk - 1) / kChunk;
+  const int myrow = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+  const bool writer = (lane & 3) == 0 && wrow + myrow < nrows;
+
+  stage(chunk_at<T>(smem, dqk, RPC), in, tok0, min(kChunk, Tn), dqk, dv, RPC, r0, nrows, vec_rows, false, nullptr,
+        nullptr, R, BHT);
+  cp_async_commit();
+
+  float c[kRW][NC], nn[NC];
+#pragma unroll
+  for (int i = 0; i < kRW; ++i)
+#pragma unroll
+    for (int u = 0; u < NC; ++u) c[i][u] = 0.0f;
+#pragma unroll
+  for (int u = 0; u < NC; ++u) nn[u] = 0.0f;
+  float S = 1.0f;
+  float m_carry = -INFINITY;          // warp 0: m after the last processed chunk
+  int slot = 0;
+
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int t0 = ch * kChunk, cnt = min(kChunk, Tn - t0);
+    if (ch + 1 < nchunks) {
+      stage(chunk_at<T>(smem + ((ch + 1) & 1) * cb, dqk, RPC), in, tok0 + t0 + kChunk,
+            min(kChunk, Tn - t0 - kChunk), dqk, dv, RPC, r0, nrows, vec_rows, false, nullptr, nullptr, R, BHT);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const Chunk<T> b = chunk_at<T>(smem + (ch & 1) * cb, dqk, RPC);
+    if (warp == 0) {
+      // the stabilizer of eqs (15)-(17) over the chunk: m_t = max(log f_t + m_{t-1}, i~_t)
+      const bool on = lane < cnt;
+      const float lf = on ? (forget_exp ? b.fg[lane] : log_sigmoid(b.fg[lane])) : 0.0f;
+      const float ig = on ? b.ig[lane] : -INFINITY;
+      float mprev;
+      const float m = maxplus_scan(lf, ig, m_carry, lane, &mprev);
+      if (on) {
+        sx.tsc[lane] = expf(lf + mprev - m);              // f'
+        sx.tsc[kChunk + lane] = expf(ig - m);             // i'
+        sx.tsc[2 * kChunk + lane] = expf(-m);             // normalizer floor
+        sx.tsc[3 * kChunk + lane] = m;
+      }
+      m_carry = __shfl_sync(0xffffffffu, m, cnt - 1);
+    }
+    __syncthreads();
+    for (int tt = 0; tt < cnt; ++tt) {
+      const float fp = sx.tsc[tt], ip = sx.tsc[kChunk + tt];
+      fold_scale(c, nn, S, fp);
+      const float a = ip * scale / S;                    // k's coefficient in the scaled update
+      float vr[kRW], dr[kRW];
+      float ov = 0.0f, dhv = 0.0f, dht = 0.0f;
+      {
+        const bool ok = lane < kRW && wrow + lane < nrows;
+        const float vv = ok ? Elem<T>::load(b.v, (size_t)tt * RPC + wrow + lane) : 0.0f;
+        dhv = ok ? Elem<T>::load(b.dh, (size_t)tt * RPC + wrow + lane) : 0.0f;
+        ov = ok && has_o ? Elem<T>::load(b.o, (size_t)tt * RPC + wrow + lane) : 0.0f;
+        dht = has_o ? sigmoid(ov) * dhv : dhv;
+#pragma unroll
+        for (int i = 0; i < kRW; ++i) {
+          vr[i] = __shfl_sync(0xffffffffu, vv, i);
+          dr[i] = __shfl_sync(0xffffffffu, dht, i);
+        }
+      }
+      float dot[kRW];
+#pragma unroll
+      for (int i = 0; i < kRW; ++i) dot[i] = 0.0f;
+      float nq = 0.0f;
+#pragma unroll
+      for (int u = 0; u < NP; ++u) {
+        const int cc = 2 * lane + 64 * u;
+        const bool in_range = cc < dqk;
+        const float2 kx = in_range ? ld2(b.k + (size_t)tt * dqk + cc) : make_float2(0.f, 0.f);
+        const float2 qx = in_range ? ld2(b.q + (size_t)tt * dqk + cc) : make_float2(0.f, 0.f);
+        const float k0 = kx.x * a, k1 = kx.y * a;
+        nn[2 * u] += k0;
+        nn[2 * u + 1] += k1;
+        nq = fmaf(nn[2 * u], qx.x, nq);
+        nq = fmaf(nn[2 * u + 1], qx.y, nq);
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kRW; ++i) {
+          c[i][2 * u] = fmaf(vr[i], k0, c[i][2 * u]);
+          c[i][2 * u + 1] = fmaf(vr[i], k1, c[i][2 * u + 1]);
+          dot[i] = fmaf(c[i][2 * u], qx.x, dot[i]);
+          dot[i] = fmaf(c[i][2 * u + 1], qx.y, dot[i]);
+          s0 = fmaf(c[i][2 * u], dr[i], s0);
+          s1 = fmaf(c[i][2 * u + 1], dr[i], s1);
+        }
+        if (in_range) {
+          *reinterpret_cast<float2*>(sx.col + ((size_t)slot * NW + warp) * dqk + cc) = make_float2(s0, s1);
+          if (warp == 0)
+            *reinterpret_cast<float2*>(sx.vec + (size_t)slot * dqk + cc) = make_float2(nn[2 * u], nn[2 * u + 1]);
+        }
+      }
+      nq = warp_sum(nq) * S;                              // n'.q
+      const float g = reduce_rows(dot, lane) * S;         // (C' q) of row myrow
+      const float fl = sx.tsc[2 * kChunk + tt];
+      const float nrm = fmaxf(fabsf(nq), fl);
+      float share = 0.0f;
+      {
+        const float dht_my = __shfl_sync(0xffffffffu, dht, myrow);
+        const float o_my = __shfl_sync(0xffffffffu, ov, myrow);
+        const float dh_my = __shfl_sync(0xffffffffu, dhv, myrow);
+        if (writer) {
+          const float hv = nrm > 0.0f ? g / nrm : 0.0f;       // h~ of row myrow
+          share = hv * dht_my;
+          if (has_o) {
+            const float so = sigmoid(o_my);
+            Elem<T>::store(dog, (tok0 + t0 + tt) * dv + r0 + wrow + myrow, hv * so * (1.0f - so) * dh_my);   // (70)
+          }
+        }
+      }
+      share = warp_sum(share);
+      if (lane == 0) {
+        sx.sw[slot * NW + warp] = share;
+        if (warp == 0) {
+          sx.sc[slot * 4 + 0] = nrm;
+          sx.sc[slot * 4 + 1] = fabsf(nq) > fl ? (nq > 0.0f ? 1.0f : -1.0f) : 0.0f;                   // Omega
+          sx.sc[slot * 4 + 2] = fmaxf(sx.tsc[3 * kChunk + tt] + logf(fabsf(nq)), 0.0f);               // log N
+          sx.sc[slot * 4 + 3] = S;
+          sx.tok[slot] = t0 + tt;
+        }
+      }
+      ++slot;
+      if (slot == kGroup || tt == cnt - 1) {
+        __syncthreads();
+        for (int j = 0; j < slot; ++j) {
+          float s = 0.0f;
+#pragma unroll
+          for (int w = 0; w < NW; ++w) s += sx.sw[j * NW + w];
+          const float nj = sx.sc[j * 4 + 0], om = sx.sc[j * 4 + 1], Sj = sx.sc[j * 4 + 3];
+          const float inv = nj > 0.0f ? Sj / nj : 0.0f;
+          const size_t orow = ((size_t)rank * BHT + tok0 + sx.tok[j]) * dqk;
+          for (int cc = threadIdx.x; cc < dqk; cc += NW * 32) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) acc += sx.col[((size_t)j * NW + w) * dqk + cc];
+            qpart[orow + cc] = (acc - s * om * sx.vec[(size_t)j * dqk + cc]) * inv;      // (64)
+          }
+          if (threadIdx.x == 0) {
+            spart[(size_t)rank * BHT + tok0 + sx.tok[j]] = s * om;
+            if (rank == 0) lnN[tok0 + sx.tok[j]] = sx.sc[j * 4 + 2];
+          }
+        }
+        __syncthreads();
+        slot = 0;
+      }
+    }
+    __syncthreads();                  // buffer ch&1 may be refilled by the next stage
+  }
+}
+
+// Sweep 2 (backward in time), same CTA layout as sweep 1.
+template <typename T, int NC, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
+rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __restrict__ lnN,
+                     T* __restrict__ dvout, float* __restrict__ kpart, int Tn, int dqk, int dv, int R, float scale,
+                     int forget_exp, long long BHT) {
+  constexpr int NP = NC / 2, RPC = NW * kRW;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int bh = (int)(blockIdx.x / R), rank = (int)(blockIdx.x % R);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r0 = rank * RPC;
+  const int nrows = max(0, min(RPC, dv - r0));
+  const int wrow = warp * kRW;
+  const bool has_o = in.o != nullptr;
+  const bool vec_rows = (dv * (int)sizeof(T)) % 16 == 0 && (nrows * (int)sizeof(T)) % 16 == 0 &&
+                        (reinterpret_cast<uintptr_t>(in.v) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(in.o) & 15) == 0 &&
+                        (reinterpret_cast<uintptr_t>(in.dh) & 15) == 0;
+  const size_t tok0 = (size_t)bh * Tn;
+  const size_t cb = chunk_bytes<T>(dqk, RPC);
+  const Scratch sx = scratch_at(smem + 2 * cb, dqk, NW);
+  const int nchunks = (Tn + kChunk - 1) / kChunk;
+  const int myrow = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+  const bool writer = (lane & 3) == 0 && wrow + myrow < nrows;
+
+  {
+    const int t0 = (nchunks - 1) * kChunk;
+    stage(chunk_at<T>(smem, dqk, RPC), in, tok0 + t0, Tn - t0, dqk, dv, RPC, r0, nrows, vec_rows, true, spart, lnN,
+          R, BHT);
+  }
+  cp_async_commit();
+
+  float dc[kRW][NC], dn[NC];
+#pragma unroll
+  for (int i = 0; i < kRW; ++i)
+#pragma unroll
+    for (int u = 0; u < NC; ++u) dc[i][u] = 0.0f;
+#pragma unroll
+  for (int u = 0; u < NC; ++u) dn[u] = 0.0f;
+  float S = 1.0f;
+  float nu_carry = -INFINITY, lf_carry = 0.0f;       // warp 0: nu and log f of the last processed token
+  int slot = 0;
+
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int ci = nchunks - 1 - ch;
+    const int t0 = ci * kChunk, cnt = min(kChunk, Tn - t0);
+    if (ch + 1 < nchunks) {
+      stage(chunk_at<T>(smem + ((ch + 1) & 1) * cb, dqk, RPC), in, tok0 + t0 - kChunk, kChunk, dqk, dv, RPC, r0,
+            nrows, vec_rows, true, spart, lnN, R, BHT);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const Chunk<T> b = chunk_at<T>(smem + (ch & 1) * cb, dqk, RPC);
+    if (warp == 0) {
+      // lane p takes the p-th token in processing order, tt = cnt-1-p:
+      // nu_t = max(log f_{t+1} + nu_{t+1}, -log N_t)
+      const bool on = lane < cnt;
+      const int tt = cnt - 1 - lane;
+      const float lf_own = on ? (forget_exp ? b.fg[tt] : log_sigmoid(b.fg[tt])) : 0.0f;
+      const float up = __shfl_up_sync(0xffffffffu, lf_own, 1);
+      const float g = lane == 0 ? lf_carry : up;                  // log f of token t+1
+      const float h = on ? -b.lnN[tt] : -INFINITY;
+      float nprev;
+      const float nu = maxplus_scan(on ? g : 0.0f, h, nu_carry, lane, &nprev);
+      if (on) {
+        float so = 0.0f;
+        for (int r = 0; r < R; ++r) so += b.sp[r * kChunk + tt];
+        sx.tsc[tt] = expf(g + nprev - nu);                        // alpha = f_{t+1} e^(nu_{t+1} - nu_t)
+        sx.tsc[kChunk + tt] = expf(h - nu);                       // beta = e^-nu_t / N_t
+        sx.tsc[2 * kChunk + tt] = expf(b.ig[tt] + nu);            // i_t e^nu_t
+        sx.tsc[3 * kChunk + tt] = so;                             // h~.dh~ Omega of the head
+      }
+      nu_carry = __shfl_sync(0xffffffffu, nu, cnt - 1);
+      lf_carry = __shfl_sync(0xffffffffu, lf_own, cnt - 1);
+    }
+    __syncthreads();
+    for (int tt = cnt - 1; tt >= 0; --tt) {
+      const float alpha = sx.tsc[tt], beta = sx.tsc[kChunk + tt];
+      fold_scale(dc, dn, S, alpha);
+      const float bs = beta / S;
+      float vr[kRW], dr[kRW];
+      {
+        const bool ok = lane < kRW && wrow + lane < nrows;
+        const float vv = ok ? Elem<T>::load(b.v, (size_t)tt * RPC + wrow + lane) : 0.0f;
+        const float dhv = ok ? Elem<T>::load(b.dh, (size_t)tt * RPC + wrow + lane) : 0.0f;
+        const float ov = ok && has_o ? Elem<T>::load(b.o, (size_t)tt * RPC + wrow + lane) : 0.0f;
+        const float dht = (has_o ? sigmoid(ov) * dhv : dhv) * bs;
+#pragma unroll
+        for (int i = 0; i < kRW; ++i) {
+          vr[i] = __shfl_sync(0xffffffffu, vv, i);
+          dr[i] = __shfl_sync(0xffffffffu, dht, i);
+        }
+      }
+      const float cn = -bs * sx.tsc[3 * kChunk + tt];
+      float dot[kRW];
+#pragma unroll
+      for (int i = 0; i < kRW; ++i) dot[i] = 0.0f;
+#pragma unroll
+      for (int u = 0; u < NP; ++u) {
+        const int cc = 2 * lane + 64 * u;
+        const bool in_range = cc < dqk;
+        const float2 kx = in_range ? ld2(b.k + (size_t)tt * dqk + cc) : make_float2(0.f, 0.f);
+        const float2 qx = in_range ? ld2(b.q + (size_t)tt * dqk + cc) : make_float2(0.f, 0.f);
+        dn[2 * u] = fmaf(cn, qx.x, dn[2 * u]);                    // (61)
+        dn[2 * u + 1] = fmaf(cn, qx.y, dn[2 * u + 1]);
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kRW; ++i) {
+          dc[i][2 * u] = fmaf(dr[i], qx.x, dc[i][2 * u]);         // (60)
+          dc[i][2 * u + 1] = fmaf(dr[i], qx.y, dc[i][2 * u + 1]);
+          dot[i] = fmaf(dc[i][2 * u], kx.x, dot[i]);
+          dot[i] = fmaf(dc[i][2 * u + 1], kx.y, dot[i]);
+          s0 = fmaf(dc[i][2 * u], vr[i], s0);
+          s1 = fmaf(dc[i][2 * u + 1], vr[i], s1);
+        }
+        if (in_range) {
+          *reinterpret_cast<float2*>(sx.col + ((size_t)slot * NW + warp) * dqk + cc) = make_float2(s0, s1);
+          if (warp == 0)
+            *reinterpret_cast<float2*>(sx.vec + (size_t)slot * dqk + cc) = make_float2(dn[2 * u], dn[2 * u + 1]);
+        }
+      }
+      const float gam = sx.tsc[2 * kChunk + tt];
+      const float g = reduce_rows(dot, lane);
+      if (writer)
+        Elem<T>::store(dvout, (tok0 + t0 + tt) * dv + r0 + wrow + myrow, gam * S * scale * g);   // (62)
+      if (lane == 0 && warp == 0) {
+        sx.sc[slot * 4 + 0] = scale * gam * S;
+        sx.tok[slot] = t0 + tt;
+      }
+      ++slot;
+      if (slot == kGroup || tt == 0) {
+        __syncthreads();
+        for (int j = 0; j < slot; ++j) {
+          const float f = sx.sc[j * 4 + 0];
+          const size_t orow = ((size_t)rank * BHT + tok0 + sx.tok[j]) * dqk;
+          for (int cc = threadIdx.x; cc < dqk; cc += NW * 32) {
+            float acc = rank == 0 ? sx.vec[(size_t)j * dqk + cc] : 0.0f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) acc += sx.col[((size_t)j * NW + w) * dqk + cc];
+            kpart[orow + cc] = f * acc;                                                    // (63)
+          }
+        }
+        __syncthreads();
+        slot = 0;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Sweep 3: one warp per token sums the R shares of dq and dk, writes them,
+// d i~ = k.dk, and r = q.dq - k.dk.
+template <typename T>
+__global__ void __launch_bounds__(256)
+rbwd_combine_kernel(const T* __restrict__ q, const T* __restrict__ k, const float* __restrict__ qpart,
+                    const float* __restrict__ kpart, T* __restrict__ dq, T* __restrict__ dk,
+                    float* __restrict__ dig, float* __restrict__ rr, int dqk, int R, long long BHT) {
+  const long long tok = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (tok >= BHT) return;
+  float qd = 0.0f, kd = 0.0f;
+  for (int c = lane; c < dqk; c += 32) {
+    float a = 0.0f, bsum = 0.0f;
+    for (int r = 0; r < R; ++r) {
+      a += qpart[((size_t)r * BHT + tok) * dqk + c];
+      bsum += kpart[((size_t)r * BHT + tok) * dqk + c];
+    }
+    Elem<T>::store(dq, (size_t)tok * dqk + c, a);
+    Elem<T>::store(dk, (size_t)tok * dqk + c, bsum);
+    qd = fmaf(Elem<T>::load(q, (size_t)tok * dqk + c), a, qd);
+    kd = fmaf(Elem<T>::load(k, (size_t)tok * dqk + c), bsum, kd);
+  }
+  qd = warp_sum(qd);
+  kd = warp_sum(kd);
+  if (lane == 0) {
+    dig[tok] = kd;            // (69)
+    rr[tok] = qd - kd;
+  }
+}
+
+// Sweep 4: one warp per head, suffix sums in fp64 from the last token down.
+__global__ void __launch_bounds__(32)
+rbwd_forget_kernel(const float* __restrict__ rr, const float* __restrict__ fg, float* __restrict__ dfg, int Tn,
+                   int forget_exp) {
+  const size_t base = (size_t)blockIdx.x * Tn;
+  const int lane = threadIdx.x;
+  double carry = 0.0;                      // sum over tokens after the current block of 32
+  for (int hi = Tn; hi > 0; hi -= 32) {
+    const int t = hi - 1 - lane;           // lane 0 takes the latest token of the block
+    double x = t >= 0 ? (double)rr[base + t] : 0.0;
+    // inclusive prefix over lanes 0..lane = suffix over tokens t..hi-1
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (t >= 0) {
+      const float f = fg[base + t];
+      const double act = forget_exp ? 1.0 : (double)sigmoid(-f);   // dlog f / df~ (eq 104)
+      dfg[base + t] = (float)((carry + x) * act);
+    }
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+}
+
+size_t r256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// The workspace is sized for 64-row CTAs, the most CTAs per head any launch
+// uses.
+struct RbLayout {
+  int R;
+  size_t qpart, kpart, spart, lnN, rr, total;
+};
+
+RbLayout rb_layout(long long BHT, int dqk, int dv) {
+  RbLayout L;
+  L.R = (dv + 63) / 64;
+  L.qpart = r256((size_t)L.R * BHT * dqk * sizeof(float));
+  L.kpart = L.qpart;
+  L.spart = r256((size_t)L.R * BHT * sizeof(float));
+  L.lnN = r256((size_t)BHT * sizeof(float));
+  L.rr = L.lnN;
+  L.total = L.qpart + L.kpart + L.spart + L.lnN + L.rr;
+  return L;
+}
+
+constexpr size_t kMaxSmem = 232448;
+
+template <typename T, int NW>
+size_t sweep_smem(int dqk) {
+  return 2 * chunk_bytes<T>(dqk, NW * kRW) + scratch_bytes(dqk, NW);
+}
+
+template <typename T, int NC, int NW>
+cudaError_t launch_sweeps(const Inputs& in, void* dog, void* dvout, float* qpart, float* kpart, float* spart,
+                          float* lnN, int BH, int Tn, int dqk, int dv, float scale, int forget_exp,
+                          cudaStream_t st) {
+  const long long BHT = (long long)BH * Tn;
+  const int R = (dv + NW * kRW - 1) / (NW * kRW);
+  const size_t smem = sweep_smem<T, NW>(dqk);
+  if (cudaFuncSetAttribute(rbwd_forward_kernel<T, NC, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(rbwd_backward_kernel<T, NC, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)(BH * R);
+  rbwd_forward_kernel<T, NC, NW><<<grid, NW * 32, smem, st>>>(in, static_cast<T*>(dog), qpart, spart, lnN, Tn, dqk,
+                                                              dv, R, scale, forget_exp, BHT);
+  rbwd_backward_kernel<T, NC, NW><<<grid, NW * 32, smem, st>>>(in, spart, lnN, static_cast<T*>(dvout), kpart, Tn,
+                                                               dqk, dv, R, scale, forget_exp, BHT);
+  return cudaGetLastError();
+}
+
+// CTAs of 8 warps (64 rows) or 12 warps (96 rows), whichever finishes the
+// heads sooner with one CTA per SM: waves of CTAs times rows per CTA.
+template <typename T>
+int pick_warps(int BH, int dqk, int dv) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms < 1) sms = 1;
+  // 12 warps leave 168 registers a thread: enough for 8 x 12 state columns,
+  // not for 8 x 16 (d_qk > 384)
+  if (dqk > 384 || sweep_smem<T, 12>(dqk) > kMaxSmem) return 8;
+  auto cost = [&](int nw) {
+    const long long ctas = (long long)BH * ((dv + 8 * nw - 1) / (8 * nw));
+    return ((ctas + sms - 1) / sms) * 8 * nw;
+  };
+  return cost(12) < cost(8) ? 12 : 8;
+}
+
+template <typename T, int NC>
+cudaError_t launch_nc(int nw, const Inputs& in, void* dog, void* dvout, float* qpart, float* kpart, float* spart,
+                      float* lnN, int BH, int Tn, int dqk, int dv, float scale, int forget_exp, cudaStream_t st) {
+  if (nw == 12)
+    return launch_sweeps<T, NC, 12>(in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+  return launch_sweeps<T, NC, 8>(in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+}
+
+template <typename T>
+cudaError_t launch_all(const Inputs& in, void* dq, void* dk, void* dvout, float* dig, float* dfg, void* dog,
+                       const RbLayout& L, char* ws, int BH, int Tn, int dqk, int dv, int forget_exp,
+                       cudaStream_t st) {
+  float* qpart = reinterpret_cast<float*>(ws);
+  float* kpart = reinterpret_cast<float*>(ws + L.qpart);
+  float* spart = reinterpret_cast<float*>(ws + L.qpart + L.kpart);
+  float* lnN = reinterpret_cast<float*>(ws + L.qpart + L.kpart + L.spart);
+  float* rr = reinterpret_cast<float*>(ws + L.qpart + L.kpart + L.spart + L.lnN);
+  const float scale = (float)(1.0 / sqrt((double)dqk));
+  const int nc = (dqk + 31) / 32;
+  const int nw = pick_warps<T>(BH, dqk, dv);
+  cudaError_t e;
+  if (nc <= 4)
+    e = launch_nc<T, 4>(nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+  else if (nc <= 8)
+    e = launch_nc<T, 8>(nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+  else if (nc <= 12)
+    e = launch_nc<T, 12>(nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+  else
+    e = launch_nc<T, 16>(nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+  if (e != cudaSuccess) return e;
+  const long long BHT = (long long)BH * Tn;
+  const int R = (dv + 8 * nw - 1) / (8 * nw);
+  rbwd_combine_kernel<T><<<(unsigned)((BHT + 7) / 8), 256, 0, st>>>(
+      static_cast<const T*>(in.q), static_cast<const T*>(in.k), qpart, kpart, static_cast<T*>(dq),
+      static_cast<T*>(dk), dig, rr, dqk, R, BHT);
+  rbwd_forget_kernel<<<(unsigned)BH, 32, 0, st>>>(rr, in.fg, dfg, Tn, forget_exp);
+  return cudaGetLastError();
+}
+
+bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+}  // namespace mlstm
+
+using namespace mlstm;
+
+extern "C" {
+
+size_t mlstm_recurrent_bwd_workspace(int B, int H, int T, int d_qk, int d_v) {
+  if (B <= 0 || H <= 0 || T <= 0 || d_qk <= 0 || d_v <= 0 || d_qk > 512 || d_v > 512) return 0;
+  return rb_layout((long long)B * H * T, d_qk, d_v).total;
+}
+
+int mlstm_recurrent_bwd(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
+                        const void* dh, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, void* d_ogate,
+                        int B, int H, int T, int d_qk, int d_v, int dtype, void* workspace, size_t workspace_bytes,
+                        const mlstm_options* opt, void* stream) {
+  if (B < 0 || H < 0 || T < 0) return MLSTM_EINVAL;
+  if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512 || d_qk % 8 != 0) return MLSTM_EINVAL;
+  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
+  const long long BH = (long long)B * H;
+  const long long BHT = BH * T;
+  const long long R = (d_v + 63) / 64;
+  if (BH * R > 0x7fffffffLL || BHT > (1LL << 40) || (BHT + 7) / 8 > 0x7fffffffLL) return MLSTM_EINVAL;
+  if (BH == 0 || T == 0) return MLSTM_OK;
+  const void* og = opt ? opt->ogate_pre : nullptr;
+  if (!q || !k || !v || !igate_pre || !fgate_pre || !dh || !dq || !dk || !dv || !d_igate || !d_fgate)
+    return MLSTM_EINVAL;
+  if (og && !d_ogate) return MLSTM_EINVAL;
+  if (!a16(q) || !a16(k)) return MLSTM_EALIGN;
+  if (!workspace || workspace_bytes < mlstm_recurrent_bwd_workspace(B, H, T, d_qk, d_v)) return MLSTM_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLSTM_EALIGN;
+  const RbLayout L = rb_layout(BHT, d_qk, d_v);
+  Inputs in{q, k, v, og, dh, igate_pre, fgate_pre};
+  const int fe = opt ? opt->forget_exp : 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const cudaError_t e =
+      dtype == MLSTM_F32
+          ? launch_all<float>(in, dq, dk, dv, d_igate, d_fgate, d_ogate, L, ws, (int)BH, T, d_qk, d_v, fe, st)
+          : launch_all<__nv_bfloat16>(in, dq, dk, dv, d_igate, d_fgate, d_ogate, L, ws, (int)BH, T, d_qk, d_v, fe,
+                                      st);
+  return e == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
+}
+
+}  // extern "C"

@@ -134,3 +134,27 @@ def test_host_call_validation(lib):
     assert host(ws=A + 16) == -2              # the workspace must be 256-byte aligned
     assert host(q=0) == -1
     assert host(T=0) == 0
+
+
+def test_recurrent_bwd_validation(lib):
+    need = lib.mlstm_recurrent_bwd_workspace(2, 3, 100, 64, 96)
+    # per-CTA dq and dk shares (two 64-row CTAs), then three per-token scalars
+    assert need >= 2 * 2 * 600 * 64 * 4 + 3 * 600 * 4
+    assert lib.mlstm_recurrent_bwd_workspace(0, 3, 100, 64, 96) == 0
+    assert lib.mlstm_recurrent_bwd_workspace(1, 1, 8, 64, 600) == 0
+
+    from mlstm_matrix_memory_gb300.binding import _Options as Opt
+
+    def rb(q=A, ws=A, wsb=need, B=2, H=3, T=100, dqk=64, dv=96, dt=1, dog=None, og=None):
+        opt = Opt(0, 0, og)
+        return lib.mlstm_recurrent_bwd(q, A, A, A, A, A, A, A, A, A, A, dog, B, H, T, dqk, dv, dt, ws, wsb,
+                                       ctypes.byref(opt), None)
+    assert rb(dqk=20) == -1                   # d_qk a multiple of 8
+    assert rb(dv=513) == -1
+    assert rb(dt=3) == -3
+    assert rb(q=A + 4) == -2
+    assert rb(q=0) == -1
+    assert rb(og=A) == -1                     # an output gate needs its gradient's buffer
+    assert rb(wsb=need - 1) == -7
+    assert rb(ws=A + 16) == -2
+    assert rb(T=0) == 0
