@@ -58,17 +58,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
-__device__ __forceinline__ float2 ld2(const __nv_bfloat16* p) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-}
-
 // One chunk of tokens in shared memory; the row arrays hold the CTA's RPC
 // rows.  Sweep 2 also stages every CTA's share of h~.dh~ Omega and log N.
 template <typename T>
 struct Chunk {
-  T* q;        // [kChunk][dqk]
-  T* k;        // [kChunk][dqk]
+  T* q;        // [kChunk][qs]
+  T* k;        // [kChunk][qs]
   T* v;        // [kChunk][RPC]
   T* o;        // [kChunk][RPC]
   T* dh;       // [kChunk][RPC]
@@ -78,17 +73,19 @@ struct Chunk {
   float* sp;   // [kMaxR][kChunk]
 };
 
+// q and k rows are qs elements apart: d_qk for bf16 (widened to fp32 rows of
+// PADC columns per chunk), PADC for fp32 (staged straight into padded rows).
 template <typename T>
-__host__ __device__ constexpr size_t chunk_bytes(int dqk, int rpc) {
-  return (size_t)kChunk * (2 * dqk + 3 * rpc) * sizeof(T) + (size_t)kChunk * (3 + kMaxR) * sizeof(float);
+__host__ __device__ constexpr size_t chunk_bytes(int qs, int rpc) {
+  return (size_t)kChunk * (2 * qs + 3 * rpc) * sizeof(T) + (size_t)kChunk * (3 + kMaxR) * sizeof(float);
 }
 
 template <typename T>
-__device__ __forceinline__ Chunk<T> chunk_at(uint8_t* base, int dqk, int rpc) {
+__device__ __forceinline__ Chunk<T> chunk_at(uint8_t* base, int qs, int rpc) {
   Chunk<T> b;
   b.q = reinterpret_cast<T*>(base);
-  b.k = b.q + kChunk * dqk;
-  b.v = b.k + kChunk * dqk;
+  b.k = b.q + kChunk * qs;
+  b.v = b.k + kChunk * qs;
   b.o = b.v + kChunk * rpc;
   b.dh = b.o + kChunk * rpc;
   b.ig = reinterpret_cast<float*>(b.dh + kChunk * rpc);
@@ -108,43 +105,62 @@ struct Inputs {
   const float* fg;
 };
 
-// Shared scratch besides the two chunk buffers:
-//  tsc  per-token scalars of the chunk in process, four arrays of kChunk
-//       (sweep 1: f', i', e^-m, m; sweep 2: alpha, beta, i e^nu, h~.dh~ Omega);
-//  col  per token of a reduction group, every warp's column share;
-//  vec  per token, n' (sweep 1) or dn^ (sweep 2) in the warps' scaled form;
-//  sw   per token, every warp's share of h~.dh~ (sweep 1);
-//  sc   per token, four scalars for the combination; tok  its token index.
+// Shared scratch besides the two staging buffers (PADC = 32 NC columns):
+//  qf, kf  the chunk's q and k rows as fp32, zero past d_qk     [kChunk][PADC]
+//          (bf16 only: fp32 rows are staged padded in the chunk buffer)
+//  tsc     per-token scalars of the chunk, four arrays of kChunk
+//          (sweep 1: f', i', e^-m, m; sweep 2: alpha, beta, i e^nu, h~.dh~ Omega)
+//  col     per token of a reduction group, every warp's column share [G][NW][PADC]
+//  vec     per token, n' (sweep 1) or dn^ (sweep 2), in the warps' scaled form
+//  gbuf    per token, the CTA's row sums (C' q or dC^ k), unscaled   [G][RPC]
+//  sc      per token, eight scalars;  tok  its token index within the chunk
 struct Scratch {
+  float* qf;
+  float* kf;
   float* tsc;
   float* col;
   float* vec;
-  float* sw;
+  float* gbuf;
   float* sc;
   int* tok;
 };
 
-__host__ __device__ constexpr size_t scratch_bytes(int dqk, int nw) {
-  return (size_t)4 * kChunk * sizeof(float) + (size_t)kGroup * (nw + 1) * dqk * sizeof(float) +
-         (size_t)kGroup * (nw + 4) * sizeof(float) + kGroup * sizeof(int);
+__host__ __device__ constexpr size_t scratch_bytes(int padc, int nw, bool wide) {
+  return (wide ? 0 : (size_t)2 * kChunk * padc * sizeof(float)) + (size_t)4 * kChunk * sizeof(float) +
+         (size_t)kGroup * (nw + 1) * padc * sizeof(float) + (size_t)kGroup * nw * kRW * sizeof(float) +
+         (size_t)kGroup * 8 * sizeof(float) + kGroup * sizeof(int);
 }
 
-__device__ __forceinline__ Scratch scratch_at(uint8_t* base, int dqk, int nw) {
+__device__ __forceinline__ Scratch scratch_at(uint8_t* base, int padc, int nw, bool wide) {
   Scratch r;
-  r.tsc = reinterpret_cast<float*>(base);
+  r.qf = reinterpret_cast<float*>(base);
+  r.kf = r.qf + (wide ? 0 : kChunk * padc);
+  r.tsc = r.kf + (wide ? 0 : kChunk * padc);
   r.col = r.tsc + 4 * kChunk;
-  r.vec = r.col + kGroup * nw * dqk;
-  r.sw = r.vec + kGroup * dqk;
-  r.sc = r.sw + kGroup * nw;
-  r.tok = reinterpret_cast<int*>(r.sc + kGroup * 4);
+  r.vec = r.col + kGroup * nw * padc;
+  r.gbuf = r.vec + kGroup * padc;
+  r.sc = r.gbuf + kGroup * nw * kRW;
+  r.tok = reinterpret_cast<int*>(r.sc + kGroup * 8);
   return r;
+}
+
+// The staged chunk's q and k rows converted to fp32 into qf, kf with rows of
+// PADC columns, zeros past d_qk and past the chunk's last token.
+template <typename T, int PADC>
+__device__ __forceinline__ void widen_qk(const Scratch& sx, const T* q, const T* k, int cnt, int dqk) {
+  for (int idx = threadIdx.x; idx < kChunk * PADC; idx += blockDim.x) {
+    const int t = idx / PADC, c = idx - t * PADC;
+    const bool on = t < cnt && c < dqk;
+    sx.qf[idx] = on ? Elem<T>::load(q, (size_t)t * dqk + c) : 0.0f;
+    sx.kf[idx] = on ? Elem<T>::load(k, (size_t)t * dqk + c) : 0.0f;
+  }
 }
 
 // Copies of tokens [tok, tok+cnt) into `b` (all nthreads threads).  `sweep2`
 // also fetches the R CTAs' shares of h~.dh~ Omega and log N.
 template <typename T>
-__device__ __forceinline__ void stage(const Chunk<T>& b, const Inputs& in, size_t tok, int cnt, int dqk, int dv,
-                                      int rpc, int r0, int nrows, bool vec_rows, bool sweep2, const float* sp,
+__device__ __forceinline__ void stage(const Chunk<T>& b, const Inputs& in, size_t tok, int cnt, int dqk, int qs,
+                                      int dv, int rpc, int r0, int nrows, bool vec_rows, bool sweep2, const float* sp,
                                       const float* lnN, int R, long long BHT) {
   constexpr int E = 16 / sizeof(T);
   const int nthreads = blockDim.x;
@@ -153,10 +169,11 @@ __device__ __forceinline__ void stage(const Chunk<T>& b, const Inputs& in, size_
   const T* v = static_cast<const T*>(in.v);
   const T* o = static_cast<const T*>(in.o);
   const T* dh = static_cast<const T*>(in.dh);
-  const int nq = cnt * dqk / E;
-  for (int p = threadIdx.x; p < nq; p += nthreads) {
-    cp_async16(b.q + p * E, q + tok * dqk + (size_t)p * E);
-    cp_async16(b.k + p * E, k + tok * dqk + (size_t)p * E);
+  const int per_row = dqk / E;
+  for (int p = threadIdx.x; p < cnt * per_row; p += nthreads) {
+    const int t = p / per_row, e = (p - t * per_row) * E;
+    cp_async16(b.q + t * qs + e, q + (tok + t) * dqk + e);
+    cp_async16(b.k + t * qs + e, k + (tok + t) * dqk + e);
   }
   if (vec_rows) {
     const int per = nrows / E;
@@ -252,13 +269,16 @@ __device__ __forceinline__ void fold_scale(float (&c)[kRW][NC], float (&vecs)[NC
 }
 
 // Sweep 1 (forward in time).  Grid: BH * R CTAs of NW warps; CTA (bh, r)
-// owns rows [r RPC, (r+1) RPC) of head bh, RPC = 8 NW.
+// owns rows [r RPC, (r+1) RPC) of head bh, RPC = 8 NW.  Per token a warp
+// updates its 8 rows and its copy of n', and leaves its rows' C'q and its
+// column share of C'^T dh~ in shared memory; every kGroup tokens the CTA
+// forms n'.q, h~, d o~ and h~.dh~ (one warp per token) and then the dq share.
 template <typename T, int NC, int NW>
 __global__ void __launch_bounds__(NW * 32, 1)
 rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, float* __restrict__ spart,
                     float* __restrict__ lnN, int Tn, int dqk, int dv, int R, float scale, int forget_exp,
                     long long BHT) {
-  constexpr int NP = NC / 2, RPC = NW * kRW;
+  constexpr int NP = NC / 2, RPC = NW * kRW, PADC = 32 * NC;
   extern __shared__ __align__(16) uint8_t smem[];
   const int bh = (int)(blockIdx.x / R), rank = (int)(blockIdx.x % R);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -271,13 +291,20 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
                         (reinterpret_cast<uintptr_t>(in.o) & 15) == 0 &&
                         (reinterpret_cast<uintptr_t>(in.dh) & 15) == 0;
   const size_t tok0 = (size_t)bh * Tn;
-  const size_t cb = chunk_bytes<T>(dqk, RPC);
-  const Scratch sx = scratch_at(smem + 2 * cb, dqk, NW);
+  constexpr bool kWide = sizeof(T) == 4;
+  const int qs = kWide ? PADC : dqk;
+  const size_t cb = chunk_bytes<T>(qs, RPC);
+  const Scratch sx = scratch_at(smem + 2 * cb, PADC, NW, kWide);
+  if (kWide)                          // the padding columns of both chunk buffers stay zero
+    for (int idx = threadIdx.x; idx < 4 * kChunk * (PADC - dqk); idx += NW * 32) {
+      const int row = idx / (PADC - dqk), cc = dqk + idx - row * (PADC - dqk);
+      reinterpret_cast<float*>(smem + (row / (2 * kChunk)) * cb)[(row % (2 * kChunk)) * PADC + cc] = 0.0f;
+    }
   const int nchunks = (Tn + kChunk - 1) / kChunk;
   const int myrow = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-  const bool writer = (lane & 3) == 0 && wrow + myrow < nrows;
+  const bool writer = (lane & 3) == 0;
 
-  stage(chunk_at<T>(smem, dqk, RPC), in, tok0, min(kChunk, Tn), dqk, dv, RPC, r0, nrows, vec_rows, false, nullptr,
+  stage(chunk_at<T>(smem, qs, RPC), in, tok0, min(kChunk, Tn), dqk, qs, dv, RPC, r0, nrows, vec_rows, false, nullptr,
         nullptr, R, BHT);
   cp_async_commit();
 
@@ -295,17 +322,20 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
   for (int ch = 0; ch < nchunks; ++ch) {
     const int t0 = ch * kChunk, cnt = min(kChunk, Tn - t0);
     if (ch + 1 < nchunks) {
-      stage(chunk_at<T>(smem + ((ch + 1) & 1) * cb, dqk, RPC), in, tok0 + t0 + kChunk,
-            min(kChunk, Tn - t0 - kChunk), dqk, dv, RPC, r0, nrows, vec_rows, false, nullptr, nullptr, R, BHT);
+      stage(chunk_at<T>(smem + ((ch + 1) & 1) * cb, qs, RPC), in, tok0 + t0 + kChunk,
+            min(kChunk, Tn - t0 - kChunk), dqk, qs, dv, RPC, r0, nrows, vec_rows, false, nullptr, nullptr, R, BHT);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
-    const Chunk<T> b = chunk_at<T>(smem + (ch & 1) * cb, dqk, RPC);
+    const Chunk<T> b = chunk_at<T>(smem + (ch & 1) * cb, qs, RPC);
+    if (!kWide) widen_qk<T, PADC>(sx, b.q, b.k, cnt, dqk);
+    const float* qf = kWide ? reinterpret_cast<const float*>(b.q) : sx.qf;
+    const float* kf = kWide ? reinterpret_cast<const float*>(b.k) : sx.kf;
     if (warp == 0) {
-      // the stabilizer of eqs (15)-(17) over the chunk: m_t = max(log f_t + m_{t-1}, i~_t)
+      // the stabilizer over the chunk: m_t = max(log f_t + m_{t-1}, i~_t)
       const bool on = lane < cnt;
       const float lf = on ? (forget_exp ? b.fg[lane] : log_sigmoid(b.fg[lane])) : 0.0f;
       const float ig = on ? b.ig[lane] : -INFINITY;
@@ -321,17 +351,15 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
     }
     __syncthreads();
     for (int tt = 0; tt < cnt; ++tt) {
-      const float fp = sx.tsc[tt], ip = sx.tsc[kChunk + tt];
-      fold_scale(c, nn, S, fp);
-      const float a = ip * scale / S;                    // k's coefficient in the scaled update
+      fold_scale(c, nn, S, sx.tsc[tt]);
+      const float a = __fdividef(sx.tsc[kChunk + tt] * scale, S);   // k's coefficient in the scaled update
       float vr[kRW], dr[kRW];
-      float ov = 0.0f, dhv = 0.0f, dht = 0.0f;
       {
         const bool ok = lane < kRW && wrow + lane < nrows;
         const float vv = ok ? Elem<T>::load(b.v, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        dhv = ok ? Elem<T>::load(b.dh, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        ov = ok && has_o ? Elem<T>::load(b.o, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        dht = has_o ? sigmoid(ov) * dhv : dhv;
+        const float dhv = ok ? Elem<T>::load(b.dh, (size_t)tt * RPC + wrow + lane) : 0.0f;
+        const float ov = ok && has_o ? Elem<T>::load(b.o, (size_t)tt * RPC + wrow + lane) : 0.0f;
+        const float dht = has_o ? sigmoid(ov) * dhv : dhv;
 #pragma unroll
         for (int i = 0; i < kRW; ++i) {
           vr[i] = __shfl_sync(0xffffffffu, vv, i);
@@ -341,18 +369,16 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
       float dot[kRW];
 #pragma unroll
       for (int i = 0; i < kRW; ++i) dot[i] = 0.0f;
-      float nq = 0.0f;
+      const float* qrow = qf + tt * PADC + 2 * lane;
+      const float* krow = kf + tt * PADC + 2 * lane;
+      float* colw = sx.col + (slot * NW + warp) * PADC + 2 * lane;
 #pragma unroll
       for (int u = 0; u < NP; ++u) {
-        const int cc = 2 * lane + 64 * u;
-        const bool in_range = cc < dqk;
-        const float2 kx = in_range ? ld2(b.k + (size_t)tt * dqk + cc) : make_float2(0.f, 0.f);
-        const float2 qx = in_range ? ld2(b.q + (size_t)tt * dqk + cc) : make_float2(0.f, 0.f);
+        const float2 kx = *reinterpret_cast<const float2*>(krow + 64 * u);
+        const float2 qx = *reinterpret_cast<const float2*>(qrow + 64 * u);
         const float k0 = kx.x * a, k1 = kx.y * a;
         nn[2 * u] += k0;
         nn[2 * u + 1] += k1;
-        nq = fmaf(nn[2 * u], qx.x, nq);
-        nq = fmaf(nn[2 * u + 1], qx.y, nq);
         float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
         for (int i = 0; i < kRW; ++i) {
@@ -363,60 +389,66 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
           s0 = fmaf(c[i][2 * u], dr[i], s0);
           s1 = fmaf(c[i][2 * u + 1], dr[i], s1);
         }
-        if (in_range) {
-          *reinterpret_cast<float2*>(sx.col + ((size_t)slot * NW + warp) * dqk + cc) = make_float2(s0, s1);
-          if (warp == 0)
-            *reinterpret_cast<float2*>(sx.vec + (size_t)slot * dqk + cc) = make_float2(nn[2 * u], nn[2 * u + 1]);
-        }
+        *reinterpret_cast<float2*>(colw + 64 * u) = make_float2(s0, s1);
       }
-      nq = warp_sum(nq) * S;                              // n'.q
-      const float g = reduce_rows(dot, lane) * S;         // (C' q) of row myrow
-      const float fl = sx.tsc[2 * kChunk + tt];
-      const float nrm = fmaxf(fabsf(nq), fl);
-      float share = 0.0f;
-      {
-        const float dht_my = __shfl_sync(0xffffffffu, dht, myrow);
-        const float o_my = __shfl_sync(0xffffffffu, ov, myrow);
-        const float dh_my = __shfl_sync(0xffffffffu, dhv, myrow);
-        if (writer) {
-          const float hv = nrm > 0.0f ? g / nrm : 0.0f;       // h~ of row myrow
-          share = hv * dht_my;
-          if (has_o) {
-            const float so = sigmoid(o_my);
-            Elem<T>::store(dog, (tok0 + t0 + tt) * dv + r0 + wrow + myrow, hv * so * (1.0f - so) * dh_my);   // (70)
-          }
-        }
+      if (warp == 0) {
+        float* vw = sx.vec + slot * PADC + 2 * lane;
+#pragma unroll
+        for (int u = 0; u < NP; ++u) *reinterpret_cast<float2*>(vw + 64 * u) = make_float2(nn[2 * u], nn[2 * u + 1]);
       }
-      share = warp_sum(share);
-      if (lane == 0) {
-        sx.sw[slot * NW + warp] = share;
-        if (warp == 0) {
-          sx.sc[slot * 4 + 0] = nrm;
-          sx.sc[slot * 4 + 1] = fabsf(nq) > fl ? (nq > 0.0f ? 1.0f : -1.0f) : 0.0f;                   // Omega
-          sx.sc[slot * 4 + 2] = fmaxf(sx.tsc[3 * kChunk + tt] + logf(fabsf(nq)), 0.0f);               // log N
-          sx.sc[slot * 4 + 3] = S;
-          sx.tok[slot] = t0 + tt;
-        }
+      const float g = reduce_rows(dot, lane);
+      if (writer) sx.gbuf[slot * RPC + wrow + myrow] = g;
+      if (threadIdx.x == 0) {
+        sx.sc[slot * 8 + 0] = S;
+        sx.tok[slot] = tt;
       }
       ++slot;
       if (slot == kGroup || tt == cnt - 1) {
         __syncthreads();
+        if (warp < slot) {
+          // token j = warp: n'.q, the normalizer, h~ of the CTA's rows, d o~ (70), h~.dh~
+          const int j = warp, tj = sx.tok[j];
+          const float Sj = sx.sc[j * 8 + 0];
+          float nq = 0.0f;
+          for (int cc = lane; cc < PADC; cc += 32) nq = fmaf(sx.vec[j * PADC + cc], qf[tj * PADC + cc], nq);
+          nq = warp_sum(nq) * Sj;
+          const float fl = sx.tsc[2 * kChunk + tj];
+          const float nrm = fmaxf(fabsf(nq), fl);
+          const float hs = nrm > 0.0f ? Sj / nrm : 0.0f;
+          float share = 0.0f;
+          for (int r = lane; r < nrows; r += 32) {
+            const float hv = hs * sx.gbuf[j * RPC + r];
+            const float dhv = Elem<T>::load(b.dh, (size_t)tj * RPC + r);
+            if (has_o) {
+              const float so = sigmoid(Elem<T>::load(b.o, (size_t)tj * RPC + r));
+              share = fmaf(hv, so * dhv, share);
+              Elem<T>::store(dog, (tok0 + t0 + tj) * dv + r0 + r, hv * so * (1.0f - so) * dhv);   // (70)
+            } else {
+              share = fmaf(hv, dhv, share);
+            }
+          }
+          share = warp_sum(share);
+          if (lane == 0) {
+            const float om = fabsf(nq) > fl ? (nq > 0.0f ? 1.0f : -1.0f) : 0.0f;                // Omega
+            sx.sc[j * 8 + 1] = hs;
+            sx.sc[j * 8 + 2] = share * om;
+            sx.sc[j * 8 + 3] = fmaxf(sx.tsc[3 * kChunk + tj] + logf(fabsf(nq)), 0.0f);          // log N
+          }
+        }
+        __syncthreads();
         for (int j = 0; j < slot; ++j) {
-          float s = 0.0f;
-#pragma unroll
-          for (int w = 0; w < NW; ++w) s += sx.sw[j * NW + w];
-          const float nj = sx.sc[j * 4 + 0], om = sx.sc[j * 4 + 1], Sj = sx.sc[j * 4 + 3];
-          const float inv = nj > 0.0f ? Sj / nj : 0.0f;
-          const size_t orow = ((size_t)rank * BHT + tok0 + sx.tok[j]) * dqk;
+          const float hs = sx.sc[j * 8 + 1], so = sx.sc[j * 8 + 2];
+          const size_t tokj = tok0 + t0 + sx.tok[j];
+          const size_t orow = ((size_t)rank * BHT + tokj) * dqk;
           for (int cc = threadIdx.x; cc < dqk; cc += NW * 32) {
             float acc = 0.0f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) acc += sx.col[((size_t)j * NW + w) * dqk + cc];
-            qpart[orow + cc] = (acc - s * om * sx.vec[(size_t)j * dqk + cc]) * inv;      // (64)
+            for (int w = 0; w < NW; ++w) acc += sx.col[(j * NW + w) * PADC + cc];
+            qpart[orow + cc] = (acc - so * sx.vec[j * PADC + cc]) * hs;                     // (64)
           }
           if (threadIdx.x == 0) {
-            spart[(size_t)rank * BHT + tok0 + sx.tok[j]] = s * om;
-            if (rank == 0) lnN[tok0 + sx.tok[j]] = sx.sc[j * 4 + 2];
+            spart[(size_t)rank * BHT + tokj] = so;
+            if (rank == 0) lnN[tokj] = sx.sc[j * 8 + 3];
           }
         }
         __syncthreads();
@@ -427,13 +459,16 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
   }
 }
 
-// Sweep 2 (backward in time), same CTA layout as sweep 1.
+// Sweep 2 (backward in time), same CTA layout as sweep 1.  Per token a warp
+// updates its 8 rows of dC^ and its copy of dn^, and leaves its rows' dC^ k
+// and its column share of dC^T v; every kGroup tokens the CTA writes the dv
+// rows and the dk share.
 template <typename T, int NC, int NW>
 __global__ void __launch_bounds__(NW * 32, 1)
 rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __restrict__ lnN,
                      T* __restrict__ dvout, float* __restrict__ kpart, int Tn, int dqk, int dv, int R, float scale,
                      int forget_exp, long long BHT) {
-  constexpr int NP = NC / 2, RPC = NW * kRW;
+  constexpr int NP = NC / 2, RPC = NW * kRW, PADC = 32 * NC;
   extern __shared__ __align__(16) uint8_t smem[];
   const int bh = (int)(blockIdx.x / R), rank = (int)(blockIdx.x % R);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -446,15 +481,22 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
                         (reinterpret_cast<uintptr_t>(in.o) & 15) == 0 &&
                         (reinterpret_cast<uintptr_t>(in.dh) & 15) == 0;
   const size_t tok0 = (size_t)bh * Tn;
-  const size_t cb = chunk_bytes<T>(dqk, RPC);
-  const Scratch sx = scratch_at(smem + 2 * cb, dqk, NW);
+  constexpr bool kWide = sizeof(T) == 4;
+  const int qs = kWide ? PADC : dqk;
+  const size_t cb = chunk_bytes<T>(qs, RPC);
+  const Scratch sx = scratch_at(smem + 2 * cb, PADC, NW, kWide);
+  if (kWide)                          // the padding columns of both chunk buffers stay zero
+    for (int idx = threadIdx.x; idx < 4 * kChunk * (PADC - dqk); idx += NW * 32) {
+      const int row = idx / (PADC - dqk), cc = dqk + idx - row * (PADC - dqk);
+      reinterpret_cast<float*>(smem + (row / (2 * kChunk)) * cb)[(row % (2 * kChunk)) * PADC + cc] = 0.0f;
+    }
   const int nchunks = (Tn + kChunk - 1) / kChunk;
   const int myrow = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-  const bool writer = (lane & 3) == 0 && wrow + myrow < nrows;
+  const bool writer = (lane & 3) == 0;
 
   {
     const int t0 = (nchunks - 1) * kChunk;
-    stage(chunk_at<T>(smem, dqk, RPC), in, tok0 + t0, Tn - t0, dqk, dv, RPC, r0, nrows, vec_rows, true, spart, lnN,
+    stage(chunk_at<T>(smem, qs, RPC), in, tok0 + t0, Tn - t0, dqk, qs, dv, RPC, r0, nrows, vec_rows, true, spart, lnN,
           R, BHT);
   }
   cp_async_commit();
@@ -474,7 +516,7 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
     const int ci = nchunks - 1 - ch;
     const int t0 = ci * kChunk, cnt = min(kChunk, Tn - t0);
     if (ch + 1 < nchunks) {
-      stage(chunk_at<T>(smem + ((ch + 1) & 1) * cb, dqk, RPC), in, tok0 + t0 - kChunk, kChunk, dqk, dv, RPC, r0,
+      stage(chunk_at<T>(smem + ((ch + 1) & 1) * cb, qs, RPC), in, tok0 + t0 - kChunk, kChunk, dqk, qs, dv, RPC, r0,
             nrows, vec_rows, true, spart, lnN, R, BHT);
       cp_async_commit();
       cp_async_wait<1>();
@@ -482,7 +524,10 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
       cp_async_wait<0>();
     }
     __syncthreads();
-    const Chunk<T> b = chunk_at<T>(smem + (ch & 1) * cb, dqk, RPC);
+    const Chunk<T> b = chunk_at<T>(smem + (ch & 1) * cb, qs, RPC);
+    if (!kWide) widen_qk<T, PADC>(sx, b.q, b.k, cnt, dqk);
+    const float* qf = kWide ? reinterpret_cast<const float*>(b.q) : sx.qf;
+    const float* kf = kWide ? reinterpret_cast<const float*>(b.k) : sx.kf;
     if (warp == 0) {
       // lane p takes the p-th token in processing order, tt = cnt-1-p:
       // nu_t = max(log f_{t+1} + nu_{t+1}, -log N_t)
@@ -507,9 +552,8 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
     }
     __syncthreads();
     for (int tt = cnt - 1; tt >= 0; --tt) {
-      const float alpha = sx.tsc[tt], beta = sx.tsc[kChunk + tt];
-      fold_scale(dc, dn, S, alpha);
-      const float bs = beta / S;
+      fold_scale(dc, dn, S, sx.tsc[tt]);
+      const float bs = __fdividef(sx.tsc[kChunk + tt], S);
       float vr[kRW], dr[kRW];
       {
         const bool ok = lane < kRW && wrow + lane < nrows;
@@ -527,12 +571,13 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
       float dot[kRW];
 #pragma unroll
       for (int i = 0; i < kRW; ++i) dot[i] = 0.0f;
+      const float* qrow = qf + tt * PADC + 2 * lane;
+      const float* krow = kf + tt * PADC + 2 * lane;
+      float* colw = sx.col + (slot * NW + warp) * PADC + 2 * lane;
 #pragma unroll
       for (int u = 0; u < NP; ++u) {
-        const int cc = 2 * lane + 64 * u;
-        const bool in_range = cc < dqk;
-        const float2 kx = in_range ? ld2(b.k + (size_t)tt * dqk + cc) : make_float2(0.f, 0.f);
-        const float2 qx = in_range ? ld2(b.q + (size_t)tt * dqk + cc) : make_float2(0.f, 0.f);
+        const float2 kx = *reinterpret_cast<const float2*>(krow + 64 * u);
+        const float2 qx = *reinterpret_cast<const float2*>(qrow + 64 * u);
         dn[2 * u] = fmaf(cn, qx.x, dn[2 * u]);                    // (61)
         dn[2 * u + 1] = fmaf(cn, qx.y, dn[2 * u + 1]);
         float s0 = 0.0f, s1 = 0.0f;
@@ -545,32 +590,34 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
           s0 = fmaf(dc[i][2 * u], vr[i], s0);
           s1 = fmaf(dc[i][2 * u + 1], vr[i], s1);
         }
-        if (in_range) {
-          *reinterpret_cast<float2*>(sx.col + ((size_t)slot * NW + warp) * dqk + cc) = make_float2(s0, s1);
-          if (warp == 0)
-            *reinterpret_cast<float2*>(sx.vec + (size_t)slot * dqk + cc) = make_float2(dn[2 * u], dn[2 * u + 1]);
-        }
+        *reinterpret_cast<float2*>(colw + 64 * u) = make_float2(s0, s1);
       }
-      const float gam = sx.tsc[2 * kChunk + tt];
+      if (warp == 0) {
+        float* vw = sx.vec + slot * PADC + 2 * lane;
+#pragma unroll
+        for (int u = 0; u < NP; ++u) *reinterpret_cast<float2*>(vw + 64 * u) = make_float2(dn[2 * u], dn[2 * u + 1]);
+      }
       const float g = reduce_rows(dot, lane);
-      if (writer)
-        Elem<T>::store(dvout, (tok0 + t0 + tt) * dv + r0 + wrow + myrow, gam * S * scale * g);   // (62)
-      if (lane == 0 && warp == 0) {
-        sx.sc[slot * 4 + 0] = scale * gam * S;
-        sx.tok[slot] = t0 + tt;
+      if (writer) sx.gbuf[slot * RPC + wrow + myrow] = g;
+      if (threadIdx.x == 0) {
+        sx.sc[slot * 8 + 0] = scale * sx.tsc[2 * kChunk + tt] * S;    // s i_t e^nu_t S
+        sx.tok[slot] = tt;
       }
       ++slot;
       if (slot == kGroup || tt == 0) {
         __syncthreads();
         for (int j = 0; j < slot; ++j) {
-          const float f = sx.sc[j * 4 + 0];
-          const size_t orow = ((size_t)rank * BHT + tok0 + sx.tok[j]) * dqk;
+          const float f = sx.sc[j * 8 + 0];
+          const size_t tokj = tok0 + t0 + sx.tok[j];
+          const size_t orow = ((size_t)rank * BHT + tokj) * dqk;
           for (int cc = threadIdx.x; cc < dqk; cc += NW * 32) {
-            float acc = rank == 0 ? sx.vec[(size_t)j * dqk + cc] : 0.0f;
+            float acc = rank == 0 ? sx.vec[j * PADC + cc] : 0.0f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) acc += sx.col[((size_t)j * NW + w) * dqk + cc];
-            kpart[orow + cc] = f * acc;                                                    // (63)
+            for (int w = 0; w < NW; ++w) acc += sx.col[(j * NW + w) * PADC + cc];
+            kpart[orow + cc] = f * acc;                                                      // (63)
           }
+          for (int r = threadIdx.x; r < nrows; r += NW * 32)
+            Elem<T>::store(dvout, tokj * dv + r0 + r, f * sx.gbuf[j * RPC + r]);            // (62)
         }
         __syncthreads();
         slot = 0;
@@ -658,9 +705,10 @@ RbLayout rb_layout(long long BHT, int dqk, int dv) {
 
 constexpr size_t kMaxSmem = 232448;
 
-template <typename T, int NW>
+template <typename T, int NC, int NW>
 size_t sweep_smem(int dqk) {
-  return 2 * chunk_bytes<T>(dqk, NW * kRW) + scratch_bytes(dqk, NW);
+  constexpr bool wide = sizeof(T) == 4;
+  return 2 * chunk_bytes<T>(wide ? 32 * NC : dqk, NW * kRW) + scratch_bytes(32 * NC, NW, wide);
 }
 
 template <typename T, int NC, int NW>
@@ -669,7 +717,8 @@ cudaError_t launch_sweeps(const Inputs& in, void* dog, void* dvout, float* qpart
                           cudaStream_t st) {
   const long long BHT = (long long)BH * Tn;
   const int R = (dv + NW * kRW - 1) / (NW * kRW);
-  const size_t smem = sweep_smem<T, NW>(dqk);
+  const size_t smem = sweep_smem<T, NC, NW>(dqk);
+  if (smem > kMaxSmem) return cudaErrorInvalidValue;
   if (cudaFuncSetAttribute(rbwd_forward_kernel<T, NC, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(rbwd_backward_kernel<T, NC, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -685,14 +734,14 @@ cudaError_t launch_sweeps(const Inputs& in, void* dog, void* dvout, float* qpart
 
 // CTAs of 8 warps (64 rows) or 12 warps (96 rows), whichever finishes the
 // heads sooner with one CTA per SM: waves of CTAs times rows per CTA.
-template <typename T>
+template <typename T, int NC>
 int pick_warps(int BH, int dqk, int dv) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms < 1) sms = 1;
   // 12 warps leave 168 registers a thread: enough for 8 x 12 state columns,
   // not for 8 x 16 (d_qk > 384)
-  if (dqk > 384 || sweep_smem<T, 12>(dqk) > kMaxSmem) return 8;
+  if (NC > 12 || sweep_smem<T, NC, 12>(dqk) > kMaxSmem) return 8;
   auto cost = [&](int nw) {
     const long long ctas = (long long)BH * ((dv + 8 * nw - 1) / (8 * nw));
     return ((ctas + sms - 1) / sms) * 8 * nw;
@@ -701,10 +750,14 @@ int pick_warps(int BH, int dqk, int dv) {
 }
 
 template <typename T, int NC>
-cudaError_t launch_nc(int nw, const Inputs& in, void* dog, void* dvout, float* qpart, float* kpart, float* spart,
+cudaError_t launch_nc(int* nw, const Inputs& in, void* dog, void* dvout, float* qpart, float* kpart, float* spart,
                       float* lnN, int BH, int Tn, int dqk, int dv, float scale, int forget_exp, cudaStream_t st) {
-  if (nw == 12)
-    return launch_sweeps<T, NC, 12>(in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+  *nw = pick_warps<T, NC>(BH, dqk, dv);
+  if constexpr (NC <= 12) {
+    if (*nw == 12)
+      return launch_sweeps<T, NC, 12>(in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp,
+                                      st);
+  }
   return launch_sweeps<T, NC, 8>(in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
 }
 
@@ -719,16 +772,16 @@ cudaError_t launch_all(const Inputs& in, void* dq, void* dk, void* dvout, float*
   float* rr = reinterpret_cast<float*>(ws + L.qpart + L.kpart + L.spart + L.lnN);
   const float scale = (float)(1.0 / sqrt((double)dqk));
   const int nc = (dqk + 31) / 32;
-  const int nw = pick_warps<T>(BH, dqk, dv);
+  int nw = 8;
   cudaError_t e;
   if (nc <= 4)
-    e = launch_nc<T, 4>(nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+    e = launch_nc<T, 4>(&nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
   else if (nc <= 8)
-    e = launch_nc<T, 8>(nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+    e = launch_nc<T, 8>(&nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
   else if (nc <= 12)
-    e = launch_nc<T, 12>(nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+    e = launch_nc<T, 12>(&nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
   else
-    e = launch_nc<T, 16>(nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
+    e = launch_nc<T, 16>(&nw, in, dog, dvout, qpart, kpart, spart, lnN, BH, Tn, dqk, dv, scale, forget_exp, st);
   if (e != cudaSuccess) return e;
   const long long BHT = (long long)BH * Tn;
   const int R = (dv + 8 * nw - 1) / (8 * nw);
