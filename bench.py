@@ -377,6 +377,33 @@ def time_backward(M, w, xd, reps):
     return ms, float(w.B * w.H * w.T * w.T * (3 * w.d_qk + 2 * w.d_v)), ws_buf.numel()
 
 
+def time_recurrent_backward(M, w, xd, reps):
+    """The recurrent backward (backpropagation through time) on the parallel
+    workload: algorithmic work 12 d_qk d_v flops per token and head (each of
+    the two sweeps makes three fused multiply-adds per state entry: the
+    state update, the row product and the column product)."""
+    lib = M.library()
+    dh = torch.randn((w.B, w.H, w.T, w.d_v), generator=torch.Generator().manual_seed(1)).to(w.dtype).cuda()
+    ws_buf = torch.empty(int(lib.mlstm_recurrent_bwd_workspace(w.B, w.H, w.T, w.d_qk, w.d_v)), dtype=torch.uint8,
+                         device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one():
+        M.recurrent_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh, workspace=ws_buf)
+
+    for _ in range(2):
+        one()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for i in range(reps):
+        ev[i][0].record(stream)
+        one()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return ms, float(12 * w.B * w.H * w.T * w.d_qk * w.d_v), ws_buf.numel()
+
+
 def fp32_alu_peak_tflops():
     """FP32 FMA peak of the CUDA cores: SMs x 128 lanes x 2 flops x the
     maximum SM clock from MEASURED_PEAKS.json (else 2070 MHz)."""
@@ -451,10 +478,11 @@ def main():
     if not args.no_step:
         rec = time_step(M, max(10, args.steps // 2), 3)
         seq = time_step_seq(M, 5)
-    bwd = None
+    bwd = rbwd = None
     if algo == "tc":
         fs = time_final_state(M, w, xd, 10)
         bwd = time_backward(M, w, xd, 5)
+        rbwd = time_recurrent_backward(M, w, xd, 3)
     clk = clocks.stop() if clocks else None
 
     flops = w.causal_flops
@@ -516,6 +544,15 @@ def main():
                             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
                                          "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
                                          "work": "causal T^2 (3 d_qk + 2 d_v) per head", "traffic": None}}
+    if rbwd is not None:
+        ms, fl, wsb = rbwd
+        tf = fl / (ms * 1e-3) / 1e12
+        alu_peak, sms, mhz = fp32_alu_peak_tflops()
+        line["recurrent_backward"] = {
+            "workload": w.name, "ms": ms, "workspace_bytes": wsb,
+            "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
+                         "peak_source": f"FP32 FMA: {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz",
+                         "work": "12 d_qk d_v per token and head (two sweeps)", "traffic": None}}
     if clk:
         line["clocks"] = clk
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -108,6 +108,9 @@ struct Inputs {
 // Shared scratch besides the two staging buffers (PADC = 32 NC columns):
 //  qf, kf  the chunk's q and k rows as fp32, zero past d_qk     [kChunk][PADC]
 //          (bf16 only: fp32 rows are staged padded in the chunk buffer)
+//  vf, dhf the chunk's v and dh~ = sigma(o~) dh rows as fp32, zero past the
+//          CTA's rows                                              [kChunk][RPC]
+//          (bf16 only: fp32 rows are used, and dh turned into dh~, in place)
 //  tsc     per-token scalars of the chunk, four arrays of kChunk
 //          (sweep 1: f', i', e^-m, m; sweep 2: alpha, beta, i e^nu, h~.dh~ Omega)
 //  col     per token of a reduction group, every warp's column share [G][NW][PADC]
@@ -117,6 +120,8 @@ struct Inputs {
 struct Scratch {
   float* qf;
   float* kf;
+  float* vf;
+  float* dhf;
   float* tsc;
   float* col;
   float* vec;
@@ -126,7 +131,7 @@ struct Scratch {
 };
 
 __host__ __device__ constexpr size_t scratch_bytes(int padc, int nw, bool wide) {
-  return (wide ? 0 : (size_t)2 * kChunk * padc * sizeof(float)) + (size_t)4 * kChunk * sizeof(float) +
+  return (wide ? 0 : (size_t)2 * kChunk * (padc + nw * kRW) * sizeof(float)) + (size_t)4 * kChunk * sizeof(float) +
          (size_t)kGroup * (nw + 1) * padc * sizeof(float) + (size_t)kGroup * nw * kRW * sizeof(float) +
          (size_t)kGroup * 8 * sizeof(float) + kGroup * sizeof(int);
 }
@@ -135,7 +140,9 @@ __device__ __forceinline__ Scratch scratch_at(uint8_t* base, int padc, int nw, b
   Scratch r;
   r.qf = reinterpret_cast<float*>(base);
   r.kf = r.qf + (wide ? 0 : kChunk * padc);
-  r.tsc = r.kf + (wide ? 0 : kChunk * padc);
+  r.vf = r.kf + (wide ? 0 : kChunk * padc);
+  r.dhf = r.vf + (wide ? 0 : kChunk * nw * kRW);
+  r.tsc = r.dhf + (wide ? 0 : kChunk * nw * kRW);
   r.col = r.tsc + 4 * kChunk;
   r.vec = r.col + kGroup * nw * padc;
   r.gbuf = r.vec + kGroup * padc;
@@ -144,15 +151,33 @@ __device__ __forceinline__ Scratch scratch_at(uint8_t* base, int padc, int nw, b
   return r;
 }
 
-// The staged chunk's q and k rows converted to fp32 into qf, kf with rows of
-// PADC columns, zeros past d_qk and past the chunk's last token.
-template <typename T, int PADC>
-__device__ __forceinline__ void widen_qk(const Scratch& sx, const T* q, const T* k, int cnt, int dqk) {
-  for (int idx = threadIdx.x; idx < kChunk * PADC; idx += blockDim.x) {
-    const int t = idx / PADC, c = idx - t * PADC;
-    const bool on = t < cnt && c < dqk;
-    sx.qf[idx] = on ? Elem<T>::load(q, (size_t)t * dqk + c) : 0.0f;
-    sx.kf[idx] = on ? Elem<T>::load(k, (size_t)t * dqk + c) : 0.0f;
+// bf16: the staged chunk's q and k rows converted to fp32 into qf, kf (rows of
+// PADC columns, zeros past d_qk and past the chunk's last token), and v and
+// dh~ = sigma(o~) dh into vf, dhf (zeros past the CTA's rows).  fp32: dh turned
+// into dh~ in place (the other rows are used as staged).
+template <typename T, int PADC, int RPC>
+__device__ __forceinline__ void widen(const Scratch& sx, const Chunk<T>& b, int cnt, int dqk, int nrows, bool has_o) {
+  if constexpr (sizeof(T) == 4) {
+    if (has_o)
+      for (int idx = threadIdx.x; idx < cnt * nrows; idx += blockDim.x) {
+        const int t = idx / nrows, r = idx - t * nrows;
+        float* d = reinterpret_cast<float*>(b.dh) + t * RPC + r;
+        *d *= sigmoid(Elem<T>::load(b.o, (size_t)t * RPC + r));
+      }
+  } else {
+    for (int idx = threadIdx.x; idx < kChunk * PADC; idx += blockDim.x) {
+      const int t = idx / PADC, c = idx - t * PADC;
+      const bool on = t < cnt && c < dqk;
+      sx.qf[idx] = on ? Elem<T>::load(b.q, (size_t)t * dqk + c) : 0.0f;
+      sx.kf[idx] = on ? Elem<T>::load(b.k, (size_t)t * dqk + c) : 0.0f;
+    }
+    for (int idx = threadIdx.x; idx < kChunk * RPC; idx += blockDim.x) {
+      const int t = idx / RPC, r = idx - t * RPC;
+      const bool on = t < cnt && r < nrows;
+      sx.vf[idx] = on ? Elem<T>::load(b.v, (size_t)idx) : 0.0f;
+      const float dhv = on ? Elem<T>::load(b.dh, (size_t)idx) : 0.0f;
+      sx.dhf[idx] = on && has_o ? sigmoid(Elem<T>::load(b.o, (size_t)idx)) * dhv : dhv;
+    }
   }
 }
 
@@ -218,6 +243,13 @@ __device__ __forceinline__ float reduce_rows(const float (&dot)[kRW], int lane) 
   g += __shfl_xor_sync(0xffffffffu, g, 2);
   g += __shfl_xor_sync(0xffffffffu, g, 1);
   return g;
+}
+
+// Eight consecutive fp32 row values (16-byte aligned), the same for every lane.
+__device__ __forceinline__ void load_rows(const float* p, float (&x)[kRW]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
 // Inclusive scans over the 32 lanes.
@@ -295,11 +327,18 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
   const int qs = kWide ? PADC : dqk;
   const size_t cb = chunk_bytes<T>(qs, RPC);
   const Scratch sx = scratch_at(smem + 2 * cb, PADC, NW, kWide);
-  if (kWide)                          // the padding columns of both chunk buffers stay zero
-    for (int idx = threadIdx.x; idx < 4 * kChunk * (PADC - dqk); idx += NW * 32) {
+  if constexpr (kWide) {              // what staging never writes stays zero in both chunk buffers:
+    for (int idx = threadIdx.x; idx < 4 * kChunk * (PADC - dqk); idx += NW * 32) {   // q, k columns past d_qk
       const int row = idx / (PADC - dqk), cc = dqk + idx - row * (PADC - dqk);
       reinterpret_cast<float*>(smem + (row / (2 * kChunk)) * cb)[(row % (2 * kChunk)) * PADC + cc] = 0.0f;
     }
+    for (int idx = threadIdx.x; idx < 4 * kChunk * (RPC - nrows); idx += NW * 32) {  // v, dh rows past the CTA's
+      const int row = idx / (RPC - nrows), r = nrows + idx - row * (RPC - nrows);
+      const int buf = row / (2 * kChunk), arr = (row / kChunk) & 1, t = row % kChunk;
+      const Chunk<T> cbuf = chunk_at<T>(smem + buf * cb, qs, RPC);
+      (arr ? cbuf.dh : cbuf.v)[t * RPC + r] = 0.0f;
+    }
+  }
   const int nchunks = (Tn + kChunk - 1) / kChunk;
   const int myrow = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
   const bool writer = (lane & 3) == 0;
@@ -331,9 +370,11 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
     }
     __syncthreads();
     const Chunk<T> b = chunk_at<T>(smem + (ch & 1) * cb, qs, RPC);
-    if (!kWide) widen_qk<T, PADC>(sx, b.q, b.k, cnt, dqk);
+    widen<T, PADC, RPC>(sx, b, cnt, dqk, nrows, has_o);
     const float* qf = kWide ? reinterpret_cast<const float*>(b.q) : sx.qf;
     const float* kf = kWide ? reinterpret_cast<const float*>(b.k) : sx.kf;
+    const float* vf = kWide ? reinterpret_cast<const float*>(b.v) : sx.vf;
+    const float* dhf = kWide ? reinterpret_cast<const float*>(b.dh) : sx.dhf;
     if (warp == 0) {
       // the stabilizer over the chunk: m_t = max(log f_t + m_{t-1}, i~_t)
       const bool on = lane < cnt;
@@ -354,18 +395,8 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
       fold_scale(c, nn, S, sx.tsc[tt]);
       const float a = __fdividef(sx.tsc[kChunk + tt] * scale, S);   // k's coefficient in the scaled update
       float vr[kRW], dr[kRW];
-      {
-        const bool ok = lane < kRW && wrow + lane < nrows;
-        const float vv = ok ? Elem<T>::load(b.v, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        const float dhv = ok ? Elem<T>::load(b.dh, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        const float ov = ok && has_o ? Elem<T>::load(b.o, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        const float dht = has_o ? sigmoid(ov) * dhv : dhv;
-#pragma unroll
-        for (int i = 0; i < kRW; ++i) {
-          vr[i] = __shfl_sync(0xffffffffu, vv, i);
-          dr[i] = __shfl_sync(0xffffffffu, dht, i);
-        }
-      }
+      load_rows(vf + tt * RPC + wrow, vr);
+      load_rows(dhf + tt * RPC + wrow, dr);
       float dot[kRW];
 #pragma unroll
       for (int i = 0; i < kRW; ++i) dot[i] = 0.0f;
@@ -418,14 +449,11 @@ rbwd_forward_kernel(Inputs in, T* __restrict__ dog, float* __restrict__ qpart, f
           float share = 0.0f;
           for (int r = lane; r < nrows; r += 32) {
             const float hv = hs * sx.gbuf[j * RPC + r];
-            const float dhv = Elem<T>::load(b.dh, (size_t)tj * RPC + r);
-            if (has_o) {
-              const float so = sigmoid(Elem<T>::load(b.o, (size_t)tj * RPC + r));
-              share = fmaf(hv, so * dhv, share);
-              Elem<T>::store(dog, (tok0 + t0 + tj) * dv + r0 + r, hv * so * (1.0f - so) * dhv);   // (70)
-            } else {
-              share = fmaf(hv, dhv, share);
-            }
+            const float dht = dhf[tj * RPC + r];
+            share = fmaf(hv, dht, share);
+            if (has_o)   // (70): h~ sigma'(o~) dh = h~ (1 - sigma(o~)) dh~
+              Elem<T>::store(dog, (tok0 + t0 + tj) * dv + r0 + r,
+                             hv * (1.0f - sigmoid(Elem<T>::load(b.o, (size_t)tj * RPC + r))) * dht);
           }
           share = warp_sum(share);
           if (lane == 0) {
@@ -485,11 +513,18 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
   const int qs = kWide ? PADC : dqk;
   const size_t cb = chunk_bytes<T>(qs, RPC);
   const Scratch sx = scratch_at(smem + 2 * cb, PADC, NW, kWide);
-  if (kWide)                          // the padding columns of both chunk buffers stay zero
-    for (int idx = threadIdx.x; idx < 4 * kChunk * (PADC - dqk); idx += NW * 32) {
+  if constexpr (kWide) {              // what staging never writes stays zero in both chunk buffers:
+    for (int idx = threadIdx.x; idx < 4 * kChunk * (PADC - dqk); idx += NW * 32) {   // q, k columns past d_qk
       const int row = idx / (PADC - dqk), cc = dqk + idx - row * (PADC - dqk);
       reinterpret_cast<float*>(smem + (row / (2 * kChunk)) * cb)[(row % (2 * kChunk)) * PADC + cc] = 0.0f;
     }
+    for (int idx = threadIdx.x; idx < 4 * kChunk * (RPC - nrows); idx += NW * 32) {  // v, dh rows past the CTA's
+      const int row = idx / (RPC - nrows), r = nrows + idx - row * (RPC - nrows);
+      const int buf = row / (2 * kChunk), arr = (row / kChunk) & 1, t = row % kChunk;
+      const Chunk<T> cbuf = chunk_at<T>(smem + buf * cb, qs, RPC);
+      (arr ? cbuf.dh : cbuf.v)[t * RPC + r] = 0.0f;
+    }
+  }
   const int nchunks = (Tn + kChunk - 1) / kChunk;
   const int myrow = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
   const bool writer = (lane & 3) == 0;
@@ -525,9 +560,11 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
     }
     __syncthreads();
     const Chunk<T> b = chunk_at<T>(smem + (ch & 1) * cb, qs, RPC);
-    if (!kWide) widen_qk<T, PADC>(sx, b.q, b.k, cnt, dqk);
+    widen<T, PADC, RPC>(sx, b, cnt, dqk, nrows, has_o);
     const float* qf = kWide ? reinterpret_cast<const float*>(b.q) : sx.qf;
     const float* kf = kWide ? reinterpret_cast<const float*>(b.k) : sx.kf;
+    const float* vf = kWide ? reinterpret_cast<const float*>(b.v) : sx.vf;
+    const float* dhf = kWide ? reinterpret_cast<const float*>(b.dh) : sx.dhf;
     if (warp == 0) {
       // lane p takes the p-th token in processing order, tt = cnt-1-p:
       // nu_t = max(log f_{t+1} + nu_{t+1}, -log N_t)
@@ -555,18 +592,10 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
       fold_scale(dc, dn, S, sx.tsc[tt]);
       const float bs = __fdividef(sx.tsc[kChunk + tt], S);
       float vr[kRW], dr[kRW];
-      {
-        const bool ok = lane < kRW && wrow + lane < nrows;
-        const float vv = ok ? Elem<T>::load(b.v, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        const float dhv = ok ? Elem<T>::load(b.dh, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        const float ov = ok && has_o ? Elem<T>::load(b.o, (size_t)tt * RPC + wrow + lane) : 0.0f;
-        const float dht = (has_o ? sigmoid(ov) * dhv : dhv) * bs;
+      load_rows(vf + tt * RPC + wrow, vr);
+      load_rows(dhf + tt * RPC + wrow, dr);
 #pragma unroll
-        for (int i = 0; i < kRW; ++i) {
-          vr[i] = __shfl_sync(0xffffffffu, vv, i);
-          dr[i] = __shfl_sync(0xffffffffu, dht, i);
-        }
-      }
+      for (int i = 0; i < kRW; ++i) dr[i] *= bs;
       const float cn = -bs * sx.tsc[3 * kChunk + tt];
       float dot[kRW];
 #pragma unroll
