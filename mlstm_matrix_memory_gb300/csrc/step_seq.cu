@@ -123,8 +123,54 @@ __device__ __forceinline__ float2 ld2(const __nv_bfloat16* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
 }
 
+// Eight consecutive row values (16-byte aligned), the same for every lane.
+__device__ __forceinline__ void load8(const float* p, float (&x)[kRW]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[kRW]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+// Inclusive max-plus scan over the lanes: x_t = max(g_t + x_{t-1}, h_t) from
+// x_{-1} = x0, in closed form x_t = cs_t + max(x0, max_{j<=t}(h_j - cs_j))
+// with cs the prefix sum of g.  Returns x_t; *xprev gets x_{t-1}.
+__device__ __forceinline__ float maxplus_scan(float g, float h, float x0, int lane, float* xprev) {
+  float cs = g;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, cs, off);
+    if (lane >= off) cs += y;
+  }
+  float mx = h - cs;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, mx, off);
+    if (lane >= off) mx = fmaxf(mx, y);
+  }
+  const float x = cs + fmaxf(x0, mx);
+  const float up = __shfl_up_sync(0xffffffffu, x, 1);
+  *xprev = lane == 0 ? x0 : up;
+  return x;
+}
+
+constexpr float kRenorm = 1.0f / 16777216.0f;   // 2^-24
+
 // NC = columns per lane (d_qk <= 32 * NC, NC even).  Lane l holds the column
-// pairs (2l + 64u, 2l + 64u + 1), u < NC/2, so every load moves a pair.
+// pairs (2l + 64u, 2l + 64u + 1), u < NC/2, so every load moves a pair.  Each
+// warp keeps its rows of C and its copy of n as S * (C^, n^) with one scale
+// S: the decay f' multiplies S alone and the rank-one term is one fused
+// multiply-add per entry; S is folded back into the entries when it falls
+// below 2^-24.  The chunk's f', i' and e^-m come from one warp (a max-plus
+// scan of the stabilizer recurrence) before its tokens are processed.
 template <typename T, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
 step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict__ m,
@@ -143,6 +189,7 @@ step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict_
                         (reinterpret_cast<uintptr_t>(v) & 15) == 0 && (reinterpret_cast<uintptr_t>(o) & 15) == 0;
   const size_t tok0 = (size_t)bh * L;
   const size_t cb = chunk_bytes<T>(dqk);
+  float* tsc = reinterpret_cast<float*>(smem + 2 * cb);     // [3][kChunk]: f', i', e^-m of the chunk
   const int nchunks = (L + kChunk - 1) / kChunk;
   // after the in-warp reduction, lane l (l % 4 == 0) holds row `myrow` of the warp
   const int myrow = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
@@ -150,6 +197,12 @@ step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict_
 
   stage_chunk(chunk_buf<T>(smem, dqk), q, k, v, o, ig, fg, tok0, min(kChunk, L), dqk, dv, r0, nrows, vec_rows);
   cp_async_commit();
+  // rows of v and o that staging never writes (past this CTA's rows) stay zero
+  for (int idx = threadIdx.x; idx < 2 * kChunk * (kRowsPerCta - nrows); idx += kThreads) {
+    const int row = idx / (kRowsPerCta - nrows), r = nrows + idx - row * (kRowsPerCta - nrows);
+    const ChunkBuf<T> cbuf = chunk_buf<T>(smem + (row / kChunk) * cb, dqk);
+    Elem<T>::store(cbuf.v, (size_t)(row % kChunk) * kRowsPerCta + r, 0.0f);
+  }
 
   float c[kRW][NC], nn[NC];
 #pragma unroll
@@ -170,7 +223,8 @@ step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict_
     nn[2 * u] = x.x;
     nn[2 * u + 1] = x.y;
   }
-  float mm = m[bh];
+  float m_carry = m[bh];              // warp 0: m after the last processed chunk
+  float S = 1.0f;
   cluster_sync();                     // every CTA of the head has read n and m
 
   for (int ch = 0; ch < nchunks; ++ch) {
@@ -185,43 +239,58 @@ step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict_
     }
     __syncthreads();                  // chunk ch is in shared memory for every thread
     const ChunkBuf<T> b = chunk_buf<T>(smem + (ch & 1) * cb, dqk);
+    if (warp == 0) {
+      // m_t = max(log f_t + m_{t-1}, i~_t) over the chunk
+      const bool on = lane < cnt;
+      const float lf = on ? (forget_exp ? b.fg[lane] : log_sigmoid(b.fg[lane])) : 0.0f;
+      const float igv = on ? b.ig[lane] : -INFINITY;
+      float mprev;
+      const float mt = maxplus_scan(lf, igv, m_carry, lane, &mprev);
+      if (on) {
+        tsc[lane] = expf(lf + mprev - mt);                 // f'
+        tsc[kChunk + lane] = expf(igv - mt);               // i'
+        tsc[2 * kChunk + lane] = expf(-mt);                // normalizer floor
+      }
+      m_carry = __shfl_sync(0xffffffffu, mt, cnt - 1);
+    }
+    __syncthreads();
     for (int tt = 0; tt < cnt; ++tt) {
-      float kk[NC], qq[NC];
+      const float s2 = S * tsc[tt];
+      if (s2 < kRenorm) {             // fold the scale into the entries
+#pragma unroll
+        for (int i = 0; i < kRW; ++i)
+#pragma unroll
+          for (int u = 0; u < NC; ++u) c[i][u] *= s2;
+#pragma unroll
+        for (int u = 0; u < NC; ++u) nn[u] *= s2;
+        S = 1.0f;
+      } else {
+        S = s2;
+      }
+      const float a = __fdividef(tsc[kChunk + tt] * scale, S);   // k's coefficient in the scaled update
+      float vr[kRW];
+      load8(b.v + (size_t)tt * kRowsPerCta + wrow, vr);
+      float dot[kRW];
+#pragma unroll
+      for (int i = 0; i < kRW; ++i) dot[i] = 0.0f;
+      float nq = 0.0f;
 #pragma unroll
       for (int u = 0; u < NP; ++u) {
         const int col = 2 * lane + 64 * u;
         const float2 kx = col < dqk ? ld2(b.k + (size_t)tt * dqk + col) : make_float2(0.f, 0.f);
         const float2 qx = col < dqk ? ld2(b.q + (size_t)tt * dqk + col) : make_float2(0.f, 0.f);
-        kk[2 * u] = kx.x * scale;
-        kk[2 * u + 1] = kx.y * scale;
-        qq[2 * u] = qx.x;
-        qq[2 * u + 1] = qx.y;
-      }
-      const float vv = (lane < kRW && wrow + lane < nrows)
-                           ? Elem<T>::load(b.v, (size_t)tt * kRowsPerCta + wrow + lane) : 0.0f;
-      const float lf = forget_exp ? b.fg[tt] : log_sigmoid(b.fg[tt]);   // exponential or sigmoid forget
-      const float igv = b.ig[tt];
-      const float m_new = fmaxf(lf + mm, igv);
-      const float fp = expf(lf + mm - m_new);
-      const float ip = expf(igv - m_new);
-      mm = m_new;
-      float nq = 0.0f;
+        const float k0 = kx.x * a, k1 = kx.y * a;
+        nn[2 * u] += k0;
+        nn[2 * u + 1] += k1;
+        nq = fmaf(nn[2 * u], qx.x, nq);
+        nq = fmaf(nn[2 * u + 1], qx.y, nq);
 #pragma unroll
-      for (int u = 0; u < NC; ++u) {
-        nn[u] = fmaf(fp, nn[u], ip * kk[u]);
-        nq = fmaf(nn[u], qq[u], nq);
-      }
-      float dot[kRW];
-#pragma unroll
-      for (int i = 0; i < kRW; ++i) {
-        const float iv = ip * __shfl_sync(0xffffffffu, vv, i);
-        float d = 0.0f;
-#pragma unroll
-        for (int u = 0; u < NC; ++u) {
-          c[i][u] = fmaf(fp, c[i][u], iv * kk[u]);
-          d = fmaf(c[i][u], qq[u], d);
+        for (int i = 0; i < kRW; ++i) {
+          c[i][2 * u] = fmaf(vr[i], k0, c[i][2 * u]);
+          c[i][2 * u + 1] = fmaf(vr[i], k1, c[i][2 * u + 1]);
+          dot[i] = fmaf(c[i][2 * u], qx.x, dot[i]);
+          dot[i] = fmaf(c[i][2 * u + 1], qx.y, dot[i]);
         }
-        dot[i] = d;
       }
       nq = warp_sum(nq);
       // reduce the eight row sums across the warp in halving steps: after the
@@ -238,8 +307,8 @@ step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict_
       g += __shfl_xor_sync(0xffffffffu, g, 2);
       g += __shfl_xor_sync(0xffffffffu, g, 1);
       if (writer) {
-        const float nrm = fmaxf(fabsf(nq), expf(-m_new));
-        float hv = nrm > 0.0f ? g / nrm : 0.0f;
+        const float nrm = fmaxf(fabsf(nq * S), tsc[2 * kChunk + tt]);
+        float hv = nrm > 0.0f ? g * S / nrm : 0.0f;
         if (o) hv *= sigmoid(Elem<T>::load(b.o, (size_t)tt * kRowsPerCta + wrow + myrow));
         Elem<T>::store(h, (tok0 + t0 + tt) * dv + r0 + wrow + myrow, hv);
       }
@@ -254,16 +323,18 @@ step_seq_kernel(float* __restrict__ C, float* __restrict__ n, float* __restrict_
     for (int u = 0; u < NP; ++u) {
       const int col = 2 * lane + 64 * u;
       if (row < dv && col < dqk)
-        *reinterpret_cast<float2*>(C + ((size_t)bh * dv + row) * dqk + col) = make_float2(c[i][2 * u], c[i][2 * u + 1]);
+        *reinterpret_cast<float2*>(C + ((size_t)bh * dv + row) * dqk + col) =
+            make_float2(c[i][2 * u] * S, c[i][2 * u + 1] * S);
     }
   }
   if (rank == 0 && warp == 0) {
 #pragma unroll
     for (int u = 0; u < NP; ++u) {
       const int col = 2 * lane + 64 * u;
-      if (col < dqk) *reinterpret_cast<float2*>(n + (size_t)bh * dqk + col) = make_float2(nn[2 * u], nn[2 * u + 1]);
+      if (col < dqk)
+        *reinterpret_cast<float2*>(n + (size_t)bh * dqk + col) = make_float2(nn[2 * u] * S, nn[2 * u + 1] * S);
     }
-    if (lane == 0) m[bh] = mm;
+    if (lane == 0) m[bh] = m_carry;
   }
 }
 
@@ -272,7 +343,7 @@ cudaError_t launch_nc(const StepArgs& a, int L, int R, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.BH * R));
   cfg.blockDim = dim3(kThreads);
-  const size_t smem = 2 * chunk_bytes<T>(a.dqk);
+  const size_t smem = 2 * chunk_bytes<T>(a.dqk) + 3 * kChunk * sizeof(float);
   if (cudaFuncSetAttribute(step_seq_kernel<T, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return cudaErrorInvalidValue;
