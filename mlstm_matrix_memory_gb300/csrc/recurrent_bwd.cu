@@ -656,8 +656,20 @@ rbwd_backward_kernel(Inputs in, const float* __restrict__ spart, const float* __
   }
 }
 
-// Sweep 3: one warp per token sums the R shares of dq and dk, writes them,
-// d i~ = k.dk, and r = q.dq - k.dk.
+// Sweep 3: one warp per token sums the R shares of dq and dk (four columns a
+// lane at a time), writes them, d i~ = k.dk, and r = q.dq - k.dk.
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) { return *reinterpret_cast<const float4*>(p); }
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256)
 rbwd_combine_kernel(const T* __restrict__ q, const T* __restrict__ k, const float* __restrict__ qpart,
@@ -667,16 +679,22 @@ rbwd_combine_kernel(const T* __restrict__ q, const T* __restrict__ k, const floa
   const int lane = threadIdx.x & 31;
   if (tok >= BHT) return;
   float qd = 0.0f, kd = 0.0f;
-  for (int c = lane; c < dqk; c += 32) {
-    float a = 0.0f, bsum = 0.0f;
+  for (int c = 4 * lane; c < dqk; c += 128) {      // d_qk is a multiple of 8
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
     for (int r = 0; r < R; ++r) {
-      a += qpart[((size_t)r * BHT + tok) * dqk + c];
-      bsum += kpart[((size_t)r * BHT + tok) * dqk + c];
+      const float4 x = *reinterpret_cast<const float4*>(qpart + ((size_t)r * BHT + tok) * dqk + c);
+      const float4 y = *reinterpret_cast<const float4*>(kpart + ((size_t)r * BHT + tok) * dqk + c);
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
     }
-    Elem<T>::store(dq, (size_t)tok * dqk + c, a);
-    Elem<T>::store(dk, (size_t)tok * dqk + c, bsum);
-    qd = fmaf(Elem<T>::load(q, (size_t)tok * dqk + c), a, qd);
-    kd = fmaf(Elem<T>::load(k, (size_t)tok * dqk + c), bsum, kd);
+    const size_t o = (size_t)tok * dqk + c;
+    Elem<T>::store(dq, o, a.x); Elem<T>::store(dq, o + 1, a.y);
+    Elem<T>::store(dq, o + 2, a.z); Elem<T>::store(dq, o + 3, a.w);
+    Elem<T>::store(dk, o, b.x); Elem<T>::store(dk, o + 1, b.y);
+    Elem<T>::store(dk, o + 2, b.z); Elem<T>::store(dk, o + 3, b.w);
+    const float4 qv = load4<T>(q + o), kv = load4<T>(k + o);
+    qd = fmaf(qv.x, a.x, fmaf(qv.y, a.y, fmaf(qv.z, a.z, fmaf(qv.w, a.w, qd))));
+    kd = fmaf(kv.x, b.x, fmaf(kv.y, b.y, fmaf(kv.z, b.z, fmaf(kv.w, b.w, kd))));
   }
   qd = warp_sum(qd);
   kd = warp_sum(kd);
@@ -686,28 +704,36 @@ rbwd_combine_kernel(const T* __restrict__ q, const T* __restrict__ k, const floa
   }
 }
 
-// Sweep 4: one warp per head, suffix sums in fp64 from the last token down.
-__global__ void __launch_bounds__(32)
+// Sweep 4: one CTA of 256 threads per head.  Each thread sums its run of
+// consecutive tokens in fp64, the CTA scans the 256 run sums (suffix
+// direction), and each thread then walks its run from the end.
+constexpr int kScanThreads = 256;
+
+__global__ void __launch_bounds__(kScanThreads)
 rbwd_forget_kernel(const float* __restrict__ rr, const float* __restrict__ fg, float* __restrict__ dfg, int Tn,
                    int forget_exp) {
+  __shared__ double part[kScanThreads];
   const size_t base = (size_t)blockIdx.x * Tn;
-  const int lane = threadIdx.x;
-  double carry = 0.0;                      // sum over tokens after the current block of 32
-  for (int hi = Tn; hi > 0; hi -= 32) {
-    const int t = hi - 1 - lane;           // lane 0 takes the latest token of the block
-    double x = t >= 0 ? (double)rr[base + t] : 0.0;
-    // inclusive prefix over lanes 0..lane = suffix over tokens t..hi-1
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
-    }
-    if (t >= 0) {
-      const float f = fg[base + t];
-      const double act = forget_exp ? 1.0 : (double)sigmoid(-f);   // dlog f / df~ (eq 104)
-      dfg[base + t] = (float)((carry + x) * act);
-    }
-    carry += __shfl_sync(0xffffffffu, x, 31);
+  const int tid = threadIdx.x;
+  const int per = (Tn + kScanThreads - 1) / kScanThreads;
+  const int lo = min(Tn, tid * per), hi = min(Tn, lo + per);
+  double run = 0.0;
+  for (int t = lo; t < hi; ++t) run += (double)rr[base + t];
+  part[tid] = run;
+  __syncthreads();
+  // suffix scan over the run sums: after it, part[i] = sum of runs i..255
+  for (int off = 1; off < kScanThreads; off <<= 1) {
+    const double y = tid + off < kScanThreads ? part[tid + off] : 0.0;
+    __syncthreads();
+    part[tid] += y;
+    __syncthreads();
+  }
+  double acc = tid + 1 < kScanThreads ? part[tid + 1] : 0.0;   // tokens after this run
+  for (int t = hi - 1; t >= lo; --t) {
+    acc += (double)rr[base + t];
+    const float f = fg[base + t];
+    const double act = forget_exp ? 1.0 : (double)sigmoid(-f);   // dlog f / df~ (eq 104)
+    dfg[base + t] = (float)(acc * act);
   }
 }
 
@@ -817,7 +843,7 @@ cudaError_t launch_all(const Inputs& in, void* dq, void* dk, void* dvout, float*
   rbwd_combine_kernel<T><<<(unsigned)((BHT + 7) / 8), 256, 0, st>>>(
       static_cast<const T*>(in.q), static_cast<const T*>(in.k), qpart, kpart, static_cast<T*>(dq),
       static_cast<T*>(dk), dig, rr, dqk, R, BHT);
-  rbwd_forget_kernel<<<(unsigned)BH, 32, 0, st>>>(rr, in.fg, dfg, Tn, forget_exp);
+  rbwd_forget_kernel<<<(unsigned)BH, kScanThreads, 0, st>>>(rr, in.fg, dfg, Tn, forget_exp);
   return cudaGetLastError();
 }
 
