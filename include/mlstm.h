@@ -209,13 +209,24 @@ int mlstm_step_seq_opt(float *C, float *n, float *m,
  *   dh         [B,H,T,d_v]  dtype: dL/dH~
  *   dq, dk     [B,H,T,d_qk] dtype out,   dv [B,H,T,d_v] dtype out
  *   d_igate, d_fgate  [B,H,T] fp32 out
- *   workspace  mlstm_parallel_bwd_workspace(B,H,T,dtype) bytes of device
- *              memory, 256-byte aligned: it holds four T x T matrices per head
- *              (fp32 S and dL/dC, the dtype's G and P), so it grows as B*H*T^2
- *              (about 1.6 GB for B=8, H=4, T=2048, bf16).
+ *   workspace  256-byte aligned device memory of
+ *              mlstm_parallel_bwd_workspace_ex(B,H,T,d_qk,d_v,dtype) bytes
+ *              (the size of the path that will run), or of
+ *              mlstm_parallel_bwd_workspace(B,H,T,dtype) bytes (enough for
+ *              either path).
+ * Two paths:
+ *  - bf16 with d_qk and d_v multiples of 8, on the sm_100 family: a forward
+ *    pass gives H~, n and the signed row sums b; one tensor-core kernel forms
+ *    S = QK^T/sqrt(d) and dC = dH~ V^T per 128 x 128 tile in TMEM and writes
+ *    G = D' (.) dC~' and P = C~'/n (bf16) and the tile's row and column sums
+ *    of dD~; dQ, dK, dV are batched GEMMs over G and P (cuBLAS).  Workspace:
+ *    two bf16 T x T matrices per head (about 0.54 GB for B=8, H=4, T=2048).
+ *  - otherwise the five T x T products are batched GEMMs (cuBLAS) with fp32
+ *    S and dL/dC materialised (about 1.6 GB for B=8, H=4, T=2048, bf16).
  * Requirements: 1 <= T <= 16384; 1 <= d_qk, d_v <= 512; no output may alias
- * an input.  The five T x T products run as batched GEMMs (cuBLAS). */
+ * an input. */
 size_t mlstm_parallel_bwd_workspace(int B, int H, int T, int dtype);
+size_t mlstm_parallel_bwd_workspace_ex(int B, int H, int T, int d_qk, int d_v, int dtype);
 
 int mlstm_parallel_bwd(const void *q, const void *k, const void *v,
                        const float *igate_pre, const float *fgate_pre, const void *dh,

@@ -70,6 +70,8 @@ def library() -> ctypes.CDLL:
         lib.mlstm_parallel_fwd_host.restype = i
         lib.mlstm_parallel_bwd_workspace.argtypes = [i, i, i, i]
         lib.mlstm_parallel_bwd_workspace.restype = sz
+        lib.mlstm_parallel_bwd_workspace_ex.argtypes = [i] * 6
+        lib.mlstm_parallel_bwd_workspace_ex.restype = sz
         lib.mlstm_parallel_bwd.argtypes = [vp] * 11 + [i] * 6 + [vp, sz, vp]
         lib.mlstm_parallel_bwd.restype = i
         op = ctypes.POINTER(_Options)
@@ -289,7 +291,7 @@ def parallel_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: t
     _need(igate_pre, "igate_pre", (B, H, T), torch.float32, dev)
     _need(fgate_pre, "fgate_pre", (B, H, T), torch.float32, dev)
     _need(dh, "dh", (B, H, T, dv), q.dtype, dev)
-    need = int(lib.mlstm_parallel_bwd_workspace(B, H, T, _DTYPES[q.dtype]))
+    need = int(lib.mlstm_parallel_bwd_workspace_ex(B, H, T, dqk, dv, _DTYPES[q.dtype]))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)

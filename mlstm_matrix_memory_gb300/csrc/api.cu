@@ -45,6 +45,15 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 size_t gate_array_bytes(long long BHT) { return round256((size_t)BHT * sizeof(float)); }
 
 }  // namespace
+
+bool current_status(DevStatus* out) {
+  int* status = nullptr;
+  if (status_ptr(&status) != kOk) return false;
+  out->word = status;
+  out->spin_limit = g_spin_limit.load();
+  return true;
+}
+
 }  // namespace mlstm
 
 using namespace mlstm;

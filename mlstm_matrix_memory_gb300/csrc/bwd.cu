@@ -22,7 +22,10 @@
 // the workspace, for all heads at once.
 #include <cublas_v2.h>
 
+#include <algorithm>
+#include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "mlstm.h"
@@ -192,12 +195,56 @@ bool gemm(cublasHandle_t h, cublasOperation_t ta, cublasOperation_t tb, int m, i
                                     ldc, sc, batch, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
 }
 
+int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
+                const void* dh, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int BH, int T, int d_qk,
+                int d_v, void* workspace, cudaStream_t st);
+
+// Workspace of the tensor-core path: gate terms, the forward's H~ (d_v
+// columns) and row statistics, bf16 G and P with rows of ldT = T rounded up
+// to 8 (16-byte pitch for TMA), the tiles' row and column sums of dD~, R,
+// Ccol.
+struct TcLayout {
+  size_t gate, hf, rowv, G, P, part, R, Ccol, total;
+  int ldT, nb;
+};
+
+TcLayout tc_layout(long long BH, int T, int dv) {
+  TcLayout L;
+  L.ldT = (T + 7) & ~7;
+  L.nb = (T + 127) / 128;
+  L.gate = mlstm_parallel_fwd_workspace(1, (int)BH, T);
+  L.hf = r256((size_t)BH * T * dv * 2);
+  L.rowv = r256((size_t)BH * T * 4);                // one of: n, b, 1/n, db
+  L.G = r256((size_t)BH * T * L.ldT * 2);
+  L.P = L.G;
+  L.part = r256((size_t)BH * L.nb * T * 4);         // one of: Rpart, Cpart
+  L.R = r256((size_t)BH * T * 4);
+  L.Ccol = L.R;
+  L.total = L.gate + L.hf + 4 * L.rowv + L.G + L.P + 2 * L.part + L.R + L.Ccol;
+  return L;
+}
+
+// The tensor-core path runs for bf16 on the sm_100 family unless
+// MLSTM_BWD_PATH=blas in the environment selects the cuBLAS path (tests).
+bool use_tc_path(int T, int dqk, int dv, int dtype) {
+  static const char* force = getenv("MLSTM_BWD_PATH");
+  if (force && force[0] == 'b') return false;
+  return bwd_tc_supported(T, dqk, dv, dtype) && device_is_sm100_family();
+}
+
 }  // namespace
 }  // namespace mlstm
 
 using namespace mlstm;
 
 extern "C" {
+
+size_t mlstm_parallel_bwd_workspace_ex(int B, int H, int T, int d_qk, int d_v, int dtype) {
+  if (B <= 0 || H <= 0 || T <= 0 || T > kMaxBwdT || d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return 0;
+  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return 0;
+  if (use_tc_path(T, d_qk, d_v, dtype)) return tc_layout((long long)B * H, T, d_v).total;
+  return bwd_layout((long long)B * H, T, dtype).total;
+}
 
 size_t mlstm_parallel_bwd_workspace(int B, int H, int T, int dtype) {
   if (B <= 0 || H <= 0 || T <= 0 || T > kMaxBwdT) return 0;
@@ -216,9 +263,13 @@ int mlstm_parallel_bwd(const void* q, const void* k, const void* v, const float*
   if (BH == 0 || T == 0) return MLSTM_OK;
   if (!q || !k || !v || !igate_pre || !fgate_pre || !dh || !dq || !dk || !dv || !d_igate || !d_fgate)
     return MLSTM_EINVAL;
-  if (!workspace || workspace_bytes < mlstm_parallel_bwd_workspace(B, H, T, dtype)) return MLSTM_EWORKSPACE;
+  if (!workspace) return MLSTM_EWORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLSTM_EALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_tc_path(T, d_qk, d_v, dtype) && workspace_bytes >= tc_layout(BH, T, d_v).total)
+    return bwd_tc_path(q, k, v, igate_pre, fgate_pre, dh, dq, dk, dv, d_igate, d_fgate, (int)BH, T, d_qk, d_v,
+                       workspace, st);
+  if (workspace_bytes < mlstm_parallel_bwd_workspace(B, H, T, dtype)) return MLSTM_EWORKSPACE;
   const BwdLayout L = bwd_layout(BH, T, dtype);
   char* w = static_cast<char*>(workspace);
   char* gate_ws = w;
@@ -285,3 +336,71 @@ int mlstm_parallel_bwd(const void* q, const void* k, const void* v, const float*
 }
 
 }  // extern "C"
+
+namespace mlstm {
+namespace {
+
+// Tensor-core path: gate pass, forward (H~, n, signed b), the tile kernel
+// (G, P, row and column sums of dD~), the three products dQ, dK, dV over G
+// and P (cuBLAS), the gate gradients.
+int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
+                const void* dh, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int BH, int T, int d_qk,
+                int d_v, void* workspace, cudaStream_t st) {
+  const TcLayout L = tc_layout(BH, T, d_v);
+  char* w = static_cast<char*>(workspace);
+  char* gate_ws = w;
+  char* hf = gate_ws + L.gate;
+  float* nrow = reinterpret_cast<float*>(hf + L.hf);
+  float* brow = reinterpret_cast<float*>(reinterpret_cast<char*>(nrow) + L.rowv);
+  float* invn = reinterpret_cast<float*>(reinterpret_cast<char*>(brow) + L.rowv);
+  float* dbv = reinterpret_cast<float*>(reinterpret_cast<char*>(invn) + L.rowv);
+  char* G = reinterpret_cast<char*>(dbv) + L.rowv;
+  char* P = G + L.G;
+  float* Rpart = reinterpret_cast<float*>(P + L.P);
+  float* Cpart = reinterpret_cast<float*>(reinterpret_cast<char*>(Rpart) + L.part);
+  float* R = reinterpret_cast<float*>(reinterpret_cast<char*>(Cpart) + L.part);
+  float* Ccol = reinterpret_cast<float*>(reinterpret_cast<char*>(R) + L.R);
+
+  int rc = mlstm_gate_prep(igate_pre, fgate_pre, 1, BH, T, gate_ws, L.gate, st);
+  if (rc != MLSTM_OK) return rc;
+  const size_t arr = L.gate / 3;
+  GateTerms g{reinterpret_cast<float*>(gate_ws), reinterpret_cast<float*>(gate_ws + arr),
+              reinterpret_cast<float*>(gate_ws + 2 * arr)};
+  DevStatus ds;
+  if (!current_status(&ds)) return MLSTM_ECUDA;
+  const float s = (float)(1.0 / sqrt((double)d_qk));
+  // forward: H~, n and the signed row sums b (eqs 79-86)
+  FwdArgs fa;
+  fa.q = q; fa.k = k; fa.v = v; fa.h = hf; fa.m_out = nullptr; fa.n_out = nrow; fa.b_out = brow;
+  fa.g = g; fa.BH = BH; fa.T = T; fa.dqk = d_qk; fa.dv = d_v; fa.dtype = kBF16; fa.scale = s; fa.st = ds;
+  rc = launch_fwd_tc(fa, st);
+  if (rc == kUnsupported) rc = launch_fwd_simt(fa, st) == cudaSuccess ? kOk : kCuda;
+  if (rc != kOk) return rc;
+  BwdTileArgs ta;
+  ta.q = q; ta.k = k; ta.v = v; ta.dh = dh; ta.h = hf; ta.nrow = nrow; ta.brow = brow; ta.g = g;
+  ta.invn = invn; ta.db = dbv; ta.G = G; ta.P = P; ta.Rpart = Rpart; ta.Cpart = Cpart; ta.R = R; ta.Ccol = Ccol;
+  ta.BH = BH; ta.T = T; ta.ldT = L.ldT; ta.dqk = d_qk; ta.dv = d_v; ta.scale = s; ta.st = ds;
+  ta.with_upper = 1;
+  rc = launch_bwd_tiles(ta, st);
+  if (rc != kOk) return rc;
+
+  cublasHandle_t h = blas_handle();
+  if (!h || cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return MLSTM_ECUDA;
+  const cudaDataType et = CUDA_R_16BF;
+  const long long TT = (long long)T * L.ldT, Tq = (long long)T * d_qk, Tv = (long long)T * d_v;
+  const int ld = L.ldT;
+  // row-major dQ = s G K  <=>  col-major dQ^T = s K^T G^T          (98)
+  if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_N, d_qk, T, T, s, k, et, d_qk, Tq, G, et, ld, TT, dq, et, d_qk, Tq, BH))
+    return MLSTM_ECUDA;
+  // row-major dK = s G^T Q  <=>  col-major dK^T = s Q^T G          (99)
+  if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, d_qk, T, T, s, q, et, d_qk, Tq, G, et, ld, TT, dk, et, d_qk, Tq, BH))
+    return MLSTM_ECUDA;
+  // row-major dV = P^T dH  <=>  col-major dV^T = dH^T P            (100)
+  if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, d_v, T, T, 1.0f, dh, et, d_v, Tv, P, et, ld, TT, dv, et, d_v, Tv, BH))
+    return MLSTM_ECUDA;
+  bwd_gates_kernel<<<(unsigned)BH, 1024, 0, st>>>(R, Ccol, fgate_pre, d_igate, d_fgate, T);
+  return cudaGetLastError() == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
+}
+
+}  // namespace
+}  // namespace mlstm

@@ -1,0 +1,384 @@
+// Tiles of the stabilized parallel mLSTM backward on the tensor cores.
+//
+// "xLSTM: Extended Long Short-Term Memory", part 28/30, "Parallel mLSTM
+// Backward Pass", eqs (87)-(95), (100), for bf16 q, k, v, dH~:
+//   dC     = dH~ V^T                                         (87)
+//   dn_i   = -(sum_j C~'_ij dC_ij) / n_i^2                    (89)
+//   db_i   = sign(b_i) dn_i where |b_i| > exp(-m_i), else 0   (90)
+//   G      = D' (.) (dC / n + db),   dD~ = S (.) G            (91)-(95)
+//   P      = C~' / n                                         (operand of eq 100)
+// with S = Q K^T / sqrt(d) and C~' = S (.) D'.  The row sum in eq (89) needs
+// no pass over the keys: sum_j C~'_ij dC_ij = dH~_i . (sum_j C~'_ij v_j)
+// = n_i dH~_i . h~_i, with h~ and n (and the signed b) from the forward.
+//
+// One CTA per 128 x 128 tile (query block ib, key block jb <= ib) of one head:
+//   S  = Q_ib K_jb^T      tcgen05.mma into TMEM columns 0..127
+//   dC = dH_ib V_jb^T     tcgen05.mma into TMEM columns 128..255
+// both contractions streamed through a ring of 64-column chunks (TMA, 128-byte
+// swizzle, zero fill past d).  Four epilogue warps (a row each per thread)
+// form G and P in fp32 from the TMEM rows, stage them as bf16 and store them
+// by TMA, and leave the tile's row and column sums of dD~ (the column sums
+// by a shuffle reduce-scatter, so every partial is formed in a fixed order).
+// Within the diagonal tile G and P are stored as zero above the diagonal; the
+// tiles above it are stored as zeros only when the products that follow read
+// whole matrices.  Two CTAs fit on an SM
+// (256 TMEM columns and about 97 KB of shared memory each), so one CTA's
+// epilogue overlaps the other's products.
+#include <cmath>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace mlstm {
+namespace {
+
+using namespace tc;
+
+constexpr int kTile = 128;            // query rows and keys of a tile
+constexpr int kThreads = 192;         // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
+constexpr int kNst = 3;               // ring stages
+constexpr uint32_t kStage = 32768;    // a stage: [128 rows x 64 columns] of A and of B
+constexpr uint32_t kCols = 256;       // TMEM: S in 0..127, dC in 128..255
+constexpr long long kDrainSpin = 1LL << 22;
+
+enum : int { kBarFull = 0, kBarEmpty = kNst, kBarDone = 2 * kNst, kBarDrain = 2 * kNst + 1, kNumBars = 2 * kNst + 2 };
+enum : int { kSiteTProducer = 41, kSiteTMma = 42, kSiteTEpi = 43 };
+
+struct TileParams {
+  const float* a2;
+  const float* p2;
+  const float* invn;
+  const float* db;
+  float* Rpart;
+  float* Cpart;
+  int T, BH, dqk, dv, nb;
+  int with_upper;       // 1: also store the zero tiles above the diagonal
+  float scale;
+  DevStatus st;
+};
+
+// 16-byte chunk q (8 bf16) of row r of a [128 x 64] box with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(uint32_t box, int r, int q) {
+  return box + (uint32_t)r * 128u + ((uint32_t)(q ^ (r & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_dh, const __grid_constant__ CUtensorMap tmap_v,
+                const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_p,
+                const TileParams p) {
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ uint32_t tmem_holder;
+  __shared__ int abort_flag;
+  __shared__ int issued_s;                    // chunks whose loads the producer issued
+  __shared__ float col_term[kTile];           // a2_j (diagonal tile) or 2^(a2_j - A)
+  __shared__ float col_red[4][kTile];         // per warp: column sums of dD~ over its 32 rows
+  __shared__ float amax_red[4];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &abort_flag;
+  // tiles: the lower triangle of each head (t = ib (ib + 1) / 2 + jb, jb <= ib),
+  // then, when the products read whole matrices, the tiles above it (zeros)
+  const int nb = p.nb, ntri = nb * (nb + 1) / 2, per_head = p.with_upper ? nb * nb : ntri;
+  const int bh = (int)(blockIdx.x / (unsigned)per_head);
+  const int t = (int)(blockIdx.x % (unsigned)per_head);
+  int ib, jb;
+  if (t < ntri) {
+    ib = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+    while (ib * (ib + 1) / 2 > t) --ib;
+    while ((ib + 1) * (ib + 2) / 2 <= t) ++ib;
+    jb = t - ib * (ib + 1) / 2;
+  } else {                                        // upper tile u = t - ntri: row ib, column jb > ib
+    int u = t - ntri;
+    ib = 0;
+    while (u >= nb - 1 - ib) { u -= nb - 1 - ib; ++ib; }
+    jb = ib + 1 + u;
+  }
+  const int i0 = ib * kTile, j0 = jb * kTile;
+  const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (jb > ib) {
+    // ---- above the diagonal: G and P are zero
+    if (warp >= 2) {
+      const int tz = threadIdx.x - 64;           // 128 threads zero one 16 KB box
+      uint4* z = reinterpret_cast<uint4*>(dsmem + (base - smem_u32(dsmem)));
+      for (int x = tz; x < 1024; x += 128) z[x] = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (tz == 0) {
+        for (int b2 = 0; b2 < 2 && j0 + 64 * b2 < p.T; ++b2) {   // boxes that start inside the matrix
+          tma_store_3d(&tmap_g, base, j0 + 64 * b2, i0, bh);
+          tma_store_3d(&tmap_p, base, j0 + 64 * b2, i0, bh);
+        }
+        tma_store_commit();
+        tma_store_wait_read();
+      }
+    }
+    return;
+  }
+
+  const int nq = (p.dqk + 63) / 64, nch = nq + (p.dv + 63) / 64;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    issued_s = 0;
+    for (int s = 0; s < kNst; ++s) {
+      mbar_init(bar(kBarFull + s), 1);
+      mbar_init(bar(kBarEmpty + s), 1);
+    }
+    mbar_init(bar(kBarDone), 1);
+    mbar_init(bar(kBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_holder), kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  const long long spin = p.st.spin_limit;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_dh);
+    tma_prefetch_desc(&tmap_v);
+    for (int c = 0; c < nch; ++c) {
+      const int s = c % kNst, u = c / kNst;
+      if (!mbar_wait(bar(kBarEmpty + s), (uint32_t)(u & 1) ^ 1u, spin, abort, p.st, kSiteTProducer)) break;
+      const uint32_t dst = base + (uint32_t)s * kStage;
+      mbar_arrive_expect_tx(bar(kBarFull + s), kStage);
+      if (c < nq) {
+        tma_load_3d(dst, &tmap_q, bar(kBarFull + s), 64 * c, i0, bh);
+        tma_load_3d(dst + kStage / 2, &tmap_k, bar(kBarFull + s), 64 * c, j0, bh);
+      } else {
+        tma_load_3d(dst, &tmap_dh, bar(kBarFull + s), 64 * (c - nq), i0, bh);
+        tma_load_3d(dst + kStage / 2, &tmap_v, bar(kBarFull + s), 64 * (c - nq), j0, bh);
+      }
+      issued_s = c + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(kTile, kTile, 0, 0);
+    bool ok = true;
+    for (int c = 0; c < nch && ok; ++c) {
+      const int s = c % kNst, u = c / kNst;
+      ok = mbar_wait(bar(kBarFull + s), (uint32_t)(u & 1), spin, abort, p.st, kSiteTMma);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a_addr = base + (uint32_t)s * kStage;
+      const uint64_t da = smem_desc_sw128(a_addr, 16, 1024);
+      const uint64_t db = smem_desc_sw128(a_addr + kStage / 2, 16, 1024);
+      const uint32_t d = tmem + (c < nq ? 0u : 128u);
+      const bool first = c == 0 || c == nq;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, da + 2 * kk, db + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+      mma_commit(bar(kBarEmpty + s));
+    }
+    if (ok) mma_commit(bar(kBarDone));
+    mma_commit(bar(kBarDrain));
+    for (long long w = 0; w < kDrainSpin; ++w)
+      if (mbar_try_wait(bar(kBarDrain), 0)) break;
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;               // 0..127: this thread's column for the column terms
+    const int qd = warp & 3;                       // TMEM lane quarter this warp may access
+    const int r = 32 * qd + lane;                  // tile row = TMEM lane
+    const int i = i0 + r;
+    const bool row_ok = i < p.T;
+    const size_t hb = (size_t)bh * p.T;
+    const bool diag = jb == ib;
+    // column terms
+    const int jc = j0 + et;
+    const float a2c = jc < p.T ? p.a2[hb + jc] : -INFINITY;
+    float rowf = 0.0f, p2i = 0.0f;
+    if (row_ok) p2i = p.p2[hb + i];
+    if (diag) {
+      col_term[et] = a2c;
+    } else {
+      // rank-one gate factor: D'_ij = 2^(a2_j - A) 2^(A - p2_i), A the tile's
+      // largest column term (every key of the tile precedes every query row)
+      const float m = warp_max(a2c);
+      if (lane == 0) amax_red[warp - 2] = m;
+      named_bar_sync(1, 128);
+      const float A = fmaxf(fmaxf(amax_red[0], amax_red[1]), fmaxf(amax_red[2], amax_red[3]));
+      col_term[et] = exp2f(a2c - A);
+      rowf = row_ok ? exp2f(A - p2i) : 0.0f;
+    }
+    const float invn = row_ok ? p.invn[hb + i] : 0.0f;
+    const float dbi = row_ok ? p.db[hb + i] : 0.0f;
+    named_bar_sync(1, 128);                        // column terms visible
+    bool ok = mbar_wait(bar(kBarDone), 0, spin, abort, p.st, kSiteTEpi);
+    tc_fence_after();
+    float rs = 0.0f;
+    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    if (ok) {
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32], cv[32];
+        tmem_ld32(tmem + lane_addr + 32 * ch, sv);
+        tmem_ld32(tmem + lane_addr + 128 + 32 * ch, cv);
+        tmem_wait_ld();
+        float dd[32];
+        uint32_t gw[16], pw[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float gv[2], pv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 32 * ch + c + e;
+            float dp;
+            if (diag) dp = (row_ok && j0 + col <= i) ? exp2f(col_term[col] - p2i) : 0.0f;
+            else dp = col_term[col] * rowf;
+            const float x = __uint_as_float(sv[c + e]) * p.scale;        // S
+            const float g = dp * fmaf(__uint_as_float(cv[c + e]), invn, dbi);   // D' (.) dC~'
+            gv[e] = g;
+            pv[e] = x * dp * invn;                                         // C~' / n
+            dd[c + e] = x * g;                                             // dD~
+            rs += dd[c + e];
+          }
+          gw[c / 2] = pack_bf16x2(gv[0], gv[1]);
+          pw[c / 2] = pack_bf16x2(pv[0], pv[1]);
+        }
+        // stage: columns 32ch..32ch+31 = 16-byte chunks 4(ch&1)..4(ch&1)+3 of box ch>>1
+        const uint32_t gbox = base + (uint32_t)(ch >> 1) * 16384u;
+        const uint32_t pbox = base + 32768u + (uint32_t)(ch >> 1) * 16384u;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const int q = 4 * (ch & 1) + g4;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz(gbox, r, q)), "r"(gw[4 * g4]),
+                       "r"(gw[4 * g4 + 1]), "r"(gw[4 * g4 + 2]), "r"(gw[4 * g4 + 3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz(pbox, r, q)), "r"(pw[4 * g4]),
+                       "r"(pw[4 * g4 + 1]), "r"(pw[4 * g4 + 2]), "r"(pw[4 * g4 + 3])
+                       : "memory");
+        }
+        // column sums over the warp's 32 rows: halving reduce-scatter; lane l
+        // ends with column 32ch + l
+#pragma unroll
+        for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+          const bool hi = lane & o;
+#pragma unroll
+          for (int k2 = 0; k2 < n / 2; ++k2) {
+            const float keep = hi ? dd[k2 + n / 2] : dd[k2];
+            const float send = hi ? dd[k2] : dd[k2 + n / 2];
+            dd[k2] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        col_red[warp - 2][32 * ch + lane] = dd[0];
+      }
+      if (row_ok) p.Rpart[((size_t)bh * nb + jb) * p.T + i] = rs;
+      fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    named_bar_sync(1, 128);
+    if (ok) {
+      if (jc < p.T)
+        p.Cpart[((size_t)bh * nb + ib) * p.T + jc] = col_red[0][et] + col_red[1][et] + col_red[2][et] + col_red[3][et];
+      if (et == 0) {
+        for (int b2 = 0; b2 < 2 && j0 + 64 * b2 < p.T; ++b2) {
+          tma_store_3d(&tmap_g, base + (uint32_t)b2 * 16384u, j0 + 64 * b2, i0, bh);
+          tma_store_3d(&tmap_p, base + 32768u + (uint32_t)b2 * 16384u, j0 + 64 * b2, i0, bh);
+        }
+        tma_store_commit();
+        tma_store_wait_read();
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+  // after an abort, loads may still be landing: wait (bounded) for every issued one
+  if (threadIdx.x == 0 && abort_flag) {
+    const int issued = issued_s;
+    for (int c = 0; c < issued; ++c) {
+      const int s = c % kNst, u = c / kNst;
+      if (c + kNst < issued) continue;             // a later round of the slot completed after it
+      for (long long w = 0; w < kDrainSpin; ++w)
+        if (mbar_try_wait(bar(kBarFull + s), (uint32_t)(u & 1))) break;
+    }
+  }
+}
+
+// Per row: 1/n_i and db_i (eqs 89-90) from the forward's H~, n, signed b and
+// the row max m.  One warp per row.
+template <typename E>
+__global__ void __launch_bounds__(256)
+bwd_rowstat_kernel(const E* __restrict__ dh, const E* __restrict__ h, const float* __restrict__ nrow,
+                   const float* __restrict__ brow, const float* __restrict__ mrow, float* __restrict__ invn,
+                   float* __restrict__ db, int dv, long long BHT) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= BHT) return;
+  float dot = 0.0f;
+  for (int c = lane; c < dv; c += 32)
+    dot = fmaf(Elem<E>::load(dh, (size_t)row * dv + c), Elem<E>::load(h, (size_t)row * dv + c), dot);
+  dot = warp_sum(dot);
+  if (lane == 0) {
+    const float n = nrow[row], b = brow[row];
+    const float inv = n > 0.0f ? 1.0f / n : 0.0f;
+    const float dn = -dot * inv;                                  // -(dH~ . h~) / n = -(sum C~' dC) / n^2
+    invn[row] = inv;
+    db[row] = fabsf(b) > expf(-mrow[row]) ? (b > 0.0f ? dn : (b < 0.0f ? -dn : 0.0f)) : 0.0f;
+  }
+}
+
+// R_i = sum over key blocks jb <= ib(i) of the tile row sums; Ccol_j = sum
+// over query blocks ib >= jb(j) of the tile column sums (fixed order).
+__global__ void bwd_tile_sums_kernel(const float* __restrict__ Rpart, const float* __restrict__ Cpart,
+                                     float* __restrict__ R, float* __restrict__ Ccol, int T, int nb, long long n) {
+  const long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= n) return;
+  const int bh = (int)(x / T), t = (int)(x % T);
+  const int blk = t / kTile;
+  float rsum = 0.0f, csum = 0.0f;
+  for (int b2 = 0; b2 <= blk; ++b2) rsum += Rpart[((size_t)bh * nb + b2) * T + t];
+  for (int b2 = blk; b2 < nb; ++b2) csum += Cpart[((size_t)bh * nb + b2) * T + t];
+  R[x] = rsum;
+  Ccol[x] = csum;
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int T, int dqk, int dv, int dtype) {
+  return dtype == kBF16 && T >= 1 && dqk % 8 == 0 && dv % 8 == 0 && dqk <= 512 && dv <= 512;
+}
+
+int launch_bwd_tiles(const BwdTileArgs& a, cudaStream_t stream) {
+  if (a.BH <= 0 || a.T <= 0) return kOk;
+  if (!bwd_tc_supported(a.T, a.dqk, a.dv, kBF16) || !device_is_sm100_family()) return kUnsupported;
+  const int nb = (a.T + kTile - 1) / kTile;
+  const long long BHT = (long long)a.BH * a.T;
+  const long long grid = (long long)a.BH * (a.with_upper ? nb * nb : nb * (nb + 1) / 2);
+  if (grid > 0x7fffffffLL || (BHT + 7) / 8 > 0x7fffffffLL) return kInval;
+  CUtensorMap mq, mk, mdh, mv, mg, mp;
+  if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kTile) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, kTile) ||
+      !make_map(&mdh, a.dh, a.dv, a.T, a.BH, kTile) || !make_map(&mv, a.v, a.dv, a.T, a.BH, kTile) ||
+      !make_map_ld(&mg, a.G, a.T, a.T, a.BH, a.ldT, kTile) || !make_map_ld(&mp, a.P, a.T, a.T, a.BH, a.ldT, kTile))
+    return kCuda;
+  bwd_rowstat_kernel<__nv_bfloat16><<<(unsigned)((BHT + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.dh), static_cast<const __nv_bfloat16*>(a.h), a.nrow, a.brow, a.g.m,
+      a.invn, a.db, a.dv, BHT);
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  TileParams p;
+  p.a2 = a.g.a2; p.p2 = a.g.p2; p.invn = a.invn; p.db = a.db;
+  p.Rpart = a.Rpart; p.Cpart = a.Cpart;
+  p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv; p.nb = nb; p.with_upper = a.with_upper;
+  p.scale = a.scale; p.st = a.st;
+  const size_t smem = (size_t)kNst * kStage + 1024;
+  if (cudaFuncSetAttribute(bwd_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return kCuda;
+  bwd_tile_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(mq, mk, mdh, mv, mg, mp, p);
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  bwd_tile_sums_kernel<<<(unsigned)((BHT + 255) / 256), 256, 0, stream>>>(a.Rpart, a.Cpart, a.R, a.Ccol, a.T, nb,
+                                                                            BHT);
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
+}  // namespace mlstm

@@ -21,7 +21,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 const float* __restrict__ a2, const float* __restrict__ p2,
-                const float* __restrict__ mrow, T* __restrict__ h, float* __restrict__ m_out,
+                const float* __restrict__ mrow, T* __restrict__ h, float* __restrict__ m_out, float* __restrict__ b_out,
                 float* __restrict__ n_out, int T_, int dqk, int dv, float scale) {
   extern __shared__ float smem[];
   const int ldk = dqk + 1;                  // padded row: conflict-free column reads
@@ -109,6 +109,7 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
   if (c8 == 0) {
     if (m_out) m_out[hq + gi] = m;
     if (n_out) n_out[hq + gi] = nrm;
+    if (b_out) b_out[hq + gi] = bsum;
   }
 }
 
@@ -127,7 +128,7 @@ cudaError_t launch_t(const FwdArgs& a, cudaStream_t stream) {
   const long long grid = nqt * a.BH;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fwd_simt_kernel<T><<<(unsigned)grid, kThreads, smem, stream>>>(
-      (const T*)a.q, (const T*)a.k, (const T*)a.v, a.g.a2, a.g.p2, a.g.m, (T*)a.h, a.m_out, a.n_out,
+      (const T*)a.q, (const T*)a.k, (const T*)a.v, a.g.a2, a.g.p2, a.g.m, (T*)a.h, a.m_out, a.b_out, a.n_out,
       a.T, a.dqk, a.dv, a.scale);
   return cudaGetLastError();
 }

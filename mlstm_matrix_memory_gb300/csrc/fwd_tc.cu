@@ -86,6 +86,7 @@ struct TcParams {
   __nv_bfloat16* h;
   float* m_out;
   float* n_out;
+  float* b_out;
   int T, BH, dqk, dv;
   int nsplit;      // CTAs per query tile along d_v (1 or 2)
   int dv_slice;    // d_v columns of the first slice (the second gets the rest)
@@ -425,9 +426,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     float* bpart = reinterpret_cast<float*>(dsmem + (sP - smem_u32(dsmem)));
     if (ok) bpart[half * kBM + rl] = bsum;
     named_bar_sync(1, 256);
-    float nrm = 0.0f, m = 0.0f;
+    float nrm = 0.0f, m = 0.0f, bsig = 0.0f;
     if (ok) {
       const float b = bpart[rl] + bpart[kBM + rl];
+      bsig = b;
       m = row_ok ? p.mrow[hbase + i] : 0.0f;
       nrm = fmaxf(fabsf(b), expf(-m));
     }
@@ -456,6 +458,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       if (row_ok && split == 0 && half == 0) {
         if (p.m_out) p.m_out[hbase + i] = m;
         if (p.n_out) p.n_out[hbase + i] = nrm;
+        if (p.b_out) p.b_out[hbase + i] = bsig;
       }
       fence_proxy_async_smem();
     }
@@ -527,7 +530,7 @@ int launch_ns(const FwdArgs& a, const Plan& pl, const CUtensorMap& mq, const CUt
     return kCuda;
   TcParams p;
   p.a2 = a.g.a2; p.p2 = a.g.p2; p.mrow = a.g.m;
-  p.h = (__nv_bfloat16*)a.h; p.m_out = a.m_out; p.n_out = a.n_out;
+  p.h = (__nv_bfloat16*)a.h; p.m_out = a.m_out; p.n_out = a.n_out; p.b_out = a.b_out;
   p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv;
   p.nsplit = pl.nsplit; p.dv_slice = pl.dv_slice; p.nst = pl.nst; p.vk = pl.vk;
   p.nqt = (a.T + kBM - 1) / kBM;
@@ -584,6 +587,18 @@ bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows) 
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * T};
   cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_ld(CUtensorMap* m, const void* base, int cols, int rows, int BH, int ld, int box_rows) {
+  EncodeTiled enc = encode_fn();
+  if (!enc || (ld * 2) % 16 != 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * 2 * rows};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -77,6 +77,7 @@ struct Tc2Params {
   const float* mrow;
   float* m_out;
   float* n_out;
+  float* b_out;
   const __nv_bfloat16* og;                // output-gate pre-activations (eq 78), or null
   int T, BH, dqk, dv;
   int nsplit, dv_slice, nk, nv, npairs;   // nk + nv ring granules (K ring, then V ring)
@@ -492,6 +493,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       if (row_ok && it.split == 0 && half == 0) {
         if (p.m_out) p.m_out[hbase + i] = m;
         if (p.n_out) p.n_out[hbase + i] = nrm;
+        if (p.b_out) p.b_out[hbase + i] = b;
       }
       if (gw == 0 && lane == 0) TRACE2(12, 0);
       const int cols = it.dv_cta / 2, c0 = half * cols;      // a multiple of 64
@@ -659,7 +661,7 @@ bool fwd_tc2_supported(int dqk, int dv) {
 int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   Tc2Params p;
   p.a2 = a.g.a2; p.p2 = a.g.p2; p.mrow = a.g.m;
-  p.m_out = a.m_out; p.n_out = a.n_out;
+  p.m_out = a.m_out; p.n_out = a.n_out; p.b_out = a.b_out;
   p.og = static_cast<const __nv_bfloat16*>(a.og);
   p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv;
   int nsbuf;

@@ -29,6 +29,7 @@ struct FwdArgs {
   void* h;
   float* m_out;   // may be null
   float* n_out;   // may be null
+  float* b_out = nullptr;   // signed row sums b (eq 83), or null (used by the backward)
   GateTerms g;
   int BH, T, dqk, dv;
   int dtype;      // kF32 / kBF16
@@ -77,6 +78,42 @@ int device_is_sm100_family();
 // CTA-pair (cta_group::2) variant of the tensor-core forward (fwd_tc2.cu).
 bool fwd_tc2_supported(int dqk, int dv);
 int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream);
+
+// The device status word and the current spin limit (false: no status word).
+bool current_status(DevStatus* out);
+
+// Tiles of the parallel backward on the tensor cores (bwd_tc.cu): from the
+// gate terms and the forward's row statistics, writes G = D' (.) dC~' and
+// P = C~'/n (bf16, [BH, T, ldT], zero above the diagonal) and the row and
+// column sums R, Ccol of dD~ = S (.) G.  Returns a Status.
+struct BwdTileArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dh;
+  const void* h;        // H~ of the forward [BH, T, dv]
+  const float* nrow;    // n_i of the forward
+  const float* brow;    // signed b_i of the forward
+  GateTerms g;
+  float* invn;          // scratch [BH*T]
+  float* db;            // scratch [BH*T]
+  void* G;
+  void* P;
+  float* Rpart;         // scratch [BH][nb][T]
+  float* Cpart;         // scratch [BH][nb][T]
+  float* R;             // out [BH*T]
+  float* Ccol;          // out [BH*T]
+  int BH, T, ldT, dqk, dv;
+  int with_upper;       // 1: store zero tiles above the diagonal too
+  float scale;
+  DevStatus st;
+};
+bool bwd_tc_supported(int T, int dqk, int dv, int dtype);
+int launch_bwd_tiles(const BwdTileArgs& a, cudaStream_t stream);
+
+// 3-D TMA map over [BH, rows, cols] bf16 with row pitch ld elements (ld*2 a
+// multiple of 16), box 64 x box_rows x 1, 128-byte swizzle (fwd_tc.cu).
+bool make_map_ld(CUtensorMap* m, const void* base, int cols, int rows, int BH, int ld, int box_rows);
 
 // 3-D TMA map over a [BH, T, d] bf16 tensor, box 64 x rows x 1, 128-byte
 // swizzle; rows past T read as zeros and are clipped on stores (fwd_tc.cu).

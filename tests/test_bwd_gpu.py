@@ -1,6 +1,8 @@
 """GPU parity of the parallel backward (mlstm_parallel_bwd) against the fp64
 oracle's eqs (87)-(105), each gradient within the forward's tolerances
-(relative to its own largest entry)."""
+(relative to its own largest entry).  bf16 cases run the tensor-core tile
+path; the same cases with MLSTM_BWD_PATH=blas in the environment run the
+cuBLAS-only path."""
 import numpy as np
 import pytest
 import torch
@@ -26,6 +28,8 @@ CASES = [
     (1, 2, 300, 64, 64, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),
     (1, 1, 777, 128, 96, torch.bfloat16, (0.0, 2.0), (5.0, 1.0)),     # long-memory gates
     (1, 1, 2048, 384, 384, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),   # one head of the 125M-scale layer
+    (2, 3, 50, 40, 24, torch.bfloat16, (-2.0, 1.5), (0.5, 1.0)),      # one partial tile, d not a multiple of 64
+    (1, 1, 129, 64, 64, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),      # a second tile row of one query
 ]
 
 
