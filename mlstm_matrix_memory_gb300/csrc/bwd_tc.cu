@@ -306,6 +306,208 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   }
 }
 
+// ---------------------------------------------------------------- products
+// The three products of eqs (98)-(100) over the lower triangle of G and P,
+// one CTA per (product, head, 128-row output block g):
+//   dQ_g = s sum_{kb <= g} G[g, kb] K[kb]       A = G block, K-major
+//   dK_g = s sum_{ib >= g} G[ib, g]^T Q[ib]     A = G^T block, MN-major
+//   dV_g =   sum_{ib >= g} P[ib, g]^T dH[ib]    A = P^T block, MN-major
+// B (K, Q or dH rows) is MN-major.  The 128 x d accumulator sits in TMEM
+// (d <= 512 columns); A blocks come through a two-slot ring, B through a
+// four-slot ring of 128-column chunks.  CTAs run longest first.
+constexpr int kPThreads = 192;          // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
+constexpr int kANst = 2, kBNst = 4;
+constexpr uint32_t kABytes = 32768, kBBytes = 32768;
+enum : int {
+  kPBarAFull = 0, kPBarAEmpty = kANst, kPBarBFull = 2 * kANst, kPBarBEmpty = 2 * kANst + kBNst,
+  kPBarDone = 2 * kANst + 2 * kBNst, kPBarDrain = kPBarDone + 1, kPNumBars = kPBarDone + 2
+};
+enum : int { kSitePProducer = 44, kSitePMma = 45, kSitePEpi = 46 };
+
+struct ProdParams {
+  int T, BH, nb, dqk, dv;
+  float scale;
+  DevStatus st;
+};
+
+__global__ void __launch_bounds__(kPThreads, 1)
+bwd_prod_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_p,
+                const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                const __grid_constant__ CUtensorMap tmap_dh, const __grid_constant__ CUtensorMap tmap_dq,
+                const __grid_constant__ CUtensorMap tmap_dk, const __grid_constant__ CUtensorMap tmap_dv,
+                const ProdParams p) {
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t bars[kPNumBars];
+  __shared__ uint32_t tmem_holder;
+  __shared__ int abort_flag;
+  __shared__ int a_issued_s, b_issued_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &abort_flag;
+
+  // work item: rank w = 0 has the most blocks to sum over (nb - w of them)
+  const int w = (int)(blockIdx.x / (3u * (unsigned)p.BH));
+  const int prod = (int)((blockIdx.x / (unsigned)p.BH) % 3u);
+  const int bh = (int)(blockIdx.x % (unsigned)p.BH);
+  const int nkb = p.nb - w;                                  // blocks in the sum
+  const int g = prod == 0 ? p.nb - 1 - w : w;                // output row block
+  const int kb0 = prod == 0 ? 0 : g;                         // first summed block
+  const int r0 = g * kTile;
+  const int d = prod == 2 ? p.dv : p.dqk;
+  const int nbox = (d + 63) / 64, nchunk = (nbox + 1) / 2;   // 64-column boxes, 128-column chunks
+  const CUtensorMap* ma = prod == 2 ? &tmap_p : &tmap_g;
+  const CUtensorMap* mb = prod == 0 ? &tmap_k : (prod == 1 ? &tmap_q : &tmap_dh);
+  const CUtensorMap* mo = prod == 0 ? &tmap_dq : (prod == 1 ? &tmap_dk : &tmap_dv);
+  const float alpha = prod == 2 ? 1.0f : p.scale;
+  const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint32_t sA = base, sB = base + kANst * kABytes;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    a_issued_s = 0;
+    b_issued_s = 0;
+    for (int s2 = 0; s2 < kANst; ++s2) {
+      mbar_init(bar(kPBarAFull + s2), 1);
+      mbar_init(bar(kPBarAEmpty + s2), 1);
+    }
+    for (int s2 = 0; s2 < kBNst; ++s2) {
+      mbar_init(bar(kPBarBFull + s2), 1);
+      mbar_init(bar(kPBarBEmpty + s2), 1);
+    }
+    mbar_init(bar(kPBarDone), 1);
+    mbar_init(bar(kPBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  const long long spin = p.st.spin_limit;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    tma_prefetch_desc(ma);
+    tma_prefetch_desc(mb);
+    int bi = 0;
+    bool ok = true;
+    for (int t = 0; t < nkb && ok; ++t) {
+      const int kb = kb0 + t;
+      const int as = t % kANst, au = t / kANst;
+      ok = mbar_wait(bar(kPBarAEmpty + as), (uint32_t)(au & 1) ^ 1u, spin, abort, p.st, kSitePProducer);
+      if (!ok) break;
+      mbar_arrive_expect_tx(bar(kPBarAFull + as), kABytes);
+      const uint32_t adst = sA + (uint32_t)as * kABytes;
+      for (int h = 0; h < 2; ++h) {
+        if (prod == 0)   // G[g rows, kb keys]: keys 128kb + 64h ..
+          tma_load_3d(adst + h * 16384u, ma, bar(kPBarAFull + as), kb * kTile + 64 * h, r0, bh);
+        else             // G[kb rows, g keys]^T: keys r0 + 64h .. as the M half h
+          tma_load_3d(adst + h * 16384u, ma, bar(kPBarAFull + as), r0 + 64 * h, kb * kTile, bh);
+      }
+      a_issued_s = t + 1;
+      for (int c = 0; c < nchunk && ok; ++c, ++bi) {
+        const int bs = bi % kBNst, bu = bi / kBNst;
+        ok = mbar_wait(bar(kPBarBEmpty + bs), (uint32_t)(bu & 1) ^ 1u, spin, abort, p.st, kSitePProducer);
+        if (!ok) break;
+        const int nb2 = min(2, nbox - 2 * c);
+        mbar_arrive_expect_tx(bar(kPBarBFull + bs), (uint32_t)nb2 * 16384u);
+        for (int h = 0; h < nb2; ++h)
+          tma_load_3d(sB + (uint32_t)bs * kBBytes + h * 16384u, mb, bar(kPBarBFull + bs), 64 * (2 * c + h),
+                      kb * kTile, bh);
+        b_issued_s = bi + 1;
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t a_mn = prod == 0 ? 0u : 1u;
+    const uint32_t id128 = idesc_bf16_f32(kTile, 128, (int)a_mn, 1), id64 = idesc_bf16_f32(kTile, 64, (int)a_mn, 1);
+    int bi = 0;
+    bool ok = true;
+    for (int t = 0; t < nkb && ok; ++t) {
+      const int as = t % kANst, au = t / kANst;
+      ok = mbar_wait(bar(kPBarAFull + as), (uint32_t)(au & 1), spin, abort, p.st, kSitePMma);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t aaddr = sA + (uint32_t)as * kABytes;
+      // K-major A: two 64-key boxes, 32 B per 16-key step within a box;
+      // MN-major A: two 64-row M halves 16 KB apart, 2 KB per 16-key step
+      const uint64_t da = prod == 0 ? smem_desc_sw128(aaddr, 16, 1024) : smem_desc_sw128(aaddr, 16384, 1024);
+      for (int c = 0; c < nchunk && ok; ++c, ++bi) {
+        const int bs = bi % kBNst, bu = bi / kBNst;
+        ok = mbar_wait(bar(kPBarBFull + bs), (uint32_t)(bu & 1), spin, abort, p.st, kSitePMma);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dbd = smem_desc_sw128(sB + (uint32_t)bs * kBBytes, 16384, 1024);
+        const uint32_t idesc = nbox - 2 * c >= 2 ? id128 : id64;
+        const uint32_t dcol = tmem + 128u * (uint32_t)c;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ak = prod == 0 ? da + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2) : da + (uint64_t)(kk * 128);
+          mma_bf16_ss(dcol, ak, dbd + (uint64_t)(kk * 128), idesc, (t | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kPBarBEmpty + bs));
+      }
+      if (ok) mma_commit(bar(kPBarAEmpty + as));
+    }
+    if (ok) mma_commit(bar(kPBarDone));
+    mma_commit(bar(kPBarDrain));
+    for (long long w2 = 0; w2 < kDrainSpin; ++w2)
+      if (mbar_try_wait(bar(kPBarDrain), 0)) break;
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int qd = warp & 3, r = 32 * qd + lane;
+    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    bool ok = mbar_wait(bar(kPBarDone), 0, spin, abort, p.st, kSitePEpi);
+    tc_fence_after();
+    if (ok) {
+      // stage the bf16 block in 64-column boxes over the (now idle) rings
+      for (int c32 = 0; c32 < 2 * nbox; ++c32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_addr + 32 * c32, v);
+        tmem_wait_ld();
+        const uint32_t box = base + (uint32_t)(c32 >> 1) * 16384u;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            wv[e] = pack_bf16x2(__uint_as_float(v[8 * g4 + 2 * e]) * alpha, __uint_as_float(v[8 * g4 + 2 * e + 1]) * alpha);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz(box, r, 4 * (c32 & 1) + g4)),
+                       "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    named_bar_sync(1, 128);
+    if (ok && threadIdx.x == 64) {
+      for (int b2 = 0; b2 < nbox; ++b2) tma_store_3d(mo, base + (uint32_t)b2 * 16384u, 64 * b2, r0, bh);
+      tma_store_commit();
+      tma_store_wait_read();
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && abort_flag) {
+    // loads may still be landing: wait (bounded) for the last round of every slot
+    const int ai = a_issued_s, bi = b_issued_s;
+    for (int c = max(0, ai - kANst); c < ai; ++c)
+      for (long long w2 = 0; w2 < kDrainSpin; ++w2)
+        if (mbar_try_wait(bar(kPBarAFull + c % kANst), (uint32_t)((c / kANst) & 1))) break;
+    for (int c = max(0, bi - kBNst); c < bi; ++c)
+      for (long long w2 = 0; w2 < kDrainSpin; ++w2)
+        if (mbar_try_wait(bar(kPBarBFull + c % kBNst), (uint32_t)((c / kBNst) & 1))) break;
+  }
+}
+
 // Per row: 1/n_i and db_i (eqs 89-90) from the forward's H~, n, signed b and
 // the row max m.  One warp per row.
 template <typename E>
@@ -345,6 +547,26 @@ __global__ void bwd_tile_sums_kernel(const float* __restrict__ Rpart, const floa
 }
 
 }  // namespace
+
+int launch_bwd_products(const BwdProdArgs& a, cudaStream_t stream) {
+  if (a.BH <= 0 || a.T <= 0) return kOk;
+  const int nb = (a.T + kTile - 1) / kTile;
+  const long long grid = 3LL * a.BH * nb;
+  if (grid > 0x7fffffffLL) return kInval;
+  CUtensorMap mg, mp, mk, mq, mdh, mdq, mdk, mdv;
+  if (!make_map_ld(&mg, a.G, a.T, a.T, a.BH, a.ldT, kTile) || !make_map_ld(&mp, a.P, a.T, a.T, a.BH, a.ldT, kTile) ||
+      !make_map(&mk, a.k, a.dqk, a.T, a.BH, kTile) || !make_map(&mq, a.q, a.dqk, a.T, a.BH, kTile) ||
+      !make_map(&mdh, a.dh, a.dv, a.T, a.BH, kTile) || !make_map(&mdq, a.dq, a.dqk, a.T, a.BH, kTile) ||
+      !make_map(&mdk, a.dk, a.dqk, a.T, a.BH, kTile) || !make_map(&mdv, a.dvo, a.dv, a.T, a.BH, kTile))
+    return kCuda;
+  ProdParams p;
+  p.T = a.T; p.BH = a.BH; p.nb = nb; p.dqk = a.dqk; p.dv = a.dv; p.scale = a.scale; p.st = a.st;
+  const size_t smem = (size_t)kANst * kABytes + (size_t)kBNst * kBBytes + 1024;
+  if (cudaFuncSetAttribute(bwd_prod_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return kCuda;
+  bwd_prod_kernel<<<(unsigned)grid, kPThreads, smem, stream>>>(mg, mp, mk, mq, mdh, mdq, mdk, mdv, p);
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
 
 bool bwd_tc_supported(int T, int dqk, int dv, int dtype) {
   return dtype == kBF16 && T >= 1 && dqk % 8 == 0 && dv % 8 == 0 && dqk <= 512 && dv <= 512;

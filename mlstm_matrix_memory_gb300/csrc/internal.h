@@ -108,6 +108,22 @@ struct BwdTileArgs {
   float scale;
   DevStatus st;
 };
+// dQ = s G K, dK = s G^T Q, dV = P^T dH over the lower triangle of G and P
+// (bf16, [BH, T, ldT]), tensor cores (bwd_tc.cu).  Returns a Status.
+struct BwdProdArgs {
+  const void* q;
+  const void* k;
+  const void* dh;
+  const void* G;
+  const void* P;
+  void* dq;
+  void* dk;
+  void* dvo;
+  int BH, T, ldT, dqk, dv;
+  float scale;
+  DevStatus st;
+};
+int launch_bwd_products(const BwdProdArgs& a, cudaStream_t stream);
 bool bwd_tc_supported(int T, int dqk, int dv, int dtype);
 int launch_bwd_tiles(const BwdTileArgs& a, cudaStream_t stream);
 
