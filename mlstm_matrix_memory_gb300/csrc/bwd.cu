@@ -167,7 +167,7 @@ bwd_gates_kernel(const float* __restrict__ R, const float* __restrict__ Ccol, co
     const double c = Ccol[hb + t];
     after += (double)R[hb + t] - c;    // now the suffix from t
     dig[hb + t] = (float)c;
-    dfg[hb + t] = (float)(after / (1.0 + exp((double)fg[hb + t])));    // sigma(-f~) d fbar
+    dfg[hb + t] = (float)(after * (double)sigmoid(-fg[hb + t]));    // sigma(-f~) d fbar (eq 104)
   }
 }
 
@@ -225,9 +225,7 @@ TcLayout tc_layout(long long BH, int T, int dv) {
 }
 
 // The tensor-core path runs for bf16 on the sm_100 family unless
-// MLSTM_BWD_PATH=blas in the environment selects the cuBLAS path;
-// MLSTM_BWD_PATH=gemm keeps the tile kernel but forms dQ, dK, dV with cuBLAS
-// over whole matrices (tests and measurements).
+// MLSTM_BWD_PATH=blas in the environment selects the cuBLAS path (tests).
 bool use_tc_path(int T, int dqk, int dv, int dtype) {
   static const char* force = getenv("MLSTM_BWD_PATH");
   if (force && force[0] == 'b') return false;
@@ -382,36 +380,15 @@ int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_
   ta.q = q; ta.k = k; ta.v = v; ta.dh = dh; ta.h = hf; ta.nrow = nrow; ta.brow = brow; ta.g = g;
   ta.invn = invn; ta.db = dbv; ta.G = G; ta.P = P; ta.Rpart = Rpart; ta.Cpart = Cpart; ta.R = R; ta.Ccol = Ccol;
   ta.BH = BH; ta.T = T; ta.ldT = L.ldT; ta.dqk = d_qk; ta.dv = d_v; ta.scale = s; ta.st = ds;
-  // the cuBLAS products read whole matrices: they need the zeros above the diagonal
-  static const char* path = getenv("MLSTM_BWD_PATH");
-  const bool blas_products = path && path[0] == 'g';
-  ta.with_upper = blas_products ? 1 : 0;
   rc = launch_bwd_tiles(ta, st);
   if (rc != kOk) return rc;
 
-  if (!blas_products) {
-    // dQ, dK, dV over the lower triangle on the tensor cores            (98)-(100)
-    BwdProdArgs pa;
-    pa.q = q; pa.k = k; pa.dh = dh; pa.G = G; pa.P = P; pa.dq = dq; pa.dk = dk; pa.dvo = dv;
-    pa.BH = BH; pa.T = T; pa.ldT = L.ldT; pa.dqk = d_qk; pa.dv = d_v; pa.scale = s; pa.st = ds;
-    rc = launch_bwd_products(pa, st);
-    if (rc != kOk) return rc;
-  } else {
-    cublasHandle_t h = blas_handle();
-    if (!h || cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return MLSTM_ECUDA;
-    const cudaDataType et = CUDA_R_16BF;
-    const long long TT = (long long)T * L.ldT, Tq = (long long)T * d_qk, Tv = (long long)T * d_v;
-    const int ld = L.ldT;
-    // row-major dQ = s G K  <=>  col-major dQ^T = s K^T G^T          (98)
-    if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_N, d_qk, T, T, s, k, et, d_qk, Tq, G, et, ld, TT, dq, et, d_qk, Tq, BH))
-      return MLSTM_ECUDA;
-    // row-major dK = s G^T Q  <=>  col-major dK^T = s Q^T G          (99)
-    if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, d_qk, T, T, s, q, et, d_qk, Tq, G, et, ld, TT, dk, et, d_qk, Tq, BH))
-      return MLSTM_ECUDA;
-    // row-major dV = P^T dH  <=>  col-major dV^T = dH^T P            (100)
-    if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, d_v, T, T, 1.0f, dh, et, d_v, Tv, P, et, ld, TT, dv, et, d_v, Tv, BH))
-      return MLSTM_ECUDA;
-  }
+  // dQ, dK, dV over the lower triangle on the tensor cores            (98)-(100)
+  BwdProdArgs pa;
+  pa.q = q; pa.k = k; pa.dh = dh; pa.G = G; pa.P = P; pa.dq = dq; pa.dk = dk; pa.dvo = dv;
+  pa.BH = BH; pa.T = T; pa.ldT = L.ldT; pa.dqk = d_qk; pa.dv = d_v; pa.scale = s; pa.st = ds;
+  rc = launch_bwd_products(pa, st);
+  if (rc != kOk) return rc;
   bwd_gates_kernel<<<(unsigned)BH, 1024, 0, st>>>(R, Ccol, fgate_pre, d_igate, d_fgate, T);
   return cudaGetLastError() == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
 }

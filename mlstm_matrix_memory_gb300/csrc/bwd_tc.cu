@@ -11,19 +11,19 @@
 // no pass over the keys: sum_j C~'_ij dC_ij = dH~_i . (sum_j C~'_ij v_j)
 // = n_i dH~_i . h~_i, with h~ and n (and the signed b) from the forward.
 //
-// One CTA per 128 x 128 tile (query block ib, key block jb <= ib) of one head:
-//   S  = Q_ib K_jb^T      tcgen05.mma into TMEM columns 0..127
-//   dC = dH_ib V_jb^T     tcgen05.mma into TMEM columns 128..255
+// Per 128 x 128 tile (query block ib, key block jb <= ib) of one head:
+//   S  = Q_ib K_jb^T      tcgen05.mma into a TMEM buffer's columns 0..127
+//   dC = dH_ib V_jb^T     tcgen05.mma into its columns 128..255
 // both contractions streamed through a ring of 64-column chunks (TMA, 128-byte
-// swizzle, zero fill past d).  Four epilogue warps (a row each per thread)
-// form G and P in fp32 from the TMEM rows, stage them as bf16 and store them
-// by TMA, and leave the tile's row and column sums of dD~ (the column sums
-// by a shuffle reduce-scatter, so every partial is formed in a fixed order).
-// Within the diagonal tile G and P are stored as zero above the diagonal; the
-// tiles above it are stored as zeros only when the products that follow read
-// whole matrices.  Two CTAs fit on an SM
-// (256 TMEM columns and about 97 KB of shared memory each), so one CTA's
-// epilogue overlaps the other's products.
+// swizzle, zero fill past d).  The kernel is persistent, one CTA per SM,
+// tiles taken round robin in head-major order; two TMEM buffers let the
+// products of one tile run while eight epilogue warps (two per TMEM lane
+// quarter, 64 columns each) turn the previous one into G and P: fp32 from the TMEM rows, bf16 staging, TMA
+// stores, and the tile's row and column sums of dD~ (the column sums by a
+// shuffle reduce-scatter, so every partial is formed in a fixed order).
+// Within the diagonal tile G and P are stored as zero above the diagonal;
+// nothing above it is ever stored or read.
+#include <algorithm>
 #include <cmath>
 
 #include "internal.h"
@@ -35,13 +35,16 @@ namespace {
 using namespace tc;
 
 constexpr int kTile = 128;            // query rows and keys of a tile
-constexpr int kThreads = 192;         // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
-constexpr int kNst = 3;               // ring stages
+constexpr int kThreads = 320;         // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 epilogue
+constexpr int kNst = 4;               // ring stages
 constexpr uint32_t kStage = 32768;    // a stage: [128 rows x 64 columns] of A and of B
-constexpr uint32_t kCols = 256;       // TMEM: S in 0..127, dC in 128..255
+constexpr uint32_t kStaging = 65536;  // bf16 G and P of a tile: four [128 x 64] boxes
 constexpr long long kDrainSpin = 1LL << 22;
 
-enum : int { kBarFull = 0, kBarEmpty = kNst, kBarDone = 2 * kNst, kBarDrain = 2 * kNst + 1, kNumBars = 2 * kNst + 2 };
+enum : int {
+  kBarFull = 0, kBarEmpty = kNst, kBarAccFull = 2 * kNst, kBarAccEmpty = 2 * kNst + 2, kBarDrain = 2 * kNst + 4,
+  kNumBars = 2 * kNst + 5
+};
 enum : int { kSiteTProducer = 41, kSiteTMma = 42, kSiteTEpi = 43 };
 
 struct TileParams {
@@ -51,8 +54,7 @@ struct TileParams {
   const float* db;
   float* Rpart;
   float* Cpart;
-  int T, BH, dqk, dv, nb;
-  int with_upper;       // 1: also store the zero tiles above the diagonal
+  int T, BH, dqk, dv, nb, nitems;
   float scale;
   DevStatus st;
 };
@@ -62,7 +64,19 @@ __device__ __forceinline__ uint32_t swz(uint32_t box, int r, int q) {
   return box + (uint32_t)r * 128u + ((uint32_t)(q ^ (r & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+// Item it -> head and tile: t = ib (ib + 1) / 2 + jb, jb <= ib.
+__device__ __forceinline__ void tile_of(int it, int nb, int* bh, int* ib, int* jb) {
+  const int ntri = nb * (nb + 1) / 2;
+  *bh = it / ntri;
+  const int t = it - *bh * ntri;
+  int i = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+  while (i * (i + 1) / 2 > t) --i;
+  while ((i + 1) * (i + 2) / 2 <= t) ++i;
+  *ib = i;
+  *jb = t - i * (i + 1) / 2;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
 bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_dh, const __grid_constant__ CUtensorMap tmap_v,
                 const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_p,
@@ -72,54 +86,20 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
   __shared__ int issued_s;                    // chunks whose loads the producer issued
-  __shared__ float col_term[kTile];           // a2_j (diagonal tile) or 2^(a2_j - A)
-  __shared__ float col_red[4][kTile];         // per warp: column sums of dD~ over its 32 rows
+  __shared__ int epi_stop;
+  __shared__ __align__(16) float col_term[kTile];   // a2_j (diagonal tile) or 2^(a2_j - A); read as float4
+  __shared__ float col_red[4][kTile];         // per lane quarter: column sums of dD~ over its 32 rows
+  __shared__ float row_red[2][kTile];         // per column half: row sums of dD~
   __shared__ float amax_red[4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &abort_flag;
-  // tiles: the lower triangle of each head (t = ib (ib + 1) / 2 + jb, jb <= ib),
-  // then, when the products read whole matrices, the tiles above it (zeros)
-  const int nb = p.nb, ntri = nb * (nb + 1) / 2, per_head = p.with_upper ? nb * nb : ntri;
-  const int bh = (int)(blockIdx.x / (unsigned)per_head);
-  const int t = (int)(blockIdx.x % (unsigned)per_head);
-  int ib, jb;
-  if (t < ntri) {
-    ib = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
-    while (ib * (ib + 1) / 2 > t) --ib;
-    while ((ib + 1) * (ib + 2) / 2 <= t) ++ib;
-    jb = t - ib * (ib + 1) / 2;
-  } else {                                        // upper tile u = t - ntri: row ib, column jb > ib
-    int u = t - ntri;
-    ib = 0;
-    while (u >= nb - 1 - ib) { u -= nb - 1 - ib; ++ib; }
-    jb = ib + 1 + u;
-  }
-  const int i0 = ib * kTile, j0 = jb * kTile;
+  const int nb = p.nb;
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint32_t sStage = base + kNst * kStage;            // staging of G (boxes 0, 1) and P (2, 3)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-
-  if (jb > ib) {
-    // ---- above the diagonal: G and P are zero
-    if (warp >= 2) {
-      const int tz = threadIdx.x - 64;           // 128 threads zero one 16 KB box
-      uint4* z = reinterpret_cast<uint4*>(dsmem + (base - smem_u32(dsmem)));
-      for (int x = tz; x < 1024; x += 128) z[x] = make_uint4(0u, 0u, 0u, 0u);
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (tz == 0) {
-        for (int b2 = 0; b2 < 2 && j0 + 64 * b2 < p.T; ++b2) {   // boxes that start inside the matrix
-          tma_store_3d(&tmap_g, base, j0 + 64 * b2, i0, bh);
-          tma_store_3d(&tmap_p, base, j0 + 64 * b2, i0, bh);
-        }
-        tma_store_commit();
-        tma_store_wait_read();
-      }
-    }
-    return;
-  }
-
   const int nq = (p.dqk + 63) / 64, nch = nq + (p.dv + 63) / 64;
+
   if (threadIdx.x == 0) {
     abort_flag = 0;
     issued_s = 0;
@@ -127,12 +107,15 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
     }
-    mbar_init(bar(kBarDone), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kBarAccFull + b), 1);
+      mbar_init(bar(kBarAccEmpty + b), 8);      // one arrival per epilogue warp
+    }
     mbar_init(bar(kBarDrain), 1);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_holder), kCols);
+    tmem_alloc(smem_u32(&tmem_holder), 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -147,162 +130,210 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_dh);
     tma_prefetch_desc(&tmap_v);
-    for (int c = 0; c < nch; ++c) {
-      const int s = c % kNst, u = c / kNst;
-      if (!mbar_wait(bar(kBarEmpty + s), (uint32_t)(u & 1) ^ 1u, spin, abort, p.st, kSiteTProducer)) break;
-      const uint32_t dst = base + (uint32_t)s * kStage;
-      mbar_arrive_expect_tx(bar(kBarFull + s), kStage);
-      if (c < nq) {
-        tma_load_3d(dst, &tmap_q, bar(kBarFull + s), 64 * c, i0, bh);
-        tma_load_3d(dst + kStage / 2, &tmap_k, bar(kBarFull + s), 64 * c, j0, bh);
-      } else {
-        tma_load_3d(dst, &tmap_dh, bar(kBarFull + s), 64 * (c - nq), i0, bh);
-        tma_load_3d(dst + kStage / 2, &tmap_v, bar(kBarFull + s), 64 * (c - nq), j0, bh);
+    int cc = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < p.nitems && ok; it += gridDim.x) {
+      int bh, ib, jb;
+      tile_of(it, nb, &bh, &ib, &jb);
+      const int i0 = ib * kTile, j0 = jb * kTile;
+      for (int c = 0; c < nch; ++c, ++cc) {
+        const int s = cc % kNst, u = cc / kNst;
+        ok = mbar_wait(bar(kBarEmpty + s), (uint32_t)(u & 1) ^ 1u, spin, abort, p.st, kSiteTProducer);
+        if (!ok) break;
+        const uint32_t dst = base + (uint32_t)s * kStage;
+        mbar_arrive_expect_tx(bar(kBarFull + s), kStage);
+        if (c < nq) {
+          tma_load_3d(dst, &tmap_q, bar(kBarFull + s), 64 * c, i0, bh);
+          tma_load_3d(dst + kStage / 2, &tmap_k, bar(kBarFull + s), 64 * c, j0, bh);
+        } else {
+          tma_load_3d(dst, &tmap_dh, bar(kBarFull + s), 64 * (c - nq), i0, bh);
+          tma_load_3d(dst + kStage / 2, &tmap_v, bar(kBarFull + s), 64 * (c - nq), j0, bh);
+        }
+        issued_s = cc + 1;
       }
-      issued_s = c + 1;
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(kTile, kTile, 0, 0);
+    int cc = 0, li = 0;
     bool ok = true;
-    for (int c = 0; c < nch && ok; ++c) {
-      const int s = c % kNst, u = c / kNst;
-      ok = mbar_wait(bar(kBarFull + s), (uint32_t)(u & 1), spin, abort, p.st, kSiteTMma);
+    for (int it = blockIdx.x; it < p.nitems && ok; it += gridDim.x, ++li) {
+      const int b = li & 1, ub = li >> 1;
+      // the epilogue has read this buffer's previous tile
+      ok = mbar_wait(bar(kBarAccEmpty + b), (uint32_t)(ub & 1) ^ 1u, spin, abort, p.st, kSiteTMma);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t a_addr = base + (uint32_t)s * kStage;
-      const uint64_t da = smem_desc_sw128(a_addr, 16, 1024);
-      const uint64_t db = smem_desc_sw128(a_addr + kStage / 2, 16, 1024);
-      const uint32_t d = tmem + (c < nq ? 0u : 128u);
-      const bool first = c == 0 || c == nq;
+      for (int c = 0; c < nch && ok; ++c, ++cc) {
+        const int s = cc % kNst, u = cc / kNst;
+        ok = mbar_wait(bar(kBarFull + s), (uint32_t)(u & 1), spin, abort, p.st, kSiteTMma);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a_addr = base + (uint32_t)s * kStage;
+        const uint64_t da = smem_desc_sw128(a_addr, 16, 1024);
+        const uint64_t db = smem_desc_sw128(a_addr + kStage / 2, 16, 1024);
+        const uint32_t d = tmem + 256u * (uint32_t)b + (c < nq ? 0u : 128u);
+        const bool first = c == 0 || c == nq;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, da + 2 * kk, db + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
-      mma_commit(bar(kBarEmpty + s));
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(d, da + 2 * kk, db + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+        mma_commit(bar(kBarEmpty + s));
+      }
+      if (ok) mma_commit(bar(kBarAccFull + b));
     }
-    if (ok) mma_commit(bar(kBarDone));
     mma_commit(bar(kBarDrain));
     for (long long w = 0; w < kDrainSpin; ++w)
       if (mbar_try_wait(bar(kBarDrain), 0)) break;
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 64;               // 0..127: this thread's column for the column terms
-    const int qd = warp & 3;                       // TMEM lane quarter this warp may access
+    // eight warps: warp w reads TMEM lane quarter w % 4 (rows 32 (w % 4) ..),
+    // columns 64 h .. 64 h + 63 with h = (w - 2) / 4
+    const int et = threadIdx.x - 64;               // 0..255; et < 128: a column of the column terms
+    const int qd = warp & 3, hf = (warp - 2) >> 2;
     const int r = 32 * qd + lane;                  // tile row = TMEM lane
-    const int i = i0 + r;
-    const bool row_ok = i < p.T;
-    const size_t hb = (size_t)bh * p.T;
-    const bool diag = jb == ib;
-    // column terms
-    const int jc = j0 + et;
-    const float a2c = jc < p.T ? p.a2[hb + jc] : -INFINITY;
-    float rowf = 0.0f, p2i = 0.0f;
-    if (row_ok) p2i = p.p2[hb + i];
-    if (diag) {
-      col_term[et] = a2c;
-    } else {
-      // rank-one gate factor: D'_ij = 2^(a2_j - A) 2^(A - p2_i), A the tile's
-      // largest column term (every key of the tile precedes every query row)
-      const float m = warp_max(a2c);
-      if (lane == 0) amax_red[warp - 2] = m;
-      named_bar_sync(1, 128);
-      const float A = fmaxf(fmaxf(amax_red[0], amax_red[1]), fmaxf(amax_red[2], amax_red[3]));
-      col_term[et] = exp2f(a2c - A);
-      rowf = row_ok ? exp2f(A - p2i) : 0.0f;
-    }
-    const float invn = row_ok ? p.invn[hb + i] : 0.0f;
-    const float dbi = row_ok ? p.db[hb + i] : 0.0f;
-    named_bar_sync(1, 128);                        // column terms visible
-    bool ok = mbar_wait(bar(kBarDone), 0, spin, abort, p.st, kSiteTEpi);
-    tc_fence_after();
-    float rs = 0.0f;
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
-    if (ok) {
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sv[32], cv[32];
-        tmem_ld32(tmem + lane_addr + 32 * ch, sv);
-        tmem_ld32(tmem + lane_addr + 128 + 32 * ch, cv);
-        tmem_wait_ld();
-        float dd[32];
-        uint32_t gw[16], pw[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float gv[2], pv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = 32 * ch + c + e;
-            float dp;
-            if (diag) dp = (row_ok && j0 + col <= i) ? exp2f(col_term[col] - p2i) : 0.0f;
-            else dp = col_term[col] * rowf;
-            const float x = __uint_as_float(sv[c + e]) * p.scale;        // S
-            const float g = dp * fmaf(__uint_as_float(cv[c + e]), invn, dbi);   // D' (.) dC~'
-            gv[e] = g;
-            pv[e] = x * dp * invn;                                         // C~' / n
-            dd[c + e] = x * g;                                             // dD~
-            rs += dd[c + e];
-          }
-          gw[c / 2] = pack_bf16x2(gv[0], gv[1]);
-          pw[c / 2] = pack_bf16x2(pv[0], pv[1]);
-        }
-        // stage: columns 32ch..32ch+31 = 16-byte chunks 4(ch&1)..4(ch&1)+3 of box ch>>1
-        const uint32_t gbox = base + (uint32_t)(ch >> 1) * 16384u;
-        const uint32_t pbox = base + 32768u + (uint32_t)(ch >> 1) * 16384u;
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          const int q = 4 * (ch & 1) + g4;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz(gbox, r, q)), "r"(gw[4 * g4]),
-                       "r"(gw[4 * g4 + 1]), "r"(gw[4 * g4 + 2]), "r"(gw[4 * g4 + 3])
-                       : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz(pbox, r, q)), "r"(pw[4 * g4]),
-                       "r"(pw[4 * g4 + 1]), "r"(pw[4 * g4 + 2]), "r"(pw[4 * g4 + 3])
-                       : "memory");
-        }
-        // column sums over the warp's 32 rows: halving reduce-scatter; lane l
-        // ends with column 32ch + l
-#pragma unroll
-        for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
-          const bool hi = lane & o;
-#pragma unroll
-          for (int k2 = 0; k2 < n / 2; ++k2) {
-            const float keep = hi ? dd[k2 + n / 2] : dd[k2];
-            const float send = hi ? dd[k2] : dd[k2 + n / 2];
-            dd[k2] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
-        }
-        col_red[warp - 2][32 * ch + lane] = dd[0];
+    int li = 0;
+    for (int it = blockIdx.x;; it += gridDim.x, ++li) {
+      // every thread of the group passes each barrier of an item, abort or not
+      if (et == 0) {
+        tma_store_wait_read();                      // the staging buffer is free again
+        epi_stop = it >= p.nitems || *abort;
       }
-      if (row_ok) p.Rpart[((size_t)bh * nb + jb) * p.T + i] = rs;
+      named_bar_sync(1, 256);
+      if (epi_stop) break;
+      int bh, ib, jb;
+      tile_of(it, nb, &bh, &ib, &jb);
+      const int i0 = ib * kTile, j0 = jb * kTile;
+      const int i = i0 + r;
+      const bool row_ok = i < p.T;
+      const size_t hb = (size_t)bh * p.T;
+      const bool diag = jb == ib;
+      const int jc = j0 + (et & 127);
+      const float a2c = (et < 128 && jc < p.T) ? p.a2[hb + jc] : -INFINITY;
+      const float p2i = row_ok ? p.p2[hb + i] : 0.0f;
+      const float invn = row_ok ? p.invn[hb + i] : 0.0f;
+      const float dbi = row_ok ? p.db[hb + i] : 0.0f;
+      const float pscale = invn * p.scale;           // P = S_raw s D' / n
+      float rowf = 0.0f;
+      if (diag) {
+        if (et < 128) col_term[et] = a2c;
+      } else {
+        // rank-one gate factor: D'_ij = 2^(a2_j - A) 2^(A - p2_i), A the tile's
+        // largest column term (every key of the tile precedes every query row)
+        const float m = warp_max(a2c);
+        if (lane == 0 && et < 128) amax_red[warp - 2] = m;
+        named_bar_sync(1, 256);
+        const float A = fmaxf(fmaxf(amax_red[0], amax_red[1]), fmaxf(amax_red[2], amax_red[3]));
+        if (et < 128) col_term[et] = exp2f(a2c - A);
+        rowf = row_ok ? exp2f(A - p2i) : 0.0f;
+      }
+      named_bar_sync(1, 256);                        // column terms visible
+      const int b = li & 1, ub = li >> 1;
+      // warp-uniform: the TMEM loads and shuffles below are warp-collective
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccFull + b), (uint32_t)(ub & 1), spin, abort,
+                                                        p.st, kSiteTEpi));
+      tc_fence_after();
+      float rs = 0.0f;                               // S_raw (.) G over this warp's columns
+      if (ok) {
+        uint32_t sv[2][32], cv[2][32];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          tmem_ld32(tmem + lane_addr + 256u * (uint32_t)b + 64 * hf + 32 * u, sv[u]);
+          tmem_ld32(tmem + lane_addr + 256u * (uint32_t)b + 128 + 64 * hf + 32 * u, cv[u]);
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarAccEmpty + b));   // the buffer is read: the products may reuse it
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int ch = 2 * hf + u;                 // 32-column chunk of the tile
+          float dd[32];
+          uint32_t gw[16], pw[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 ct = *reinterpret_cast<const float4*>(&col_term[32 * ch + c]);
+            const float ctv[4] = {ct.x, ct.y, ct.z, ct.w};
+            float gv[4], pv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int col = 32 * ch + c + e;
+              float dp;
+              if (diag) dp = (row_ok && j0 + col <= i) ? exp2f(ctv[e] - p2i) : 0.0f;
+              else dp = ctv[e] * rowf;
+              const float sr = __uint_as_float(sv[u][c + e]);                     // S / s
+              const float g = dp * fmaf(__uint_as_float(cv[u][c + e]), invn, dbi); // D' (.) dC~'
+              gv[e] = g;
+              pv[e] = sr * pscale * dp;                                           // C~' / n
+              dd[c + e] = sr * g;                                                 // dD~ / s
+              rs += dd[c + e];
+            }
+            gw[c / 2] = pack_bf16x2(gv[0], gv[1]);
+            gw[c / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
+            pw[c / 2] = pack_bf16x2(pv[0], pv[1]);
+            pw[c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+          }
+          // stage: columns 32ch..32ch+31 = 16-byte chunks 4(ch&1)..4(ch&1)+3 of box ch>>1
+          const uint32_t gbox = sStage + (uint32_t)(ch >> 1) * 16384u;
+          const uint32_t pbox = sStage + 32768u + (uint32_t)(ch >> 1) * 16384u;
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            const int q = 4 * (ch & 1) + g4;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz(gbox, r, q)), "r"(gw[4 * g4]),
+                         "r"(gw[4 * g4 + 1]), "r"(gw[4 * g4 + 2]), "r"(gw[4 * g4 + 3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz(pbox, r, q)), "r"(pw[4 * g4]),
+                         "r"(pw[4 * g4 + 1]), "r"(pw[4 * g4 + 2]), "r"(pw[4 * g4 + 3])
+                         : "memory");
+          }
+          // column sums over the warp's 32 rows: halving reduce-scatter; lane l
+          // ends with column 32ch + l
+#pragma unroll
+          for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+            const bool hi = lane & o;
+#pragma unroll
+            for (int k2 = 0; k2 < n / 2; ++k2) {
+              const float keep = hi ? dd[k2 + n / 2] : dd[k2];
+              const float send = hi ? dd[k2] : dd[k2 + n / 2];
+              dd[k2] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          col_red[qd][32 * ch + lane] = dd[0];
+        }
+        row_red[hf][r] = rs;
+      }
       fence_proxy_async_smem();
+      named_bar_sync(1, 256);                        // staging and partial sums complete
+      if (ok) {
+        if (et < 128) {
+          if (jc < p.T)
+            p.Cpart[((size_t)bh * nb + ib) * p.T + jc] =
+                p.scale * (col_red[0][et] + col_red[1][et] + col_red[2][et] + col_red[3][et]);
+          if (i0 + et < p.T) p.Rpart[((size_t)bh * nb + jb) * p.T + i0 + et] = p.scale * (row_red[0][et] + row_red[1][et]);
+        }
+        if (et == 0) {
+          for (int b2 = 0; b2 < 2 && j0 + 64 * b2 < p.T; ++b2) {   // boxes that start inside the matrix
+            tma_store_3d(&tmap_g, sStage + (uint32_t)b2 * 16384u, j0 + 64 * b2, i0, bh);
+            tma_store_3d(&tmap_p, sStage + 32768u + (uint32_t)b2 * 16384u, j0 + 64 * b2, i0, bh);
+          }
+          tma_store_commit();
+        }
+      }
     }
     tc_fence_before();
-    named_bar_sync(1, 128);
-    if (ok) {
-      if (jc < p.T)
-        p.Cpart[((size_t)bh * nb + ib) * p.T + jc] = col_red[0][et] + col_red[1][et] + col_red[2][et] + col_red[3][et];
-      if (et == 0) {
-        for (int b2 = 0; b2 < 2 && j0 + 64 * b2 < p.T; ++b2) {
-          tma_store_3d(&tmap_g, base + (uint32_t)b2 * 16384u, j0 + 64 * b2, i0, bh);
-          tma_store_3d(&tmap_p, base + 32768u + (uint32_t)b2 * 16384u, j0 + 64 * b2, i0, bh);
-        }
-        tma_store_commit();
-        tma_store_wait_read();
-      }
-    }
   }
 
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kCols);
+    tmem_dealloc(tmem, 512);
   }
-  // after an abort, loads may still be landing: wait (bounded) for every issued one
+  // after an abort, loads may still be landing: wait (bounded) for the last
+  // round of every slot
   if (threadIdx.x == 0 && abort_flag) {
     const int issued = issued_s;
-    for (int c = 0; c < issued; ++c) {
-      const int s = c % kNst, u = c / kNst;
-      if (c + kNst < issued) continue;             // a later round of the slot completed after it
+    for (int c = max(0, issued - kNst); c < issued; ++c)
       for (long long w = 0; w < kDrainSpin; ++w)
-        if (mbar_try_wait(bar(kBarFull + s), (uint32_t)(u & 1))) break;
-    }
+        if (mbar_try_wait(bar(kBarFull + c % kNst), (uint32_t)((c / kNst) & 1))) break;
   }
 }
 
@@ -314,7 +345,8 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 //   dV_g =   sum_{ib >= g} P[ib, g]^T dH[ib]    A = P^T block, MN-major
 // B (K, Q or dH rows) is MN-major.  The 128 x d accumulator sits in TMEM
 // (d <= 512 columns); A blocks come through a two-slot ring, B through a
-// four-slot ring of 128-column chunks.  CTAs run longest first.
+// four-slot ring of 128-column chunks.  CTAs run head by head, longest first
+// within a head.
 constexpr int kPThreads = 192;          // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int kANst = 2, kBNst = 4;
 constexpr uint32_t kABytes = 32768, kBBytes = 32768;
@@ -344,10 +376,11 @@ bwd_prod_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &abort_flag;
 
-  // work item: rank w = 0 has the most blocks to sum over (nb - w of them)
-  const int w = (int)(blockIdx.x / (3u * (unsigned)p.BH));
-  const int prod = (int)((blockIdx.x / (unsigned)p.BH) % 3u);
-  const int bh = (int)(blockIdx.x % (unsigned)p.BH);
+  // work item: head-major (the CTAs in flight share a few heads' G, P, K, Q,
+  // dH in L2), within a head longest first: rank w sums nb - w blocks
+  const int bh = (int)(blockIdx.x / (3u * (unsigned)p.nb));
+  const int w = (int)((blockIdx.x % (3u * (unsigned)p.nb)) / 3u);
+  const int prod = (int)(blockIdx.x % 3u);
   const int nkb = p.nb - w;                                  // blocks in the sum
   const int g = prod == 0 ? p.nb - 1 - w : w;                // output row block
   const int kb0 = prod == 0 ? 0 : g;                         // first summed block
@@ -460,7 +493,8 @@ bwd_prod_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constan
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3, r = 32 * qd + lane;
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
-    bool ok = mbar_wait(bar(kPBarDone), 0, spin, abort, p.st, kSitePEpi);
+    // warp-uniform: the TMEM loads below are warp-collective
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kPBarDone), 0, spin, abort, p.st, kSitePEpi));
     tc_fence_after();
     if (ok) {
       // stage the bf16 block in 64-column boxes over the (now idle) rings
@@ -577,8 +611,8 @@ int launch_bwd_tiles(const BwdTileArgs& a, cudaStream_t stream) {
   if (!bwd_tc_supported(a.T, a.dqk, a.dv, kBF16) || !device_is_sm100_family()) return kUnsupported;
   const int nb = (a.T + kTile - 1) / kTile;
   const long long BHT = (long long)a.BH * a.T;
-  const long long grid = (long long)a.BH * (a.with_upper ? nb * nb : nb * (nb + 1) / 2);
-  if (grid > 0x7fffffffLL || (BHT + 7) / 8 > 0x7fffffffLL) return kInval;
+  const long long nitems = (long long)a.BH * (nb * (nb + 1) / 2);
+  if (nitems > 0x7fffffffLL || (BHT + 7) / 8 > 0x7fffffffLL) return kInval;
   CUtensorMap mq, mk, mdh, mv, mg, mp;
   if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kTile) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, kTile) ||
       !make_map(&mdh, a.dh, a.dv, a.T, a.BH, kTile) || !make_map(&mv, a.v, a.dv, a.T, a.BH, kTile) ||
@@ -591,11 +625,15 @@ int launch_bwd_tiles(const BwdTileArgs& a, cudaStream_t stream) {
   TileParams p;
   p.a2 = a.g.a2; p.p2 = a.g.p2; p.invn = a.invn; p.db = a.db;
   p.Rpart = a.Rpart; p.Cpart = a.Cpart;
-  p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv; p.nb = nb; p.with_upper = a.with_upper;
+  p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv; p.nb = nb; p.nitems = (int)nitems;
   p.scale = a.scale; p.st = a.st;
-  const size_t smem = (size_t)kNst * kStage + 1024;
+  const size_t smem = (size_t)kNst * kStage + kStaging + 1024;
   if (cudaFuncSetAttribute(bwd_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return kCuda;
+  int dev = 0, sms = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return kCuda;
+  const int grid = (int)std::min<long long>(nitems, sms);   // persistent: one CTA per SM
   bwd_tile_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(mq, mk, mdh, mv, mg, mp, p);
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   bwd_tile_sums_kernel<<<(unsigned)((BHT + 255) / 256), 256, 0, stream>>>(a.Rpart, a.Cpart, a.R, a.Ccol, a.T, nb,

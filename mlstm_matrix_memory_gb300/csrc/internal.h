@@ -84,8 +84,9 @@ bool current_status(DevStatus* out);
 
 // Tiles of the parallel backward on the tensor cores (bwd_tc.cu): from the
 // gate terms and the forward's row statistics, writes G = D' (.) dC~' and
-// P = C~'/n (bf16, [BH, T, ldT], zero above the diagonal) and the row and
-// column sums R, Ccol of dD~ = S (.) G.  Returns a Status.
+// P = C~'/n (bf16, [BH, T, ldT]: the tiles on and below the diagonal, zero
+// above it within the diagonal tiles) and the row and column sums R, Ccol of
+// dD~ = S (.) G.  Returns a Status.
 struct BwdTileArgs {
   const void* q;
   const void* k;
@@ -104,7 +105,6 @@ struct BwdTileArgs {
   float* R;             // out [BH*T]
   float* Ccol;          // out [BH*T]
   int BH, T, ldT, dqk, dv;
-  int with_upper;       // 1: store zero tiles above the diagonal too
   float scale;
   DevStatus st;
 };
