@@ -216,10 +216,11 @@ int mlstm_step_seq_opt(float *C, float *n, float *m,
  *              either path).
  * Two paths:
  *  - bf16 with d_qk and d_v multiples of 8, on the sm_100 family: a forward
- *    pass gives H~, n and the signed row sums b; one tensor-core kernel forms
- *    S = QK^T/sqrt(d) and dC = dH~ V^T per 128 x 128 tile in TMEM and writes
- *    G = D' (.) dC~' and P = C~'/n (bf16) and the tile's row and column sums
- *    of dD~; dQ, dK, dV are batched GEMMs over G and P (cuBLAS).  Workspace:
+ *    pass gives H~, n and the signed row sums b; a persistent tensor-core
+ *    kernel forms S = QK^T/sqrt(d) and dC = dH~ V^T per 128 x 128 tile on or
+ *    below the diagonal in TMEM and writes G = D' (.) dC~' and P = C~'/n
+ *    (bf16) and the tile's row and column sums of dD~; a second tensor-core
+ *    kernel forms dQ, dK, dV over the lower triangle of G and P.  Workspace:
  *    two bf16 T x T matrices per head (about 0.54 GB for B=8, H=4, T=2048).
  *  - otherwise the five T x T products are batched GEMMs (cuBLAS) with fp32
  *    S and dL/dC materialised (about 1.6 GB for B=8, H=4, T=2048, bf16).
