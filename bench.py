@@ -355,7 +355,8 @@ def time_final_state(M, w, xd, reps):
 def time_backward(M, w, xd, reps):
     """The parallel backward on the parallel workload for a seeded output
     gradient: algorithmic work T^2 (3 d_qk + 2 d_v) flops per head (the five
-    causal products S, dC, dQ, dK, dV)."""
+    causal products S, dC, dQ, dK, dV).  Also timed given the forward's saved
+    outputs (no forward pass inside)."""
     lib = M.library()
     dh = torch.randn((w.B, w.H, w.T, w.d_v), generator=torch.Generator().manual_seed(1)).to(w.dtype).cuda()
     ws_buf = torch.empty(int(lib.mlstm_parallel_bwd_workspace(w.B, w.H, w.T, 1 if w.dtype == torch.bfloat16 else 0)),
@@ -365,17 +366,29 @@ def time_backward(M, w, xd, reps):
     def one():
         M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh, workspace=ws_buf)
 
-    for _ in range(2):
-        one()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    torch.cuda.synchronize()
-    for i in range(reps):
-        ev[i][0].record(stream)
-        one()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    return ms, float(w.B * w.H * w.T * w.T * (3 * w.d_qk + 2 * w.d_v)), ws_buf.numel()
+    # the same with the forward's saved H~, n and signed b (a training step's backward)
+    saved = M.parallel_fwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], return_stats=True)
+    saved = (saved[0], saved[2], saved[3])
+
+    def one_saved():
+        M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh, workspace=ws_buf,
+                       saved=saved)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for i in range(reps):
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    ms = timed(one)
+    ms_saved = timed(one_saved)
+    return ms, float(w.B * w.H * w.T * w.T * (3 * w.d_qk + 2 * w.d_v)), ws_buf.numel(), ms_saved
 
 
 def time_recurrent_backward(M, w, xd, reps):
@@ -550,9 +563,10 @@ def main():
                                             "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
                                             "traffic": None}}
     if bwd is not None:
-        ms, fl, wsb = bwd
+        ms, fl, wsb, ms_saved = bwd
         tf = fl / (ms * 1e-3) / 1e12
         line["backward"] = {"workload": w.name, "ms": ms, "workspace_bytes": wsb,
+                            "ms_with_saved_forward": ms_saved,
                             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
                                          "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
                                          "work": "causal T^2 (3 d_qk + 2 d_v) per head", "traffic": None}}

@@ -173,11 +173,15 @@ int mlstm_parallel_fwd_host(const void *q, const void *k, const void *v,
  *               pre-activations, 16-byte aligned, or NULL.  When given, h =
  *               sigmoid(ogate_pre) (.) H~ (eq 78) instead of H~ (eq 77); the
  *               CTA-pair kernel applies it in its epilogue, the other kernels
- *               in a separate elementwise pass. */
+ *               in a separate elementwise pass.
+ *   b_out       the parallel forward only: [B,H,T] fp32 out, the signed row
+ *               sums b of eq (83) (n = max(|b|, exp(-m))), or NULL.  With H~
+ *               and n they are what mlstm_parallel_bwd_saved takes. */
 typedef struct {
     int algo;
     int forget_exp;
     const void *ogate_pre;
+    float *b_out;
 } mlstm_options;
 
 int mlstm_parallel_fwd_opt(const void *q, const void *k, const void *v,
@@ -228,6 +232,20 @@ int mlstm_step_seq_opt(float *C, float *n, float *m,
  * an input. */
 size_t mlstm_parallel_bwd_workspace(int B, int H, int T, int dtype);
 size_t mlstm_parallel_bwd_workspace_ex(int B, int H, int T, int d_qk, int d_v, int dtype);
+
+/* mlstm_parallel_bwd given what the forward already produced, as a training
+ * step keeps it: h = H~ (the forward's output without an output gate), n
+ * (its n_out) and b (its options' b_out), all from mlstm_parallel_fwd_opt
+ * on the same inputs.  On the tensor-core path the forward pass inside the
+ * backward is then skipped; otherwise h, n, b are ignored and the result is
+ * that of mlstm_parallel_bwd.  Arguments and workspace as there, plus
+ *   h          [B,H,T,d_v] dtype, n, b [B,H,T] fp32 (all non-NULL). */
+int mlstm_parallel_bwd_saved(const void *q, const void *k, const void *v,
+                             const float *igate_pre, const float *fgate_pre, const void *dh,
+                             const void *h, const float *n, const float *b,
+                             void *dq, void *dk, void *dv, float *d_igate, float *d_fgate,
+                             int B, int H, int T, int d_qk, int d_v, int dtype,
+                             void *workspace, size_t workspace_bytes, void *stream);
 
 int mlstm_parallel_bwd(const void *q, const void *k, const void *v,
                        const float *igate_pre, const float *fgate_pre, const void *dh,

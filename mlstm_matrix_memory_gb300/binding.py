@@ -74,6 +74,8 @@ def library() -> ctypes.CDLL:
         lib.mlstm_parallel_bwd_workspace_ex.restype = sz
         lib.mlstm_parallel_bwd.argtypes = [vp] * 11 + [i] * 6 + [vp, sz, vp]
         lib.mlstm_parallel_bwd.restype = i
+        lib.mlstm_parallel_bwd_saved.argtypes = [vp] * 14 + [i] * 6 + [vp, sz, vp]
+        lib.mlstm_parallel_bwd_saved.restype = i
         op = ctypes.POINTER(_Options)
         lib.mlstm_parallel_fwd_opt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, op, vp]
         lib.mlstm_parallel_fwd_opt.restype = i
@@ -106,16 +108,19 @@ def status_str(code: int) -> str:
 
 class _Options(ctypes.Structure):
     """``mlstm_options`` of include/mlstm.h."""
-    _fields_ = [("algo", ctypes.c_int), ("forget_exp", ctypes.c_int), ("ogate_pre", ctypes.c_void_p)]
+    _fields_ = [("algo", ctypes.c_int), ("forget_exp", ctypes.c_int), ("ogate_pre", ctypes.c_void_p),
+                ("b_out", ctypes.c_void_p)]
 
 
 FORGET = {"sigmoid": 0, "exp": 1}
 
 
-def _options(algo: str = "auto", forget: str = "sigmoid", ogate: Optional[torch.Tensor] = None) -> _Options:
+def _options(algo: str = "auto", forget: str = "sigmoid", ogate: Optional[torch.Tensor] = None,
+             b_out: Optional[torch.Tensor] = None) -> _Options:
     if forget not in FORGET:
         raise ValueError(f"forget must be one of {sorted(FORGET)}")
-    return _Options(ALGOS[algo], FORGET[forget], None if ogate is None else ogate.data_ptr())
+    return _Options(ALGOS[algo], FORGET[forget], None if ogate is None else ogate.data_ptr(),
+                    None if b_out is None else b_out.data_ptr())
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
@@ -145,7 +150,7 @@ def parallel_fwd_workspace_bytes(B: int, H: int, T: int) -> int:
 
 def parallel_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: torch.Tensor,
                  fgate_pre: torch.Tensor, *, h: Optional[torch.Tensor] = None,
-                 return_mn: bool = False, workspace: Optional[torch.Tensor] = None,
+                 return_mn: bool = False, return_stats: bool = False, workspace: Optional[torch.Tensor] = None,
                  algo: str = "auto", ogate: Optional[torch.Tensor] = None, forget: str = "sigmoid"):
     """Stabilized parallel mLSTM forward pass.
 
@@ -154,7 +159,9 @@ def parallel_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: t
     input dtype: H~, or sigmoid(ogate) * H~ when the output-gate
     pre-activations ``ogate`` [B,H,T,d_v] are given; ``forget`` selects the
     forget activation ("sigmoid" or "exp").  With ``return_mn`` also the row
-    stabilizer m and the normalizer n, both [B,H,T] fp32.  Runs on the
+    stabilizer m and the normalizer n, both [B,H,T] fp32; with
+    ``return_stats`` (h, m, n, b), b the signed row sums [B,H,T] fp32 (what
+    ``parallel_bwd(..., saved=(h, n, b))`` takes).  Runs on the
     current stream.
     """
     lib = library()
@@ -176,9 +183,12 @@ def parallel_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: t
         h = torch.empty((B, H, T, dv), dtype=q.dtype, device=dev)
     _need(h, "h", (B, H, T, dv), q.dtype, dev)
     m = n = None
-    if return_mn:
+    b = None
+    if return_mn or return_stats:
         m = torch.empty((B, H, T), dtype=torch.float32, device=dev)
         n = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    if return_stats:
+        b = torch.empty((B, H, T), dtype=torch.float32, device=dev)
     ws_bytes = int(lib.mlstm_parallel_fwd_workspace(B, H, T))
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -186,13 +196,15 @@ def parallel_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: t
         raise ValueError(f"workspace must hold {ws_bytes} bytes on {dev}")
     if ogate is not None:
         _need(ogate, "ogate", (B, H, T, dv), q.dtype, dev)
-    opt = _options(algo, forget, ogate)
+    opt = _options(algo, forget, ogate, b)
     rc = lib.mlstm_parallel_fwd_opt(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(h),
                                     _ptr(m), _ptr(n), B, H, T, dqk, dv, _DTYPES[q.dtype],
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     ctypes.byref(opt), _stream(dev))
     if rc != 0:
         raise MlstmError(rc, "mlstm_parallel_fwd")
+    if return_stats:
+        return h, m, n, b
     return (h, m, n) if return_mn else h
 
 
@@ -274,9 +286,13 @@ def parallel_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_p
 
 
 def parallel_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: torch.Tensor,
-                 fgate_pre: torch.Tensor, dh: torch.Tensor, *, workspace: Optional[torch.Tensor] = None):
+                 fgate_pre: torch.Tensor, dh: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
+                 saved=None):
     """``mlstm_parallel_bwd``: gradients (dq, dk, dv, d_igate, d_fgate) of the
-    parallel forward for the output gradient dh = dL/dH~ (CUDA tensors)."""
+    parallel forward for the output gradient dh = dL/dH~ (CUDA tensors).
+    ``saved`` = (h, n, b) from ``parallel_fwd(..., return_stats=True)`` on the
+    same inputs (``mlstm_parallel_bwd_saved``) lets the tensor-core path skip
+    its forward pass."""
     lib = library()
     B, H, T, dqk = q.shape
     dv = v.shape[-1]
@@ -296,9 +312,20 @@ def parallel_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: t
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dig, dfg = torch.empty_like(igate_pre), torch.empty_like(fgate_pre)
-    rc = lib.mlstm_parallel_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh), _ptr(dq),
-                                _ptr(dk), _ptr(dvv), _ptr(dig), _ptr(dfg), B, H, T, dqk, dv, _DTYPES[q.dtype],
-                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev))
+    if saved is not None:
+        hs, ns, bs = saved
+        _need(hs, "saved h", (B, H, T, dv), q.dtype, dev)
+        _need(ns, "saved n", (B, H, T), torch.float32, dev)
+        _need(bs, "saved b", (B, H, T), torch.float32, dev)
+        rc = lib.mlstm_parallel_bwd_saved(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh),
+                                          _ptr(hs), _ptr(ns), _ptr(bs), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(dig),
+                                          _ptr(dfg), B, H, T, dqk, dv, _DTYPES[q.dtype], _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(dev))
+    else:
+        rc = lib.mlstm_parallel_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh),
+                                    _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(dig), _ptr(dfg), B, H, T, dqk, dv,
+                                    _DTYPES[q.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(dev))
     if rc != 0:
         raise MlstmError(rc, "mlstm_parallel_bwd")
     return dq, dk, dvv, dig, dfg

@@ -126,7 +126,7 @@ namespace {
 
 int fwd_gated(const void* q, const void* k, const void* v, void* h, float* m_out, float* n_out, int B, int H,
               int T, int d_qk, int d_v, int dtype, const void* workspace, size_t workspace_bytes, int algo,
-              bool after_gate_prep, const void* og, void* stream) {
+              bool after_gate_prep, const void* og, void* stream, float* b_out = nullptr) {
   int rc = check_sizes(B, H, T);
   if (rc != MLSTM_OK) return rc;
   if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
@@ -160,6 +160,7 @@ int fwd_gated(const void* q, const void* k, const void* v, void* h, float* m_out
   a.st.spin_limit = g_spin_limit.load();
   a.after_gate_prep = after_gate_prep;
   a.og = og;
+  a.b_out = b_out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (use_tc) return launch_fwd_tc(a, s);
   if (launch_fwd_simt(a, s) != cudaSuccess) return MLSTM_ECUDA;
@@ -198,7 +199,7 @@ int mlstm_parallel_fwd_opt(const void* q, const void* k, const void* v, const fl
   rc = mlstm_gate_prep_opt(igate_pre, fgate_pre, B, H, T, workspace, workspace_bytes, opt, stream);
   if (rc != MLSTM_OK) return rc;
   return fwd_gated(q, k, v, h, m_out, n_out, B, H, T, d_qk, d_v, dtype, workspace, workspace_bytes, algo, true,
-                   og, stream);
+                   og, stream, opt ? opt->b_out : nullptr);
 }
 
 int mlstm_parallel_fwd_ex(const void* q, const void* k, const void* v, const float* igate_pre,

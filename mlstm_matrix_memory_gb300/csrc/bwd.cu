@@ -197,7 +197,8 @@ bool gemm(cublasHandle_t h, cublasOperation_t ta, cublasOperation_t tb, int m, i
 
 int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
                 const void* dh, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int BH, int T, int d_qk,
-                int d_v, void* workspace, cudaStream_t st);
+                int d_v, void* workspace, cudaStream_t st, const void* h_saved = nullptr,
+                const float* n_saved = nullptr, const float* b_saved = nullptr);
 
 // Workspace of the tensor-core path: gate terms, the forward's H~ (d_v
 // columns) and row statistics, bf16 G and P with rows of ldT = T rounded up
@@ -335,6 +336,28 @@ int mlstm_parallel_bwd(const void* q, const void* k, const void* v, const float*
   return cudaGetLastError() == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
 }
 
+int mlstm_parallel_bwd_saved(const void* q, const void* k, const void* v, const float* igate_pre,
+                             const float* fgate_pre, const void* dh, const void* h, const float* n, const float* b,
+                             void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int B, int H, int T,
+                             int d_qk, int d_v, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || H < 0 || T < 0 || T > kMaxBwdT) return MLSTM_EINVAL;
+  if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
+  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
+  const long long BH = (long long)B * H;
+  if (BH > (1 << 20)) return MLSTM_EINVAL;
+  if (BH == 0 || T == 0) return MLSTM_OK;
+  if (!h || !n || !b) return MLSTM_EINVAL;
+  if (!q || !k || !v || !igate_pre || !fgate_pre || !dh || !dq || !dk || !dv || !d_igate || !d_fgate)
+    return MLSTM_EINVAL;
+  if (!workspace) return MLSTM_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLSTM_EALIGN;
+  if (use_tc_path(T, d_qk, d_v, dtype) && workspace_bytes >= tc_layout(BH, T, d_v).total)
+    return bwd_tc_path(q, k, v, igate_pre, fgate_pre, dh, dq, dk, dv, d_igate, d_fgate, (int)BH, T, d_qk, d_v,
+                       workspace, static_cast<cudaStream_t>(stream), h, n, b);
+  return mlstm_parallel_bwd(q, k, v, igate_pre, fgate_pre, dh, dq, dk, dv, d_igate, d_fgate, B, H, T, d_qk, d_v,
+                            dtype, workspace, workspace_bytes, stream);
+}
+
 }  // extern "C"
 
 namespace mlstm {
@@ -345,7 +368,8 @@ namespace {
 // lower triangle of G and P, the gate gradients.
 int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
                 const void* dh, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int BH, int T, int d_qk,
-                int d_v, void* workspace, cudaStream_t st) {
+                int d_v, void* workspace, cudaStream_t st, const void* h_saved, const float* n_saved,
+                const float* b_saved) {
   const TcLayout L = tc_layout(BH, T, d_v);
   char* w = static_cast<char*>(workspace);
   char* gate_ws = w;
@@ -369,15 +393,21 @@ int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_
   DevStatus ds;
   if (!current_status(&ds)) return MLSTM_ECUDA;
   const float s = (float)(1.0 / sqrt((double)d_qk));
-  // forward: H~, n and the signed row sums b (eqs 79-86)
-  FwdArgs fa;
-  fa.q = q; fa.k = k; fa.v = v; fa.h = hf; fa.m_out = nullptr; fa.n_out = nrow; fa.b_out = brow;
-  fa.g = g; fa.BH = BH; fa.T = T; fa.dqk = d_qk; fa.dv = d_v; fa.dtype = kBF16; fa.scale = s; fa.st = ds;
-  rc = launch_fwd_tc(fa, st);
-  if (rc == kUnsupported) rc = launch_fwd_simt(fa, st) == cudaSuccess ? kOk : kCuda;
-  if (rc != kOk) return rc;
+  const bool saved = h_saved && n_saved && b_saved;
+  if (!saved) {
+    // forward: H~, n and the signed row sums b (eqs 79-86)
+    FwdArgs fa;
+    fa.q = q; fa.k = k; fa.v = v; fa.h = hf; fa.m_out = nullptr; fa.n_out = nrow; fa.b_out = brow;
+    fa.g = g; fa.BH = BH; fa.T = T; fa.dqk = d_qk; fa.dv = d_v; fa.dtype = kBF16; fa.scale = s; fa.st = ds;
+    rc = launch_fwd_tc(fa, st);
+    if (rc == kUnsupported) rc = launch_fwd_simt(fa, st) == cudaSuccess ? kOk : kCuda;
+    if (rc != kOk) return rc;
+  }
   BwdTileArgs ta;
-  ta.q = q; ta.k = k; ta.v = v; ta.dh = dh; ta.h = hf; ta.nrow = nrow; ta.brow = brow; ta.g = g;
+  ta.q = q; ta.k = k; ta.v = v; ta.dh = dh; ta.g = g;
+  ta.h = saved ? h_saved : hf;
+  ta.nrow = saved ? n_saved : nrow;
+  ta.brow = saved ? b_saved : brow;
   ta.invn = invn; ta.db = dbv; ta.G = G; ta.P = P; ta.Rpart = Rpart; ta.Cpart = Cpart; ta.R = R; ta.Ccol = Ccol;
   ta.BH = BH; ta.T = T; ta.ldT = L.ldT; ta.dqk = d_qk; ta.dv = d_v; ta.scale = s; ta.st = ds;
   rc = launch_bwd_tiles(ta, st);

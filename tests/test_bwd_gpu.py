@@ -46,3 +46,28 @@ def test_bwd_matches_oracle(M, case):
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
     for name, g, w in zip(("dq", "dk", "dv", "d_igate", "d_fgate"), got, want):
         assert rel_err(g, w) <= tol, name
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 300, 64, 64), (2, 2, 1024, 384, 384)])
+def test_bwd_with_saved_forward(M, shape):
+    """mlstm_parallel_bwd_saved with the forward's own H~, n and signed b gives
+    bit for bit the gradients of the recomputing backward; |b| equals n where
+    the normalizer floor exp(-m) is not engaged."""
+    B, H, T, dqk, dv = shape
+    x = W.sequence_inputs(B, H, T, dqk, dv, torch.bfloat16, seed=T + 3)
+    dh = torch.randn((B, H, T, dv), generator=torch.Generator().manual_seed(T)).to(torch.bfloat16)
+    xd = {k: v.cuda() for k, v in x.items()}
+    dhd = dh.cuda()
+    h, m, n, b = M.parallel_fwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], return_stats=True)
+    got = M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dhd, saved=(h, n, b))
+    ref = M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dhd)
+    torch.cuda.synchronize()
+    assert M.last_device_status() == 0
+    for name, g, r in zip(("dq", "dk", "dv", "d_igate", "d_fgate"), got, ref):
+        assert torch.equal(g, r), name
+    above = n > torch.exp(-m) * 1.001
+    assert torch.allclose(b.abs()[above], n[above], rtol=1e-6, atol=0)
+    want = oracle.parallel_backward(x["q"][:1, :1], x["k"][:1, :1], x["v"][:1, :1], x["igate_pre"][:1, :1],
+                                    x["fgate_pre"][:1, :1], dh[:1, :1])
+    for name, g, w in zip(("dq", "dk", "dv", "d_igate", "d_fgate"), got, want):
+        assert rel_err(g[:1, :1], w) <= TOL_BF16, name
