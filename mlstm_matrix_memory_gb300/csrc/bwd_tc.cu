@@ -18,9 +18,10 @@
 // swizzle, zero fill past d).  The kernel is persistent, one CTA per SM,
 // tiles taken round robin in head-major order; two TMEM buffers let the
 // products of one tile run while eight epilogue warps (two per TMEM lane
-// quarter, 64 columns each) turn the previous one into G and P: fp32 from the TMEM rows, bf16 staging, TMA
-// stores, and the tile's row and column sums of dD~ (the column sums by a
-// shuffle reduce-scatter, so every partial is formed in a fixed order).
+// quarter, 64 columns each) turn the previous one into G and P: fp32 from
+// the TMEM rows, bf16 staging, TMA stores, and the tile's row and column sums
+// of dD~ (the column sums by a shuffle reduce-scatter, so every partial is
+// formed in a fixed order).
 // Within the diagonal tile G and P are stored as zero above the diagonal;
 // nothing above it is ever stored or read.
 #include <algorithm>
