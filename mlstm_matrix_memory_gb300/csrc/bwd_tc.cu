@@ -65,6 +65,38 @@ __device__ __forceinline__ uint32_t swz(uint32_t box, int r, int q) {
   return box + (uint32_t)r * 128u + ((uint32_t)(q ^ (r & 7)) << 4);
 }
 
+// G, P and dD~/s of 32 consecutive columns (first key j0c) of one row i from
+// the TMEM words of S/s and dC.  DIAG: the diagonal tile, D' = 2^(a2_j - p2_i)
+// for j <= i (ct holds a2); otherwise D' = ct_j rowf (ct holds 2^(a2_j - A)).
+template <bool DIAG>
+__device__ __forceinline__ void tile_values(const uint32_t (&sv)[32], const uint32_t (&cv)[32], const float* ct,
+                                            int j0c, int i, bool row_ok, float p2i, float rowf, float invn,
+                                            float dbi, float pscale, float (&dd)[32], uint32_t (&gw)[16],
+                                            uint32_t (&pw)[16], float& rs) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const float4 c4 = *reinterpret_cast<const float4*>(ct + c);
+    const float ctv[4] = {c4.x, c4.y, c4.z, c4.w};
+    float gv[4], pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float dp;
+      if (DIAG) dp = (row_ok && j0c + c + e <= i) ? exp2f(ctv[e] - p2i) : 0.0f;
+      else dp = ctv[e] * rowf;
+      const float sr = __uint_as_float(sv[c + e]);                     // S / s
+      const float g = dp * fmaf(__uint_as_float(cv[c + e]), invn, dbi);  // D' (.) dC~'
+      gv[e] = g;
+      pv[e] = sr * pscale * dp;                                          // C~' / n
+      dd[c + e] = sr * g;                                                // dD~ / s
+      rs += dd[c + e];
+    }
+    gw[c / 2] = pack_bf16x2(gv[0], gv[1]);
+    gw[c / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
+    pw[c / 2] = pack_bf16x2(pv[0], pv[1]);
+    pw[c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+  }
+}
+
 // Item it -> head and tile: t = ib (ib + 1) / 2 + jb, jb <= ib.
 __device__ __forceinline__ void tile_of(int it, int nb, int* bh, int* ib, int* jb) {
   const int ntri = nb * (nb + 1) / 2;
@@ -250,29 +282,12 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           const int ch = 2 * hf + u;                 // 32-column chunk of the tile
           float dd[32];
           uint32_t gw[16], pw[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 4) {
-            const float4 ct = *reinterpret_cast<const float4*>(&col_term[32 * ch + c]);
-            const float ctv[4] = {ct.x, ct.y, ct.z, ct.w};
-            float gv[4], pv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int col = 32 * ch + c + e;
-              float dp;
-              if (diag) dp = (row_ok && j0 + col <= i) ? exp2f(ctv[e] - p2i) : 0.0f;
-              else dp = ctv[e] * rowf;
-              const float sr = __uint_as_float(sv[u][c + e]);                     // S / s
-              const float g = dp * fmaf(__uint_as_float(cv[u][c + e]), invn, dbi); // D' (.) dC~'
-              gv[e] = g;
-              pv[e] = sr * pscale * dp;                                           // C~' / n
-              dd[c + e] = sr * g;                                                 // dD~ / s
-              rs += dd[c + e];
-            }
-            gw[c / 2] = pack_bf16x2(gv[0], gv[1]);
-            gw[c / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
-            pw[c / 2] = pack_bf16x2(pv[0], pv[1]);
-            pw[c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-          }
+          if (diag)
+            tile_values<true>(sv[u], cv[u], col_term + 32 * ch, j0 + 32 * ch, i, row_ok, p2i, rowf, invn, dbi,
+                              pscale, dd, gw, pw, rs);
+          else
+            tile_values<false>(sv[u], cv[u], col_term + 32 * ch, j0 + 32 * ch, i, row_ok, p2i, rowf, invn, dbi,
+                               pscale, dd, gw, pw, rs);
           // stage: columns 32ch..32ch+31 = 16-byte chunks 4(ch&1)..4(ch&1)+3 of box ch>>1
           const uint32_t gbox = sStage + (uint32_t)(ch >> 1) * 16384u;
           const uint32_t pbox = sStage + 32768u + (uint32_t)(ch >> 1) * 16384u;
