@@ -47,10 +47,11 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-step", action="store_true", help="skip the recurrent-step measurement")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-kernel", choices=("fwd", "step", "step_seq", "rbwd"), default=None,
+    p.add_argument("--profile-kernel", choices=("fwd", "step", "step_seq", "rbwd", "bwd"), default=None,
                    help="no timing: one warm-up and one launch of the fused forward kernel (on --workload), "
                         "of the recurrent step (B=64, H=4, d=512: 256 MB of state), of the 64-token prefill "
-                        "(same heads) or of the recurrent backward (B=4, H=8, T=256, d=384), for ncu captures")
+                        "(same heads), of the recurrent backward (B=4, H=8, T=256, d=384) or of the parallel "
+                        "backward (on --workload), for ncu captures")
     return p.parse_args()
 
 
@@ -442,6 +443,12 @@ def profile_once(args):
         M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
         for _ in range(2):
             M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=args.algo)
+    elif args.profile_kernel == "bwd":
+        w = W.PARALLEL_WORKLOADS[args.workload]
+        xd = {k: v.cuda() for k, v in W.parallel_inputs(w, 0).items()}
+        dh = torch.randn((w.B, w.H, w.T, w.d_v), generator=torch.Generator().manual_seed(1)).to(w.dtype).cuda()
+        for _ in range(2):
+            M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh)
     elif args.profile_kernel == "rbwd":
         # the recurrent backward on 32 heads of the 125M-scale layer's shape, T=256
         x = {k: v.cuda() for k, v in W.sequence_inputs(4, 8, 256, 384, 384, torch.bfloat16, seed=1).items()}
