@@ -158,3 +158,30 @@ def test_recurrent_bwd_validation(lib):
     assert rb(wsb=need - 1) == -7
     assert rb(ws=A + 16) == -2
     assert rb(T=0) == 0
+
+
+def test_parallel_bwd_validation(lib):
+    big = lib.mlstm_parallel_bwd_workspace(2, 3, 100, 1)
+    ex = lib.mlstm_parallel_bwd_workspace_ex(2, 3, 100, 64, 64, 1)
+    assert 0 < ex <= big                      # the exact size never exceeds the size for either path
+    assert lib.mlstm_parallel_bwd_workspace_ex(2, 3, 100, 64, 600, 1) == 0
+    assert lib.mlstm_parallel_bwd_workspace_ex(2, 3, 0, 64, 64, 1) == 0
+    assert lib.mlstm_parallel_bwd_workspace_ex(2, 3, 100, 64, 64, 5) == 0
+
+    def bwd(T=100, dqk=64, dv=64, dt=1, ws=A, wsb=big, q=A):
+        return lib.mlstm_parallel_bwd(q, A, A, A, A, A, A, A, A, A, A, 2, 3, T, dqk, dv, dt, ws, wsb, None)
+
+    def saved(h=A, n=A, b=A, T=100, dt=1, ws=A, wsb=big):
+        return lib.mlstm_parallel_bwd_saved(A, A, A, A, A, A, h, n, b, A, A, A, A, A, 2, 3, T, 64, 64, dt, ws,
+                                            wsb, None)
+    assert bwd(dqk=0) == -1
+    assert bwd(dv=513) == -1
+    assert bwd(dt=4) == -3
+    assert bwd(q=0) == -1
+    assert bwd(ws=0) == -7
+    assert bwd(ws=A + 16) == -2               # 256-byte aligned workspace
+    assert bwd(T=0) == 0
+    assert saved(h=0) == -1                   # the saved forward outputs are required
+    assert saved(b=0) == -1
+    assert saved(dt=7) == -3
+    assert saved(T=0) == 0
