@@ -26,6 +26,7 @@
 // nothing above it is ever stored or read.
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -558,6 +559,230 @@ bwd_prod_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constan
   }
 }
 
+// ---------------------------------------------------------------- products on CTA pairs
+// The same three products with M = 256 on a cluster of two CTAs (tcgen05
+// cta_group::2): CTA rank r owns output block 2 gp + r of a block pair gp and
+// holds its own A blocks; the B chunk (K, Q or dH rows) is split by columns
+// between the two CTAs, so each SM loads half of the B bytes a single-CTA
+// block needs.  A pair sums over the union of its two blocks' ranges; the
+// extra block reads the tile (2 gp, 2 gp + 1) above the diagonal, which
+// bwd_zero_tiles_kernel stores as zeros.  Requires d_qk and d_v multiples of
+// 128 (a B chunk is 256 columns, or 128 for the last, split in halves).
+__global__ void __launch_bounds__(kPThreads, 1)
+bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_p,
+                 const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                 const __grid_constant__ CUtensorMap tmap_dh, const __grid_constant__ CUtensorMap tmap_dq,
+                 const __grid_constant__ CUtensorMap tmap_dk, const __grid_constant__ CUtensorMap tmap_dv,
+                 const ProdParams p) {
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t bars[kPNumBars];
+  __shared__ uint32_t tmem_holder;
+  __shared__ int abort_flag;
+  __shared__ int a_issued_s, b_issued_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &abort_flag;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  // work item of the pair: head-major, longest first within a head
+  const int np = (p.nb + 1) / 2;
+  const int cid = (int)(blockIdx.x >> 1);
+  const int bh = cid / (3 * np);
+  const int w = (cid % (3 * np)) / 3;
+  const int prod = cid % 3;
+  const int gp = prod == 0 ? np - 1 - w : w;
+  const int g0 = 2 * gp, gr = g0 + (int)rank;                // this CTA's output block
+  const int kb0 = prod == 0 ? 0 : g0;
+  const int nkb = prod == 0 ? min(g0 + 2, p.nb) : p.nb - g0;
+  const int r0 = gr * kTile;
+  const int d = prod == 2 ? p.dv : p.dqk;
+  const int nbox = d / 64;                                   // a multiple of 2
+  const int nchunk = (nbox + 3) / 4;                         // 256-column chunks (the last may be 128)
+  const CUtensorMap* ma = prod == 2 ? &tmap_p : &tmap_g;
+  const CUtensorMap* mb = prod == 0 ? &tmap_k : (prod == 1 ? &tmap_q : &tmap_dh);
+  const CUtensorMap* mo = prod == 0 ? &tmap_dq : (prod == 1 ? &tmap_dk : &tmap_dv);
+  const float alpha = prod == 2 ? 1.0f : p.scale;
+  const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint32_t sA = base, sB = base + kANst * kABytes;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto lbar = [&](int i) { return mapa_shared(smem_u32(&bars[i]), 0); };   // the leader's barrier
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    a_issued_s = 0;
+    b_issued_s = 0;
+    for (int s2 = 0; s2 < kANst; ++s2) {
+      mbar_init(bar(kPBarAFull + s2), 1);
+      mbar_init(bar(kPBarAEmpty + s2), 1);
+    }
+    for (int s2 = 0; s2 < kBNst; ++s2) {
+      mbar_init(bar(kPBarBFull + s2), 1);
+      mbar_init(bar(kPBarBEmpty + s2), 1);
+    }
+    mbar_init(bar(kPBarDone), 1);
+    mbar_init(bar(kPBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&tmem_holder), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();                        // peer barriers initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  const long long spin = p.st.spin_limit;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producers (both CTAs)
+    // Each CTA loads its own A blocks and its half of every B chunk into its
+    // own buffers; completion is counted on the leader's full barriers, whose
+    // expected bytes (both CTAs) only the leader posts.
+    tma_prefetch_desc(ma);
+    tma_prefetch_desc(mb);
+    int bi = 0;
+    bool ok = true;
+    for (int t = 0; t < nkb && ok; ++t) {
+      const int kb = kb0 + t;
+      const int as = t % kANst, au = t / kANst;
+      ok = mbar_wait(bar(kPBarAEmpty + as), (uint32_t)(au & 1) ^ 1u, spin, abort, p.st, kSitePProducer);
+      if (!ok) break;
+      if (leader) mbar_arrive_expect_tx(bar(kPBarAFull + as), 2u * kABytes);
+      const uint32_t adst = sA + (uint32_t)as * kABytes;
+      for (int h = 0; h < 2; ++h) {
+        if (prod == 0)   // G[gr rows, kb keys]
+          tma_load_3d_pair(adst + h * 16384u, ma, lbar(kPBarAFull + as), kb * kTile + 64 * h, r0, bh);
+        else             // G[kb rows, gr keys]^T
+          tma_load_3d_pair(adst + h * 16384u, ma, lbar(kPBarAFull + as), r0 + 64 * h, kb * kTile, bh);
+      }
+      a_issued_s = t + 1;
+      for (int c = 0; c < nchunk && ok; ++c, ++bi) {
+        const int bs = bi % kBNst, bu = bi / kBNst;
+        ok = mbar_wait(bar(kPBarBEmpty + bs), (uint32_t)(bu & 1) ^ 1u, spin, abort, p.st, kSitePProducer);
+        if (!ok) break;
+        const bool wide = nbox - 4 * c >= 4;            // 256 columns: two boxes a CTA, else one
+        const int col0 = 256 * c;
+        if (leader) mbar_arrive_expect_tx(bar(kPBarBFull + bs), 2u * (wide ? 32768u : 16384u));
+        if (wide) {
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d_pair(sB + (uint32_t)bs * kBBytes + h * 16384u, mb, lbar(kPBarBFull + bs),
+                             col0 + 128 * (int)rank + 64 * h, kb * kTile, bh);
+        } else {
+          tma_load_3d_pair(sB + (uint32_t)bs * kBBytes, mb, lbar(kPBarBFull + bs), col0 + 64 * (int)rank,
+                           kb * kTile, bh);
+        }
+        b_issued_s = bi + 1;
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    const uint32_t a_mn = prod == 0 ? 0u : 1u;
+    const uint32_t id256 = idesc_bf16_f32(2 * kTile, 256, (int)a_mn, 1), id128 = idesc_bf16_f32(2 * kTile, 128, (int)a_mn, 1);
+    int bi = 0;
+    bool ok = true;
+    for (int t = 0; t < nkb && ok; ++t) {
+      const int as = t % kANst, au = t / kANst;
+      ok = mbar_wait(bar(kPBarAFull + as), (uint32_t)(au & 1), spin, abort, p.st, kSitePMma);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t aaddr = sA + (uint32_t)as * kABytes;
+      const uint64_t da = prod == 0 ? smem_desc_sw128(aaddr, 16, 1024) : smem_desc_sw128(aaddr, 16384, 1024);
+      for (int c = 0; c < nchunk && ok; ++c, ++bi) {
+        const int bs = bi % kBNst, bu = bi / kBNst;
+        ok = mbar_wait(bar(kPBarBFull + bs), (uint32_t)(bu & 1), spin, abort, p.st, kSitePMma);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dbd = smem_desc_sw128(sB + (uint32_t)bs * kBBytes, 16384, 1024);
+        const uint32_t idesc = nbox - 4 * c >= 4 ? id256 : id128;
+        const uint32_t dcol = tmem + 256u * (uint32_t)c;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ak = prod == 0 ? da + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2) : da + (uint64_t)(kk * 128);
+          mma_bf16_ss_pair(dcol, ak, dbd + (uint64_t)(kk * 128), idesc, (t | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit_pair_mc(bar(kPBarBEmpty + bs), 0x3);
+      }
+      if (ok) mma_commit_pair_mc(bar(kPBarAEmpty + as), 0x3);
+    }
+    if (ok) mma_commit_pair_mc(bar(kPBarDone), 0x3);
+    mma_commit_pair(bar(kPBarDrain));
+    for (long long w2 = 0; w2 < kDrainSpin; ++w2)
+      if (mbar_try_wait(bar(kPBarDrain), 0)) break;
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue (both CTAs, own rows)
+    const int qd = warp & 3, r = 32 * qd + lane;
+    const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
+    // warp-uniform: the TMEM loads below are warp-collective
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(kPBarDone), 0, spin, abort, p.st, kSitePEpi));
+    tc_fence_after();
+    const bool store = ok && r0 < p.T;
+    if (store) {
+      // stage the bf16 block in 64-column boxes over the (now idle) rings
+      for (int c32 = 0; c32 < 2 * nbox; ++c32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_addr + 32 * c32, v);
+        tmem_wait_ld();
+        const uint32_t box = base + (uint32_t)(c32 >> 1) * 16384u;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            wv[e] = pack_bf16x2(__uint_as_float(v[8 * g4 + 2 * e]) * alpha, __uint_as_float(v[8 * g4 + 2 * e + 1]) * alpha);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz(box, r, 4 * (c32 & 1) + g4)),
+                       "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    named_bar_sync(1, 128);
+    if (store && threadIdx.x == 64) {
+      for (int b2 = 0; b2 < nbox; ++b2) tma_store_3d(mo, base + (uint32_t)b2 * 16384u, 64 * b2, r0, bh);
+      tma_store_commit();
+      tma_store_wait_read();
+    }
+  }
+
+  __syncthreads();
+  // after an abort, loads of this pair may still be landing: the leader waits
+  // (bounded) for the last round of every slot (its barriers count both CTAs)
+  if (threadIdx.x == 0 && leader && abort_flag) {
+    const int ai = a_issued_s, bi = b_issued_s;
+    for (int c = max(0, ai - kANst); c < ai; ++c)
+      for (long long w2 = 0; w2 < kDrainSpin; ++w2)
+        if (mbar_try_wait(bar(kPBarAFull + c % kANst), (uint32_t)((c / kANst) & 1))) break;
+    for (int c = max(0, bi - kBNst); c < bi; ++c)
+      for (long long w2 = 0; w2 < kDrainSpin; ++w2)
+        if (mbar_try_wait(bar(kPBarBFull + c % kBNst), (uint32_t)((c / kBNst) & 1))) break;
+  }
+  // both CTAs are done with TMEM and with each other's shared memory
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+// G and P tiles (ib, ib + 1) for even ib, above the diagonal: zeros (the
+// extra block a product pair reads).  One CTA per tile.
+__global__ void __launch_bounds__(256)
+bwd_zero_tiles_kernel(__nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__ P, int T, int ldT, int nb) {
+  const int np = nb / 2;                     // tiles (2 gp, 2 gp + 1) with 2 gp + 1 < nb
+  const int bh = blockIdx.x / np, gp = blockIdx.x % np;
+  const int i0 = 2 * gp * kTile, j0 = i0 + kTile;
+  const int rows = min(kTile, T - i0), cols8 = (min(kTile, ldT - j0) + 7) / 8;
+  for (int x = threadIdx.x; x < rows * cols8; x += blockDim.x) {
+    const int rr = x / cols8, c8 = x % cols8;
+    const size_t off = ((size_t)bh * T + i0 + rr) * ldT + j0 + 8 * c8;
+    *reinterpret_cast<uint4*>(G + off) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(P + off) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // Per row: 1/n_i and db_i (eqs 89-90) from the forward's H~, n, signed b and
 // the row max m.  One warp per row.
 template <typename E>
@@ -612,6 +837,34 @@ int launch_bwd_products(const BwdProdArgs& a, cudaStream_t stream) {
   ProdParams p;
   p.T = a.T; p.BH = a.BH; p.nb = nb; p.dqk = a.dqk; p.dv = a.dv; p.scale = a.scale; p.st = a.st;
   const size_t smem = (size_t)kANst * kABytes + (size_t)kBNst * kBBytes + 1024;
+  static const char* force = getenv("MLSTM_BWD_PROD");       // "single": one CTA per block (tests)
+  if (a.dqk % 128 == 0 && a.dv % 128 == 0 && !(force && force[0] == 's')) {
+    // CTA pairs: zero the tiles above the diagonal that a pair's extra block reads
+    if (nb >= 2) {
+      bwd_zero_tiles_kernel<<<(unsigned)(a.BH * (nb / 2)), 256, 0, stream>>>(
+          static_cast<__nv_bfloat16*>(const_cast<void*>(a.G)), static_cast<__nv_bfloat16*>(const_cast<void*>(a.P)),
+          a.T, a.ldT, nb);
+      if (cudaGetLastError() != cudaSuccess) return kCuda;
+    }
+    if (cudaFuncSetAttribute(bwd_prod2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return kCuda;
+    const long long pairs = 3LL * a.BH * ((nb + 1) / 2);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, bwd_prod2_kernel, mg, mp, mk, mq, mdh, mdq, mdk, mdv, p) != cudaSuccess)
+      return kCuda;
+    return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+  }
   if (cudaFuncSetAttribute(bwd_prod_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return kCuda;
   bwd_prod_kernel<<<(unsigned)grid, kPThreads, smem, stream>>>(mg, mp, mk, mq, mdh, mdq, mdk, mdv, p);

@@ -30,6 +30,8 @@ CASES = [
     (1, 1, 2048, 384, 384, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),   # one head of the 125M-scale layer
     (2, 3, 50, 40, 24, torch.bfloat16, (-2.0, 1.5), (0.5, 1.0)),      # one partial tile, d not a multiple of 64
     (1, 1, 129, 64, 64, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),      # a second tile row of one query
+    (1, 2, 600, 128, 256, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # CTA-pair products, odd block count
+    (2, 1, 129, 128, 128, torch.bfloat16, (-2.0, 1.5), (0.5, 1.0)),   # CTA-pair products, one-query block
 ]
 
 
