@@ -73,3 +73,21 @@ def test_bwd_with_saved_forward(M, shape):
                                     x["fgate_pre"][:1, :1], dh[:1, :1])
     for name, g, w in zip(("dq", "dk", "dv", "d_igate", "d_fgate"), got, want):
         assert rel_err(g[:1, :1], w) <= TOL_BF16, name
+
+
+def test_bwd_full_size_sampled_heads(M):
+    """The 125M-scale layer (B=8, H=4, T=2048, d=384, bf16) in one launch, as
+    the benchmark times it; the first and last heads against the oracle."""
+    B, H, T, d = 8, 4, 2048, 384
+    x = W.sequence_inputs(B, H, T, d, d, torch.bfloat16, seed=11)
+    dh = torch.randn((B, H, T, d), generator=torch.Generator().manual_seed(11)).to(torch.bfloat16)
+    xd = {k: v.cuda() for k, v in x.items()}
+    got = M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh.cuda())
+    torch.cuda.synchronize()
+    assert M.last_device_status() == 0
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        sl = lambda t: t[b:b + 1, h:h + 1]
+        want = oracle.parallel_backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["igate_pre"]), sl(x["fgate_pre"]),
+                                        sl(dh))
+        for name, g, w in zip(("dq", "dk", "dv", "d_igate", "d_fgate"), got, want):
+            assert rel_err(sl(g), w) <= TOL_BF16, f"head ({b},{h}) {name}"
