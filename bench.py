@@ -47,9 +47,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-step", action="store_true", help="skip the recurrent-step measurement")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-kernel", choices=("fwd", "step", "step_seq", "rbwd", "bwd"), default=None,
+    p.add_argument("--profile-kernel", choices=("fwd", "fs", "step", "step_seq", "rbwd", "bwd"), default=None,
                    help="no timing: one warm-up and one launch of the fused forward kernel (on --workload), "
-                        "of the recurrent step (B=64, H=4, d=512: 256 MB of state), of the 64-token prefill "
+                        "of the parallel-to-recurrent hand-off (on --workload), of the recurrent step (B=64, H=4, d=512: 256 MB of state), of the 64-token prefill "
                         "(same heads), of the recurrent backward (B=4, H=8, T=256, d=384) or of the parallel "
                         "backward (on --workload), for ncu captures")
     return p.parse_args()
@@ -443,6 +443,14 @@ def profile_once(args):
         M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
         for _ in range(2):
             M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=args.algo)
+    elif args.profile_kernel == "fs":
+        # the parallel-to-recurrent hand-off (final C, n, m) on the parallel workload
+        w = W.PARALLEL_WORKLOADS[args.workload]
+        xd = {k: v.cuda() for k, v in W.parallel_inputs(w, 0).items()}
+        ws = torch.empty(M.parallel_fwd_workspace_bytes(w.B, w.H, w.T), dtype=torch.uint8, device="cuda")
+        M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
+        for _ in range(2):
+            M.parallel_final_state(xd["k"], xd["v"], ws)
     elif args.profile_kernel == "bwd":
         w = W.PARALLEL_WORKLOADS[args.workload]
         xd = {k: v.cuda() for k, v in W.parallel_inputs(w, 0).items()}

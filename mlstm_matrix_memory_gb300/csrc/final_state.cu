@@ -15,9 +15,10 @@
 // Tensor-core version (bf16, d_qk and d_v multiples of 64): one CTA owns 128
 // rows of C (d_v) and all d_qk columns, accumulated in TMEM over a range of
 // tokens.  Per 64-token stage a TMA thread loads V [64 x 128] and K
-// [64 x d_qk] (128-byte swizzle); four warps scale each V row by its token's
-// weight s*D'_Tj in shared memory and sum their slice of the weighted K
-// columns into n (the head's tile CTAs share the columns); one
+// [64 x d_qk] (128-byte swizzle); eight warps (two per SM sub-partition, so
+// that one hides the other's shared-memory latency) scale each V row by its
+// token's weight s*D'_Tj in shared memory and sum their slice of the weighted
+// K columns into n (the head's tile CTAs share the columns); one
 // thread issues tcgen05.mma with both operands MN-major (M = d_v rows,
 // N = d_qk columns, K = tokens).  CUDA-core version (fp32, other sizes): 64 x
 // 64 tiles of C in registers, 32 weighted tokens staged at a time.  Both
@@ -118,7 +119,8 @@ final_state_kernel(const E* __restrict__ k, const E* __restrict__ v, GateTerms g
 
 // ---------------------------------------------------------------- tensor cores
 using namespace tc;
-constexpr int kTcTok = 64, kTcM = 128, kTcThreads = 256;
+constexpr int kTcTok = 64, kTcM = 128, kTcThreads = 384;
+constexpr int kTcScaleWarps = 8;            // warps 2..5 and 8..11: weights, n, epilogue
 constexpr int kTcProducers = 3;             // warps 0, 6, 7: one issuing thread moves only ~30 B/clk
 constexpr int kTcMaxStages = 4;
 enum : int { kFsFull = 0, kFsScaled = kTcMaxStages, kFsEmpty = 2 * kTcMaxStages, kFsAcc = 3 * kTcMaxStages,
@@ -163,7 +165,7 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     abort_flag = 0;
     for (int s2 = 0; s2 < kTcMaxStages; ++s2) {
       mbar_init(bar(kFsFull + s2), 1);
-      mbar_init(bar(kFsScaled + s2), 4);
+      mbar_init(bar(kFsScaled + s2), kTcScaleWarps);
       mbar_init(bar(kFsEmpty + s2), 1);
     }
     mbar_init(bar(kFsAcc), 1);
@@ -180,7 +182,7 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
 
-  if ((warp == 0 || warp >= 6) && lane == 0) {
+  if ((warp == 0 || warp == 6 || warp == 7) && lane == 0) {
     // ---- TMA producers: the stage's 2 + nkb boxes dealt round-robin; the
     // bytes of all of them are posted by warp 0
     const int pi = warp == 0 ? 0 : warp - 5;
@@ -218,9 +220,10 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
       mma_commit(bar(kFsEmpty + s2));
     }
     if (ok) mma_commit(bar(kFsAcc));
-  } else if (warp >= 2 && warp < 6) {
-    // ---- weights, V scaling, n, then the epilogue (four warps: all TMEM lane quarters)
-    const int t2 = threadIdx.x - 64;                 // 0..127
+  } else if ((warp >= 2 && warp < 6) || warp >= 8) {
+    // ---- weights, V scaling, n, then the epilogue (eight warps: each TMEM
+    // lane quarter twice, one per half of the columns)
+    const int t2 = warp < 6 ? threadIdx.x - 64 : threadIdx.x - 128;   // 0..255, a warp's lanes consecutive
     const float p2T = p.g.p2[hb + p.T - 1];
     // n = sum_j w_j k_j: the tile CTAs of a head share the columns (slice
     // [ncol0, ncol1), a multiple of 64).  A thread sums one 8-column chunk
@@ -229,8 +232,8 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     const int cs = ((p.dqk / 64 + p.ntr - 1) / p.ntr) * 64;
     const int ncol0 = min(p.dqk, tr * cs), ncol1 = min(p.dqk, ncol0 + cs);
     const int nchk = (ncol1 - ncol0) / 8;                     // 8-column chunks in the slice (<= 64)
-    int groups = 1;                                          // token groups per chunk: a power of 2 <= 8
-    while (groups < 8 && 2 * groups * nchk <= 128) groups *= 2;
+    int groups = 1;                                          // token groups per chunk: a power of 2 <= 16
+    while (groups < 16 && 2 * groups * nchk <= 256) groups *= 2;
     const int chunk = t2 / groups, tg = t2 % groups;
     const bool n_thread = chunk < nchk;
     const int tpg = kTcTok / groups;                         // tokens per group
@@ -251,18 +254,18 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
       const uint32_t u = (uint32_t)(i / p.nst);
       ok = mbar_wait(bar(kFsFull + s2), u & 1u, spin, abort, p.st, 23);
       if (!ok) break;
-      named_bar_sync(1, 128);                        // w_s[s2] written by every thread
+      named_bar_sync(1, 256);                        // w_s[s2] written by every thread
       const uint32_t sb = base + (uint32_t)s2 * stage_bytes;
       {
-        // V row (token) t2 % 64 of box t2 / 64: eight 16-byte chunks, taken
-        // in an order rotated by the row so that neighbouring lanes (rows 128
-        // bytes apart) hit different banks
+        // V row (token) t2 % 64 of box (t2 / 64) % 2: four of its eight
+        // 16-byte chunks (the half t2 / 128), taken in an order rotated by the
+        // row so that neighbouring lanes (rows 128 bytes apart) hit different banks
         const int j = t2 & 63;
         const float w = w_s[s2][j];
-        const uint32_t row = sb + (uint32_t)(t2 >> 6) * 8192u + (uint32_t)j * 128u;
+        const uint32_t row = sb + (uint32_t)((t2 >> 6) & 1) * 8192u + (uint32_t)j * 128u;
 #pragma unroll
-        for (int q0 = 0; q0 < 8; ++q0) {
-          const uint32_t q = (uint32_t)((q0 + j) & 7);
+        for (int q0 = 0; q0 < 4; ++q0) {
+          const uint32_t q = (uint32_t)((4 * (t2 >> 7) + q0 + j) & 7);
           uint32_t x[4];
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(row + q * 16u));
@@ -307,13 +310,14 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
 #pragma unroll
     for (int e = 0; e < 8; ++e)
       for (int o = 1; o < groups; o <<= 1) nacc[e] += __shfl_xor_sync(0xffffffffu, nacc[e], o);
-    // epilogue: row r0 + 32*(warp%4) + lane of C from TMEM
+    // epilogue: row r0 + 32*(warp%4) + lane of C from TMEM, the column half
+    // of this warp group
     if (ok && c1 > c0) ok = mbar_wait(bar(kFsAcc), 0, spin, abort, p.st, 24);
     tc_fence_after();
-    const int qd = warp & 3;
+    const int qd = warp & 3, hc = p.dqk / 2;
     const int r = r0 + 32 * qd + lane;
     if (ok && c1 > c0) {
-      for (int cb = 0; cb < p.dqk; cb += 32) {
+      for (int cb = warp < 6 ? 0 : hc; cb < (warp < 6 ? hc : p.dqk); cb += 32) {
         uint32_t o[32];
         tmem_ld32(tmem + ((uint32_t)(32 * qd) << 16) + cb, o);
         tmem_wait_ld();

@@ -38,6 +38,8 @@ SHAPES = [
     (1, 1, 5, 8, 8, torch.float32, (0.0, 1.0), (3.0, 1.0)),
     (1, 1, 777, 96, 200, torch.bfloat16, (0.0, 2.0), (5.0, 1.0)),
     (1, 2, 2048, 384, 384, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),
+    (8, 4, 256, 384, 384, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # one token range per tile (96 tiles)
+    (2, 2, 192, 512, 128, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # d_qk 512: 64 n chunks per tile
 ]
 
 
