@@ -569,14 +569,14 @@ def main():
                                      "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak,
                                                   "unit": "TFLOP/s", "frac": tf / alu_peak,
                                                   "peak_source": f"FP32 FMA: {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz",
-                                                  "traffic": None}}
+                                                  "traffic": kernel_traffic(f"step_seq_{sw.name}_L{L}")}}
     if fs is not None:
         ms, fl = fs
         tf = fl / (ms * 1e-3) / 1e12
         line["final_state"] = {"workload": w.name, "ms": ms,
                                "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
                                             "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
-                                            "traffic": None}}
+                                            "traffic": kernel_traffic("final_state_" + w.name)}}
     if bwd is not None:
         ms, fl, wsb, ms_saved = bwd
         tf = fl / (ms * 1e-3) / 1e12
