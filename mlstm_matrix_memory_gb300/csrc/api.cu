@@ -193,6 +193,7 @@ int mlstm_parallel_fwd_opt(const void* q, const void* k, const void* v, const fl
   if ((long long)B * H * T == 0) return MLSTM_OK;
   if (!q || !k || !v || !igate_pre || !fgate_pre || !h) return MLSTM_EINVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(h)) return MLSTM_EALIGN;
+  if (og && !aligned16(og)) return MLSTM_EALIGN;          // before the gate pass writes the workspace
   if (!workspace || workspace_bytes < mlstm_parallel_fwd_workspace(B, H, T)) return MLSTM_EWORKSPACE;
   if (!aligned16(workspace)) return MLSTM_EALIGN;
   if (algo == MLSTM_ALGO_TC && !fwd_tc_supported(d_qk, d_v, dtype)) return MLSTM_EUNSUPPORTED;

@@ -46,7 +46,12 @@ int scratch_ptr(void** out) {
 extern "C" int mlstm_parallel_fwd_noalloc(const void* q, const void* k, const void* v, const float* igate_pre,
                                           const float* fgate_pre, void* h, float* m_out, float* n_out, int B,
                                           int H, int T, int d_qk, int d_v, int dtype, void* stream) {
+  // the shape checks of mlstm_parallel_fwd, in its order, before the device scratch is touched
   if (B < 0 || H < 0 || T < 0) return MLSTM_EINVAL;
+  if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
+  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
+  const int vec = dtype == MLSTM_F32 ? 4 : 8;
+  if (d_qk % vec != 0 || d_v % vec != 0) return MLSTM_EINVAL;
   if ((long long)B * H * T == 0) return MLSTM_OK;
   const size_t need = mlstm_parallel_fwd_workspace(B, H, T);
   if (need == 0 || need > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES) return MLSTM_EWORKSPACE;

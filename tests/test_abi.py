@@ -185,3 +185,87 @@ def test_parallel_bwd_validation(lib):
     assert saved(b=0) == -1
     assert saved(dt=7) == -3
     assert saved(T=0) == 0
+
+
+def test_plain_parallel_validation(lib):
+    def pf(q=A, h=A, B=1, T=8, dqk=64, dv=64, dt=1, ws=A, wsb=1 << 20):
+        return lib.mlstm_parallel_fwd(q, A, A, A, A, h, None, None, B, 1, T, dqk, dv, dt, ws, wsb, None)
+    assert pf(dqk=0) == -1
+    assert pf(dv=520) == -1
+    assert pf(dt=7) == -3
+    assert pf(q=A + 4) == -2
+    assert pf(h=0) == -1
+    assert pf(wsb=64) == -7
+    assert pf(B=0) == 0
+
+
+def test_gate_prep_validation(lib):
+    from mlstm_matrix_memory_gb300.binding import _Options as Opt
+    opt = Opt(0, 1, None, None)                # exponential forget gate: same argument rules
+
+    def gp(ig=A, fg=A, B=2, T=100, ws=A, wsb=1 << 20, with_opt=False):
+        if with_opt:
+            return lib.mlstm_gate_prep_opt(ig, fg, B, 3, T, ws, wsb, ctypes.byref(opt), None)
+        return lib.mlstm_gate_prep(ig, fg, B, 3, T, ws, wsb, None)
+    need = lib.mlstm_parallel_fwd_workspace(2, 3, 100)
+    for w in (False, True):
+        assert gp(B=-1, with_opt=w) == -1
+        assert gp(T=0, with_opt=w) == 0
+        assert gp(ig=0, with_opt=w) == -1
+        assert gp(fg=0, with_opt=w) == -1
+        assert gp(ws=0, with_opt=w) == -7
+        assert gp(wsb=need - 1, with_opt=w) == -7
+        assert gp(ws=A + 8, with_opt=w) == -2
+
+
+def test_gated_and_options_validation(lib):
+    from mlstm_matrix_memory_gb300.binding import _Options as Opt
+
+    def gated(q=A, h=A, T=8, dqk=64, dv=64, dt=1, ws=A, wsb=1 << 20, algo=0):
+        return lib.mlstm_parallel_fwd_gated(q, A, A, h, None, None, 1, 1, T, dqk, dv, dt, ws, wsb, algo, None)
+    assert gated(dqk=513) == -1
+    assert gated(dqk=12) == -1                 # bf16 rows must be 16 bytes
+    assert gated(dt=2) == -3
+    assert gated(algo=9) == -1
+    assert gated(h=A + 8) == -2
+    assert gated(ws=0) == -7
+    assert gated(T=0) == 0
+
+    def opt_fwd(opt, dqk=64, dv=64, dt=1):
+        return lib.mlstm_parallel_fwd_opt(A, A, A, A, A, A, None, None, 1, 1, 8, dqk, dv, dt, A, 1 << 20,
+                                          ctypes.byref(opt), None)
+    assert opt_fwd(Opt(9, 0, None, None)) == -1                    # unknown kernel choice
+    assert opt_fwd(Opt(0, 0, A + 2, None)) == -2                   # output gate not 16-byte aligned
+    assert opt_fwd(Opt(2, 0, None, None), dqk=40, dv=40) == -6     # tensor cores forced on d = 40
+    assert opt_fwd(Opt(0, 0, None, None), dt=7) == -3
+
+
+def test_noalloc_validation(lib):
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.mlstm_parallel_fwd_noalloc.argtypes = [vp] * 8 + [i] * 6 + [vp]
+    lib.mlstm_parallel_fwd_noalloc.restype = i
+
+    def na(B=1, T=8, dqk=64, dv=64, dt=1):
+        return lib.mlstm_parallel_fwd_noalloc(A, A, A, A, A, A, None, None, B, 1, T, dqk, dv, dt, None)
+    assert na(B=-1) == -1
+    assert na(dqk=0) == -1                      # shape checks come before the device scratch
+    assert na(dt=5) == -3
+    assert na(dv=12) == -1
+    assert na(T=0) == 0
+    assert na(T=1 << 20) == -7                 # beyond the fixed scratch
+
+
+def test_step_seq_opt_validation(lib):
+    from mlstm_matrix_memory_gb300.binding import _Options as Opt
+    opt = Opt(0, 1, None, None)
+
+    def ss(C=A, q=A, L=4, dqk=64, dv=64, dt=1):
+        return lib.mlstm_step_seq_opt(C, A, A, q, A, A, None, A, A, A, 2, 2, L, dqk, dv, dt, ctypes.byref(opt),
+                                      None)
+    assert ss(L=-1) == -1
+    assert ss(dqk=12) == -1
+    assert ss(dv=600) == -1
+    assert ss(dt=3) == -3
+    assert ss(C=A + 4) == -2
+    assert ss(q=0) == -1
+    assert ss(L=0) == 0
