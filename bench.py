@@ -174,13 +174,23 @@ def oracle_rows(w, heads: int, stride: int = 8):
     return x, rows, flops
 
 
-def oracle_time(x, rows, reps_or_seconds, by_time):
+def host_cores() -> int:
+    """The host cores this process may run on: the oracle's OpenMP team, set
+    explicitly (a launcher such as torch.distributed.run exports
+    OMP_NUM_THREADS=1 to every rank, while only rank 0 times the oracle)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_time(x, rows, reps_or_seconds, by_time, threads):
     import oracle
     a = (x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"])
     f = [oracle.f64(t) for t in a]            # widen once, outside the timed region
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle.parallel_rows(*f, rows)
+        oracle.parallel_rows(*f, rows, nthreads=threads)
         n += 1
         el = time.perf_counter() - t0
         if (by_time and el >= reps_or_seconds) or (not by_time and n >= reps_or_seconds):
@@ -188,10 +198,9 @@ def oracle_time(x, rows, reps_or_seconds, by_time):
 
 
 def cpu_baseline(w, seconds):
-    import oracle
-    cores = oracle.max_threads()
+    cores = host_cores()
     x, rows, flops = oracle_rows(w, heads=max(1, cores))
-    n, el = oracle_time(x, rows, seconds, by_time=True)
+    n, el = oracle_time(x, rows, seconds, by_time=True, threads=cores)
     return {"value": n * flops / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"every 8th query row of {max(1, cores)} heads of {w.name} (fp64, OpenMP over rows), "
                       f"{n} passes in {el:.1f} s"}
@@ -203,11 +212,10 @@ def run_reference(args, ws, rank):
     w = W.PARALLEL_WORKLOADS[args.workload]
     if rank != 0:
         return
-    import oracle
-    cores = oracle.max_threads()
+    cores = host_cores()
     x, rows, flops = oracle_rows(w, heads=max(1, cores))
-    oracle_time(x, rows[: max(1, len(rows) // 16)], args.warmup, by_time=False)
-    n, el = oracle_time(x, rows, args.steps, by_time=False)
+    oracle_time(x, rows[: max(1, len(rows) // 16)], args.warmup, by_time=False, threads=cores)
+    n, el = oracle_time(x, rows, args.steps, by_time=False, threads=cores)
     ms = el * 1e3 / n
     tflops = flops / (ms * 1e-3) / 1e12
     sample = f"every 8th query row of {max(1, cores)} heads of {w.name} per step (fp64, OpenMP over rows)"
