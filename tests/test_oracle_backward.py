@@ -86,3 +86,39 @@ def test_recurrent_backward_exp_forget_finite_differences():
     with oracle.forget_exp():
         got = oracle.recurrent_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh, x["ogate_pre"])
         pins._recurrent_fd(x, dh, got, 1e-6, "exp forget recurrent backward")
+
+
+@pytest.mark.parametrize("exp_forget", [False, True], ids=["sigmoid", "exp"])
+@pytest.mark.parametrize("case", [
+    dict(B=2, H=2, T=40, dqk=8, dv=6, ig=(0.0, 1.0), fg=(3.0, 1.0), seed=3),
+    dict(B=1, H=2, T=33, dqk=4, dv=8, ig=(-4.0, 0.5), fg=(0.0, 1.0), seed=4),   # the normaliser floor engages
+])
+def test_gate_gradients_from_the_products(case, exp_forget):
+    """The gate gradients equal sums of the key and query products' own
+    gradients: with S_ij = s q_i.k_j, the total gradient reaching D~_ij is
+    dS_ij S_ij, so the column sums give d i~_j = k_j.dk_j and the row sums
+    give q_i.dq_i, and d log f_t = sum_{u >= t} (q_u.dq_u - k_u.dk_u) (the
+    rows from t on, minus the columns from t on).  The kernels of the
+    recurrent backward rest on these; here they tie the oracle's gate
+    gradients (eqs 101-105) to its dq, dk (eqs 98-99), two separate
+    derivations."""
+    c = case
+    fg = (-0.05, 0.05) if exp_forget else c["fg"]
+    x = W.sequence_inputs(c["B"], c["H"], c["T"], c["dqk"], c["dv"], torch.float32, seed=c["seed"], ig=c["ig"],
+                          fg=fg)
+    dh = np.random.default_rng(c["seed"]).standard_normal((c["B"], c["H"], c["T"], c["dv"]))
+    if exp_forget:
+        with oracle.forget_exp():
+            dq, dk, _, dig, dfg = oracle.parallel_backward(x["q"], x["k"], x["v"], x["igate_pre"],
+                                                           x["fgate_pre"], dh)
+    else:
+        dq, dk, _, dig, dfg = oracle.parallel_backward(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"], dh)
+    q, k = oracle.f64(x["q"]), oracle.f64(x["k"])
+    f = oracle.f64(x["fgate_pre"])
+    col = np.einsum("bhtd,bhtd->bht", k, dk)
+    row = np.einsum("bhtd,bhtd->bht", q, dq)
+    dlogf = np.cumsum((row - col)[..., ::-1], axis=-1)[..., ::-1]
+    dlogf_dpre = 1.0 if exp_forget else 1.0 / (1.0 + np.exp(f))          # d log sigmoid(x)/dx = sigmoid(-x)
+    scale = max(1.0, float(np.max(np.abs(dig))), float(np.max(np.abs(dfg))))
+    np.testing.assert_allclose(dig, col, rtol=0, atol=1e-10 * scale)
+    np.testing.assert_allclose(dfg, dlogf_dpre * dlogf, rtol=0, atol=1e-10 * scale)
