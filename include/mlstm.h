@@ -281,8 +281,9 @@ int mlstm_parallel_bwd(const void *q, const void *k, const void *v,
  *              H=4, T=2048, d=384).
  * Requirements: 1 <= d_qk, d_v <= 512, d_qk a multiple of 8; no output may
  * alias an input.  B*H*T = 0 returns MLSTM_OK without work.  Four kernels on
- * `stream`: the forward and backward sweeps (state in registers, 64 rows of
- * one head per CTA), the per-token combination, the per-head suffix sums. */
+ * `stream`: the forward and backward sweeps (state in registers, 64 or 96
+ * rows of one head per CTA: 96 when those CTAs fill the GPU in one wave), the
+ * per-token combination, the per-head suffix sums. */
 size_t mlstm_recurrent_bwd_workspace(int B, int H, int T, int d_qk, int d_v);
 
 int mlstm_recurrent_bwd(const void *q, const void *k, const void *v,
