@@ -579,6 +579,7 @@ bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_consta
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
   __shared__ int a_issued_s, b_issued_s;
+  __shared__ int peer_s[3];                  // (leader) the peer's A and B load counts and abort flag, sent at exit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &abort_flag;
   const uint32_t rank = cluster_ctarank();
@@ -747,16 +748,34 @@ bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_consta
   }
 
   __syncthreads();
-  // after an abort, loads of this pair may still be landing: the leader waits
-  // (bounded) for the last round of every slot (its barriers count both CTAs)
-  if (threadIdx.x == 0 && leader && abort_flag) {
-    const int ai = a_issued_s, bi = b_issued_s;
-    for (int c = max(0, ai - kANst); c < ai; ++c)
-      for (long long w2 = 0; w2 < kDrainSpin; ++w2)
-        if (mbar_try_wait(bar(kPBarAFull + c % kANst), (uint32_t)((c / kANst) & 1))) break;
-    for (int c = max(0, bi - kBNst); c < bi; ++c)
-      for (long long w2 = 0; w2 < kDrainSpin; ++w2)
-        if (mbar_try_wait(bar(kPBarBFull + c % kBNst), (uint32_t)((c / kBNst) & 1))) break;
+  // Every issuer of both CTAs has stopped.  The peer sends the leader its
+  // load counts and abort flag; after an abort in either CTA the leader makes
+  // the last phase of every slot complete exactly when the loads issued for
+  // it (by either CTA; the two counts differ by at most one round, as every
+  // round waits for the previous one to be consumed) have landed, and waits
+  // (bounded), so no copy can still write shared memory once the pair exits.
+  if (!leader && threadIdx.x < 3) {
+    const int v = threadIdx.x == 0 ? a_issued_s : (threadIdx.x == 1 ? b_issued_s : abort_flag);
+    st_shared_cluster_u32(mapa_shared(smem_u32(&peer_s[threadIdx.x]), 0), (uint32_t)v);
+  }
+  cluster_sync_all();
+  if (threadIdx.x == 0 && leader && (abort_flag || peer_s[2])) {
+    const int ai[2] = {a_issued_s, peer_s[0]}, bi[2] = {b_issued_s, peer_s[1]};
+    // rounds of slot s among the first n loads of a ring of ns slots
+    auto rounds = [](int n, int s, int ns) { return n > s ? (n - 1 - s) / ns + 1 : 0; };
+    for (int s2 = 0; s2 < kANst; ++s2) {
+      const int fl = rounds(ai[0], s2, kANst), fp = rounds(ai[1], s2, kANst), f = max(fl, fp);
+      settle_last_phase(bar(kPBarAFull + s2), f, fl == f, 2u * kABytes,
+                        (fl == f ? kABytes : 0u) + (fp == f ? kABytes : 0u), kDrainSpin);
+    }
+    for (int s2 = 0; s2 < kBNst; ++s2) {
+      const int fl = rounds(bi[0], s2, kBNst), fp = rounds(bi[1], s2, kBNst), f = max(fl, fp);
+      if (f == 0) continue;
+      const int c = ((f - 1) * kBNst + s2) % nchunk;           // the chunk of the last round
+      const uint32_t half = nbox - 4 * c >= 4 ? 32768u : 16384u;
+      settle_last_phase(bar(kPBarBFull + s2), f, fl == f, 2u * half, (fl == f ? half : 0u) + (fp == f ? half : 0u),
+                        kDrainSpin);
+    }
   }
   // both CTAs are done with TMEM and with each other's shared memory
   tc_fence_before();

@@ -144,6 +144,7 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
   __shared__ __align__(8) uint64_t bars[kFsBars];
   __shared__ uint32_t tmem_holder;
   __shared__ float w_s[kTcMaxStages][kTcTok];
+  __shared__ int issued_s[kTcProducers];     // stages each producer has issued (settled after an abort)
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -163,6 +164,7 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    for (int q = 0; q < kTcProducers; ++q) issued_s[q] = 0;
     for (int s2 = 0; s2 < kTcMaxStages; ++s2) {
       mbar_init(bar(kFsFull + s2), 1);
       mbar_init(bar(kFsScaled + s2), kTcScaleWarps);
@@ -196,6 +198,7 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
         if (b < 2) tma_load_3d(dst + b * 8192u, &tmap_v, bar(kFsFull + s2), r0 + 64 * b, c * kTcTok, bh);
         else tma_load_3d(dst + 16384u + (b - 2) * 8192u, &tmap_k, bar(kFsFull + s2), 64 * (b - 2), c * kTcTok, bh);
       }
+      issued_s[pi] = i + 1;
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer: C[128 x d_qk] += (w V)^T K over the stage's 64 tokens
@@ -252,9 +255,10 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     for (int c = c0, i = 0; c < c1 && ok; ++c, ++i) {
       const int s2 = i % p.nst;
       const uint32_t u = (uint32_t)(i / p.nst);
-      ok = mbar_wait(bar(kFsFull + s2), u & 1u, spin, abort, p.st, 23);
+      // the eight warps leave the loop together: each brings its own wait
+      // result to the barrier that also orders the weights w_s[s2]
+      ok = bar_red_and(1, 256, mbar_wait_warp(bar(kFsFull + s2), u & 1u, spin, abort, p.st, 23));
       if (!ok) break;
-      named_bar_sync(1, 256);                        // w_s[s2] written by every thread
       const uint32_t sb = base + (uint32_t)s2 * stage_bytes;
       {
         // V row (token) t2 % 64 of box (t2 / 64) % 2: four of its eight
@@ -312,7 +316,7 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
       for (int o = 1; o < groups; o <<= 1) nacc[e] += __shfl_xor_sync(0xffffffffu, nacc[e], o);
     // epilogue: row r0 + 32*(warp%4) + lane of C from TMEM, the column half
     // of this warp group
-    if (ok && c1 > c0) ok = mbar_wait(bar(kFsAcc), 0, spin, abort, p.st, 24);
+    if (ok && c1 > c0) ok = mbar_wait_warp(bar(kFsAcc), 0, spin, abort, p.st, 24);
     tc_fence_after();
     const int qd = warp & 3, hc = p.dqk / 2;
     const int r = r0 + 32 * qd + lane;
@@ -350,12 +354,18 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
   }
   __syncthreads();
   if (warp == 0 && lane == 0 && abort_flag) {
-    // after an abort, wait (bounded) for loads that may still be landing
-    const int issued = c1 - c0;
-    for (int i = max(0, issued - p.nst); i < issued; ++i) {
-      const int s2 = i % p.nst;
-      for (long long w = 0; w < (1LL << 22); ++w)
-        if (mbar_try_wait(bar(kFsFull + s2), (uint32_t)(i / p.nst) & 1u)) break;
+    // After an abort the producers may have stopped at different stages (they
+    // are at most nst stages apart, as each waits for the stage nst back to be
+    // consumed, so only the last nst stages can be partial): make each of those
+    // phases complete when the boxes that were issued for it land, and wait.
+    int f = 0;
+    for (int q = 0; q < kTcProducers; ++q) f = max(f, issued_s[q]);
+    for (int i = max(0, f - p.nst); i < f; ++i) {
+      uint32_t land = 0;
+      for (int q = 0; q < kTcProducers; ++q)
+        if (issued_s[q] > i)
+          for (int b = q; b < 2 + nkb; b += kTcProducers) land += 8192u;
+      settle_last_phase(bar(kFsFull + i % p.nst), i / p.nst + 1, issued_s[0] > i, stage_bytes, land, 1LL << 22);
     }
   }
   __syncthreads();

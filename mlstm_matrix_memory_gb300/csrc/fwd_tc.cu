@@ -356,7 +356,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
         for (int t = 0; t < HALF / 32; ++t) av[t] = A == -INFINITY ? 0.0f : exp2f(av[t] - A);
       }
-      ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
+      ok = mbar_wait_warp(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
       if (!ok) break;
       tc_fence_after();
       if (gw == 0 && lane == 0) TRACE(6, j);
@@ -399,7 +399,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       }
       // the previous tile's O MMA must be done reading P before it is overwritten
       if (gw == 0 && lane == 0) TRACE(8, j);
-      ok = mbar_wait(bar(kBarPEmpty), (j & 1) ^ 1, spin, abort, p.st, kSiteGate);
+      ok = mbar_wait_warp(bar(kBarPEmpty), (j & 1) ^ 1, spin, abort, p.st, kSiteGate);
       if (!ok) break;
       if (gw == 0 && lane == 0) TRACE(9, j);
 #pragma unroll
@@ -417,7 +417,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     }
 
     // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n
-    if (ok) ok = mbar_wait(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
+    if (ok) ok = mbar_wait_warp(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
     tc_fence_after();
     if (gw == 0 && lane == 0) TRACE(11, 0);
     // After the last O MMA no operand is read any more: the P tile combines the
@@ -425,7 +425,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     // rows x dv_cta in 64-column boxes with the 128-byte swizzle) for TMA stores.
     float* bpart = reinterpret_cast<float*>(dsmem + (sP - smem_u32(dsmem)));
     if (ok) bpart[half * kBM + rl] = bsum;
-    named_bar_sync(1, 256);
+    // every gating warp arrives here whatever its waits returned; all of them
+    // take the result of the whole group from here on
+    ok = bar_red_and(1, 256, ok);
     float nrm = 0.0f, m = 0.0f, bsig = 0.0f;
     if (ok) {
       const float b = bpart[rl] + bpart[kBM + rl];

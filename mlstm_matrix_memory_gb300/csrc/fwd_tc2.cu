@@ -145,13 +145,19 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
   __shared__ int s_issued_s;                // global key tile of the last fully issued S product
-  __shared__ int last_par_s[kMaxSlots];
-  __shared__ int q_par_s;
+  // Loads this CTA issued (fills of each ring granule; Q fills of each
+  // producer) and, in the leader, the peer's counts and abort flag, sent at
+  // exit: after an abort the leader settles every load of the pair.
+  __shared__ int fills_s[kMaxSlots];
+  __shared__ int qfills_s[kProducers];
+  __shared__ int peer_fills_s[kMaxSlots];
+  __shared__ int peer_qfills_s[kProducers];
+  __shared__ int peer_abort_s;
   __shared__ float bpart[2 * kBM];
   volatile int* abort = &abort_flag;
   volatile int* s_issued = &s_issued_s;
-  volatile int* last_par = last_par_s;      // parity of each granule's last fill, -1 if never filled
-  volatile int* q_par = &q_par_s;           // parity of the last Q fill, -1 if none
+  volatile int* fills = fills_s;
+  volatile int* qfills = qfills_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -174,10 +180,17 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   auto lbar = [&](int i) { return mapa_shared(smem_u32(&bars[i]), 0); };   // leader's barrier
 
-  if (threadIdx.x < kMaxSlots) last_par_s[threadIdx.x] = -1;
+  if (threadIdx.x < kMaxSlots) {
+    fills_s[threadIdx.x] = 0;
+    peer_fills_s[threadIdx.x] = 0;
+  }
+  if (threadIdx.x < kProducers) {
+    qfills_s[threadIdx.x] = 0;
+    peer_qfills_s[threadIdx.x] = 0;
+  }
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    q_par_s = -1;
+    peer_abort_s = 0;
     s_issued_s = -1;
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
@@ -234,7 +247,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       if (leader) mbar_arrive_expect_tx(bar(kBarFull + g), 2u * kSlotBytes);
       for (int b2 = 0; b2 < nbox; ++b2)
         tma_load_3d_pair(sRing + g * kSlotBytes + b2 * box_bytes, map, lbar(kBarFull + g), x0 + b2 * dx, y, it.bh);
-      last_par[g] = (int)ph;
+      fills[g] = fills[g] + 1;
       if (++st == n) { st = 0; ph ^= 1; }
     };
     int qi = 0;
@@ -242,13 +255,11 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       if (!item_at(p, r, cid, rank, it)) continue;
       if (qi > 0) ok = mbar_wait(bar(kBarQEmpty), (uint32_t)(qi - 1) & 1u, spin, abort, p.st, kSiteProducer);
       if (!ok) break;
-      if (leader && pi == 0) {
-        mbar_arrive_expect_tx(bar(kBarQFull), 2u * (uint32_t)p.dqk * kBM * 2);
-        *q_par = qi & 1;
-      }
+      if (leader && pi == 0) mbar_arrive_expect_tx(bar(kBarQFull), 2u * (uint32_t)p.dqk * kBM * 2);
       for (int b2 = pi; b2 < p.dqk / 64; b2 += kProducers)
         tma_load_3d_pair(sQ + b2 * 16384u, &tmap_q, lbar(kBarQFull), b2 * 64, it.i0, it.bh);
       ++qi;
+      qfills[pi] = qi;
       const int nch = it.dv_cta / 128, nvc = (nch + 1) / 2;
       if (pi == 0) {
         for (int j = 0; j < it.nkv && ok; ++j)
@@ -380,6 +391,11 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     const int rl = 32 * qd + lane;
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
     const uint32_t l_sempty0 = lbar(kBarSEmpty), l_sempty1 = lbar(kBarSEmpty + 1), l_pfull = lbar(kBarPFull);
+    // Exit rule: each wait below is warp-uniform, and a warp that gives up
+    // leaves the tile loop at once; the eight warps of the CTA then meet once
+    // per item at the reducing barrier after the O wait, and all of them go
+    // on with the epilogue or all leave.  So every named barrier below is
+    // reached by all 256 threads (or all 128 of a half) on every path.
     bool ok = true;
     int qi = 0, gt = 0;
     for (int r = 0; r * p.nclusters < p.n_items && ok; ++r) {
@@ -416,7 +432,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
 #pragma unroll
           for (int t = 0; t < HALF / 32; ++t) av[t] = A == -INFINITY ? 0.0f : exp2f(av[t] - A);
         }
-        ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
+        ok = mbar_wait_warp(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
         if (!ok) break;
         tc_fence_after();
         if (gw == 0 && lane == 0) TRACE2(6, j);
@@ -457,7 +473,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
           }
         }
         if (gw == 0 && lane == 0) TRACE2(7, j);
-        ok = mbar_wait(bar(kBarPEmpty), ((uint32_t)gt & 1u) ^ 1u, spin, abort, p.st, kSiteGate);
+        ok = mbar_wait_warp(bar(kBarPEmpty), ((uint32_t)gt & 1u) ^ 1u, spin, abort, p.st, kSiteGate);
         if (!ok) break;
         if (gw == 0 && lane == 0) TRACE2(8, j);
 #pragma unroll
@@ -476,17 +492,16 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         if (lane == 0) mbar_arrive_cluster(l_pfull);
         if (gw == 0 && lane == 0) TRACE2(9, j);
       }
-      if (!ok) break;
 
       // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n.  Each half stages its
       // 64-column boxes one at a time in its 16 KB of the P buffer (free until
       // the next item's first P) and stores each by TMA as soon as it is written.
-      ok = mbar_wait(bar(kBarOFull), (uint32_t)qi & 1u, spin, abort, p.st, kSiteEpilogue);
-      if (!ok) break;
+      if (ok) ok = mbar_wait_warp(bar(kBarOFull), (uint32_t)qi & 1u, spin, abort, p.st, kSiteEpilogue);
       tc_fence_after();
       if (gw == 0 && lane == 0) TRACE2(10, 0);
       bpart[half * kBM + rl] = bsum;
-      named_bar_sync(1, 256);
+      ok = bar_red_and(1, 256, ok);          // all eight warps leave together, or none
+      if (!ok) break;
       const float b = bpart[rl] + bpart[kBM + rl];
       const float nrm = fmaxf(fabsf(b), expf(-m));
       const float inv = nrm > 0.0f ? 1.0f / nrm : 0.0f;
@@ -554,20 +569,34 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   }
 
   __syncthreads();
-  if (warp == 0) {
-    // after an abort, loads of this pair may never have been consumed: the
-    // leader waits (bounded) for the last phase of Q and of every granule
-    if (lane == 0 && leader && abort_flag) {
-      if (*q_par >= 0)
-        for (long long w = 0; w < kDrainSpin; ++w)
-          if (mbar_try_wait(bar(kBarQFull), (uint32_t)*q_par)) break;
-      for (int s2 = 0; s2 < p.nk + p.nv; ++s2)
-        if (last_par[s2] >= 0) {
-          for (long long w = 0; w < kDrainSpin; ++w)
-            if (mbar_try_wait(bar(kBarFull + s2), (uint32_t)last_par[s2])) break;
-        }
+  // Every issuer of both CTAs has stopped.  The peer sends the leader its
+  // load counts and abort flag; after an abort in either CTA the leader makes
+  // the last phase of Q and of every granule complete exactly when the loads
+  // that were issued for it (by either CTA) have landed, and waits for that
+  // (bounded), so no copy can still write shared memory once the pair exits.
+  const int nslots = p.nk + p.nv;
+  if (!leader) {
+    const int t = threadIdx.x;
+    if (t < nslots) st_shared_cluster_u32(mapa_shared(smem_u32(&peer_fills_s[t]), 0), (uint32_t)fills_s[t]);
+    else if (t < kMaxSlots + kProducers && t >= kMaxSlots)
+      st_shared_cluster_u32(mapa_shared(smem_u32(&peer_qfills_s[t - kMaxSlots]), 0), (uint32_t)qfills_s[t - kMaxSlots]);
+    else if (t == kMaxSlots + kProducers)
+      st_shared_cluster_u32(mapa_shared(smem_u32(&peer_abort_s), 0), (uint32_t)abort_flag);
+  }
+  cluster_sync_all();
+  if (leader && threadIdx.x == 0 && (abort_flag || peer_abort_s)) {
+    const uint32_t qhalf = (uint32_t)p.dqk * kBM;          // Q bytes of one producer (half a CTA's rows x d)
+    int fq = 0;
+    for (int pi = 0; pi < kProducers; ++pi) fq = max(fq, max(qfills_s[pi], peer_qfills_s[pi]));
+    uint32_t qland = 0;
+    for (int pi = 0; pi < kProducers; ++pi)
+      qland += (qfills_s[pi] == fq ? qhalf : 0u) + (peer_qfills_s[pi] == fq ? qhalf : 0u);
+    settle_last_phase(bar(kBarQFull), fq, qfills_s[0] == fq, 4u * qhalf, qland, kDrainSpin);
+    for (int s2 = 0; s2 < nslots; ++s2) {
+      const int f = max(fills_s[s2], peer_fills_s[s2]);
+      const uint32_t land = (fills_s[s2] == f ? (uint32_t)kSlotBytes : 0u) + (peer_fills_s[s2] == f ? (uint32_t)kSlotBytes : 0u);
+      settle_last_phase(bar(kBarFull + s2), f, fills_s[s2] == f, 2u * kSlotBytes, land, kDrainSpin);
     }
-    __syncwarp();
   }
   // both CTAs are done with TMEM and with each other's shared memory
   tc_fence_before();

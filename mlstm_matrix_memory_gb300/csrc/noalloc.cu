@@ -46,13 +46,16 @@ int scratch_ptr(void** out) {
 extern "C" int mlstm_parallel_fwd_noalloc(const void* q, const void* k, const void* v, const float* igate_pre,
                                           const float* fgate_pre, void* h, float* m_out, float* n_out, int B,
                                           int H, int T, int d_qk, int d_v, int dtype, void* stream) {
-  // the shape checks of mlstm_parallel_fwd, in its order, before the device scratch is touched
+  // the shape checks of mlstm_parallel_fwd (the same bounds on B*H and
+  // B*H*T, so no product below can overflow), before the scratch is touched
   if (B < 0 || H < 0 || T < 0) return MLSTM_EINVAL;
+  const long long BH = (long long)B * H;
+  if (BH > 0x7fffffffLL || BH * T > (1LL << 40)) return MLSTM_EINVAL;
   if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
   if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
   const int vec = dtype == MLSTM_F32 ? 4 : 8;
   if (d_qk % vec != 0 || d_v % vec != 0) return MLSTM_EINVAL;
-  if ((long long)B * H * T == 0) return MLSTM_OK;
+  if (BH * T == 0) return MLSTM_OK;
   const size_t need = mlstm_parallel_fwd_workspace(B, H, T);
   if (need == 0 || need > (size_t)MLSTM_NOALLOC_SCRATCH_BYTES) return MLSTM_EWORKSPACE;
   void* scratch = nullptr;

@@ -55,11 +55,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Gives up
-// after `limit` polls or as soon as *abort is set by another role; on giving
-// up it records the site in the device status word and raises *abort.
+// after `limit` polls or as soon as *abort is set by another role (also on
+// the fast path: once any role of the CTA has given up, no wait succeeds); on
+// giving up it records the site in the device status word and raises *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit,
                                           volatile int* abort, const DevStatus& st, int site) {
-  if (mbar_test_wait(bar, parity)) return true;      // fast path: already complete
+  const int aborted = *abort;
+  if (mbar_test_wait(bar, parity)) return aborted == 0;   // fast path: already complete
+  if (aborted) return false;
   for (long long it = 0; it < limit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
@@ -67,6 +70,38 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
   report_timeout(st, site);
   *abort = 1;
   return false;
+}
+
+// The same wait executed by all 32 lanes of a warp, with one result for the
+// whole warp: true only if every lane saw the phase complete (each lane then
+// holds its own acquire of the barrier).  Warp-collective code (tcgen05.ld,
+// shuffles, .aligned barriers) may follow on either result.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, long long limit,
+                                               volatile int* abort, const DevStatus& st, int site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit, abort, st, site));
+}
+
+// Named barrier over `nthreads` threads (whole warps) that also reduces a
+// predicate: every thread receives the AND of all participants' `pred`.
+// Used wherever a group of warps must leave a loop together: each warp brings
+// its own wait results, and all of them take the same branch afterwards.
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Count `bytes` of the current phase's expected transaction bytes as arrived
+// without any copy (bytes that were posted but will never be written).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
@@ -256,6 +291,33 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   *abort = 1;
   return false;
 }
+// 32-bit store into the shared memory of a CTA of the cluster (address from mapa).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// After an abort: make the last phase of a `full` barrier (one arrival,
+// posted by one issuer together with the bytes of every issuer of that
+// phase) complete exactly when every load that was issued for it has landed,
+// and wait for it (bounded).  `fills` is the number of phases begun (1 + the
+// last phase's index); `posted` says whether the posting issuer began the
+// last one; `expected` are the bytes it posts per phase, `landing` the bytes
+// actually issued for the last phase by all issuers.  Called by one thread
+// of the barrier's CTA after every issuer has stopped, so that no copy can
+// still write shared memory once the CTA (or CTA pair) exits.
+__device__ __forceinline__ void settle_last_phase(uint32_t bar, int fills, bool posted, uint32_t expected,
+                                                  uint32_t landing, long long limit) {
+  if (fills <= 0) return;
+  if (posted) {
+    if (expected > landing) mbar_complete_tx(bar, expected - landing);   // parts that were never issued
+  } else {
+    mbar_arrive_expect_tx(bar, landing);                                 // issued without the post
+  }
+  const uint32_t parity = (uint32_t)(fills - 1) & 1u;
+  for (long long w = 0; w < limit; ++w)
+    if (mbar_try_wait(bar, parity)) break;
+}
+
 // Tensor load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA (cluster address).
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* desc, uint32_t bar_cluster, int c0,

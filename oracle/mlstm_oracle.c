@@ -53,12 +53,16 @@
 
 int oracle_mutation(void) { return ORACLE_MUTATION; }
 
-static void set_threads(int nthreads)
+/* Team size of one call: the caller's count, or the OpenMP default when it
+ * passes 0.  Given to each parallel region by a num_threads clause, so that one
+ * call's choice never carries over to the next (unlike omp_set_num_threads). */
+static int team_size(int nthreads)
 {
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
+    return nthreads > 0 ? nthreads : omp_get_max_threads();
 #else
     (void)nthreads;
+    return 1;
 #endif
 }
 
@@ -182,9 +186,10 @@ int oracle_parallel_stabilized(int B, int H, int T, int dqk, int dv,
                                double *h, double *m_out, double *n_out, int nthreads)
 {
     if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
-    set_threads(nthreads);
+    const int nteam = team_size(nthreads);
+    (void)nteam;
     const long BH = (long)B * H;
-#pragma omp parallel
+#pragma omp parallel num_threads(nteam)
     {
         double *dt = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
         double *cp = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
@@ -215,11 +220,12 @@ int oracle_parallel_rows(int B, int H, int T, int dqk, int dv,
                          double *h_out, double *m_out, double *n_out, int nthreads)
 {
     if (B < 0 || H < 0 || T <= 0 || dqk <= 0 || dv <= 0 || nrows < 0) return -1;
-    set_threads(nthreads);
+    const int nteam = team_size(nthreads);
+    (void)nteam;
     const long BHT = (long)B * H * T;
     for (int r = 0; r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= BHT) return -1;
-#pragma omp parallel
+#pragma omp parallel num_threads(nteam)
     {
         double *dt = (double *)malloc(sizeof(double) * T);
         double *cp = (double *)malloc(sizeof(double) * T);
@@ -251,10 +257,11 @@ int oracle_parallel_unstabilized(int B, int H, int T, int dqk, int dv,
                                  double *h, int nthreads)
 {
     if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
-    set_threads(nthreads);
+    const int nteam = team_size(nthreads);
+    (void)nteam;
     const long BH = (long)B * H;
     const double s = key_scale(dqk);
-#pragma omp parallel
+#pragma omp parallel num_threads(nteam)
     {
         double *ct = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
 #pragma omp for schedule(dynamic, 1)
@@ -344,9 +351,10 @@ int oracle_step(int B, int H, int dqk, int dv, double *C, double *n, double *m,
                 const double *ig, const double *fg, double *h, int nthreads)
 {
     if (B < 0 || H < 0 || dqk <= 0 || dv <= 0) return -1;
-    set_threads(nthreads);
+    const int nteam = team_size(nthreads);
+    (void)nteam;
     const long BH = (long)B * H;
-#pragma omp parallel for schedule(static)
+#pragma omp parallel for schedule(static) num_threads(nteam)
     for (long bh = 0; bh < BH; ++bh)
         step_head(dqk, dv, C + (size_t)bh * dv * dqk, n + (size_t)bh * dqk, m + bh,
                   q + (size_t)bh * dqk, k + (size_t)bh * dqk, v + (size_t)bh * dv,
@@ -363,9 +371,10 @@ int oracle_recurrent_stabilized(int B, int H, int T, int dqk, int dv,
                                 int nthreads)
 {
     if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
-    set_threads(nthreads);
+    const int nteam = team_size(nthreads);
+    (void)nteam;
     const long BH = (long)B * H;
-#pragma omp parallel
+#pragma omp parallel num_threads(nteam)
     {
         double *C = (double *)malloc(sizeof(double) * dv * dqk);
         double *n = (double *)malloc(sizeof(double) * dqk);
@@ -398,10 +407,11 @@ int oracle_recurrent_unstabilized(int B, int H, int T, int dqk, int dv,
                                   double *h, int nthreads)
 {
     if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
-    set_threads(nthreads);
+    const int nteam = team_size(nthreads);
+    (void)nteam;
     const long BH = (long)B * H;
     const double s = key_scale(dqk);
-#pragma omp parallel
+#pragma omp parallel num_threads(nteam)
     {
         double *C = (double *)malloc(sizeof(double) * dv * dqk);
         double *n = (double *)malloc(sizeof(double) * dqk);
@@ -563,11 +573,12 @@ int oracle_parallel_backward(int B, int H, int T, int dqk, int dv,
                              double *dq, double *dk, double *dvv, double *dig, double *dfg, int nthreads)
 {
     if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
-    set_threads(nthreads);
+    const int nteam = team_size(nthreads);
+    (void)nteam;
     const long BH = (long)B * H;
     const size_t TT = (size_t)(T > 0 ? T : 1) * (size_t)(T > 0 ? T : 1);
     int fail = 0;
-#pragma omp parallel
+#pragma omp parallel num_threads(nteam)
     {
         double *buf = (double *)malloc(sizeof(double) * (5 * TT + 4 * (size_t)(T > 0 ? T : 1)));
         if (!buf) {
@@ -618,12 +629,13 @@ int oracle_recurrent_backward(int B, int H, int T, int dqk, int dv,
                               int nthreads)
 {
     if (B < 0 || H < 0 || T < 0 || dqk <= 0 || dv <= 0) return -1;
-    set_threads(nthreads);
+    const int nteam = team_size(nthreads);
+    (void)nteam;
     const long BH = (long)B * H;
     const double s = key_scale(dqk);
     const size_t CS = (size_t)dv * dqk;
     int fail = 0;
-#pragma omp parallel
+#pragma omp parallel num_threads(nteam)
     {
         /* C_t, n_t for t = -1..T-1 (index t+1), plus dC, dn, dh~, h~ */
         double *Cs = (double *)malloc(sizeof(double) * CS * (size_t)(T + 1));

@@ -245,9 +245,13 @@ def test_noalloc_validation(lib):
     lib.mlstm_parallel_fwd_noalloc.argtypes = [vp] * 8 + [i] * 6 + [vp]
     lib.mlstm_parallel_fwd_noalloc.restype = i
 
-    def na(B=1, T=8, dqk=64, dv=64, dt=1):
-        return lib.mlstm_parallel_fwd_noalloc(A, A, A, A, A, A, None, None, B, 1, T, dqk, dv, dt, None)
+    def na(B=1, T=8, dqk=64, dv=64, dt=1, H=1):
+        return lib.mlstm_parallel_fwd_noalloc(A, A, A, A, A, A, None, None, B, H, T, dqk, dv, dt, None)
     assert na(B=-1) == -1
+    big = (1 << 31) - 1
+    assert na(B=big, H=big, T=big) == -1       # B*H beyond int: rejected before any product is formed
+    assert na(B=1 << 16, H=1 << 16) == -1
+    assert na(B=1 << 20, T=1 << 21) == -1      # B*H*T beyond 2^40, as mlstm_parallel_fwd
     assert na(dqk=0) == -1                      # shape checks come before the device scratch
     assert na(dt=5) == -3
     assert na(dv=12) == -1
