@@ -35,6 +35,9 @@ from mlstm_matrix_memory_gb300 import workloads as W  # noqa: E402
 
 METRIC = "mLSTM parallel fwd causal TFLOP/s + tokens/s at T=2048 (1×GB300, % of peak)"
 L2_FLUSH_BYTES = 512 << 20          # > 129 MB L2
+# nominal GB300 figures, beside the measured denominators
+NOMINAL_BF16_TFLOPS = 2250.0        # dense bf16
+NOMINAL_HBM_GBS = 8000.0            # HBM3e
 
 
 def parse():
@@ -47,8 +50,11 @@ def parse():
     p.add_argument("--algo", default="auto", choices=("auto", "tc", "simt"))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-step", action="store_true", help="skip the recurrent-step measurement")
+    p.add_argument("--no-other-configs", action="store_true",
+                   help="skip the forward on the other bf16 layer shapes (350M-scale, T=16384)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-kernel", choices=("fwd", "fs", "step", "step_seq", "rbwd", "bwd"), default=None,
+    p.add_argument("--profile-kernel", choices=("fwd", "fwd_call", "fs", "step", "step_seq", "rbwd", "bwd"),
+                   default=None,
                    help="no timing: one warm-up and one launch of the fused forward kernel (on --workload), "
                         "of the parallel-to-recurrent hand-off (on --workload), of the recurrent step (B=64, H=4, d=512: 256 MB of state), of the 64-token prefill "
                         "(same heads), of the recurrent backward (B=4, H=8, T=256, d=384) or of the parallel "
@@ -263,6 +269,21 @@ def time_parallel(M, w, xd, algo, steps, warmup, flush):
     return step_ms, fwd_ms, gate_ms
 
 
+def time_other_parallel(M, w, steps, warmup, flush):
+    """The forward (public call) and the fused kernel alone on another bf16
+    layer shape, timed as the main workload is."""
+    xd = {k: v.cuda() for k, v in W.parallel_inputs(w, 0).items()}
+    algo = "tc" if M.tc_supported(w.d_qk, w.d_v, w.dtype) else "simt"
+    step_ms, fwd_ms, gate_ms = time_parallel(M, w, xd, algo, steps, warmup, flush)
+    del xd
+    return statistics.mean(step_ms), statistics.mean(fwd_ms), statistics.mean(gate_ms), algo
+
+
+def launches_per_step(w, algo):
+    """Kernel launches of one forward call: the gate pass and the fused kernel."""
+    return 2
+
+
 def time_e2e(M, w, xh, algo, steps, warmup):
     """Through the public host-buffer call (``mlstm_parallel_fwd_host``): the
     step's inputs in pinned host memory, h returned to pinned host memory,
@@ -454,6 +475,15 @@ def profile_once(args):
         M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
         for _ in range(2):
             M.parallel_fwd_gated(xd["q"], xd["k"], xd["v"], ws, h, algo=args.algo)
+    elif args.profile_kernel == "fwd_call":
+        # the public forward call as the benchmark's step makes it
+        w = W.PARALLEL_WORKLOADS[args.workload]
+        xd = {k: v.cuda() for k, v in W.parallel_inputs(w, 0).items()}
+        ws = torch.empty(M.parallel_fwd_workspace_bytes(w.B, w.H, w.T), dtype=torch.uint8, device="cuda")
+        h = torch.empty((w.B, w.H, w.T, w.d_v), dtype=w.dtype, device="cuda")
+        for _ in range(2):
+            M.parallel_fwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], h=h, workspace=ws,
+                           algo=args.algo)
     elif args.profile_kernel == "fs":
         # the parallel-to-recurrent hand-off (final C, n, m) on the parallel workload
         w = W.PARALLEL_WORKLOADS[args.workload]
@@ -529,6 +559,11 @@ def main():
     if not args.no_step:
         rec = time_step(M, max(10, args.steps // 2), 3)
         seq = time_step_seq(M, 5)
+    others = {}
+    if not args.no_other_configs and w.name == W.L125M.name:
+        for key, ow in (("parallel_350m", W.L350M), ("parallel_long", W.LONG)):
+            others[key] = (ow, time_other_parallel(M, ow, max(10, args.steps // 2) if ow.T <= 2048 else 10, 3,
+                                                   flush))
     bwd = rbwd = None
     if algo == "tc":
         fs = time_final_state(M, w, xd, 10)
@@ -539,7 +574,11 @@ def main():
     flops = w.causal_flops
     value = ws * flops / (t_step * 1e-3) / 1e12
     peak_tf, peak_bw, src = peaks()
-    achieved = flops / (t_fwd * 1e-3) / 1e12
+    nlaunch = launches_per_step(w, algo)
+    # the dominant kernel: with one launch per step it is the step itself
+    # (gate terms computed inside); else the fused kernel timed alone
+    t_kern = t_step if nlaunch == 1 else t_fwd
+    achieved = flops / (t_kern * 1e-3) / 1e12
     traffic = kernel_traffic("fwd_tc_" + w.name) if algo == "tc" else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
@@ -548,6 +587,7 @@ def main():
         "data": "synthetic (seeded N(0,1) q/k/v, N(0,1) input and N(3,1) forget pre-activations)",
         "tokens_per_s": ws * w.tokens / (t_step * 1e-3),
         "frac_of_peak": value / ws / peak_tf,
+        "frac_of_nominal_peak": value / ws / NOMINAL_BF16_TFLOPS,
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_qk": w.d_qk, "d_v": w.d_v,
                    "kernel": algo, "l2": "flushed before every timed step (512 MB memset)",
                    "parallelism": f"{ws} independent replica(s), heads independent, no collective"},
@@ -555,12 +595,16 @@ def main():
         "fused_kernel_ms_alone": statistics.mean(fwd_ms),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
+                     "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                     "nominal_peak": NOMINAL_BF16_TFLOPS,
                      "traffic": traffic, "kernel": f"mlstm fwd_{algo}",
                      "work": "causal flops T^2 (d_qk+d_v) per head per launch",
-                     "timing": "fused kernel alone, CUDA events per launch, L2 flushed before each"},
+                     "timing": ("the step's single launch (gate terms computed in the kernel)" if nlaunch == 1
+                                else "fused kernel alone") + ", CUDA events per launch, L2 flushed before each"},
         "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": nlaunch * args.steps,
+        "launches_per_step": nlaunch,
     }
     if rec is not None:
         ms, nbytes, sw = rec
@@ -570,6 +614,8 @@ def main():
                                   "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_bw,
                                                "unit": "GB/s", "frac": gbs / peak_bw,
                                                "peak_source": f"{src} copy bandwidth",
+                                               "frac_of_nominal": gbs / NOMINAL_HBM_GBS,
+                                               "nominal_peak": NOMINAL_HBM_GBS,
                                                "traffic": kernel_traffic("step_" + sw.name)}}
     if seq is not None:
         ms, fl, sw, L = seq
@@ -581,6 +627,19 @@ def main():
                                                   "unit": "TFLOP/s", "frac": tf / alu_peak,
                                                   "peak_source": f"FP32 FMA: {sms} SMs x 128 lanes x 2 x {mhz:.0f} MHz",
                                                   "traffic": kernel_traffic(f"step_seq_{sw.name}_L{L}")}}
+    for key, (ow, (oms, ofwd, ogate, oalgo)) in others.items():
+        fl = ow.causal_flops
+        onl = launches_per_step(ow, oalgo)
+        tf_step, tf_kern = fl / (oms * 1e-3) / 1e12, fl / ((oms if onl == 1 else ofwd) * 1e-3) / 1e12
+        line[key] = {"workload": ow.name, "B": ow.B, "H": ow.H, "T": ow.T, "d_qk": ow.d_qk, "d_v": ow.d_v,
+                     "kernel": oalgo, "ms": oms, "TFLOP_per_s": tf_step, "tokens_per_s": ow.tokens / (oms * 1e-3),
+                     "frac_of_peak": tf_step / peak_tf, "frac_of_nominal_peak": tf_step / NOMINAL_BF16_TFLOPS,
+                     "gate_prep_ms_alone": ogate, "fused_kernel_ms_alone": ofwd, "launches_per_step": onl,
+                     "roofline": {"bound": "tensor", "achieved": tf_kern, "peak": peak_tf, "unit": "TFLOP/s",
+                                  "frac": tf_kern / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
+                                  "frac_of_nominal": tf_kern / NOMINAL_BF16_TFLOPS,
+                                  "traffic": kernel_traffic("fwd_tc_" + ow.name) if oalgo == "tc" else None,
+                                  "work": "causal flops T^2 (d_qk+d_v) per head per launch"}}
     if fs is not None:
         ms, fl = fs
         tf = fl / (ms * 1e-3) / 1e12

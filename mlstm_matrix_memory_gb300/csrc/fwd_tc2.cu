@@ -619,6 +619,21 @@ extern "C" int mlstm_trace2_read(long long* host) {
 namespace {
 #endif
 
+// Static shared memory of the kernel (the largest instantiation), read once.
+size_t static_smem() {
+  static const size_t bytes = [] {
+    size_t mx = 0;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fwd_tc2_kernel<1, false>) == cudaSuccess) mx = std::max(mx, fa.sharedSizeBytes);
+    if (cudaFuncGetAttributes(&fa, fwd_tc2_kernel<2, false>) == cudaSuccess) mx = std::max(mx, fa.sharedSizeBytes);
+    if (cudaFuncGetAttributes(&fa, fwd_tc2_kernel<1, true>) == cudaSuccess) mx = std::max(mx, fa.sharedSizeBytes);
+    if (cudaFuncGetAttributes(&fa, fwd_tc2_kernel<2, true>) == cudaSuccess) mx = std::max(mx, fa.sharedSizeBytes);
+    cudaGetLastError();
+    return mx > 0 ? mx : (size_t)4096;
+  }();
+  return bytes;
+}
+
 // Clusters of two that fit on the device at once with this shared-memory size
 // (queried once per size; half the SM count if the query fails).
 int resident_pairs(size_t smem) {
@@ -702,7 +717,7 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   p.log2_scale = log2f(a.scale);
   p.st = a.st;
   const size_t fixed = 1024 + (size_t)a.dqk * kBM * 2 + (size_t)kBN * kBM * 2;
-  const long long room = (long long)kSmemLimit - 2048 - (long long)fixed;   // 2 KB for static shared
+  const long long room = (long long)kSmemLimit - (long long)static_smem() - (long long)fixed;
   const int total = (int)std::min<long long>(kMaxSlots, room / kSlotBytes);
   if (total < 2) return kUnsupported;
   // split the granules between the rings in proportion to the bytes a key

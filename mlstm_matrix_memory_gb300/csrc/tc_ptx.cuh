@@ -55,14 +55,16 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Gives up
-// after `limit` polls or as soon as *abort is set by another role (also on
-// the fast path: once any role of the CTA has given up, no wait succeeds); on
-// giving up it records the site in the device status word and raises *abort.
+// after `limit` polls or as soon as *abort is set by another role; on giving
+// up it records the site in the device status word and raises *abort.  A
+// phase found complete on the first test is reported as such even after an
+// abort: the result of an aborted launch is discarded, and every group of
+// warps agrees on its exit at a reducing barrier (bar_red_and), so one role
+// passing a completed phase cannot strand another.  (The abort flag is not
+// read on this path: the load would sit on every issuer's critical path.)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit,
                                           volatile int* abort, const DevStatus& st, int site) {
-  const int aborted = *abort;
-  if (mbar_test_wait(bar, parity)) return aborted == 0;   // fast path: already complete
-  if (aborted) return false;
+  if (mbar_test_wait(bar, parity)) return true;      // fast path: already complete
   for (long long it = 0; it < limit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
