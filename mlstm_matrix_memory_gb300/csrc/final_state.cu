@@ -251,69 +251,75 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     };
     if (c0 < c1) weights(load_a2(c0), 0);
     a2_next = load_a2(c0 + 1);
+    // The loop is the hot path of this kernel; its wait and exit are kept in
+    // their plainest form (per-lane wait, early exit), which measured fastest:
+    // a warp-level vote or a reducing barrier per stage cost 6-10 us of the
+    // 49 us 125M-scale hand-off.  A warp that leaves early (its wait gave up,
+    // raising the abort flag) then arrives on the barriers of the stages it
+    // skipped, so every stage's barrier still counts all eight warps, and the
+    // group agrees on the result once, after the loop.  The 32 lanes of a warp
+    // poll the same barrier with the same instructions and take the same exit.
     bool ok = true;
-    for (int c = c0, i = 0; c < c1; ++c, ++i) {
+    int done = 0;
+    for (int c = c0, i = 0; c < c1 && ok; ++c, ++i) {
       const int s2 = i % p.nst;
       const uint32_t u = (uint32_t)(i / p.nst);
-      // Every warp reaches this barrier (which also orders the weights
-      // w_s[s2]) on every stage, whatever its waits returned; a warp whose
-      // wait gave up does no further work, and the group agrees on the result
-      // once, after the loop.
-      if (ok) ok = mbar_wait_warp(bar(kFsFull + s2), u & 1u, spin, abort, p.st, 23);
-      named_bar_sync(1, 256);
-      if (ok) {
-        const uint32_t sb = base + (uint32_t)s2 * stage_bytes;
-        {
-          // V row (token) t2 % 64 of box (t2 / 64) % 2: four of its eight
-          // 16-byte chunks (the half t2 / 128), taken in an order rotated by the
-          // row so that neighbouring lanes (rows 128 bytes apart) hit different banks
-          const int j = t2 & 63;
-          const float w = w_s[s2][j];
-          const uint32_t row = sb + (uint32_t)((t2 >> 6) & 1) * 8192u + (uint32_t)j * 128u;
+      ok = mbar_wait(bar(kFsFull + s2), u & 1u, spin, abort, p.st, 23);
+      if (!ok) break;
+      named_bar_sync(1, 256);                        // w_s[s2] written by every thread
+      ++done;
+      const uint32_t sb = base + (uint32_t)s2 * stage_bytes;
+      {
+        // V row (token) t2 % 64 of box (t2 / 64) % 2: four of its eight
+        // 16-byte chunks (the half t2 / 128), taken in an order rotated by the
+        // row so that neighbouring lanes (rows 128 bytes apart) hit different banks
+        const int j = t2 & 63;
+        const float w = w_s[s2][j];
+        const uint32_t row = sb + (uint32_t)((t2 >> 6) & 1) * 8192u + (uint32_t)j * 128u;
 #pragma unroll
-          for (int q0 = 0; q0 < 4; ++q0) {
-            const uint32_t q = (uint32_t)((4 * (t2 >> 7) + q0 + j) & 7);
-            uint32_t x[4];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(row + q * 16u));
+        for (int q0 = 0; q0 < 4; ++q0) {
+          const uint32_t q = (uint32_t)((4 * (t2 >> 7) + q0 + j) & 7);
+          uint32_t x[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(row + q * 16u));
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[e]));
-              x[e] = pack_bf16x2(f.x * w, f.y * w);
-            }
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + q * 16u), "r"(x[0]), "r"(x[1]),
-                         "r"(x[2]), "r"(x[3])
-                         : "memory");
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[e]));
+            x[e] = pack_bf16x2(f.x * w, f.y * w);
           }
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + q * 16u), "r"(x[0]), "r"(x[1]),
+                       "r"(x[2]), "r"(x[3])
+                       : "memory");
         }
-        if (n_thread) {
-          const int col = ncol0 + chunk * 8;
-          const uint32_t kb = sb + 16384u + (uint32_t)(col >> 6) * 8192u;
-          const int cq = (col & 63) >> 3;
-          for (int jj = 0; jj < tpg; ++jj) {
-            const int j = jj * groups + tg;       // neighbouring lanes: neighbouring rows, distinct swizzled chunks
-            uint32_t x[4];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                         : "r"(kb + (uint32_t)j * 128u + (uint32_t)((cq ^ (j & 7)) << 4)));
-            const float w = w_s[s2][j];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[e]));
-              nacc[2 * e] = fmaf(w, f.x, nacc[2 * e]);
-              nacc[2 * e + 1] = fmaf(w, f.y, nacc[2 * e + 1]);
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kFsScaled + s2));
       }
+      if (n_thread) {
+        const int col = ncol0 + chunk * 8;
+        const uint32_t kb = sb + 16384u + (uint32_t)(col >> 6) * 8192u;
+        const int cq = (col & 63) >> 3;
+        for (int jj = 0; jj < tpg; ++jj) {
+          const int j = jj * groups + tg;       // neighbouring lanes: neighbouring rows, distinct swizzled chunks
+          uint32_t x[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                       : "r"(kb + (uint32_t)j * 128u + (uint32_t)((cq ^ (j & 7)) << 4)));
+          const float w = w_s[s2][j];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x[e]));
+            nacc[2 * e] = fmaf(w, f.x, nacc[2 * e]);
+            nacc[2 * e + 1] = fmaf(w, f.y, nacc[2 * e + 1]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kFsScaled + s2));
       if (c + 1 < c1) {
         weights(a2_next, (i + 1) % p.nst);
         a2_next = load_a2(c + 2);
       }
     }
+    for (int c = c0 + done; c < c1; ++c) named_bar_sync(1, 256);   // stages this warp skipped
     ok = bar_red_and(1, 256, ok);
     // the token groups of each chunk meet (neighbouring lanes)
 #pragma unroll

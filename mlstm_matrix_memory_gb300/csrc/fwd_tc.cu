@@ -337,6 +337,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       const int col = half * HALF + lane + 32 * t;
       av_next[t] = col < p.T ? p.a2[hbase + col] : -INFINITY;
     }
+    // A warp whose wait gives up (raising the abort flag) leaves the tile loop,
+    // which has no group barrier; the gating warps agree on the result at the
+    // reducing barrier of the epilogue, which every one of them reaches.
     for (int j = 0; j < nkv && ok; ++j) {
       const int j0 = j * BN, cbase = j0 + half * HALF;
       const int buf = j % NSBUF, u = j / NSBUF;
@@ -356,7 +359,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 #pragma unroll
         for (int t = 0; t < HALF / 32; ++t) av[t] = A == -INFINITY ? 0.0f : exp2f(av[t] - A);
       }
-      ok = mbar_wait_warp(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
+      ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
       if (!ok) break;
       tc_fence_after();
       if (gw == 0 && lane == 0) TRACE(6, j);
@@ -399,7 +402,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       }
       // the previous tile's O MMA must be done reading P before it is overwritten
       if (gw == 0 && lane == 0) TRACE(8, j);
-      ok = mbar_wait_warp(bar(kBarPEmpty), (j & 1) ^ 1, spin, abort, p.st, kSiteGate);
+      ok = mbar_wait(bar(kBarPEmpty), (j & 1) ^ 1, spin, abort, p.st, kSiteGate);
       if (!ok) break;
       if (gw == 0 && lane == 0) TRACE(9, j);
 #pragma unroll
@@ -417,7 +420,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     }
 
     // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n
-    if (ok) ok = mbar_wait_warp(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
+    if (ok) ok = mbar_wait(bar(kBarOFull), 0, spin, abort, p.st, kSiteEpilogue);
     tc_fence_after();
     if (gw == 0 && lane == 0) TRACE(11, 0);
     // After the last O MMA no operand is read any more: the P tile combines the

@@ -145,18 +145,17 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
   __shared__ int s_issued_s;                // global key tile of the last fully issued S product
-  // Loads this CTA issued (fills of each ring granule; Q fills of each
-  // producer) and, in the leader, the peer's counts and abort flag, sent at
-  // exit: after an abort the leader settles every load of the pair.
-  __shared__ int fills_s[kMaxSlots];
+  // Loads each producer of this CTA issued (ring granules, written once at
+  // its exit; Q fills) and, in the leader, the peer's counts and abort flag,
+  // sent at exit: after an abort the leader settles every load of the pair.
+  __shared__ int loads_s[kProducers];
   __shared__ int qfills_s[kProducers];
-  __shared__ int peer_fills_s[kMaxSlots];
+  __shared__ int peer_loads_s[kProducers];
   __shared__ int peer_qfills_s[kProducers];
   __shared__ int peer_abort_s;
   __shared__ float bpart[2 * kBM];
   volatile int* abort = &abort_flag;
   volatile int* s_issued = &s_issued_s;
-  volatile int* fills = fills_s;
   volatile int* qfills = qfills_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -180,12 +179,10 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   auto lbar = [&](int i) { return mapa_shared(smem_u32(&bars[i]), 0); };   // leader's barrier
 
-  if (threadIdx.x < kMaxSlots) {
-    fills_s[threadIdx.x] = 0;
-    peer_fills_s[threadIdx.x] = 0;
-  }
   if (threadIdx.x < kProducers) {
+    loads_s[threadIdx.x] = 0;
     qfills_s[threadIdx.x] = 0;
+    peer_loads_s[threadIdx.x] = 0;
     peer_qfills_s[threadIdx.x] = 0;
   }
   if (threadIdx.x == 0) {
@@ -235,7 +232,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     // leader posts.
     const int pi = warp == 0 ? 0 : 1;
     const int base_slot = pi == 0 ? 0 : p.nk, n = pi == 0 ? p.nk : p.nv;
-    int st = 0;
+    int st = 0, nloads = 0;                  // nloads: granules filled (round-robin over the ring)
     uint32_t ph = 0;
     bool ok = true;
     // loads the ring's next granule
@@ -247,7 +244,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       if (leader) mbar_arrive_expect_tx(bar(kBarFull + g), 2u * kSlotBytes);
       for (int b2 = 0; b2 < nbox; ++b2)
         tma_load_3d_pair(sRing + g * kSlotBytes + b2 * box_bytes, map, lbar(kBarFull + g), x0 + b2 * dx, y, it.bh);
-      fills[g] = fills[g] + 1;
+      ++nloads;
       if (++st == n) { st = 0; ph ^= 1; }
     };
     int qi = 0;
@@ -281,6 +278,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
           }
       }
     }
+    loads_s[pi] = nloads;
   } else if ((warp == 1 || warp == 2) && lane == 0 && leader) {
     // ------------------------------------------------------------ MMA issuers (leader only)
     // Warp 1 issues S = Q K^T, warp 2 issues O += P V.  The two products use
@@ -391,11 +389,15 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     const int rl = 32 * qd + lane;
     const uint32_t lane_addr = (uint32_t)(32 * qd) << 16;
     const uint32_t l_sempty0 = lbar(kBarSEmpty), l_sempty1 = lbar(kBarSEmpty + 1), l_pfull = lbar(kBarPFull);
-    // Exit rule: each wait below is warp-uniform, and a warp that gives up
-    // leaves the tile loop at once; the eight warps of the CTA then meet once
-    // per item at the reducing barrier after the O wait, and all of them go
-    // on with the epilogue or all leave.  So every named barrier below is
-    // reached by all 256 threads (or all 128 of a half) on every path.
+    // Exit rule: a warp whose wait gives up (raising the abort flag, after
+    // which every wait returns at once) leaves the item's tile loop; the tile
+    // loop has no group barrier.  The eight warps of the CTA then meet once
+    // per item at the reducing barrier after the O wait, and all of them go on
+    // with the epilogue or all leave.  So every named barrier below is reached
+    // by all 256 threads (or all 128 of a half) on every path.  The 32 lanes
+    // of a warp poll the same barrier with the same instructions and take the
+    // same exit; the waits are kept in this plainest form because a warp vote
+    // per wait measured slower.
     bool ok = true;
     int qi = 0, gt = 0;
     for (int r = 0; r * p.nclusters < p.n_items && ok; ++r) {
@@ -432,7 +434,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
 #pragma unroll
           for (int t = 0; t < HALF / 32; ++t) av[t] = A == -INFINITY ? 0.0f : exp2f(av[t] - A);
         }
-        ok = mbar_wait_warp(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
+        ok = mbar_wait(bar(kBarSFull + buf), u & 1, spin, abort, p.st, kSiteGate);
         if (!ok) break;
         tc_fence_after();
         if (gw == 0 && lane == 0) TRACE2(6, j);
@@ -473,7 +475,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
           }
         }
         if (gw == 0 && lane == 0) TRACE2(7, j);
-        ok = mbar_wait_warp(bar(kBarPEmpty), ((uint32_t)gt & 1u) ^ 1u, spin, abort, p.st, kSiteGate);
+        ok = mbar_wait(bar(kBarPEmpty), ((uint32_t)gt & 1u) ^ 1u, spin, abort, p.st, kSiteGate);
         if (!ok) break;
         if (gw == 0 && lane == 0) TRACE2(8, j);
 #pragma unroll
@@ -496,7 +498,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       // ---- epilogue: n = max(|b|, exp(-m)), H~ = O / n.  Each half stages its
       // 64-column boxes one at a time in its 16 KB of the P buffer (free until
       // the next item's first P) and stores each by TMA as soon as it is written.
-      if (ok) ok = mbar_wait_warp(bar(kBarOFull), (uint32_t)qi & 1u, spin, abort, p.st, kSiteEpilogue);
+      if (ok) ok = mbar_wait(bar(kBarOFull), (uint32_t)qi & 1u, spin, abort, p.st, kSiteEpilogue);
       tc_fence_after();
       if (gw == 0 && lane == 0) TRACE2(10, 0);
       bpart[half * kBM + rl] = bsum;
@@ -574,13 +576,12 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   // the last phase of Q and of every granule complete exactly when the loads
   // that were issued for it (by either CTA) have landed, and waits for that
   // (bounded), so no copy can still write shared memory once the pair exits.
-  const int nslots = p.nk + p.nv;
   if (!leader) {
     const int t = threadIdx.x;
-    if (t < nslots) st_shared_cluster_u32(mapa_shared(smem_u32(&peer_fills_s[t]), 0), (uint32_t)fills_s[t]);
-    else if (t < kMaxSlots + kProducers && t >= kMaxSlots)
-      st_shared_cluster_u32(mapa_shared(smem_u32(&peer_qfills_s[t - kMaxSlots]), 0), (uint32_t)qfills_s[t - kMaxSlots]);
-    else if (t == kMaxSlots + kProducers)
+    if (t < kProducers) st_shared_cluster_u32(mapa_shared(smem_u32(&peer_loads_s[t]), 0), (uint32_t)loads_s[t]);
+    else if (t < 2 * kProducers)
+      st_shared_cluster_u32(mapa_shared(smem_u32(&peer_qfills_s[t - kProducers]), 0), (uint32_t)qfills_s[t - kProducers]);
+    else if (t == 2 * kProducers)
       st_shared_cluster_u32(mapa_shared(smem_u32(&peer_abort_s), 0), (uint32_t)abort_flag);
   }
   cluster_sync_all();
@@ -592,10 +593,15 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     for (int pi = 0; pi < kProducers; ++pi)
       qland += (qfills_s[pi] == fq ? qhalf : 0u) + (peer_qfills_s[pi] == fq ? qhalf : 0u);
     settle_last_phase(bar(kBarQFull), fq, qfills_s[0] == fq, 4u * qhalf, qland, kDrainSpin);
-    for (int s2 = 0; s2 < nslots; ++s2) {
-      const int f = max(fills_s[s2], peer_fills_s[s2]);
-      const uint32_t land = (fills_s[s2] == f ? (uint32_t)kSlotBytes : 0u) + (peer_fills_s[s2] == f ? (uint32_t)kSlotBytes : 0u);
-      settle_last_phase(bar(kBarFull + s2), f, fills_s[s2] == f, 2u * kSlotBytes, land, kDrainSpin);
+    // granule s of a ring of n has had one fill per round of loads reaching it
+    auto rounds = [](int loads, int s, int n) { return loads > s ? (loads - 1 - s) / n + 1 : 0; };
+    for (int pi = 0; pi < kProducers; ++pi) {
+      const int base_slot = pi == 0 ? 0 : p.nk, n = pi == 0 ? p.nk : p.nv;
+      for (int s2 = 0; s2 < n; ++s2) {
+        const int fl = rounds(loads_s[pi], s2, n), fp = rounds(peer_loads_s[pi], s2, n), f = max(fl, fp);
+        const uint32_t land = (fl == f ? (uint32_t)kSlotBytes : 0u) + (fp == f ? (uint32_t)kSlotBytes : 0u);
+        settle_last_phase(bar(kBarFull + base_slot + s2), f, fl == f, 2u * kSlotBytes, land, kDrainSpin);
+      }
     }
   }
   // both CTAs are done with TMEM and with each other's shared memory
