@@ -208,6 +208,8 @@ int mlstm_step_seq_opt(float *C, float *n, float *m,
  * output gradient dh = dL/dH~, the gradients of q, k, v and of the gate
  * pre-activations.  The stabilizer m is held constant, as on the pages (its
  * gradients cancel); eq (90) is read with sign(b), the derivative of |b|.
+ * (mlstm_parallel_bwd_opt below adds the output gate and the exponential
+ * forget activation.)
  *
  *   q, k, v, igate_pre, fgate_pre   the forward's inputs (layouts as there)
  *   dh         [B,H,T,d_v]  dtype: dL/dH~
@@ -226,8 +228,10 @@ int mlstm_step_seq_opt(float *C, float *n, float *m,
  *    (bf16) and the tile's row and column sums of dD~; a second tensor-core
  *    kernel forms dQ, dK, dV over the lower triangle of G and P.  Workspace:
  *    two bf16 T x T matrices per head (about 0.54 GB for B=8, H=4, T=2048).
- *  - otherwise the five T x T products are batched GEMMs (cuBLAS) with fp32
- *    S and dL/dC materialised (about 1.6 GB for B=8, H=4, T=2048, bf16).
+ *  - otherwise (fp32, or shapes the tensor-core kernels do not tile) the five
+ *    T x T products run in a batched CUDA-core GEMM kernel of the library
+ *    (fp32 accumulation, each over its causal part only), with fp32 S and
+ *    dL/dC materialised (about 1.6 GB for B=8, H=4, T=2048, bf16).
  * Requirements: 1 <= T <= 16384; 1 <= d_qk, d_v <= 512; no output may alias
  * an input. */
 size_t mlstm_parallel_bwd_workspace(int B, int H, int T, int dtype);
@@ -252,6 +256,39 @@ int mlstm_parallel_bwd(const void *q, const void *k, const void *v,
                        void *dq, void *dk, void *dv, float *d_igate, float *d_fgate,
                        int B, int H, int T, int d_qk, int d_v, int dtype,
                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* mlstm_parallel_bwd with options: the backward of mlstm_parallel_fwd_opt.
+ *   opt->forget_exp  the exponential forget activation (log f = f~, part
+ *               28/30 eq 70's gamma = exp): d f~ = dL/dlog f instead of
+ *               sigmoid(-f~) dL/dlog f (eq 104)
+ *   opt->ogate_pre   [B,H,T,d_v] dtype output-gate pre-activations, or NULL.
+ *               When given, the forward was h = sigmoid(o~) (.) H~ (eq 78),
+ *               dh is dL/dh, and d_ogate ([B,H,T,d_v] dtype out, required)
+ *               receives dL/do~ = dh (.) H~ (.) sigmoid(o~)(1 - sigmoid(o~));
+ *               the rest of the backward runs on dL/dH~ = dh (.) sigmoid(o~).
+ *   opt->algo, opt->b_out are ignored.
+ *   h_saved, n_saved, b_saved   all NULL, or all given as for
+ *               mlstm_parallel_bwd_saved: H~ (the forward's output WITHOUT the
+ *               output gate, i.e. of mlstm_parallel_fwd_opt with ogate_pre
+ *               NULL), n and the signed b of the forward on the same inputs
+ *               and forget activation.
+ *   workspace   mlstm_parallel_bwd_workspace_opt(B,H,T,d_qk,d_v,dtype,opt)
+ *               bytes (256-byte aligned): the path's workspace, plus one
+ *               [B,H,T,d_v] dtype buffer with an output gate (two on the
+ *               CUDA-core path, which also forms H~).
+ * Other arguments, requirements and errors as mlstm_parallel_bwd;
+ * MLSTM_EINVAL when only some of h_saved, n_saved, b_saved are given or
+ * ogate_pre is set without d_ogate. */
+size_t mlstm_parallel_bwd_workspace_opt(int B, int H, int T, int d_qk, int d_v, int dtype,
+                                        const mlstm_options *opt);
+
+int mlstm_parallel_bwd_opt(const void *q, const void *k, const void *v,
+                           const float *igate_pre, const float *fgate_pre, const void *dh,
+                           const void *h_saved, const float *n_saved, const float *b_saved,
+                           void *dq, void *dk, void *dv, float *d_igate, float *d_fgate, void *d_ogate,
+                           int B, int H, int T, int d_qk, int d_v, int dtype,
+                           void *workspace, size_t workspace_bytes,
+                           const mlstm_options *opt, void *stream);
 
 /* Backward pass of the recurrent form (backpropagation through time, part
  * 28/30 eqs 59-70) of the cell the recurrent step and mlstm_step_seq compute

@@ -83,6 +83,10 @@ def library() -> ctypes.CDLL:
         lib.mlstm_gate_prep_opt.restype = i
         lib.mlstm_step_seq_opt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, op, vp]
         lib.mlstm_step_seq_opt.restype = i
+        lib.mlstm_parallel_bwd_workspace_opt.argtypes = [i] * 6 + [op]
+        lib.mlstm_parallel_bwd_workspace_opt.restype = sz
+        lib.mlstm_parallel_bwd_opt.argtypes = [vp] * 15 + [i] * 6 + [vp, sz, op, vp]
+        lib.mlstm_parallel_bwd_opt.restype = i
         lib.mlstm_recurrent_bwd_workspace.argtypes = [i, i, i, i, i]
         lib.mlstm_recurrent_bwd_workspace.restype = sz
         lib.mlstm_recurrent_bwd.argtypes = [vp] * 12 + [i] * 6 + [vp, sz, op, vp]
@@ -287,11 +291,14 @@ def parallel_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_p
 
 def parallel_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: torch.Tensor,
                  fgate_pre: torch.Tensor, dh: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
-                 saved=None):
-    """``mlstm_parallel_bwd``: gradients (dq, dk, dv, d_igate, d_fgate) of the
-    parallel forward for the output gradient dh = dL/dH~ (CUDA tensors).
-    ``saved`` = (h, n, b) from ``parallel_fwd(..., return_stats=True)`` on the
-    same inputs (``mlstm_parallel_bwd_saved``) lets the tensor-core path skip
+                 saved=None, ogate: Optional[torch.Tensor] = None, forget: str = "sigmoid"):
+    """``mlstm_parallel_bwd`` / ``mlstm_parallel_bwd_opt``: gradients (dq, dk,
+    dv, d_igate, d_fgate) of the parallel forward for the output gradient dh
+    (CUDA tensors); with ``ogate`` (the output-gate pre-activations
+    [B,H,T,d_v], forward h = sigmoid(ogate) * H~) dh is dL/dh and d_ogate is
+    returned sixth.  ``forget`` selects the forget activation ("sigmoid" or
+    "exp").  ``saved`` = (h, n, b) from ``parallel_fwd(..., return_stats=True)``
+    without an output gate, on the same inputs, lets the tensor-core path skip
     its forward pass."""
     lib = library()
     B, H, T, dqk = q.shape
@@ -307,27 +314,29 @@ def parallel_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, igate_pre: t
     _need(igate_pre, "igate_pre", (B, H, T), torch.float32, dev)
     _need(fgate_pre, "fgate_pre", (B, H, T), torch.float32, dev)
     _need(dh, "dh", (B, H, T, dv), q.dtype, dev)
-    need = int(lib.mlstm_parallel_bwd_workspace_ex(B, H, T, dqk, dv, _DTYPES[q.dtype]))
+    if ogate is not None:
+        _need(ogate, "ogate", (B, H, T, dv), q.dtype, dev)
+    opt = _options(forget=forget, ogate=ogate)
+    need = int(lib.mlstm_parallel_bwd_workspace_opt(B, H, T, dqk, dv, _DTYPES[q.dtype], ctypes.byref(opt)))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dig, dfg = torch.empty_like(igate_pre), torch.empty_like(fgate_pre)
+    dog = torch.empty_like(dh) if ogate is not None else None
+    hs = ns = bs = None
     if saved is not None:
         hs, ns, bs = saved
         _need(hs, "saved h", (B, H, T, dv), q.dtype, dev)
         _need(ns, "saved n", (B, H, T), torch.float32, dev)
         _need(bs, "saved b", (B, H, T), torch.float32, dev)
-        rc = lib.mlstm_parallel_bwd_saved(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh),
-                                          _ptr(hs), _ptr(ns), _ptr(bs), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(dig),
-                                          _ptr(dfg), B, H, T, dqk, dv, _DTYPES[q.dtype], _ptr(workspace),
-                                          workspace.numel() * workspace.element_size(), _stream(dev))
-    else:
-        rc = lib.mlstm_parallel_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh),
-                                    _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(dig), _ptr(dfg), B, H, T, dqk, dv,
-                                    _DTYPES[q.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                    _stream(dev))
+    rc = lib.mlstm_parallel_bwd_opt(_ptr(q), _ptr(k), _ptr(v), _ptr(igate_pre), _ptr(fgate_pre), _ptr(dh),
+                                    _ptr(hs), _ptr(ns), _ptr(bs), _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(dig),
+                                    _ptr(dfg), _ptr(dog), B, H, T, dqk, dv, _DTYPES[q.dtype], _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), ctypes.byref(opt), _stream(dev))
     if rc != 0:
-        raise MlstmError(rc, "mlstm_parallel_bwd")
+        raise MlstmError(rc, "mlstm_parallel_bwd_opt")
+    if ogate is not None:
+        return dq, dk, dvv, dig, dfg, dog
     return dq, dk, dvv, dig, dfg
 
 

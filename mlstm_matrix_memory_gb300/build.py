@@ -67,10 +67,8 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
     tmp = f"{OUT}.tmp{os.getpid()}"
-    # cuBLAS serves the plain batched GEMMs of the backward pass
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
-    r = subprocess.run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lcublas",
-                        f"-Xlinker=-rpath={cuda_lib}"], capture_output=True, text=True)
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs], capture_output=True,
+                       text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, OUT)

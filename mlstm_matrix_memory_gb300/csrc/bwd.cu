@@ -13,14 +13,15 @@
 // stabilizer m is a constant, as on the pages.  S and dC stay in fp32 (in
 // bf16 the cancellation in dC/n + db costs dq about 3 % at T = 300: measured).
 //
-// The five T x T products are plain batched GEMMs (cuBLAS, tensor cores for
-// bf16); the elementwise work between them is one kernel of this file: a warp
-// per query row recomputes D' from the gate terms, forms C~', b, n, dn, db,
-// writes G and P = C~'/n (zero above the diagonal), the row sums of dD~ and
-// per-block column sums.  A last kernel turns the row and column sums into
-// the gate gradients with suffix sums.  Every T x T matrix is materialised in
-// the workspace, for all heads at once.
-#include <cublas_v2.h>
+// CUDA-core path (fp32, and bf16 shapes the tensor-core kernels do not
+// tile): the five T x T products run in one batched GEMM kernel of this file
+// (fp32 accumulation), each over its causal part only; the elementwise work
+// between them is a second kernel: a warp per query row recomputes D' from
+// the gate terms, forms C~', b, n, dn, db, writes G and P = C~'/n (zero above
+// the diagonal), the row sums of dD~ and per-block column sums.  A last
+// kernel turns the row and column sums into the gate gradients with suffix
+// sums.  Every T x T matrix is materialised in the workspace, for all heads
+// at once.
 
 #include <algorithm>
 #include <cstdlib>
@@ -130,12 +131,12 @@ __global__ void bwd_colsum_kernel(const float* __restrict__ Cpart, float* __rest
   Ccol[x] = c;
 }
 
-// Gate gradients of one head (one CTA): column sums from the block partials,
-// then d i~_k = Ccol_k and d fbar_k = sum_{i>=k} R_i - sum_{j>=k} Ccol_j
-// (the rows >= k minus the columns >= k of the lower triangle), in fp64.
+// Gate gradients of one head (one CTA): d i~_k = Ccol_k and d log f_k =
+// sum_{i>=k} R_i - sum_{j>=k} Ccol_j (the rows >= k minus the columns >= k of
+// the lower triangle), in fp64, times d log f / d f~.
 __global__ void __launch_bounds__(1024)
 bwd_gates_kernel(const float* __restrict__ R, const float* __restrict__ Ccol, const float* __restrict__ fg,
-                 float* __restrict__ dig, float* __restrict__ dfg, int T) {
+                 float* __restrict__ dig, float* __restrict__ dfg, int T, int forget_exp) {
   __shared__ double sh[32];
   const int bh = blockIdx.x;
   const size_t hb = (size_t)bh * T;
@@ -167,38 +168,127 @@ bwd_gates_kernel(const float* __restrict__ R, const float* __restrict__ Ccol, co
     const double c = Ccol[hb + t];
     after += (double)R[hb + t] - c;    // now the suffix from t
     dig[hb + t] = (float)c;
-    dfg[hb + t] = (float)(after * (double)sigmoid(-fg[hb + t]));    // sigma(-f~) d fbar (eq 104)
+    // d f~ = (d log f / d f~) d log f: sigma(-f~) for log f = log sigmoid(f~)
+    // (eq 104), 1 for the exponential activation log f = f~ (eq 70's gamma = exp)
+    dfg[hb + t] = (float)(after * (forget_exp ? 1.0 : (double)sigmoid(-fg[hb + t])));
   }
 }
 
-struct Blas {
-  cublasHandle_t h = nullptr;
-};
-Blas g_blas[64];
-std::mutex g_blas_mu;
+// ---------------------------------------------------------------- batched GEMM (CUDA cores)
+// Row-major C[m][n] = alpha sum_k opA(m, k) opB(k, n) for every head b of a
+// batch, fp32 accumulation: opA(m, k) = A[m][k] (TA: A[k][m]), opB(k, n) =
+// B[k][n] (TB: B[n][k]).  The products of eqs (82), (87), (98)-(100) use only
+// the causal part of a T x T operand, which `causal` restricts to:
+//   kLowerOut  output tiles with some n <= m (S, dC: read for j <= i only;
+//              tiles wholly above the diagonal are not written),
+//   kKUpToM    k <= m (dQ = s G K: G[i][j] = 0 for j > i),
+//   kKFromM    k >= m (dK = s G^T Q, dV = P^T dH: G, P zero above the diagonal).
+// 64 x 64 output tiles, 16-deep k steps through shared memory, 256 threads,
+// a 4 x 4 block of outputs per thread.
+enum Causal : int { kFull = 0, kLowerOut = 1, kKUpToM = 2, kKFromM = 3 };
+constexpr int kGBM = 64, kGBN = 64, kGBK = 16;
 
-cublasHandle_t blas_handle() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(g_blas_mu);
-  if (!g_blas[dev].h && cublasCreate(&g_blas[dev].h) != CUBLAS_STATUS_SUCCESS) g_blas[dev].h = nullptr;
-  return g_blas[dev].h;
+template <typename EA, typename EB, typename EC, bool TA, bool TB, int CAUSAL>
+__global__ void __launch_bounds__(256)
+gemm_kernel(const EA* __restrict__ A, const EB* __restrict__ B, EC* __restrict__ C, int M, int N, int K, int lda,
+            int ldb, int ldc, long long sA, long long sB, long long sC, float alpha, int tiles_m, int tiles_n) {
+  __shared__ float As[kGBK][kGBM + 4];
+  __shared__ float Bs[kGBK][kGBN + 4];
+  const long long tiles = (long long)tiles_m * tiles_n;
+  const long long bid = blockIdx.x;
+  const int b = (int)(bid / tiles);
+  const int tile = (int)(bid % tiles);
+  const int m0 = (tile / tiles_n) * kGBM, n0 = (tile % tiles_n) * kGBN;
+  if (CAUSAL == kLowerOut && n0 > m0 + kGBM - 1) return;          // wholly above the diagonal
+  const int k_lo = CAUSAL == kKFromM ? (m0 / kGBK) * kGBK : 0;
+  const int k_hi = CAUSAL == kKUpToM ? min(K, m0 + kGBM) : K;
+  A += (size_t)b * sA;
+  B += (size_t)b * sB;
+  C += (size_t)b * sC;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;          // 16 x 16 threads, 4 x 4 outputs each
+  float acc[4][4] = {};
+  for (int k0 = k_lo; k0 < k_hi; k0 += kGBK) {
+    // stage a 16 x 64 slab of opA (k x m) and of opB (k x n): 1024 values each, 4 per thread
+    for (int e = threadIdx.x; e < kGBK * kGBM; e += 256) {
+      int kk, mm;
+      if (TA) { mm = e % kGBM; kk = e / kGBM; } else { kk = e % kGBK; mm = e / kGBK; }
+      const int gk = k0 + kk, gm = m0 + mm;
+      float x = 0.0f;
+      if (gk < k_hi && gm < M) x = Elem<EA>::load(A, TA ? (size_t)gk * lda + gm : (size_t)gm * lda + gk);
+      As[kk][mm] = x;
+    }
+    for (int e = threadIdx.x; e < kGBK * kGBN; e += 256) {
+      int kk, nn;
+      if (TB) { kk = e % kGBK; nn = e / kGBK; } else { nn = e % kGBN; kk = e / kGBN; }
+      const int gk = k0 + kk, gn = n0 + nn;
+      float x = 0.0f;
+      if (gk < k_hi && gn < N) x = Elem<EB>::load(B, TB ? (size_t)gn * ldb + gk : (size_t)gk * ldb + gn);
+      Bs[kk][nn] = x;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kGBK; ++kk) {
+      float a[4], bb[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = As[kk][ty * 4 + r];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bb[c] = Bs[kk][tx * 4 + c];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], bb[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int gm = m0 + ty * 4 + r;
+    if (gm >= M) continue;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int gn = n0 + tx * 4 + c;
+      if (gn < N) Elem<EC>::store(C, (size_t)gm * ldc + gn, alpha * acc[r][c]);
+    }
+  }
 }
 
-// Column-major batched GEMM C = op(A) op(B) (the row-major products of this
-// file are expressed through their transposes).
-bool gemm(cublasHandle_t h, cublasOperation_t ta, cublasOperation_t tb, int m, int n, int k, float alpha,
-          const void* A, cudaDataType ta_t, int lda, long long sa, const void* B, cudaDataType tb_t, int ldb,
-          long long sb, void* C, cudaDataType tc_t, int ldc, long long sc, int batch) {
-  const float beta = 0.0f;
-  return cublasGemmStridedBatchedEx(h, ta, tb, m, n, k, &alpha, A, ta_t, lda, sa, B, tb_t, ldb, sb, &beta, C, tc_t,
-                                    ldc, sc, batch, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+template <typename EA, typename EB, typename EC, bool TA, bool TB, int CAUSAL>
+bool gemm(const void* A, const void* B, void* C, int M, int N, int K, int lda, int ldb, int ldc, long long sA,
+          long long sB, long long sC, float alpha, int batch, cudaStream_t st) {
+  const int tm = (M + kGBM - 1) / kGBM, tn = (N + kGBN - 1) / kGBN;
+  const long long blocks = (long long)batch * tm * tn;
+  if (blocks > 0x7fffffffLL) return false;
+  gemm_kernel<EA, EB, EC, TA, TB, CAUSAL><<<(unsigned)blocks, 256, 0, st>>>(
+      static_cast<const EA*>(A), static_cast<const EB*>(B), static_cast<EC*>(C), M, N, K, lda, ldb, ldc, sA, sB, sC,
+      alpha, tm, tn);
+  return cudaGetLastError() == cudaSuccess;
 }
 
-int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
-                const void* dh, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int BH, int T, int d_qk,
-                int d_v, void* workspace, cudaStream_t st, const void* h_saved = nullptr,
-                const float* n_saved = nullptr, const float* b_saved = nullptr);
+// The five products of the CUDA-core path for element type E (q, k, v, dh,
+// G, P, dq, dk, dv), S and dC in fp32.
+template <typename E>
+bool bwd_products_simt(const void* q, const void* k, const void* v, const void* dh, float* S, float* dC,
+                       const void* G, const void* P, void* dq, void* dk, void* dv, int BH, int T, int d_qk, int d_v,
+                       float s, cudaStream_t st, bool first_half) {
+  const long long TT = (long long)T * T, Tq = (long long)T * d_qk, Tv = (long long)T * d_v;
+  if (first_half) {
+    // S = s Q K^T (82) and dC = dH V^T (87), their lower triangles
+    return gemm<E, E, float, false, true, kLowerOut>(q, k, S, T, T, d_qk, d_qk, d_qk, T, Tq, Tq, TT, s, BH, st) &&
+           gemm<E, E, float, false, true, kLowerOut>(dh, v, dC, T, T, d_v, d_v, d_v, T, Tv, Tv, TT, 1.0f, BH, st);
+  }
+  // dQ = s G K (98), dK = s G^T Q (99), dV = P^T dH (100) over the lower triangle of G, P
+  return gemm<E, E, E, false, false, kKUpToM>(G, k, dq, T, d_qk, T, T, d_qk, d_qk, TT, Tq, Tq, s, BH, st) &&
+         gemm<E, E, E, true, false, kKFromM>(G, q, dk, T, d_qk, T, T, d_qk, d_qk, TT, Tq, Tq, s, BH, st) &&
+         gemm<E, E, E, true, false, kKFromM>(P, dh, dv, T, d_v, T, T, d_v, d_v, TT, Tv, Tv, 1.0f, BH, st);
+}
+
+// The tensor-core path (defined at the end of this file).  Gate terms are in
+// `gate_ws` already; dh is dL/dH~; the forward's H~ goes to (or, saved, is
+// read from) `*hf_out`.
+int bwd_tc_path(const void* q, const void* k, const void* v, const float* fgate_pre, const void* dh, void* dq,
+                void* dk, void* dv, float* d_igate, float* d_fgate, int BH, int T, int d_qk, int d_v,
+                void* workspace, cudaStream_t st, int forget_exp, const void* h_saved, const float* n_saved,
+                const float* b_saved, const void** hf_out);
 
 // Workspace of the tensor-core path: gate terms, the forward's H~ (d_v
 // columns) and row statistics, bf16 G and P with rows of ldT = T rounded up
@@ -238,13 +328,153 @@ bool use_tc_path(int T, int dqk, int dv, int dtype) {
 
 using namespace mlstm;
 
+namespace {
+
+// Extra workspace of the options, after the path's own layout: dL/dH~ of an
+// output gate, and (CUDA-core path) the forward's H~, which the output-gate
+// gradient needs.
+size_t og_extra(long long BH, int T, int d_v, int dtype, bool tc, const mlstm_options* opt) {
+  if (!opt || !opt->ogate_pre) return 0;
+  const size_t es = dtype == MLSTM_F32 ? 4 : 2;
+  const size_t one = r256((size_t)BH * T * d_v * es);
+  return tc ? one : 2 * one;
+}
+
+// Workspace of the path that will run for these sizes and options, and
+// whether it is the tensor-core path.
+size_t bwd_need(long long BH, int T, int d_qk, int d_v, int dtype, const mlstm_options* opt, bool* tc) {
+  *tc = use_tc_path(T, d_qk, d_v, dtype);
+  const size_t base = *tc ? tc_layout(BH, T, d_v).total : bwd_layout(BH, T, dtype).total;
+  return base + og_extra(BH, T, d_v, dtype, *tc, opt);
+}
+
+// The parallel backward for every entry point (part 28/30 eqs 87-105; the
+// output gate of eq 78 and the forget activation of eq 70 from `opt`).
+int bwd_impl(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
+             const void* dh, const void* h_saved, const float* n_saved, const float* b_saved, void* dq, void* dk,
+             void* dv, float* d_igate, float* d_fgate, void* d_ogate, int B, int H, int T, int d_qk, int d_v,
+             int dtype, void* workspace, size_t workspace_bytes, const mlstm_options* opt, void* stream) {
+  if (B < 0 || H < 0 || T < 0 || T > kMaxBwdT) return MLSTM_EINVAL;
+  if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
+  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
+  const long long BH = (long long)B * H;
+  if (BH > (1 << 20)) return MLSTM_EINVAL;
+  if (BH == 0 || T == 0) return MLSTM_OK;
+  if (!q || !k || !v || !igate_pre || !fgate_pre || !dh || !dq || !dk || !dv || !d_igate || !d_fgate)
+    return MLSTM_EINVAL;
+  const void* og = opt ? opt->ogate_pre : nullptr;
+  if (og && !d_ogate) return MLSTM_EINVAL;
+  const int fexp = opt ? opt->forget_exp : 0;
+  if (!workspace) return MLSTM_EWORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLSTM_EALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bool tc = false;
+  size_t need = bwd_need(BH, T, d_qk, d_v, dtype, opt, &tc);
+  if (tc && workspace_bytes < need) {            // too small for the tensor-core path: the CUDA-core one
+    tc = false;
+    need = bwd_layout(BH, T, dtype).total + og_extra(BH, T, d_v, dtype, false, opt);
+  }
+  if (workspace_bytes < need) return MLSTM_EWORKSPACE;
+  char* w = static_cast<char*>(workspace);
+  const size_t base = tc ? tc_layout(BH, T, d_v).total : bwd_layout(BH, T, dtype).total;
+  const size_t es = dtype == MLSTM_F32 ? 4 : 2;
+  const size_t vbytes = r256((size_t)BH * T * d_v * es);
+  const long long nv = BH * T * d_v;
+
+  // output gate: the core works on dL/dH~ = dL/dh (.) sigmoid(o~)     (78)
+  const void* dht = dh;
+  if (og) {
+    if (launch_ogate_bwd_in(dh, og, w + base, nv, dtype, st) != cudaSuccess) return MLSTM_ECUDA;
+    dht = w + base;
+  }
+  // gate terms of eqs (79)-(81) with the chosen forget activation: a2, p2, m
+  const size_t gate_bytes = mlstm_parallel_fwd_workspace(1, (int)BH, T);
+  int rc = mlstm_gate_prep_opt(igate_pre, fgate_pre, 1, (int)BH, T, w, gate_bytes, opt, stream);
+  if (rc != MLSTM_OK) return rc;
+  const size_t arr = gate_bytes / 3;           // three arrays of equal, 256-aligned size
+  GateTerms g{reinterpret_cast<float*>(w), reinterpret_cast<float*>(w + arr), reinterpret_cast<float*>(w + 2 * arr)};
+  const bool saved = h_saved && n_saved && b_saved;
+  const void* ht = saved ? h_saved : nullptr;   // H~ of the forward, for the output-gate gradient
+
+  if (tc) {
+    rc = bwd_tc_path(q, k, v, fgate_pre, dht, dq, dk, dv, d_igate, d_fgate, (int)BH, T, d_qk, d_v, workspace, st,
+                     fexp, saved ? h_saved : nullptr, saved ? n_saved : nullptr, saved ? b_saved : nullptr, &ht);
+    if (rc != MLSTM_OK) return rc;
+  } else {
+    const BwdLayout L = bwd_layout(BH, T, dtype);
+    char* S = w + L.gate;
+    char* dC = S + L.S;
+    char* G = dC + L.dC;
+    char* P = G + L.G;
+    float* R = reinterpret_cast<float*>(P + L.P);
+    float* Cpart = reinterpret_cast<float*>(reinterpret_cast<char*>(R) + L.R);
+    float* Ccol = reinterpret_cast<float*>(reinterpret_cast<char*>(Cpart) + L.Cpart);
+    const float s = (float)(1.0 / sqrt((double)d_qk));
+    const bool f32 = dtype == MLSTM_F32;
+    // S = s Q K^T (82) and dC = dH~ V^T (87) over the lower triangle
+    if (!(f32 ? bwd_products_simt<float>(q, k, v, dht, (float*)S, (float*)dC, G, P, dq, dk, dv, (int)BH, T, d_qk,
+                                         d_v, s, st, true)
+              : bwd_products_simt<__nv_bfloat16>(q, k, v, dht, (float*)S, (float*)dC, G, P, dq, dk, dv, (int)BH, T,
+                                                 d_qk, d_v, s, st, true)))
+      return MLSTM_ECUDA;
+    const int nblk = L.nblk;
+    const size_t smem = (size_t)T * sizeof(float);
+    if (f32) {
+      if (cudaFuncSetAttribute(bwd_rows_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+        return MLSTM_ECUDA;
+      bwd_rows_kernel<float><<<(unsigned)(BH * nblk), kRowsPerCta * 32, smem, st>>>(
+          reinterpret_cast<const float*>(S), reinterpret_cast<const float*>(dC), g, reinterpret_cast<float*>(G),
+          reinterpret_cast<float*>(P), R, Cpart, T, nblk);
+    } else {
+      if (cudaFuncSetAttribute(bwd_rows_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem) != cudaSuccess)
+        return MLSTM_ECUDA;
+      bwd_rows_kernel<__nv_bfloat16><<<(unsigned)(BH * nblk), kRowsPerCta * 32, smem, st>>>(
+          reinterpret_cast<const float*>(S), reinterpret_cast<const float*>(dC), g,
+          reinterpret_cast<__nv_bfloat16*>(G), reinterpret_cast<__nv_bfloat16*>(P), R, Cpart, T, nblk);
+    }
+    if (cudaGetLastError() != cudaSuccess) return MLSTM_ECUDA;
+    // dQ = s G K (98), dK = s G^T Q (99), dV = P^T dH~ (100) over the lower triangle of G, P
+    if (!(f32 ? bwd_products_simt<float>(q, k, v, dht, (float*)S, (float*)dC, G, P, dq, dk, dv, (int)BH, T, d_qk,
+                                         d_v, s, st, false)
+              : bwd_products_simt<__nv_bfloat16>(q, k, v, dht, (float*)S, (float*)dC, G, P, dq, dk, dv, (int)BH, T,
+                                                 d_qk, d_v, s, st, false)))
+      return MLSTM_ECUDA;
+    const long long ncol = BH * T;
+    bwd_colsum_kernel<<<(unsigned)((ncol + 255) / 256), 256, 0, st>>>(Cpart, Ccol, T, nblk, ncol);
+    bwd_gates_kernel<<<(unsigned)BH, 1024, 0, st>>>(R, Ccol, fgate_pre, d_igate, d_fgate, T, fexp);
+    if (cudaGetLastError() != cudaSuccess) return MLSTM_ECUDA;
+    if (og && !ht) {
+      // the forward's H~ (eqs 79-86) for the output-gate gradient
+      FwdArgs fa;
+      fa.q = q; fa.k = k; fa.v = v; fa.h = w + base + vbytes; fa.m_out = nullptr; fa.n_out = nullptr;
+      fa.g = g; fa.BH = (int)BH; fa.T = T; fa.dqk = d_qk; fa.dv = d_v; fa.dtype = dtype; fa.scale = s;
+      if (!current_status(&fa.st)) return MLSTM_ECUDA;
+      rc = launch_fwd_tc(fa, st);
+      if (rc == kUnsupported) rc = launch_fwd_simt(fa, st) == cudaSuccess ? kOk : kCuda;
+      if (rc != kOk) return rc;
+      ht = fa.h;
+    }
+  }
+  // dL/do~ = dL/dh (.) H~ (.) sigmoid'(o~)                              (78), (70)
+  if (og && launch_ogate_bwd_out(dh, og, ht, d_ogate, nv, dtype, st) != cudaSuccess) return MLSTM_ECUDA;
+  return MLSTM_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
-size_t mlstm_parallel_bwd_workspace_ex(int B, int H, int T, int d_qk, int d_v, int dtype) {
+size_t mlstm_parallel_bwd_workspace_opt(int B, int H, int T, int d_qk, int d_v, int dtype, const mlstm_options* opt) {
   if (B <= 0 || H <= 0 || T <= 0 || T > kMaxBwdT || d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return 0;
   if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return 0;
-  if (use_tc_path(T, d_qk, d_v, dtype)) return tc_layout((long long)B * H, T, d_v).total;
-  return bwd_layout((long long)B * H, T, dtype).total;
+  bool tc = false;
+  return bwd_need((long long)B * H, T, d_qk, d_v, dtype, opt, &tc);
+}
+
+size_t mlstm_parallel_bwd_workspace_ex(int B, int H, int T, int d_qk, int d_v, int dtype) {
+  return mlstm_parallel_bwd_workspace_opt(B, H, T, d_qk, d_v, dtype, nullptr);
 }
 
 size_t mlstm_parallel_bwd_workspace(int B, int H, int T, int dtype) {
@@ -256,106 +486,28 @@ size_t mlstm_parallel_bwd_workspace(int B, int H, int T, int dtype) {
 int mlstm_parallel_bwd(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
                        const void* dh, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int B, int H,
                        int T, int d_qk, int d_v, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  if (B < 0 || H < 0 || T < 0 || T > kMaxBwdT) return MLSTM_EINVAL;
-  if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
-  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
-  const long long BH = (long long)B * H;
-  if (BH > (1 << 20)) return MLSTM_EINVAL;
-  if (BH == 0 || T == 0) return MLSTM_OK;
-  if (!q || !k || !v || !igate_pre || !fgate_pre || !dh || !dq || !dk || !dv || !d_igate || !d_fgate)
-    return MLSTM_EINVAL;
-  if (!workspace) return MLSTM_EWORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLSTM_EALIGN;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (use_tc_path(T, d_qk, d_v, dtype) && workspace_bytes >= tc_layout(BH, T, d_v).total)
-    return bwd_tc_path(q, k, v, igate_pre, fgate_pre, dh, dq, dk, dv, d_igate, d_fgate, (int)BH, T, d_qk, d_v,
-                       workspace, st);
-  if (workspace_bytes < mlstm_parallel_bwd_workspace(B, H, T, dtype)) return MLSTM_EWORKSPACE;
-  const BwdLayout L = bwd_layout(BH, T, dtype);
-  char* w = static_cast<char*>(workspace);
-  char* gate_ws = w;
-  char* S = w + L.gate;
-  char* dC = w + L.gate + L.S;
-  char* G = w + L.gate + L.S + L.dC;
-  char* P = G + L.G;
-  float* R = reinterpret_cast<float*>(P + L.P);
-  float* Cpart = reinterpret_cast<float*>(reinterpret_cast<char*>(R) + L.R);
-  float* Ccol = reinterpret_cast<float*>(reinterpret_cast<char*>(Cpart) + L.Cpart);
-
-  // gate terms of eqs (79)-(81): a2, p2, m
-  int rc = mlstm_gate_prep(igate_pre, fgate_pre, 1, (int)BH, T, gate_ws, L.gate, stream);
-  if (rc != MLSTM_OK) return rc;
-  const long long BHT = BH * T;
-  const size_t arr = (L.gate) / 3;           // three arrays of equal, 256-aligned size
-  GateTerms g{reinterpret_cast<float*>(gate_ws), reinterpret_cast<float*>(gate_ws + arr),
-              reinterpret_cast<float*>(gate_ws + 2 * arr)};
-  (void)BHT;
-
-  cublasHandle_t h = blas_handle();
-  if (!h || cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return MLSTM_ECUDA;
-  const cudaDataType et = dtype == MLSTM_F32 ? CUDA_R_32F : CUDA_R_16BF;
-  const float s = (float)(1.0 / sqrt((double)d_qk));
-  const long long TT = (long long)T * T, Tq = (long long)T * d_qk, Tv = (long long)T * d_v;
-  const int nb = (int)BH;
-  // row-major S = s Q K^T  <=>  col-major S^T = s K Q^T
-  if (!gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, T, T, d_qk, s, k, et, d_qk, Tq, q, et, d_qk, Tq, S, CUDA_R_32F, T, TT, nb))
-    return MLSTM_ECUDA;
-  // row-major dC = dH V^T  (87)
-  if (!gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, T, T, d_v, 1.0f, v, et, d_v, Tv, dh, et, d_v, Tv, dC, CUDA_R_32F, T, TT, nb))
-    return MLSTM_ECUDA;
-  const int nblk = L.nblk;
-  const size_t smem = (size_t)T * sizeof(float);
-  if (dtype == MLSTM_F32) {
-    if (cudaFuncSetAttribute(bwd_rows_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return MLSTM_ECUDA;
-    bwd_rows_kernel<float><<<(unsigned)(BH * nblk), kRowsPerCta * 32, smem, st>>>(
-        reinterpret_cast<const float*>(S), reinterpret_cast<const float*>(dC), g, reinterpret_cast<float*>(G),
-        reinterpret_cast<float*>(P), R, Cpart, T, nblk);
-  } else {
-    if (cudaFuncSetAttribute(bwd_rows_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return MLSTM_ECUDA;
-    bwd_rows_kernel<__nv_bfloat16><<<(unsigned)(BH * nblk), kRowsPerCta * 32, smem, st>>>(
-        reinterpret_cast<const float*>(S), reinterpret_cast<const float*>(dC), g,
-        reinterpret_cast<__nv_bfloat16*>(G), reinterpret_cast<__nv_bfloat16*>(P), R, Cpart, T, nblk);
-  }
-  if (cudaGetLastError() != cudaSuccess) return MLSTM_ECUDA;
-  // row-major dQ = s G K  <=>  col-major dQ^T = s K^T G^T          (98)
-  if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_N, d_qk, T, T, s, k, et, d_qk, Tq, G, et, T, TT, dq, et, d_qk, Tq, nb))
-    return MLSTM_ECUDA;
-  // row-major dK = s G^T Q  <=>  col-major dK^T = s Q^T G          (99)
-  if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, d_qk, T, T, s, q, et, d_qk, Tq, G, et, T, TT, dk, et, d_qk, Tq, nb))
-    return MLSTM_ECUDA;
-  // row-major dV = P^T dH  <=>  col-major dV^T = dH^T P            (100)
-  if (!gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, d_v, T, T, 1.0f, dh, et, d_v, Tv, P, et, T, TT, dv, et, d_v, Tv, nb))
-    return MLSTM_ECUDA;
-  const long long ncol = BH * T;
-  bwd_colsum_kernel<<<(unsigned)((ncol + 255) / 256), 256, 0, st>>>(Cpart, Ccol, T, nblk, ncol);
-  bwd_gates_kernel<<<(unsigned)BH, 1024, 0, st>>>(R, Ccol, fgate_pre, d_igate, d_fgate, T);
-  return cudaGetLastError() == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
+  return bwd_impl(q, k, v, igate_pre, fgate_pre, dh, nullptr, nullptr, nullptr, dq, dk, dv, d_igate, d_fgate, nullptr,
+                  B, H, T, d_qk, d_v, dtype, workspace, workspace_bytes, nullptr, stream);
 }
 
 int mlstm_parallel_bwd_saved(const void* q, const void* k, const void* v, const float* igate_pre,
                              const float* fgate_pre, const void* dh, const void* h, const float* n, const float* b,
                              void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int B, int H, int T,
                              int d_qk, int d_v, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  if (B < 0 || H < 0 || T < 0 || T > kMaxBwdT) return MLSTM_EINVAL;
-  if (d_qk < 1 || d_v < 1 || d_qk > 512 || d_v > 512) return MLSTM_EINVAL;
-  if (dtype != MLSTM_F32 && dtype != MLSTM_BF16) return MLSTM_EDTYPE;
-  const long long BH = (long long)B * H;
-  if (BH > (1 << 20)) return MLSTM_EINVAL;
-  if (BH == 0 || T == 0) return MLSTM_OK;
   if (!h || !n || !b) return MLSTM_EINVAL;
-  if (!q || !k || !v || !igate_pre || !fgate_pre || !dh || !dq || !dk || !dv || !d_igate || !d_fgate)
-    return MLSTM_EINVAL;
-  if (!workspace) return MLSTM_EWORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return MLSTM_EALIGN;
-  if (use_tc_path(T, d_qk, d_v, dtype) && workspace_bytes >= tc_layout(BH, T, d_v).total)
-    return bwd_tc_path(q, k, v, igate_pre, fgate_pre, dh, dq, dk, dv, d_igate, d_fgate, (int)BH, T, d_qk, d_v,
-                       workspace, static_cast<cudaStream_t>(stream), h, n, b);
-  return mlstm_parallel_bwd(q, k, v, igate_pre, fgate_pre, dh, dq, dk, dv, d_igate, d_fgate, B, H, T, d_qk, d_v,
-                            dtype, workspace, workspace_bytes, stream);
+  return bwd_impl(q, k, v, igate_pre, fgate_pre, dh, h, n, b, dq, dk, dv, d_igate, d_fgate, nullptr, B, H, T, d_qk,
+                  d_v, dtype, workspace, workspace_bytes, nullptr, stream);
+}
+
+int mlstm_parallel_bwd_opt(const void* q, const void* k, const void* v, const float* igate_pre,
+                           const float* fgate_pre, const void* dh, const void* h_saved, const float* n_saved,
+                           const float* b_saved, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate,
+                           void* d_ogate, int B, int H, int T, int d_qk, int d_v, int dtype, void* workspace,
+                           size_t workspace_bytes, const mlstm_options* opt, void* stream) {
+  const int nsaved = (h_saved != nullptr) + (n_saved != nullptr) + (b_saved != nullptr);
+  if (nsaved != 0 && nsaved != 3) return MLSTM_EINVAL;
+  return bwd_impl(q, k, v, igate_pre, fgate_pre, dh, h_saved, n_saved, b_saved, dq, dk, dv, d_igate, d_fgate,
+                  d_ogate, B, H, T, d_qk, d_v, dtype, workspace, workspace_bytes, opt, stream);
 }
 
 }  // extern "C"
@@ -363,13 +515,13 @@ int mlstm_parallel_bwd_saved(const void* q, const void* k, const void* v, const 
 namespace mlstm {
 namespace {
 
-// Tensor-core path: gate pass, forward (H~, n, signed b), the tile kernel
-// (G, P, row and column sums of dD~), the three products dQ, dK, dV over the
-// lower triangle of G and P, the gate gradients.
-int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_pre, const float* fgate_pre,
-                const void* dh, void* dq, void* dk, void* dv, float* d_igate, float* d_fgate, int BH, int T, int d_qk,
-                int d_v, void* workspace, cudaStream_t st, const void* h_saved, const float* n_saved,
-                const float* b_saved) {
+// Tensor-core path: the forward (H~, n, signed b) unless given, the tile
+// kernel (G, P, row and column sums of dD~), the three products dQ, dK, dV
+// over the lower triangle of G and P, the gate gradients.
+int bwd_tc_path(const void* q, const void* k, const void* v, const float* fgate_pre, const void* dh, void* dq,
+                void* dk, void* dv, float* d_igate, float* d_fgate, int BH, int T, int d_qk, int d_v,
+                void* workspace, cudaStream_t st, int forget_exp, const void* h_saved, const float* n_saved,
+                const float* b_saved, const void** hf_out) {
   const TcLayout L = tc_layout(BH, T, d_v);
   char* w = static_cast<char*>(workspace);
   char* gate_ws = w;
@@ -385,8 +537,7 @@ int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_
   float* R = reinterpret_cast<float*>(reinterpret_cast<char*>(Cpart) + L.part);
   float* Ccol = reinterpret_cast<float*>(reinterpret_cast<char*>(R) + L.R);
 
-  int rc = mlstm_gate_prep(igate_pre, fgate_pre, 1, BH, T, gate_ws, L.gate, st);
-  if (rc != MLSTM_OK) return rc;
+  // the gate terms are in the workspace already (the caller's gate pass)
   const size_t arr = L.gate / 3;
   GateTerms g{reinterpret_cast<float*>(gate_ws), reinterpret_cast<float*>(gate_ws + arr),
               reinterpret_cast<float*>(gate_ws + 2 * arr)};
@@ -394,6 +545,7 @@ int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_
   if (!current_status(&ds)) return MLSTM_ECUDA;
   const float s = (float)(1.0 / sqrt((double)d_qk));
   const bool saved = h_saved && n_saved && b_saved;
+  int rc;
   if (!saved) {
     // forward: H~, n and the signed row sums b (eqs 79-86)
     FwdArgs fa;
@@ -403,6 +555,7 @@ int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_
     if (rc == kUnsupported) rc = launch_fwd_simt(fa, st) == cudaSuccess ? kOk : kCuda;
     if (rc != kOk) return rc;
   }
+  *hf_out = saved ? h_saved : hf;
   BwdTileArgs ta;
   ta.q = q; ta.k = k; ta.v = v; ta.dh = dh; ta.g = g;
   ta.h = saved ? h_saved : hf;
@@ -419,7 +572,7 @@ int bwd_tc_path(const void* q, const void* k, const void* v, const float* igate_
   pa.BH = BH; pa.T = T; pa.ldT = L.ldT; pa.dqk = d_qk; pa.dv = d_v; pa.scale = s; pa.st = ds;
   rc = launch_bwd_products(pa, st);
   if (rc != kOk) return rc;
-  bwd_gates_kernel<<<(unsigned)BH, 1024, 0, st>>>(R, Ccol, fgate_pre, d_igate, d_fgate, T);
+  bwd_gates_kernel<<<(unsigned)BH, 1024, 0, st>>>(R, Ccol, fgate_pre, d_igate, d_fgate, T, forget_exp);
   return cudaGetLastError() == cudaSuccess ? MLSTM_OK : MLSTM_ECUDA;
 }
 

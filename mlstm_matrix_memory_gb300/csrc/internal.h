@@ -72,6 +72,12 @@ cudaError_t launch_final_state(const void* k, const void* v, GateTerms g, float*
 // h *= sigmoid(o) elementwise (the output gate, eq 78), for the kernels that
 // do not apply it in their epilogue.
 cudaError_t launch_apply_ogate(void* h, const void* og, long long n, int dtype, cudaStream_t stream);
+// Backward of the output gate (ogate.cu): dht = dh (.) sigmoid(og), and
+// dog = dh (.) ht (.) sigmoid'(og), n elements of dtype each.
+cudaError_t launch_ogate_bwd_in(const void* dh, const void* og, void* dht, long long n, int dtype,
+                                cudaStream_t stream);
+cudaError_t launch_ogate_bwd_out(const void* dh, const void* og, const void* ht, void* dog, long long n, int dtype,
+                                 cudaStream_t stream);
 // 1 when the current device runs tcgen05 code (sm_100 family).
 int device_is_sm100_family();
 

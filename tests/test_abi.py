@@ -187,6 +187,28 @@ def test_parallel_bwd_validation(lib):
     assert saved(T=0) == 0
 
 
+def test_parallel_bwd_opt_validation(lib):
+    from mlstm_matrix_memory_gb300.binding import _Options as Opt
+    plain = Opt(0, 0, None, None)
+    gated = Opt(0, 1, A, None)
+    base = lib.mlstm_parallel_bwd_workspace_opt(2, 3, 100, 64, 64, 1, ctypes.byref(plain))
+    assert base == lib.mlstm_parallel_bwd_workspace_ex(2, 3, 100, 64, 64, 1)
+    with_og = lib.mlstm_parallel_bwd_workspace_opt(2, 3, 100, 64, 64, 1, ctypes.byref(gated))
+    assert with_og >= base + 2 * 3 * 100 * 64 * 2        # at least one [B,H,T,d_v] bf16 buffer more
+    assert lib.mlstm_parallel_bwd_workspace_opt(2, 3, 100, 64, 64, 1, None) == base
+    assert lib.mlstm_parallel_bwd_workspace_opt(2, 3, 100, 64, 600, 1, ctypes.byref(plain)) == 0
+
+    def bo(opt, dog=A, h=None, n=None, b=None, T=100, dt=1, wsb=with_og):
+        return lib.mlstm_parallel_bwd_opt(A, A, A, A, A, A, h, n, b, A, A, A, A, A, dog, 2, 3, T, 64, 64, dt, A,
+                                          wsb, ctypes.byref(opt), None)
+    assert bo(gated, dog=None) == -1          # an output gate needs somewhere for its gradient
+    assert bo(plain, h=A) == -1               # the saved forward outputs come all three or none
+    assert bo(plain, h=A, n=A) == -1
+    assert bo(gated, dt=9) == -3
+    assert bo(gated, T=0) == 0
+    assert bo(gated, wsb=base) == -7          # the path's workspace alone is too small with a gate
+
+
 def test_plain_parallel_validation(lib):
     def pf(q=A, h=A, B=1, T=8, dqk=64, dv=64, dt=1, ws=A, wsb=1 << 20):
         return lib.mlstm_parallel_fwd(q, A, A, A, A, h, None, None, B, 1, T, dqk, dv, dt, ws, wsb, None)
