@@ -598,6 +598,37 @@ bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows) 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [BH, T, d] bf16 viewed as a 4-D tensor (64 columns, T, d / 64 column
+// blocks, BH), so that one box (64 x rows x blocks x 1, 128-byte swizzle)
+// lands as `blocks` consecutive 64-column tiles of rows x 128 bytes: the layout
+// of that many separate 64-column boxes, in one copy.  Rows past T and blocks
+// past d read as zeros.
+bool make_map_blocks(CUtensorMap* m, const void* base, int d, int T, int BH, int rows, int blocks) {
+  EncodeTiled enc = encode_fn();
+  if (!enc || d % 64 != 0) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)T, (cuuint64_t)(d / 64), (cuuint64_t)BH};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, 128, (cuuint64_t)d * 2 * T};
+  cuuint32_t box[4] = {64, (cuuint32_t)rows, (cuuint32_t)blocks, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [BH, rows, cols] fp32 viewed as a 3-D tensor (cols fastest); box = box_cols
+// x box_rows x 1 with 128-byte swizzle (box_cols * 4 <= 128).
+bool make_map_f32(CUtensorMap* m, float* base, int cols, int rows, int BH, int box_cols, int box_rows) {
+  EncodeTiled enc = encode_fn();
+  if (!enc || (cols * 4) % 16 != 0 || box_cols * 4 > 128) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 4, (cuuint64_t)cols * 4 * rows};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_ld(CUtensorMap* m, const void* base, int cols, int rows, int BH, int ld, int box_rows) {
   EncodeTiled enc = encode_fn();
   if (!enc || (ld * 2) % 16 != 0) return false;

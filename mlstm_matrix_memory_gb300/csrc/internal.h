@@ -140,5 +140,10 @@ bool make_map_ld(CUtensorMap* m, const void* base, int cols, int rows, int BH, i
 // 3-D TMA map over a [BH, T, d] bf16 tensor, box 64 x rows x 1, 128-byte
 // swizzle; rows past T read as zeros and are clipped on stores (fwd_tc.cu).
 bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows);
+// [BH, T, d] bf16 as 4-D (64 columns, T, d / 64 blocks, BH): one box is
+// `blocks` consecutive 64-column x rows tiles (128-byte swizzle).
+bool make_map_blocks(CUtensorMap* m, const void* base, int d, int T, int BH, int rows, int blocks);
+// [BH, rows, cols] fp32 (cols fastest), box box_cols x box_rows x 1, 128-byte swizzle.
+bool make_map_f32(CUtensorMap* m, float* base, int cols, int rows, int BH, int box_cols, int box_rows);
 
 }  // namespace mlstm

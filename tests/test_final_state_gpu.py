@@ -40,6 +40,12 @@ SHAPES = [
     (1, 2, 2048, 384, 384, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),
     (8, 4, 256, 384, 384, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # one token range per tile (96 tiles)
     (2, 2, 192, 512, 128, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # d_qk 512: 64 n chunks per tile
+    # how the (tile, 64-token chunk) units fall on the CTAs of a 152-SM part:
+    (76, 4, 128, 64, 128, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # 304 tiles: two whole tiles per CTA
+    (25, 8, 128, 128, 128, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),   # ranges on tile bounds, two pieces per CTA
+    (10, 5, 150, 128, 128, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),   # ranges cut tiles: pieces added in C
+    (2, 3, 500, 128, 192, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # d_v 192: half of the last row tile unused
+    (5, 1, 448, 384, 384, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # three row-tile groups, heads cut between CTAs
 ]
 
 
@@ -79,3 +85,20 @@ def test_prefill_then_generation(M, dtype):
     assert rel_err(C, wC) <= tol
     assert rel_err(n, wn) <= tol
     assert np.max(np.abs(m.cpu().numpy() - wm)) <= 1e-4 * max(1.0, float(np.max(np.abs(wm))))
+
+
+@pytest.mark.parametrize("name", ["mlstm125m_B8_H4_T2048_d384_bf16", "mlstm350m_B4_H4_T2048_d512_bf16"])
+def test_final_state_full_size_sampled_heads(M, name):
+    """The benchmark's hand-off launch at full size (every head computed in one
+    call, heads cut between CTAs and added in C), checked on sampled heads
+    against the oracle's recurrence over those heads' inputs (heads are
+    independent)."""
+    w = W.PARALLEL_WORKLOADS[name]
+    x = W.parallel_inputs(w, 0)
+    C, n, m = final_state(M, to_dev(x))
+    for b, h in ((0, 0), (w.B - 1, w.H - 1), (w.B // 2, 1)):
+        xs = {k: v[b:b + 1, h:h + 1] for k, v in x.items()}
+        _, wC, wn, wm = oracle.recurrent_stabilized(xs["q"], xs["k"], xs["v"], xs["igate_pre"], xs["fgate_pre"])
+        assert rel_err(C[b:b + 1, h:h + 1], wC) <= TOL_BF16
+        assert rel_err(n[b:b + 1, h:h + 1], wn) <= TOL_BF16
+        assert np.max(np.abs(m[b:b + 1, h:h + 1].numpy() - wm)) <= 1e-4 * max(1.0, float(np.max(np.abs(wm))))
