@@ -307,20 +307,41 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     const bool n_thread = chunk < nchk;
     const int tpg = kTcTok / groups;                       // tokens per group: 4..64, a multiple of 4
     float nacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // weight exponent a2_j - p2_T of token t2 of a unit (p2_T: the row of the head's last token)
-    auto load_a2 = [&](int bh, int c, bool valid) {
-      const int j = c * kTcTok + t2;
-      if (!valid || t2 >= kTcTok || j >= p.T) return -INFINITY;
+    // Gate terms of token tk = t2 - 128 of a unit (warps 8 and 9, which sum no
+    // n: the stage loop waits for its slowest warp): a2_j and p2_T (the row of
+    // the head's last token), weight exp2(a2_j - p2_T) s.  Unit u's are fetched four
+    // units before their use into register pair u % 4 (a switch picks the
+    // pair, so no register holding a load in flight is ever copied, which
+    // would wait for it), so that a load from DRAM (microseconds under load)
+    // never holds up the stage loop.
+    constexpr int kAhead = 4;
+    const int tk = t2 - 128;
+    const bool gate_thread = tk >= 0 && tk < kTcTok;
+    auto load_gate = [&](int bh, int c, bool valid, float& a, float& q) {
+      const int j = c * kTcTok + tk;
       const size_t hb = (size_t)bh * p.T;
-      return p.g.a2[hb + j] - p.g.p2[hb + p.T - 1];
+      const bool v = valid && gate_thread && j < p.T;
+      a = v ? p.g.a2[hb + j] : -INFINITY;
+      q = v ? p.g.p2[hb + p.T - 1] : 0.0f;
     };
-    auto weights = [&](float e, int s2) {
-      if (t2 < kTcTok) w_s[s2][t2] = e == -INFINITY ? 0.0f : exp2f(e) * p.scale;
+    auto weights = [&](float a, float q, int s2) {
+      if (gate_thread) w_s[s2][tk] = a == -INFINITY ? 0.0f : exp2f(a - q) * p.scale;
     };
-    int bh2 = bh0, c2 = cc0;                       // the unit two ahead, for the gate-term prefetch
-    if (nu > 0) weights(load_a2(bh2, c2, true), 0);
+    int bh2 = bh0, c2 = cc0;                       // the unit kAhead + 1 ahead of the loop
+    float ga0, gq0, ga1, gq1, ga2, gq2, ga3, gq3;  // gate terms of unit u in pair u % 4
+    {
+      float a, q;
+      load_gate(bh2, c2, nu > 0, a, q);
+      if (nu > 0) weights(a, q, 0);
+    }
     next_unit(bh2, c2, p.nchunk);
-    float a2_next = load_a2(bh2, c2, nu > 1);
+    load_gate(bh2, c2, 1 < nu, ga1, gq1);
+    next_unit(bh2, c2, p.nchunk);
+    load_gate(bh2, c2, 2 < nu, ga2, gq2);
+    next_unit(bh2, c2, p.nchunk);
+    load_gate(bh2, c2, 3 < nu, ga3, gq3);
+    next_unit(bh2, c2, p.nchunk);
+    load_gate(bh2, c2, 4 < nu, ga0, gq0);
     next_unit(bh2, c2, p.nchunk);
     bool waited_zero = false;
     // The stage loop's wait and exit are kept in their plainest form (per-lane
@@ -365,10 +386,14 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
                                 (uint32_t)((((m & 63) >> 3) ^ (k & 7)) << 4),
                             x[blk]);
         }
+        // the two token blocks' weights, loaded before the first TMEM store
+        // (an asm statement that the compiler does not move loads across)
+        const float4 wb0 = *reinterpret_cast<const float4*>(&w_s[s2][32 * th + 4 * (lane & 3)]);
+        const float4 wb1 = *reinterpret_cast<const float4*>(&w_s[s2][32 * th + 16 + 4 * (lane & 3)]);
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
           const int m0 = 32 * qd + 16 * (blk >> 1), k0 = 32 * th + 16 * (blk & 1);
-          const float4 w = *reinterpret_cast<const float4*>(&w_s[s2][k0 + 4 * (lane & 3)]);
+          const float4 w = (blk & 1) ? wb1 : wb0;
           uint32_t y[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -441,9 +466,15 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kFsScaled + s2));
-      if (i + 1 < nu) {
-        weights(a2_next, (i + 1) % p.nst);
-        a2_next = load_a2(bh2, c2, i + 2 < nu);
+      if (gate_thread && i + 1 < nu) {
+        // unit i + 1's weights, then unit i + 1 + kAhead's gate terms into the same pair
+        const bool more = i + 1 + kAhead < nu;
+        switch ((i + 1) & 3) {
+          case 0: weights(ga0, gq0, (i + 1) % p.nst); load_gate(bh2, c2, more, ga0, gq0); break;
+          case 1: weights(ga1, gq1, (i + 1) % p.nst); load_gate(bh2, c2, more, ga1, gq1); break;
+          case 2: weights(ga2, gq2, (i + 1) % p.nst); load_gate(bh2, c2, more, ga2, gq2); break;
+          default: weights(ga3, gq3, (i + 1) % p.nst); load_gate(bh2, c2, more, ga3, gq3); break;
+        }
         next_unit(bh2, c2, p.nchunk);
       }
       if (!pend) continue;
