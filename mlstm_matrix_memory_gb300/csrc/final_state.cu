@@ -134,7 +134,7 @@ constexpr int kTcMaxStages = 4;
 constexpr uint32_t kCBoxBytes = 16384;      // one 128 x 32 fp32 box of C (128-byte swizzle)
 constexpr uint32_t kStagingBytes = 2 * kCBoxBytes;
 enum : int { kFsFull = 0, kFsScaled = kTcMaxStages, kFsEmpty = 2 * kTcMaxStages, kFsAccFull = 3 * kTcMaxStages,
-             kFsAccEmpty = 3 * kTcMaxStages + 1, kFsBars = 3 * kTcMaxStages + 2 };
+             kFsAccEmpty = 3 * kTcMaxStages + 1, kFsDrain = 3 * kTcMaxStages + 2, kFsBars = 3 * kTcMaxStages + 3 };
 
 struct FsTcParams {
   GateTerms g;
@@ -217,6 +217,7 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     }
     mbar_init(bar(kFsAccFull), 1);
     mbar_init(bar(kFsAccEmpty), kTcScaleWarps);
+    mbar_init(bar(kFsDrain), 1);
     fence_barrier_init();
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
@@ -288,6 +289,12 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
         mma_commit(bar(kFsAccFull));
         ++piece;
       }
+    }
+    // every MMA this thread issued has finished before the CTA frees TMEM and
+    // its stages (on an abort nobody else waits for the last ones)
+    // (a bounded wait that does not give up on the abort flag)
+    mma_commit(bar(kFsDrain));
+    for (long long it = 0; it < (1LL << 22) && !mbar_try_wait(bar(kFsDrain), 0); ++it) {
     }
   } else if ((warp >= 2 && warp < 6) || warp >= 8) {
     // ---- weights, V scaling, n, and each piece's epilogue (eight warps: each

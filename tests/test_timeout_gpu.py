@@ -30,3 +30,34 @@ def test_exhausted_wait_budget_reports_timeout_then_recovers():
     assert M.last_device_status() == 0
     want, _, _ = oracle.parallel_stabilized(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"])
     assert rel_err(h, want) <= TOL_BF16
+
+
+@pytest.mark.parametrize("shape", [(10, 5, 150, 128, 128), (2, 2, 192, 512, 128)],
+                         ids=["heads-cut-tmem-A", "dqk512-smem-A"])
+def test_handoff_exhausted_wait_budget_reports_timeout_then_recovers(shape):
+    """The same for the tensor-core hand-off: heads cut between CTAs with
+    several pieces per CTA (weighted V^T in TMEM), and d_qk = 512 (weighted V
+    in shared memory).  Every warp group leaves through its agreement
+    barriers; the next call is correct."""
+    import mlstm_matrix_memory_gb300 as M
+    B, H, T, dqk, dv = shape
+    x = W.sequence_inputs(B, H, T, dqk, dv, torch.bfloat16, seed=37)
+    xd = to_dev(x)
+    ws = torch.empty(M.parallel_fwd_workspace_bytes(B, H, T), dtype=torch.uint8, device="cuda")
+    M.gate_prep(xd["igate_pre"], xd["fgate_pre"], ws)
+    torch.cuda.synchronize()
+    assert M.last_device_status() == 0
+    M.set_spin_limit(1)
+    try:
+        M.parallel_final_state(xd["k"], xd["v"], ws)
+        torch.cuda.synchronize()
+        status = M.last_device_status()
+    finally:
+        M.set_spin_limit(0)
+    assert status == -5                     # MLSTM_ETIMEOUT
+    C, n, m = M.parallel_final_state(xd["k"], xd["v"], ws)
+    torch.cuda.synchronize()
+    assert M.last_device_status() == 0
+    _, wC, wn, _ = oracle.recurrent_stabilized(x["q"], x["k"], x["v"], x["igate_pre"], x["fgate_pre"])
+    assert rel_err(C, wC) <= TOL_BF16
+    assert rel_err(n, wn) <= TOL_BF16
