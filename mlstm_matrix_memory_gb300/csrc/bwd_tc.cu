@@ -74,28 +74,39 @@ __device__ __forceinline__ void tile_values(const uint32_t (&sv)[32], const uint
                                             int j0c, int i, bool row_ok, float p2i, float rowf, float invn,
                                             float dbi, float pscale, float (&dd)[32], uint32_t (&gw)[16],
                                             uint32_t (&pw)[16], float& rs) {
+  // column pairs in packed fp32 (each element rounded as in scalar fp32; the
+  // row sum runs in two lanes, added at the end)
+  const f32x2 rowf2 = f2_make(rowf, rowf), invn2 = f2_make(invn, invn), dbi2 = f2_make(dbi, dbi);
+  const f32x2 ps2 = f2_make(pscale, pscale);
+  f32x2 rs2 = f2_make(0.0f, 0.0f);
 #pragma unroll
   for (int c = 0; c < 32; c += 4) {
     const float4 c4 = *reinterpret_cast<const float4*>(ct + c);
-    const float ctv[4] = {c4.x, c4.y, c4.z, c4.w};
-    float gv[4], pv[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float dp;
-      if (DIAG) dp = (row_ok && j0c + c + e <= i) ? exp2f(ctv[e] - p2i) : 0.0f;
-      else dp = ctv[e] * rowf;
-      const float sr = __uint_as_float(sv[c + e]);                     // S / s
-      const float g = dp * fmaf(__uint_as_float(cv[c + e]), invn, dbi);  // D' (.) dC~'
-      gv[e] = g;
-      pv[e] = sr * pscale * dp;                                          // C~' / n
-      dd[c + e] = sr * g;                                                // dD~ / s
-      rs += dd[c + e];
+    for (int e = 0; e < 4; e += 2) {
+      f32x2 dp;
+      if (DIAG) {
+        const float ca = e == 0 ? c4.x : c4.z, cb = e == 0 ? c4.y : c4.w;
+        dp = f2_make((row_ok && j0c + c + e <= i) ? exp2f(ca - p2i) : 0.0f,
+                     (row_ok && j0c + c + e + 1 <= i) ? exp2f(cb - p2i) : 0.0f);
+      } else {
+        dp = f2_mul(e == 0 ? f2_make(c4.x, c4.y) : f2_make(c4.z, c4.w), rowf2);
+      }
+      const f32x2 sr = f2_make(__uint_as_float(sv[c + e]), __uint_as_float(sv[c + e + 1]));   // S / s
+      const f32x2 cc = f2_make(__uint_as_float(cv[c + e]), __uint_as_float(cv[c + e + 1]));
+      const f32x2 g = f2_mul(dp, f2_fma(cc, invn2, dbi2));         // D' (.) dC~'
+      const f32x2 pv = f2_mul(f2_mul(sr, ps2), dp);                // C~' / n
+      const f32x2 d2 = f2_mul(sr, g);                              // dD~ / s
+      rs2 = f2_add(rs2, d2);
+      const float2 gf = f2_split(g), pf = f2_split(pv), df = f2_split(d2);
+      dd[c + e] = df.x;
+      dd[c + e + 1] = df.y;
+      gw[(c + e) / 2] = pack_bf16x2(gf.x, gf.y);
+      pw[(c + e) / 2] = pack_bf16x2(pf.x, pf.y);
     }
-    gw[c / 2] = pack_bf16x2(gv[0], gv[1]);
-    gw[c / 2 + 1] = pack_bf16x2(gv[2], gv[3]);
-    pw[c / 2] = pack_bf16x2(pv[0], pv[1]);
-    pw[c / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
   }
+  const float2 r2 = f2_split(rs2);
+  rs += r2.x + r2.y;
 }
 
 // Item it -> head and tile: t = ib (ib + 1) / 2 + jb, jb <= ib.
@@ -307,11 +318,20 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
           for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
             const bool hi = lane & o;
+            if (n >= 4) {
 #pragma unroll
-            for (int k2 = 0; k2 < n / 2; ++k2) {
-              const float keep = hi ? dd[k2 + n / 2] : dd[k2];
-              const float send = hi ? dd[k2] : dd[k2 + n / 2];
-              dd[k2] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+              for (int k2 = 0; k2 < n / 2; k2 += 2) {       // two columns per packed add
+                const f32x2 keep = hi ? f2_make(dd[k2 + n / 2], dd[k2 + 1 + n / 2]) : f2_make(dd[k2], dd[k2 + 1]);
+                const float s0 = hi ? dd[k2] : dd[k2 + n / 2], s1 = hi ? dd[k2 + 1] : dd[k2 + 1 + n / 2];
+                const float2 sum = f2_split(f2_add(keep, f2_make(__shfl_xor_sync(0xffffffffu, s0, o),
+                                                                 __shfl_xor_sync(0xffffffffu, s1, o))));
+                dd[k2] = sum.x;
+                dd[k2 + 1] = sum.y;
+              }
+            } else {
+              const float keep = hi ? dd[1] : dd[0];
+              const float send = hi ? dd[0] : dd[1];
+              dd[0] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
           }
           col_red[qd][32 * ch + lane] = dd[0];
