@@ -53,7 +53,8 @@ def parse():
     p.add_argument("--no-other-configs", action="store_true",
                    help="skip the forward on the other bf16 layer shapes (350M-scale, T=16384)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
-    p.add_argument("--profile-kernel", choices=("fwd", "fwd_call", "fs", "step", "step_seq", "rbwd", "bwd"),
+    p.add_argument("--profile-kernel", choices=("fwd", "fwd_call", "fs", "step", "step_full", "step_seq", "rbwd", "bwd",
+                                                "bwd_saved"),
                    default=None,
                    help="no timing: one warm-up and one launch of the fused forward kernel (on --workload), "
                         "of the parallel-to-recurrent hand-off (on --workload), of the recurrent step (B=64, H=4, d=512: 256 MB of state), of the 64-token prefill "
@@ -399,7 +400,7 @@ def time_final_state(M, w, xd, reps, flush):
     return ms, 2.0 * w.B * w.H * w.T * w.d_qk * w.d_v, nbytes
 
 
-def time_backward(M, w, xd, reps):
+def time_backward(M, w, xd, reps, flush):
     """The parallel backward on the parallel workload for a seeded output
     gradient: algorithmic work T^2 (3 d_qk + 2 d_v) flops per head (the five
     causal products S, dC, dQ, dK, dV).  Also timed given the forward's saved
@@ -427,6 +428,7 @@ def time_backward(M, w, xd, reps):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         torch.cuda.synchronize()
         for i in range(reps):
+            flush.zero_()
             ev[i][0].record(stream)
             fn()
             ev[i][1].record(stream)
@@ -512,6 +514,15 @@ def profile_once(args):
         dh = torch.randn((w.B, w.H, w.T, w.d_v), generator=torch.Generator().manual_seed(1)).to(w.dtype).cuda()
         for _ in range(2):
             M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh)
+    elif args.profile_kernel == "bwd_saved":
+        # the training-step backward: one forward (its launches first), then two
+        # backward calls given its saved outputs
+        w = W.PARALLEL_WORKLOADS[args.workload]
+        xd = {k: v.cuda() for k, v in W.parallel_inputs(w, 0).items()}
+        dh = torch.randn((w.B, w.H, w.T, w.d_v), generator=torch.Generator().manual_seed(1)).to(w.dtype).cuda()
+        sv = M.parallel_fwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], return_stats=True)
+        for _ in range(2):
+            M.parallel_bwd(xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], dh, saved=(sv[0], sv[2], sv[3]))
     elif args.profile_kernel == "rbwd":
         # the recurrent backward on 32 heads of the 125M-scale layer's shape, T=256
         x = {k: v.cuda() for k, v in W.sequence_inputs(4, 8, 256, 384, 384, torch.bfloat16, seed=1).items()}
@@ -523,6 +534,11 @@ def profile_once(args):
         for _ in range(2):
             M.step_seq(xd["C"], xd["n"], xd["m"], xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"],
                        xd["o"])
+    elif args.profile_kernel == "step_full":
+        # the benchmark's recurrent step at full size: B=256, H=4, d=512 (1 GiB of state)
+        xd = {k: v.cuda() for k, v in W.step_inputs(W.STEP, 0).items()}
+        for _ in range(2):
+            M.step(xd["C"], xd["n"], xd["m"], xd["q"], xd["k"], xd["v"], xd["igate_pre"], xd["fgate_pre"], xd["o"])
     else:
         xd = {k: v.cuda() for k, v in W.step_inputs(W.STEP, 0, B=64).items()}
         for _ in range(2):
@@ -581,7 +597,7 @@ def main():
     bwd = rbwd = None
     if algo == "tc":
         fs = time_final_state(M, w, xd, 10, flush)
-        bwd = time_backward(M, w, xd, 5)
+        bwd = time_backward(M, w, xd, 5, flush)
         rbwd = time_recurrent_backward(M, w, xd, 3)
     clk = clocks.stop() if clocks else None
 
@@ -674,10 +690,15 @@ def main():
                                "tensor": {"achieved_tflops": tf, "frac": tf / peak_tf,
                                           "frac_of_nominal": tf / NOMINAL_BF16_TFLOPS}}
     if bwd is not None:
-        ms, fl, wsb, ms_saved = bwd
+        # The backward of a training step: the forward's H~, n and b are saved
+        # (mlstm_parallel_bwd_saved) and the call computes the five causal
+        # products and the gate gradients.  The call that recomputes the
+        # forward first is timed beside it.
+        ms_recompute, fl, wsb, ms = bwd
         tf = fl / (ms * 1e-3) / 1e12
-        line["backward"] = {"workload": w.name, "ms": ms, "workspace_bytes": wsb,
-                            "ms_with_saved_forward": ms_saved,
+        line["backward"] = {"workload": w.name, "ms": ms, "call": "with the forward's saved outputs",
+                            "workspace_bytes": wsb, "ms_with_forward_recompute": ms_recompute,
+                            "tflops_with_forward_recompute": fl / (ms_recompute * 1e-3) / 1e12,
                             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
                                          "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
                                          "work": "causal T^2 (3 d_qk + 2 d_v) per head", "traffic": None}}
