@@ -833,8 +833,25 @@ bwd_rowstat_kernel(const E* __restrict__ dh, const E* __restrict__ h, const floa
   const int lane = threadIdx.x & 31;
   if (row >= BHT) return;
   float dot = 0.0f;
-  for (int c = lane; c < dv; c += 32)
-    dot = fmaf(Elem<E>::load(dh, (size_t)row * dv + c), Elem<E>::load(h, (size_t)row * dv + c), dot);
+  if (sizeof(E) == 2 && dv % 8 == 0 && (((uintptr_t)dh | (uintptr_t)h) & 15u) == 0) {
+    // 16-byte loads (8 bf16 of each operand); rows are then 16-byte aligned
+    const uint4* a = reinterpret_cast<const uint4*>(dh + (size_t)row * dv);
+    const uint4* b = reinterpret_cast<const uint4*>(h + (size_t)row * dv);
+    for (int c8 = lane; c8 < dv / 8; c8 += 32) {
+      const uint4 x = a[c8], y = b[c8];
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
+        const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[e]));
+        dot = fmaf(fx.x, fy.x, dot);
+        dot = fmaf(fx.y, fy.y, dot);
+      }
+    }
+  } else {
+    for (int c = lane; c < dv; c += 32)
+      dot = fmaf(Elem<E>::load(dh, (size_t)row * dv + c), Elem<E>::load(h, (size_t)row * dv + c), dot);
+  }
   dot = warp_sum(dot);
   if (lane == 0) {
     const float n = nrow[row], b = brow[row];
@@ -854,8 +871,25 @@ __global__ void bwd_tile_sums_kernel(const float* __restrict__ Rpart, const floa
   const int bh = (int)(x / T), t = (int)(x % T);
   const int blk = t / kTile;
   float rsum = 0.0f, csum = 0.0f;
-  for (int b2 = 0; b2 <= blk; ++b2) rsum += Rpart[((size_t)bh * nb + b2) * T + t];
-  for (int b2 = blk; b2 < nb; ++b2) csum += Cpart[((size_t)bh * nb + b2) * T + t];
+  // four loads in flight at a time; the additions keep the block order
+  const float* rp = Rpart + (size_t)bh * nb * T + t;
+  const float* cp = Cpart + (size_t)bh * nb * T + t;
+  for (int b2 = 0; b2 <= blk; b2 += 4) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = b2 + u <= blk ? rp[(size_t)(b2 + u) * T] : 0.0f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (b2 + u <= blk) rsum += v[u];
+  }
+  for (int b2 = blk; b2 < nb; b2 += 4) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = b2 + u < nb ? cp[(size_t)(b2 + u) * T] : 0.0f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (b2 + u < nb) csum += v[u];
+  }
   R[x] = rsum;
   Ccol[x] = csum;
 }
