@@ -701,6 +701,7 @@ def main():
                             "tflops_with_forward_recompute": fl / (ms_recompute * 1e-3) / 1e12,
                             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
                                          "frac": tf / peak_tf, "peak_source": f"{src} bf16 dense (burst)",
+                                         "frac_of_nominal": tf / NOMINAL_BF16_TFLOPS,
                                          "work": "causal T^2 (3 d_qk + 2 d_v) per head",
                                          "traffic": kernel_traffic("backward_saved_" + w.name),
                                          "traffic_scope": "all kernels of one call"}}
