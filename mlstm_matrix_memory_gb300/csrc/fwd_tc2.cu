@@ -727,11 +727,14 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   p.npairs = (nqt + 1) / 2;
   p.log2_scale = log2f(a.scale);
   p.st = a.st;
-  // L2 prefetch of the next key tile: measured 114.0 -> 107.7 us on the
-  // 350M-scale layer and 1150 -> 1116 us on the T = 16384 workload (d = 512);
-  // neutral at d = 384.  MLSTM_TC_L2PF=0 in the environment turns it off.
+  // L2 prefetch of the next key tile, where the d_v slices of a query block
+  // (two CTA pairs) read the same K/V: measured 114.0 -> 107.7 us on the
+  // 350M-scale layer and 1150 -> 1116 us on the T = 16384 workload (d = 512).
+  // With one slice (d_v <= 384) it measured ~1 us slower on the 125M-scale
+  // layer (109.4 against 110.9 us, three alternating runs), so it is off there.
+  // MLSTM_TC_L2PF=0 or 1 in the environment overrides the choice.
   static const char* pf_env = getenv("MLSTM_TC_L2PF");
-  p.l2_prefetch = (pf_env && pf_env[0] == '0') ? 0 : 1;
+  p.l2_prefetch = pf_env ? (pf_env[0] == '0' ? 0 : 1) : (p.nsplit > 1 ? 1 : 0);
   const size_t fixed = 1024 + (size_t)a.dqk * kBM * 2 + (size_t)kBN * kBM * 2;
   const long long room = (long long)kSmemLimit - (long long)static_smem() - (long long)fixed;
   const int total = (int)std::min<long long>(kMaxSlots, room / kSlotBytes);
