@@ -126,9 +126,10 @@ final_state_kernel(const E* __restrict__ k, const E* __restrict__ v, GateTerms g
 
 // ---------------------------------------------------------------- tensor cores
 using namespace tc;
-constexpr int kTcTok = 64, kTcM = 128, kTcThreads = 384;
+constexpr int kTcTok = 64, kTcM = 128, kTcThreads = 512;
 constexpr int kSmemLimit = 232448;         // opt-in shared memory per block on sm_100-family
-constexpr int kTcScaleWarps = 8;            // warps 2..5 and 8..11: weights, n, epilogue
+constexpr int kTcScaleWarps = 8;            // warps 2..5 and 8..11: weighted V, C epilogue
+constexpr int kTcNWarps = 4;                // warps 12..15: n (and, 12..13, the weights)
 constexpr int kTcProducers = 3;             // warps 0, 6, 7: one issuing thread moves only ~30 B/clk
 constexpr int kTcMaxStages = 4;
 constexpr uint32_t kCBoxBytes = 16384;      // one 128 x 32 fp32 box of C (128-byte swizzle)
@@ -213,7 +214,7 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     for (int s2 = 0; s2 < kTcMaxStages; ++s2) {
       mbar_init(bar(kFsFull + s2), 1);
       mbar_init(bar(kFsScaled + s2), kTcScaleWarps);
-      mbar_init(bar(kFsEmpty + s2), 1);
+      mbar_init(bar(kFsEmpty + s2), 1 + kTcNWarps);   // the MMA commit and the n warps' reads of K
     }
     mbar_init(bar(kFsAccFull), 1);
     mbar_init(bar(kFsAccEmpty), kTcScaleWarps);
@@ -296,10 +297,19 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     mma_commit(bar(kFsDrain));
     for (long long it = 0; it < (1LL << 22) && !mbar_try_wait(bar(kFsDrain), 0); ++it) {
     }
-  } else if ((warp >= 2 && warp < 6) || warp >= 8) {
-    // ---- weights, V scaling, n, and each piece's epilogue (eight warps: each
-    // TMEM lane quarter twice, one per half of the columns)
-    const int t2 = warp < 6 ? threadIdx.x - 64 : threadIdx.x - 128;   // 0..255, a warp's lanes consecutive
+  } else if (warp >= 2 && warp != 6 && warp != 7) {
+    // ---- twelve warps share the stage loop:
+    //  - V warps (2..5, 8..11): the weighted V and each piece's C epilogue,
+    //    each TMEM lane quarter twice (one per token half, then per half of
+    //    the columns);
+    //  - n warps (12..15): n over their slice of K, and (12, 13) the next
+    //    unit's weights.
+    // No warp does two of these per unit: the stage barrier waits for the
+    // slowest, and two weighting warps per sub-partition hid too little
+    // latency.
+    const bool vw = warp < 12;
+    const int t2 = vw ? (warp < 6 ? threadIdx.x - 64 : threadIdx.x - 128) : -1;   // V warps: 0..255
+    const int tn = vw ? -1 : threadIdx.x - 384;                                   // n warps: 0..127
     const int qd = warp & 3;
     // n = sum_j w_j k_j: the row tiles of a head share the columns (slice
     // [ncol0, ncol0 + 8 nchk) of row tile tr, a multiple of 64).  A thread sums
@@ -309,20 +319,19 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     const int ncol0 = min(p.dqk, tr * cs);
     const int nchk = (min(p.dqk, ncol0 + cs) - ncol0) / 8;  // 8-column chunks in the slice (<= 64)
     int groups = 1;                                        // token groups per chunk: a power of 2 <= 16
-    while (groups < 16 && 2 * groups * nchk <= 256) groups *= 2;
-    const int chunk = t2 / groups, tg = t2 % groups;
-    const bool n_thread = chunk < nchk;
+    while (groups < 16 && 2 * groups * nchk <= 128) groups *= 2;   // the 128 n threads cover every chunk
+    const int chunk = max(tn, 0) / groups, tg = max(tn, 0) % groups;
+    const bool n_thread = tn >= 0 && chunk < nchk;
     const int tpg = kTcTok / groups;                       // tokens per group: 4..64, a multiple of 4
     float nacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // Gate terms of token tk = t2 - 128 of a unit (warps 8 and 9, which sum no
-    // n: the stage loop waits for its slowest warp): a2_j and p2_T (the row of
-    // the head's last token), weight exp2(a2_j - p2_T) s.  Unit u's are fetched four
+    // Gate terms of token tk = tn of a unit (warps 12 and 13): a2_j and p2_T
+    // (the row of the head's last token), weight exp2(a2_j - p2_T) s.  Unit u's are fetched four
     // units before their use into register pair u % 4 (a switch picks the
     // pair, so no register holding a load in flight is ever copied, which
     // would wait for it), so that a load from DRAM (microseconds under load)
     // never holds up the stage loop.
     constexpr int kAhead = 4;
-    const int tk = t2 - 128;
+    const int tk = tn;
     const bool gate_thread = tk >= 0 && tk < kTcTok;
     auto load_gate = [&](int bh, int c, bool valid, float& a, float& q) {
       const int j = c * kTcTok + tk;
@@ -356,8 +365,8 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     // reducing barrier per stage cost 6-10 us of the 49 us 125M-scale
     // hand-off.  A warp that leaves early (its wait gave up, raising the abort
     // flag) then arrives on the barriers of the stages it skipped, so every
-    // stage's barrier still counts all eight warps, and the group agrees on the
-    // result once, after the loop.  The 32 lanes of a warp poll the same
+    // stage's barrier still counts all twelve warps, and the group agrees on
+    // the result once, after the loop.  The 32 lanes of a warp poll the same
     // barrier with the same instructions and take the same exit.
     bool ok = true;
     int done = 0, piece = 0, pc0 = 0, bh = bh0, c = cc0;
@@ -371,10 +380,12 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
       }
       ok = mbar_wait(bar(kFsFull + s2), u & 1u, spin, abort, p.st, 23);
       if (!ok) break;
-      named_bar_sync(1, 256);                        // w_s[s2] written by every thread
+      named_bar_sync(1, 384);                        // w_s[s2] written
       ++done;
       const uint32_t sb = base + (uint32_t)s2 * stage_bytes;
-      if (AT) {
+      if (!vw) {
+        // (n warps: below)
+      } else if (AT) {
         // A = (w V)^T into TMEM slot s2: this warp's lane quarter (d_v rows
         // 32 qd ..) and token half (32 th ..), as 2 x 2 blocks of 16 rows x 16
         // tokens.  ldmatrix.trans turns 8 x 8 blocks of the token-major V
@@ -465,14 +476,19 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
             }
         }
       }
-      if (AT) {
-        tmem_wait_st();                              // this thread's A stores are in TMEM
-        tc_fence_before();
+      if (!vw) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kFsEmpty + s2));   // this warp has read the stage's K
       } else {
-        fence_proxy_async_smem();                    // the scaled V is visible to the tensor core
+        if (AT) {
+          tmem_wait_st();                            // this thread's A stores are in TMEM
+          tc_fence_before();
+        } else {
+          fence_proxy_async_smem();                  // the scaled V is visible to the tensor core
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kFsScaled + s2));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kFsScaled + s2));
       if (gate_thread && i + 1 < nu) {
         // unit i + 1's weights, then unit i + 1 + kAhead's gate terms into the same pair
         const bool more = i + 1 + kAhead < nu;
@@ -493,9 +509,10 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
         fence_proxy_async_global();
         waited_zero = true;
       }
+      if (!vw)
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        for (int o = 1; o < groups; o <<= 1) nacc[e] += __shfl_xor_sync(0xffffffffu, nacc[e], o);
+        for (int e = 0; e < 8; ++e)
+          for (int o = 1; o < groups; o <<= 1) nacc[e] += __shfl_xor_sync(0xffffffffu, nacc[e], o);
       if (n_thread && tg == 0) {
         float* dst = p.n + (size_t)bh * p.dqk + ncol0 + chunk * 8;
         const float4 v0 = make_float4(nacc[0], nacc[1], nacc[2], nacc[3]);
@@ -512,8 +529,12 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
       for (int e = 0; e < 8; ++e) nacc[e] = 0.0f;
       // the eight warps agree that the piece's accumulator is complete before
       // any of them enters the epilogue's group barriers
-      ok = bar_red_and(4, 256, mbar_wait_warp(bar(kFsAccFull), (uint32_t)piece & 1u, spin, abort, p.st, 24));
+      ok = bar_red_and(4, 384, mbar_wait_warp(bar(kFsAccFull), (uint32_t)piece & 1u, spin, abort, p.st, 24));
       if (!ok) break;                                // (this unit's barriers are done)
+      if (!vw) {
+        ++piece;
+        continue;
+      }
       tc_fence_after();
       // C leaves TMEM in 128-row x 32-column boxes (16 KB, 128-byte swizzle):
       // the four warps of a column half each write their 32 rows of a box, one
@@ -562,10 +583,10 @@ final_state_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_c
     // agreement (reporting failure), so that the other warps' barriers count
     // all eight warps and they leave at the next piece end.
     for (int j = done; j < nu; ++j) {
-      named_bar_sync(1, 256);
-      if (j == nu - 1 || (int)((va + j) % p.nchunk) == p.nchunk - 1) bar_red_and(4, 256, false);
+      named_bar_sync(1, 384);
+      if (j == nu - 1 || (int)((va + j) % p.nchunk) == p.nchunk - 1) bar_red_and(4, 384, false);
     }
-    ok = bar_red_and(1, 256, ok);
+    ok = bar_red_and(1, 384, ok);
     if (lane == 0) tma_store_wait_read();            // staging boxes read out before the CTA exits
     __syncwarp();
     tc_fence_before();
