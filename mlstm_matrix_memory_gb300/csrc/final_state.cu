@@ -18,15 +18,16 @@
 // the same sequence of (head, chunk) units side by side, each CTA a contiguous
 // range of it (whole heads when they spread evenly over the SMs, else an even
 // share of units, so that every SM has work).  Per unit, TMA threads load V
-// [64 x 128] and K [64 x d_qk] (128-byte swizzle); eight warps (two per SM
-// sub-partition, so that one hides the other's shared-memory latency) scale
-// each V row by its token's weight s*D'_Tj in shared memory and sum their
-// slice of the weighted K columns into n (the row tiles of a head share the
-// columns); one thread issues tcgen05.mma with both operands MN-major (M = d_v
-// rows, N = d_qk columns, K = tokens).  At the end of each piece (the part of
-// a head a CTA holds) the eight warps move C out of TMEM through 32 x 32
-// boxes in shared memory to TMA stores (a whole head) or TMA adds (a head cut
-// between CTAs, into C and n zeroed by a pass launched just before).
+// [64 x 128] and K [64 x d_qk] (128-byte swizzle); eight V warps (two per SM
+// sub-partition) scale each V row by its token's weight s*D'_Tj into the
+// MMA's A operand (in TMEM, or in place in shared memory at d_qk = 512); four
+// n warps sum their slice of the weighted K columns into n (the row tiles of
+// a head share the columns) and two of them prepare the next unit's weights;
+// one thread issues tcgen05.mma (M = d_v rows, N = d_qk columns, K = tokens).
+// At the end of each piece (the part of a head a CTA holds) the V warps move C
+// out of TMEM through 128 x 32 boxes in shared memory to TMA stores (a whole
+// head) or TMA adds (a head cut between CTAs, into C and n zeroed by a pass
+// launched just before).
 // CUDA-core version (fp32, other sizes): 64 x 64 tiles of C in registers, 32
 // weighted tokens staged at a time, the token range split when there are too
 // few tiles to fill the GPU and the partial results added into C and n
