@@ -237,17 +237,26 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
     uint32_t ph = 0;
     bool ok = true;
     // loads the ring's next granule; with pf_next, first asks L2 for the same
-    // boxes of the next key tile, so that their own loads, a tile later, hit L2
-    auto load = [&](const CUtensorMap* map, int nbox, uint32_t box_bytes, int x0, int dx, int y, bool pf_next) {
+    // boxes of the next key tile, so that their own loads, a tile later, hit L2.
+    // kblk > 0: the granule is one 4-D box of kblk 64-column blocks starting at
+    // block x0 / 64 (one copy instead of kblk: each issuing thread handles its
+    // copies one after another); otherwise nbox 3-D boxes.
+    auto load = [&](const CUtensorMap* map, int nbox, int kblk, uint32_t box_bytes, int x0, int dx, int y,
+                    bool pf_next) {
       if (!ok) return;
       const int g = base_slot + st;
-      if (pf_next)
-        for (int b2 = 0; b2 < nbox; ++b2) tma_prefetch_l2_3d(map, x0 + b2 * dx, y + kBN, it.bh);
+      if (pf_next) {
+        if (kblk > 0) tma_prefetch_l2_4d(map, 0, y + kBN, x0 / 64, it.bh);
+        else
+          for (int b2 = 0; b2 < nbox; ++b2) tma_prefetch_l2_3d(map, x0 + b2 * dx, y + kBN, it.bh);
+      }
       ok = mbar_wait(bar(kBarEmpty + g), ph ^ 1, spin, abort, p.st, kSiteProducer);
       if (!ok) return;
       if (leader) mbar_arrive_expect_tx(bar(kBarFull + g), 2u * kSlotBytes);
-      for (int b2 = 0; b2 < nbox; ++b2)
-        tma_load_3d_pair(sRing + g * kSlotBytes + b2 * box_bytes, map, lbar(kBarFull + g), x0 + b2 * dx, y, it.bh);
+      if (kblk > 0) tma_load_4d_pair(sRing + g * kSlotBytes, map, lbar(kBarFull + g), 0, y, x0 / 64, it.bh);
+      else
+        for (int b2 = 0; b2 < nbox; ++b2)
+          tma_load_3d_pair(sRing + g * kSlotBytes + b2 * box_bytes, map, lbar(kBarFull + g), x0 + b2 * dx, y, it.bh);
       ++nloads;
       if (++st == n) { st = 0; ph ^= 1; }
     };
@@ -257,15 +266,18 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
       if (qi > 0) ok = mbar_wait(bar(kBarQEmpty), (uint32_t)(qi - 1) & 1u, spin, abort, p.st, kSiteProducer);
       if (!ok) break;
       if (leader && pi == 0) mbar_arrive_expect_tx(bar(kBarQFull), 2u * (uint32_t)p.dqk * kBM * 2);
-      for (int b2 = pi; b2 < p.dqk / 64; b2 += kProducers)
-        tma_load_3d_pair(sQ + b2 * 16384u, &tmap_q, lbar(kBarQFull), b2 * 64, it.i0, it.bh);
+      {
+        // each producer loads its half of Q's 64-column blocks as one 4-D box
+        const int qb = p.dqk / 64 / kProducers;
+        tma_load_4d_pair(sQ + (uint32_t)(pi * qb) * 16384u, &tmap_q, lbar(kBarQFull), 0, it.i0, pi * qb, it.bh);
+      }
       ++qi;
       qfills[pi] = qi;
       const int nch = it.dv_cta / 128, nvc = (nch + 1) / 2;
       if (pi == 0) {
         for (int j = 0; j < it.nkv && ok; ++j)
           for (int c = 0; c < nkg; ++c)
-            load(&tmap_k, 2, 8192u, c * 128, 64, j * kBN + (int)rank * 64, p.l2_prefetch && j + 1 < it.nkv);
+            load(&tmap_k, 1, 2, 0u, c * 128, 0, j * kBN + (int)rank * 64, p.l2_prefetch && j + 1 < it.nkv);
       } else {
         for (int j = 0; j < it.nkv && ok; ++j)
           for (int e = 0; e < nvc; ++e) {
@@ -274,11 +286,12 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             // is its own N=128 burst over one granule (this CTA holds 64 columns)
             if (2 * e + 1 < nch && st + 1 < n) {
               const int col = it.dv_off + (2 * e + (int)rank) * 128;
-              load(&tmap_v, 1, 0u, col, 0, j * kBN, p.l2_prefetch && j + 1 < it.nkv);
-              load(&tmap_v, 1, 0u, col + 64, 0, j * kBN, p.l2_prefetch && j + 1 < it.nkv);
+              load(&tmap_v, 1, 0, 0u, col, 0, j * kBN, p.l2_prefetch && j + 1 < it.nkv);
+              load(&tmap_v, 1, 0, 0u, col + 64, 0, j * kBN, p.l2_prefetch && j + 1 < it.nkv);
             } else {
               for (int q = 2 * e; q < min(2 * e + 2, nch); ++q)
-                load(&tmap_v, 1, 0u, it.dv_off + q * 128 + (int)rank * 64, 0, j * kBN, p.l2_prefetch && j + 1 < it.nkv);
+                load(&tmap_v, 1, 0, 0u, it.dv_off + q * 128 + (int)rank * 64, 0, j * kBN,
+                     p.l2_prefetch && j + 1 < it.nkv);
             }
           }
       }
@@ -752,7 +765,9 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
   p.n_items = (int)items;
   p.nclusters = std::min(p.n_items, resident_pairs(smem));
   CUtensorMap mq, mk, mv, mh;
-  if (!make_map(&mq, a.q, a.dqk, a.T, a.BH, kBM) || !make_map(&mk, a.k, a.dqk, a.T, a.BH, 64) ||
+  // K granules (64 keys x 128 d_qk) load as one 4-D box of two 64-column blocks
+  if (!make_map_blocks(&mq, a.q, a.dqk, a.T, a.BH, kBM, a.dqk / 64 / kProducers) ||
+      !make_map_blocks(&mk, a.k, a.dqk, a.T, a.BH, 64, 2) ||
       !make_map(&mv, a.v, a.dv, a.T, a.BH, kBN) || !make_map(&mh, a.h, a.dv, a.T, a.BH, kBM))
     return kCuda;
   if (p.og)
