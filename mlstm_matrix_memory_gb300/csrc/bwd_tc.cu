@@ -395,6 +395,7 @@ enum : int { kSitePProducer = 44, kSitePMma = 45, kSitePEpi = 46 };
 
 struct ProdParams {
   int T, BH, nb, dqk, dv;
+  int a4;                    // CTA pairs: A blocks load through their 4-D view (T a multiple of 64)
   float scale;
   DevStatus st;
 };
@@ -593,7 +594,9 @@ bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_consta
                  const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                  const __grid_constant__ CUtensorMap tmap_dh, const __grid_constant__ CUtensorMap tmap_dq,
                  const __grid_constant__ CUtensorMap tmap_dk, const __grid_constant__ CUtensorMap tmap_dv,
-                 const ProdParams p) {
+                 const __grid_constant__ CUtensorMap tmap_g4, const __grid_constant__ CUtensorMap tmap_p4,
+                 const __grid_constant__ CUtensorMap tmap_k4, const __grid_constant__ CUtensorMap tmap_q4,
+                 const __grid_constant__ CUtensorMap tmap_dh4, const ProdParams p) {
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t bars[kPNumBars];
   __shared__ uint32_t tmem_holder;
@@ -623,6 +626,10 @@ bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_consta
   const CUtensorMap* mb = prod == 0 ? &tmap_k : (prod == 1 ? &tmap_q : &tmap_dh);
   const CUtensorMap* mo = prod == 0 ? &tmap_dq : (prod == 1 ? &tmap_dk : &tmap_dv);
   const float alpha = prod == 2 ? 1.0f : p.scale;
+  // the A and B operands as 4-D views: one box of two 64-column blocks (the A
+  // view only when T is a multiple of 64, p.a4)
+  const CUtensorMap* ma4 = prod == 2 ? &tmap_p4 : &tmap_g4;
+  const CUtensorMap* mb4 = prod == 0 ? &tmap_k4 : (prod == 1 ? &tmap_q4 : &tmap_dh4);
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sA = base, sB = base + kANst * kABytes;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
@@ -662,6 +669,8 @@ bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_consta
     // expected bytes (both CTAs) only the leader posts.
     tma_prefetch_desc(ma);
     tma_prefetch_desc(mb);
+    tma_prefetch_desc(ma4);
+    tma_prefetch_desc(mb4);
     int bi = 0;
     bool ok = true;
     for (int t = 0; t < nkb && ok; ++t) {
@@ -671,11 +680,16 @@ bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_consta
       if (!ok) break;
       if (leader) mbar_arrive_expect_tx(bar(kPBarAFull + as), 2u * kABytes);
       const uint32_t adst = sA + (uint32_t)as * kABytes;
-      for (int h = 0; h < 2; ++h) {
-        if (prod == 0)   // G[gr rows, kb keys]
-          tma_load_3d_pair(adst + h * 16384u, ma, lbar(kPBarAFull + as), kb * kTile + 64 * h, r0, bh);
-        else             // G[kb rows, gr keys]^T
-          tma_load_3d_pair(adst + h * 16384u, ma, lbar(kPBarAFull + as), r0 + 64 * h, kb * kTile, bh);
+      if (p.a4) {        // the block's two 64-column halves in one copy
+        if (prod == 0) tma_load_4d_pair(adst, ma4, lbar(kPBarAFull + as), 0, r0, 2 * kb, bh);
+        else tma_load_4d_pair(adst, ma4, lbar(kPBarAFull + as), 0, kb * kTile, r0 / 64, bh);
+      } else {
+        for (int h = 0; h < 2; ++h) {
+          if (prod == 0)   // G[gr rows, kb keys]
+            tma_load_3d_pair(adst + h * 16384u, ma, lbar(kPBarAFull + as), kb * kTile + 64 * h, r0, bh);
+          else             // G[kb rows, gr keys]^T
+            tma_load_3d_pair(adst + h * 16384u, ma, lbar(kPBarAFull + as), r0 + 64 * h, kb * kTile, bh);
+        }
       }
       a_issued_s = t + 1;
       for (int c = 0; c < nchunk && ok; ++c, ++bi) {
@@ -685,10 +699,9 @@ bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_consta
         const bool wide = nbox - 4 * c >= 4;            // 256 columns: two boxes a CTA, else one
         const int col0 = 256 * c;
         if (leader) mbar_arrive_expect_tx(bar(kPBarBFull + bs), 2u * (wide ? 32768u : 16384u));
-        if (wide) {
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d_pair(sB + (uint32_t)bs * kBBytes + h * 16384u, mb, lbar(kPBarBFull + bs),
-                             col0 + 128 * (int)rank + 64 * h, kb * kTile, bh);
+        if (wide) {       // this CTA's two 64-column blocks in one copy
+          tma_load_4d_pair(sB + (uint32_t)bs * kBBytes, mb4, lbar(kPBarBFull + bs), 0, kb * kTile,
+                           (col0 + 128 * (int)rank) / 64, bh);
         } else {
           tma_load_3d_pair(sB + (uint32_t)bs * kBBytes, mb, lbar(kPBarBFull + bs), col0 + 64 * (int)rank,
                            kb * kTile, bh);
@@ -908,7 +921,7 @@ int launch_bwd_products(const BwdProdArgs& a, cudaStream_t stream) {
       !make_map(&mdk, a.dk, a.dqk, a.T, a.BH, kTile) || !make_map(&mdv, a.dvo, a.dv, a.T, a.BH, kTile))
     return kCuda;
   ProdParams p;
-  p.T = a.T; p.BH = a.BH; p.nb = nb; p.dqk = a.dqk; p.dv = a.dv; p.scale = a.scale; p.st = a.st;
+  p.T = a.T; p.BH = a.BH; p.nb = nb; p.dqk = a.dqk; p.dv = a.dv; p.scale = a.scale; p.st = a.st; p.a4 = 0;
   const size_t smem = (size_t)kANst * kABytes + (size_t)kBNst * kBBytes + 1024;
   static const char* force = getenv("MLSTM_BWD_PROD");       // "single": one CTA per block (tests)
   if (a.dqk % 128 == 0 && a.dv % 128 == 0 && !(force && force[0] == 's')) {
@@ -920,6 +933,15 @@ int launch_bwd_products(const BwdProdArgs& a, cudaStream_t stream) {
       if (cudaGetLastError() != cudaSuccess) return kCuda;
     }
     if (cudaFuncSetAttribute(bwd_prod2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return kCuda;
+    // 4-D views: A blocks and wide B chunks as one box of two 64-column blocks
+    // (an issuing thread handles its copies one after another)
+    CUtensorMap mg4 = mg, mp4 = mp, mk4, mq4, mdh4;
+    p.a4 = a.T % 64 == 0 && make_map_ld_blocks(&mg4, a.G, a.T, a.T, a.BH, a.ldT, kTile, 2) &&
+           make_map_ld_blocks(&mp4, a.P, a.T, a.T, a.BH, a.ldT, kTile, 2);
+    if (!p.a4) { mg4 = mg; mp4 = mp; }
+    if (!make_map_blocks(&mk4, a.k, a.dqk, a.T, a.BH, kTile, 2) || !make_map_blocks(&mq4, a.q, a.dqk, a.T, a.BH, kTile, 2) ||
+        !make_map_blocks(&mdh4, a.dh, a.dv, a.T, a.BH, kTile, 2))
       return kCuda;
     const long long pairs = 3LL * a.BH * ((nb + 1) / 2);
     cudaLaunchConfig_t cfg = {};
@@ -934,7 +956,8 @@ int launch_bwd_products(const BwdProdArgs& a, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, bwd_prod2_kernel, mg, mp, mk, mq, mdh, mdq, mdk, mdv, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, bwd_prod2_kernel, mg, mp, mk, mq, mdh, mdq, mdk, mdv, mg4, mp4, mk4, mq4, mdh4, p) !=
+        cudaSuccess)
       return kCuda;
     return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
   }

@@ -615,6 +615,24 @@ bool make_map_blocks(CUtensorMap* m, const void* base, int d, int T, int BH, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [BH, rows, cols] bf16 with row pitch ld (ld*2 a multiple of 16) viewed as
+// 4-D (64 columns, rows, cols / 64 column blocks, BH): one box (64 x box_rows x
+// blocks x 1, 128-byte swizzle) lands as `blocks` consecutive 64-column tiles.
+// cols must be a multiple of 64 (a partial last block would read the pitch
+// padding instead of zeros).
+bool make_map_ld_blocks(CUtensorMap* m, const void* base, int cols, int rows, int BH, int ld, int box_rows,
+                        int blocks) {
+  EncodeTiled enc = encode_fn();
+  if (!enc || (ld * 2) % 16 != 0 || cols % 64 != 0) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64), (cuuint64_t)BH};
+  cuuint64_t strides[3] = {(cuuint64_t)ld * 2, 128, (cuuint64_t)ld * 2 * rows};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, (cuuint32_t)blocks, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [BH, rows, cols] fp32 viewed as a 3-D tensor (cols fastest); box = box_cols
 // x box_rows x 1 with 128-byte swizzle (box_cols * 4 <= 128).
 bool make_map_f32(CUtensorMap* m, float* base, int cols, int rows, int BH, int box_cols, int box_rows) {

@@ -143,6 +143,10 @@ bool make_map(CUtensorMap* m, const void* base, int d, int T, int BH, int rows);
 // [BH, T, d] bf16 as 4-D (64 columns, T, d / 64 blocks, BH): one box is
 // `blocks` consecutive 64-column x rows tiles (128-byte swizzle).
 bool make_map_blocks(CUtensorMap* m, const void* base, int d, int T, int BH, int rows, int blocks);
+// [BH, rows, cols] bf16 with row pitch ld as 4-D (64 columns, rows, cols / 64
+// blocks, BH); cols a multiple of 64.
+bool make_map_ld_blocks(CUtensorMap* m, const void* base, int cols, int rows, int BH, int ld, int box_rows,
+                        int blocks);
 // [BH, rows, cols] fp32 (cols fastest), box box_cols x box_rows x 1, 128-byte swizzle.
 bool make_map_f32(CUtensorMap* m, float* base, int cols, int rows, int BH, int box_cols, int box_rows);
 

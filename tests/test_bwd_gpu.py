@@ -37,6 +37,7 @@ CASES = [
     (1, 1, 129, 64, 64, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),      # a second tile row of one query
     (1, 2, 600, 128, 256, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # CTA-pair products, odd block count
     (2, 1, 129, 128, 128, torch.bfloat16, (-2.0, 1.5), (0.5, 1.0)),   # CTA-pair products, one-query block
+    (1, 2, 576, 128, 128, torch.bfloat16, (0.0, 1.0), (3.0, 1.0)),    # CTA-pair products, A through the 4-D view, half a last key block
 ]
 
 
