@@ -50,6 +50,7 @@ enum : int {
 enum : int { kSiteTProducer = 41, kSiteTMma = 42, kSiteTEpi = 43 };
 
 struct TileParams {
+  int wide;                  // two 64-column chunks a stage through 4-D views (d_qk, d_v multiples of 64)
   const float* a2;
   const float* p2;
   const float* invn;
@@ -125,6 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_dh, const __grid_constant__ CUtensorMap tmap_v,
                 const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_p,
+                const __grid_constant__ CUtensorMap tmap_q4, const __grid_constant__ CUtensorMap tmap_k4,
+                const __grid_constant__ CUtensorMap tmap_dh4, const __grid_constant__ CUtensorMap tmap_v4,
                 const TileParams p) {
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t bars[kNumBars];
@@ -143,7 +146,12 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sStage = base + kNst * kStage;            // staging of G (boxes 0, 1) and P (2, 3)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  const int nq = (p.dqk + 63) / 64, nch = nq + (p.dv + 63) / 64;
+  // ring stages: four of one 64-column chunk of A and of B, or (p.wide: d_qk
+  // and d_v multiples of 64) two of two chunks, each operand one 4-D box
+  const int nst = p.wide ? 2 : kNst;
+  const uint32_t stage = p.wide ? 2u * kStage : kStage;
+  const int cw = p.wide ? 128 : 64;
+  const int nq = (p.dqk + cw - 1) / cw, nch = nq + (p.dv + cw - 1) / cw;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -182,17 +190,26 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       tile_of(it, nb, &bh, &ib, &jb);
       const int i0 = ib * kTile, j0 = jb * kTile;
       for (int c = 0; c < nch; ++c, ++cc) {
-        const int s = cc % kNst, u = cc / kNst;
+        const int s = cc % nst, u = cc / nst;
         ok = mbar_wait(bar(kBarEmpty + s), (uint32_t)(u & 1) ^ 1u, spin, abort, p.st, kSiteTProducer);
         if (!ok) break;
-        const uint32_t dst = base + (uint32_t)s * kStage;
-        mbar_arrive_expect_tx(bar(kBarFull + s), kStage);
-        if (c < nq) {
+        const uint32_t dst = base + (uint32_t)s * stage;
+        mbar_arrive_expect_tx(bar(kBarFull + s), stage);
+        if (p.wide) {
+          // two 64-column chunks per operand, each operand one 4-D box
+          if (c < nq) {
+            tma_load_4d(dst, &tmap_q4, bar(kBarFull + s), 0, i0, 2 * c, bh);
+            tma_load_4d(dst + stage / 2, &tmap_k4, bar(kBarFull + s), 0, j0, 2 * c, bh);
+          } else {
+            tma_load_4d(dst, &tmap_dh4, bar(kBarFull + s), 0, i0, 2 * (c - nq), bh);
+            tma_load_4d(dst + stage / 2, &tmap_v4, bar(kBarFull + s), 0, j0, 2 * (c - nq), bh);
+          }
+        } else if (c < nq) {
           tma_load_3d(dst, &tmap_q, bar(kBarFull + s), 64 * c, i0, bh);
-          tma_load_3d(dst + kStage / 2, &tmap_k, bar(kBarFull + s), 64 * c, j0, bh);
+          tma_load_3d(dst + stage / 2, &tmap_k, bar(kBarFull + s), 64 * c, j0, bh);
         } else {
           tma_load_3d(dst, &tmap_dh, bar(kBarFull + s), 64 * (c - nq), i0, bh);
-          tma_load_3d(dst + kStage / 2, &tmap_v, bar(kBarFull + s), 64 * (c - nq), j0, bh);
+          tma_load_3d(dst + stage / 2, &tmap_v, bar(kBarFull + s), 64 * (c - nq), j0, bh);
         }
         issued_s = cc + 1;
       }
@@ -209,18 +226,21 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       if (!ok) break;
       tc_fence_after();
       for (int c = 0; c < nch && ok; ++c, ++cc) {
-        const int s = cc % kNst, u = cc / kNst;
+        const int s = cc % nst, u = cc / nst;
         ok = mbar_wait(bar(kBarFull + s), (uint32_t)(u & 1), spin, abort, p.st, kSiteTMma);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a_addr = base + (uint32_t)s * kStage;
-        const uint64_t da = smem_desc_sw128(a_addr, 16, 1024);
-        const uint64_t db = smem_desc_sw128(a_addr + kStage / 2, 16, 1024);
+        const uint32_t a_addr = base + (uint32_t)s * stage;
         const uint32_t d = tmem + 256u * (uint32_t)b + (c < nq ? 0u : 128u);
         const bool first = c == 0 || c == nq;
+        // one or two K-major 128-byte-swizzle atoms (64 columns each, 16 KB apart)
+        for (int at = 0; at < (p.wide ? 2 : 1); ++at) {
+          const uint64_t da = smem_desc_sw128(a_addr + (uint32_t)at * 16384u, 16, 1024);
+          const uint64_t db = smem_desc_sw128(a_addr + stage / 2 + (uint32_t)at * 16384u, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(d, da + 2 * kk, db + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, da + 2 * kk, db + 2 * kk, idesc, (first && at == 0 && kk == 0) ? 0u : 1u);
+        }
         mma_commit(bar(kBarEmpty + s));
       }
       if (ok) mma_commit(bar(kBarAccFull + b));
@@ -368,9 +388,9 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   // round of every slot
   if (threadIdx.x == 0 && abort_flag) {
     const int issued = issued_s;
-    for (int c = max(0, issued - kNst); c < issued; ++c)
+    for (int c = max(0, issued - nst); c < issued; ++c)
       for (long long w = 0; w < kDrainSpin; ++w)
-        if (mbar_try_wait(bar(kBarFull + c % kNst), (uint32_t)((c / kNst) & 1))) break;
+        if (mbar_try_wait(bar(kBarFull + c % nst), (uint32_t)((c / nst) & 1))) break;
   }
 }
 
@@ -992,6 +1012,13 @@ int launch_bwd_tiles(const BwdTileArgs& a, cudaStream_t stream) {
   p.Rpart = a.Rpart; p.Cpart = a.Cpart;
   p.T = a.T; p.BH = a.BH; p.dqk = a.dqk; p.dv = a.dv; p.nb = nb; p.nitems = (int)nitems;
   p.scale = a.scale; p.st = a.st;
+  // 4-D views for two-chunk stages: one box per operand and stage instead of
+  // two (an issuing thread handles its copies one after another)
+  CUtensorMap mq4 = mq, mk4 = mk, mdh4 = mdh, mv4 = mv;
+  p.wide = a.dqk % 64 == 0 && a.dv % 64 == 0 && make_map_blocks(&mq4, a.q, a.dqk, a.T, a.BH, kTile, 2) &&
+           make_map_blocks(&mk4, a.k, a.dqk, a.T, a.BH, kTile, 2) && make_map_blocks(&mdh4, a.dh, a.dv, a.T, a.BH, kTile, 2) &&
+           make_map_blocks(&mv4, a.v, a.dv, a.T, a.BH, kTile, 2);
+  if (const char* e = getenv("MLSTM_BWD_TILE_NARROW")) p.wide = p.wide && e[0] == '0';   // (tuning)
   const size_t smem = (size_t)kNst * kStage + kStaging + 1024;
   if (cudaFuncSetAttribute(bwd_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return kCuda;
@@ -999,7 +1026,7 @@ int launch_bwd_tiles(const BwdTileArgs& a, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return kCuda;
   const int grid = (int)std::min<long long>(nitems, sms);   // persistent: one CTA per SM
-  bwd_tile_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(mq, mk, mdh, mv, mg, mp, p);
+  bwd_tile_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(mq, mk, mdh, mv, mg, mp, mq4, mk4, mdh4, mv4, p);
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   bwd_tile_sums_kernel<<<(unsigned)((BHT + 255) / 256), 256, 0, stream>>>(a.Rpart, a.Cpart, a.R, a.Ccol, a.T, nb,
                                                                             BHT);
