@@ -131,46 +131,66 @@ __global__ void bwd_colsum_kernel(const float* __restrict__ Cpart, float* __rest
   Ccol[x] = c;
 }
 
+// An unevaluated sum hi + lo of fp32 values, added with error-free (two-sum)
+// steps: suffix sums over 16k tokens as accurate as fp64 at fp32 speed (the
+// fp64 rate of this part is a small fraction of its fp32 rate).
+struct Sum2 {
+  float hi, lo;
+};
+__device__ __forceinline__ Sum2 sum2_add(Sum2 a, float b) {
+  const float s = a.hi + b, bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b - bb);        // a.hi + b == s + e exactly
+  const float lo = a.lo + e, hi = s + lo;
+  return {hi, lo - (hi - s)};
+}
+__device__ __forceinline__ Sum2 sum2_add(Sum2 a, Sum2 b) { return sum2_add(sum2_add(a, b.hi), b.lo); }
+__device__ __forceinline__ Sum2 sum2_shfl_down(Sum2 v, int o) {
+  return {__shfl_down_sync(0xffffffffu, v.hi, o), __shfl_down_sync(0xffffffffu, v.lo, o)};
+}
+
 // Gate gradients of one head (one CTA): d i~_k = Ccol_k and d log f_k =
 // sum_{i>=k} R_i - sum_{j>=k} Ccol_j (the rows >= k minus the columns >= k of
-// the lower triangle), in fp64, times d log f / d f~.
+// the lower triangle), in two-sum fp32 arithmetic, times d log f / d f~.
 __global__ void __launch_bounds__(1024)
 bwd_gates_kernel(const float* __restrict__ R, const float* __restrict__ Ccol, const float* __restrict__ fg,
                  float* __restrict__ dig, float* __restrict__ dfg, int T, int forget_exp) {
-  __shared__ double sh[32];
+  __shared__ Sum2 sh[32];
   const int bh = blockIdx.x;
   const size_t hb = (size_t)bh * T;
   const int per = (T + blockDim.x - 1) / blockDim.x;
   const int t0 = min(T, (int)threadIdx.x * per), t1 = min(T, t0 + per);
   // local totals of (R - Ccol) over this thread's segment
-  double seg = 0.0;
-  for (int t = t0; t < t1; ++t) seg += (double)R[hb + t] - (double)Ccol[hb + t];
+  Sum2 seg = {0.0f, 0.0f};
+  for (int t = t0; t < t1; ++t) seg = sum2_add(sum2_add(seg, R[hb + t]), -Ccol[hb + t]);
   // exclusive suffix sum of the segment totals over threads (reverse scan)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double x = seg;
+  Sum2 x = seg;
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_down_sync(0xffffffffu, x, o);
-    if (lane + o < 32) x += y;
+    const Sum2 y = sum2_shfl_down(x, o);
+    if (lane + o < 32) x = sum2_add(x, y);
   }
   if (lane == 0) sh[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    double w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0.0;
+    Sum2 w = lane < (int)(blockDim.x >> 5) ? sh[lane] : Sum2{0.0f, 0.0f};
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_down_sync(0xffffffffu, w, o);
-      if (lane + o < 32) w += y;
+      const Sum2 y = sum2_shfl_down(w, o);
+      if (lane + o < 32) w = sum2_add(w, y);
     }
     sh[lane] = w;                      // inclusive suffix over warps
   }
   __syncthreads();
-  double after = (warp + 1 < (int)(blockDim.x >> 5) ? sh[warp + 1] : 0.0) + (x - seg);   // totals of later threads
+  // totals of later threads: the later warps', then this warp's later lanes
+  // (x minus seg: this lane's inclusive suffix without its own segment)
+  Sum2 after = warp + 1 < (int)(blockDim.x >> 5) ? sh[warp + 1] : Sum2{0.0f, 0.0f};
+  after = sum2_add(after, sum2_add(x, Sum2{-seg.hi, -seg.lo}));
   for (int t = t1 - 1; t >= t0; --t) {
-    const double c = Ccol[hb + t];
-    after += (double)R[hb + t] - c;    // now the suffix from t
-    dig[hb + t] = (float)c;
+    const float c = Ccol[hb + t];
+    after = sum2_add(sum2_add(after, R[hb + t]), -c);   // now the suffix from t
+    dig[hb + t] = c;
     // d f~ = (d log f / d f~) d log f: sigma(-f~) for log f = log sigmoid(f~)
     // (eq 104), 1 for the exponential activation log f = f~ (eq 70's gamma = exp)
-    dfg[hb + t] = (float)(after * (forget_exp ? 1.0 : (double)sigmoid(-fg[hb + t])));
+    dfg[hb + t] = (after.hi + after.lo) * (forget_exp ? 1.0f : sigmoid(-fg[hb + t]));
   }
 }
 

@@ -607,7 +607,7 @@ bwd_prod_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constan
 // between the two CTAs, so each SM loads half of the B bytes a single-CTA
 // block needs.  A pair sums over the union of its two blocks' ranges; the
 // extra block reads the tile (2 gp, 2 gp + 1) above the diagonal, which
-// bwd_zero_tiles_kernel stores as zeros.  Requires d_qk and d_v multiples of
+// the row-statistics launch stores as zeros.  Requires d_qk and d_v multiples of
 // 128 (a B chunk is 256 columns, or 128 for the last, split in halves).
 __global__ void __launch_bounds__(kPThreads, 1)
 bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_constant__ CUtensorMap tmap_p,
@@ -840,11 +840,11 @@ bwd_prod2_kernel(const __grid_constant__ CUtensorMap tmap_g, const __grid_consta
 }
 
 // G and P tiles (ib, ib + 1) for even ib, above the diagonal: zeros (the
-// extra block a product pair reads).  One CTA per tile.
-__global__ void __launch_bounds__(256)
-bwd_zero_tiles_kernel(__nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__ P, int T, int ldT, int nb) {
+// extra block a product pair reads).  One block per tile.
+__device__ void bwd_zero_tile(__nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__ P, int T, int ldT, int nb,
+                              int tile) {
   const int np = nb / 2;                     // tiles (2 gp, 2 gp + 1) with 2 gp + 1 < nb
-  const int bh = blockIdx.x / np, gp = blockIdx.x % np;
+  const int bh = tile / np, gp = tile % np;
   const int i0 = 2 * gp * kTile, j0 = i0 + kTile;
   const int rows = min(kTile, T - i0), cols8 = (min(kTile, ldT - j0) + 7) / 8;
   for (int x = threadIdx.x; x < rows * cols8; x += blockDim.x) {
@@ -856,23 +856,38 @@ bwd_zero_tiles_kernel(__nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__
 }
 
 // Per row: 1/n_i and db_i (eqs 89-90) from the forward's H~, n, signed b and
-// the row max m.  One warp per row.
+// the row max m.  Sixteen threads per row, every load of a row issued before
+// the first product (16-byte loads of bf16 where rows allow).  Blocks past
+// the rows' (zero_base and on) instead zero the tiles above the diagonal that
+// a product pair reads (one tile each; see bwd_zero_tile).
 template <typename E>
 __global__ void __launch_bounds__(256)
 bwd_rowstat_kernel(const E* __restrict__ dh, const E* __restrict__ h, const float* __restrict__ nrow,
                    const float* __restrict__ brow, const float* __restrict__ mrow, float* __restrict__ invn,
-                   float* __restrict__ db, int dv, long long BHT) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= BHT) return;
+                   float* __restrict__ db, int dv, long long BHT, unsigned zero_base, __nv_bfloat16* G,
+                   __nv_bfloat16* P, int T, int ldT, int nb) {
+  if (blockIdx.x >= zero_base) {
+    bwd_zero_tile(G, P, T, ldT, nb, (int)(blockIdx.x - zero_base));
+    return;
+  }
+  const long long row = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);
+  const int l16 = threadIdx.x & 15;
+  const bool live = row < BHT;
   float dot = 0.0f;
-  if (sizeof(E) == 2 && dv % 8 == 0 && (((uintptr_t)dh | (uintptr_t)h) & 15u) == 0) {
-    // 16-byte loads (8 bf16 of each operand); rows are then 16-byte aligned
-    const uint4* a = reinterpret_cast<const uint4*>(dh + (size_t)row * dv);
-    const uint4* b = reinterpret_cast<const uint4*>(h + (size_t)row * dv);
-    for (int c8 = lane; c8 < dv / 8; c8 += 32) {
-      const uint4 x = a[c8], y = b[c8];
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+  if (sizeof(E) == 2 && dv % 8 == 0 && dv <= 512 && (((uintptr_t)dh | (uintptr_t)h) & 15u) == 0) {
+    const uint4* a = reinterpret_cast<const uint4*>(dh + (size_t)(live ? row : 0) * dv);
+    const uint4* b = reinterpret_cast<const uint4*>(h + (size_t)(live ? row : 0) * dv);
+    uint4 xa[4], xb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c8 = l16 + 16 * u;
+      const bool in = live && c8 < dv / 8;
+      xa[u] = in ? a[c8] : make_uint4(0u, 0u, 0u, 0u);
+      xb[u] = in ? b[c8] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t xs[4] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w}, ys[4] = {xb[u].x, xb[u].y, xb[u].z, xb[u].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
@@ -881,12 +896,13 @@ bwd_rowstat_kernel(const E* __restrict__ dh, const E* __restrict__ h, const floa
         dot = fmaf(fx.y, fy.y, dot);
       }
     }
-  } else {
-    for (int c = lane; c < dv; c += 32)
+  } else if (live) {
+    for (int c = l16; c < dv; c += 16)
       dot = fmaf(Elem<E>::load(dh, (size_t)row * dv + c), Elem<E>::load(h, (size_t)row * dv + c), dot);
   }
-  dot = warp_sum(dot);
-  if (lane == 0) {
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);   // within the 16 lanes of a row
+  if (live && l16 == 0) {
     const float n = nrow[row], b = brow[row];
     const float inv = n > 0.0f ? 1.0f / n : 0.0f;
     const float dn = -dot * inv;                                  // -(dH~ . h~) / n = -(sum C~' dC) / n^2
@@ -929,6 +945,13 @@ __global__ void bwd_tile_sums_kernel(const float* __restrict__ Rpart, const floa
 
 }  // namespace
 
+// The products run on CTA pairs when d_qk and d_v are multiples of 128
+// (MLSTM_BWD_PROD=single forces one CTA per block, for the tests).
+bool bwd_prod_pairs(int dqk, int dv) {
+  static const char* force = getenv("MLSTM_BWD_PROD");
+  return dqk % 128 == 0 && dv % 128 == 0 && !(force && force[0] == 's');
+}
+
 int launch_bwd_products(const BwdProdArgs& a, cudaStream_t stream) {
   if (a.BH <= 0 || a.T <= 0) return kOk;
   const int nb = (a.T + kTile - 1) / kTile;
@@ -943,15 +966,9 @@ int launch_bwd_products(const BwdProdArgs& a, cudaStream_t stream) {
   ProdParams p;
   p.T = a.T; p.BH = a.BH; p.nb = nb; p.dqk = a.dqk; p.dv = a.dv; p.scale = a.scale; p.st = a.st; p.a4 = 0;
   const size_t smem = (size_t)kANst * kABytes + (size_t)kBNst * kBBytes + 1024;
-  static const char* force = getenv("MLSTM_BWD_PROD");       // "single": one CTA per block (tests)
-  if (a.dqk % 128 == 0 && a.dv % 128 == 0 && !(force && force[0] == 's')) {
-    // CTA pairs: zero the tiles above the diagonal that a pair's extra block reads
-    if (nb >= 2) {
-      bwd_zero_tiles_kernel<<<(unsigned)(a.BH * (nb / 2)), 256, 0, stream>>>(
-          static_cast<__nv_bfloat16*>(const_cast<void*>(a.G)), static_cast<__nv_bfloat16*>(const_cast<void*>(a.P)),
-          a.T, a.ldT, nb);
-      if (cudaGetLastError() != cudaSuccess) return kCuda;
-    }
+  if (bwd_prod_pairs(a.dqk, a.dv)) {
+    // CTA pairs (the tiles above the diagonal that a pair's extra block reads
+    // were zeroed with the row statistics)
     if (cudaFuncSetAttribute(bwd_prod2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return kCuda;
     // 4-D views: A blocks and wide B chunks as one box of two 64-column blocks
@@ -1003,9 +1020,15 @@ int launch_bwd_tiles(const BwdTileArgs& a, cudaStream_t stream) {
       !make_map(&mdh, a.dh, a.dv, a.T, a.BH, kTile) || !make_map(&mv, a.v, a.dv, a.T, a.BH, kTile) ||
       !make_map_ld(&mg, a.G, a.T, a.T, a.BH, a.ldT, kTile) || !make_map_ld(&mp, a.P, a.T, a.T, a.BH, a.ldT, kTile))
     return kCuda;
-  bwd_rowstat_kernel<__nv_bfloat16><<<(unsigned)((BHT + 7) / 8), 256, 0, stream>>>(
+  // row statistics, plus (CTA-pair products) one block per tile above the
+  // diagonal that a pair's extra block reads, zeroed
+  const long long row_blocks = (BHT + 15) / 16;
+  const long long zero_blocks = bwd_prod_pairs(a.dqk, a.dv) && nb >= 2 ? (long long)a.BH * (nb / 2) : 0;
+  if (row_blocks + zero_blocks > 0x7fffffffLL) return kInval;
+  bwd_rowstat_kernel<__nv_bfloat16><<<(unsigned)(row_blocks + zero_blocks), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.dh), static_cast<const __nv_bfloat16*>(a.h), a.nrow, a.brow, a.g.m,
-      a.invn, a.db, a.dv, BHT);
+      a.invn, a.db, a.dv, BHT, (unsigned)row_blocks, static_cast<__nv_bfloat16*>(a.G), static_cast<__nv_bfloat16*>(a.P),
+      a.T, a.ldT, nb);
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   TileParams p;
   p.a2 = a.g.a2; p.p2 = a.g.p2; p.invn = a.invn; p.db = a.db;
