@@ -922,6 +922,25 @@ int resident_clusters(size_t smem) {
   return n;
 }
 
+// The device's L2 size in bytes (queried once per device).
+size_t l2_bytes() {
+  static std::mutex mu;
+  static int last_dev = -1;
+  static size_t last = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int dev = 0, v = 0;
+  cudaGetDevice(&dev);
+  if (dev != last_dev) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+      cudaGetLastError();
+      v = 0;
+    }
+    last_dev = dev;
+    last = (size_t)v;
+  }
+  return last;
+}
+
 template <int NSBUF, bool OG, bool QUAD>
 int launch_pair(const FwdArgs& a, const Tc2Params& p, size_t smem, const CUtensorMap& mq, const CUtensorMap& mk,
                 const CUtensorMap& mv, const CUtensorMap& mh, cudaStream_t stream) {
@@ -1026,13 +1045,19 @@ int launch_fwd_tc2(const FwdArgs& a, cudaStream_t stream) {
     // halves (comparison and tests)
     const char* xch = getenv("MLSTM_TC_XCH");   // read per call: tests switch it
     p.dv_slice = 256;
-    p.l2_prefetch = pf_env ? (pf_env[0] == '0' ? 0 : 1) : 1;
     if (!(xch && xch[0] == '0')) {
+      // The four-CTA form prefetches where the layer's K and V take at most
+      // three quarters of L2: on the 350M-scale layer (64 MiB) it measured
+      // 102.4 -> 101.4 us, on the T = 16384 workload (128 MiB, all of L2)
+      // 938 -> 991 us.
+      const double kv = (double)a.BH * a.T * (a.dqk + a.dv) * 2.0;
       p.nsplit = 1;
+      p.l2_prefetch = pf_env ? (pf_env[0] == '0' ? 0 : 1) : (kv <= 0.75 * (double)l2_bytes() ? 1 : 0);
       const int rc = plan_and_launch<true>(a, p, 2, stream);
       if (rc != kUnsupported) return rc;
     }
     p.nsplit = 2;
+    p.l2_prefetch = pf_env ? (pf_env[0] == '0' ? 0 : 1) : 1;
     return plan_and_launch<false>(a, p, 2, stream);
   }
   p.nsplit = 1;

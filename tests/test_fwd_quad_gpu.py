@@ -49,7 +49,8 @@ SHAPES = [
     (1, 1, 100, 512, 512),
     (1, 2, 129, 512, 512),      # two tiles; the pair's second CTA holds one valid row
     (2, 1, 384, 128, 512),      # three tiles: the pairs' turns shift across items
-    (1, 1, 777, 256, 512),
+    (1, 1, 777, 256, 512),      # five V granules: N=256 bursts alternate with N=128 pairs
+    (1, 2, 500, 384, 512),      # d_qk 384: three K granules a tile
     (8, 8, 640, 512, 512),      # 192 items: several rounds of the schedule
     (1, 1, 2048, 512, 512),
 ]
