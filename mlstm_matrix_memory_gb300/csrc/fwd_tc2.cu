@@ -691,6 +691,28 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                                                         p.st, kSiteGate);
       }
       gt += it.nkv;
+      if constexpr (!QUAD) {
+        // the next item's gate terms (its rows' p2 and m, the first two key
+        // tiles' a2) into L2 while this epilogue runs: read at its start, they
+        // otherwise wait on DRAM (up to ~4,000 cycles, clock traces).  125M-
+        // scale layer 105.9 -> 104.7 us; in the four-CTA form, whose first
+        // tile of an item waits on the other pair anyway, it measured 0.7 %
+        // slower, so it is left out there.
+        Item nx;
+        if (item_at(p, r + 1, cid, prank, pr, nx)) {
+          const size_t nb = (size_t)nx.bh * p.T;
+          const int ni = nx.i0 + rl;
+          if (ni < p.T) {
+            prefetch_l2(p.p2 + nb + ni);
+            prefetch_l2(p.mrow + nb + ni);
+          }
+#pragma unroll
+          for (int t = 0; t < 2 * (HALF / 32); ++t) {
+            const int col = (t / (HALF / 32)) * kBN + half * HALF + lane + 32 * (t % (HALF / 32));
+            if (col < p.T) prefetch_l2(p.a2 + nb + col);
+          }
+        }
+      }
 
       if constexpr (QUAD) {
         bpart[half * kBM + rl] = bsum;
