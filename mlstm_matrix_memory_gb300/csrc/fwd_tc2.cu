@@ -28,11 +28,12 @@
 // by the pair whose turn it is.  Its gating warps write the bf16 P tile twice:
 // into their own TMEM, over the S columns they have just read (the A operand
 // of their own pair's O product, which then frees that S buffer), and into the
-// shared-memory P buffer of the other pair's CTA of the same rows (16-byte
-// remote stores), where the other pair's O product reads it.  The row sums b
-// of eq (83) are split the same way and exchanged before the epilogue.  Each
-// pair thus issues the S product of every other tile only, and a pair's P
-// never waits for the other pair's buffer.
+// shared-memory P buffer of the other pair's CTA of the same rows, where the
+// other pair's O product reads it (16-byte remote stores into a K-major layout
+// without swizzle, so that each warp store covers 512 contiguous bytes).  The
+// row sums b of eq (83) are split the same way and exchanged before the
+// epilogue.  Each pair thus issues the S product of every other tile only, and
+// its own O product never waits for the other pair's buffer.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -198,7 +199,7 @@ fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
-  __shared__ int s_issued_s;                // global key tile of the last fully issued S product
+  __shared__ int s_issued_s;                // key tile of the last fully issued S product (read by the two-CTA form only)
   // Loads each producer of this CTA issued (ring granules, written once at
   // its exit; Q fills) and, in the pair leader, the peer's counts and abort
   // flag, sent at exit: after an abort the leader settles every load of the pair.
