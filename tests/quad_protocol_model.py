@@ -1,0 +1,321 @@
+"""Model of the synchronisation of the fused forward's four-CTA form (d_v = 512,
+`fwd_tc2.cu`, QUAD): test infrastructure, no arithmetic of the method.
+
+Every role of one cluster of four CTAs (two pairs over the same query rows) is
+a generator that yields the steps the kernel takes on its mbarriers and named
+barriers, in the kernel's order, with the kernel's arrival counts:
+  ('wait', key, k)      block until phase k of barrier `key` has completed
+  ('arrive', key)       one arrival
+  ('nb', key, n)        named barrier of n warps
+  ('use', buf, op, x)   an access to a buffer (checked for overlaps, below)
+Copies and MMAs complete at once; only the order of steps matters here.
+
+A scheduler runs the roles in random interleavings and reports
+  - deadlock: no role can take a step and some have not finished;
+  - overrun: a wait for phase k finds k + 2 or more phases completed, or k - 1
+    (a parity wait cannot tell phase k from k + 2, and passes at k - 1);
+  - hazards on the buffers that the barriers protect: the pair's O accumulator
+    (the epilogue's reads against the next item's first O product); each S
+    buffer in TMEM (the S product writing it against the pair's own P stored
+    over it and read by the O product); and each CTA's shared-memory P buffer
+    (the other pair's P writes against this pair's O product that consumes them
+    and against the epilogue, which stages its output through the same buffer).
+
+`mutation` plants one mistake (tests check that each is caught).
+"""
+import random
+from collections import defaultdict
+
+BM = 128          # query rows per CTA, keys per tile
+
+
+def cluster_items(n_clusters, c, B, H, T):
+    """Work items of cluster c in the kernel's serpentine longest-first order:
+    (head, number of key tiles)."""
+    BH = B * H
+    npairs = ((T + BM - 1) // BM + 1) // 2
+    n_items = npairs * BH
+    out, r = [], 0
+    while r * n_clusters < n_items:
+        w = r * n_clusters + ((n_clusters - 1 - c) if (r & 1) else c)
+        if w < n_items:
+            pair = npairs - 1 - w // BH
+            out.append((w % BH, (min(T, (2 * pair + 2) * BM) - 1) // BM + 1))
+        r += 1
+    return out
+
+
+def roles(items, nkg=4, nk=2, nv=2, mutation=None):
+    """The cluster's roles.  nkg: K granules per key tile (d_qk / 128); nk, nv:
+    ring granules; every tile takes two V granules of each CTA."""
+    counts = {}
+    NS = 2                                   # S buffers
+
+    def own(pr, g):                          # tile g of the sequence belongs to pair g & 1
+        return (g & 1) == pr
+
+    for cta in range(4):
+        counts[(cta, 'QFull')] = 4           # two producers in each CTA of the pair
+        counts[(cta, 'QEmpty')] = 1
+        for b in range(NS):
+            counts[(cta, f'SFull{b}')] = 1
+            counts[(cta, f'SEmpty{b}')] = 1  # the own-tile O product
+            counts[(cta, f'PFull{b}')] = 16  # eight gating warps in each CTA of the pair
+        if mutation == 'single_pfull':
+            counts[(cta, 'PFull0')] = 16
+        counts[(cta, 'PEmpty')] = 1
+        counts[(cta, 'OFull')] = 1
+        counts[(cta, 'BxFull')] = 2 if mutation == 'bx_count' else 4
+        counts[(cta, 'EpiDone')] = 1
+        counts[(cta, 'ODrained')] = 2
+        counts[(cta, 'PRx')] = 8 if mutation == 'prx_count' else 16
+        for s in range(nk + nv):
+            counts[(cta, f'Full{s}')] = 2    # the loads of both CTAs of the pair
+            counts[(cta, f'Empty{s}')] = 1
+
+    def pfull(buf):
+        return 'PFull0' if mutation == 'single_pfull' else f'PFull{buf}'
+
+    def pfull_phase(gs):
+        return gs if mutation == 'single_pfull' else gs // NS
+
+    def producer(cta, pi):
+        lead, pr = cta & ~1, cta >> 1
+        base, n = (0, nk) if pi == 0 else (nk, nv)
+        st, g0, fills = 0, 0, defaultdict(int)
+        for qi, (_, nkv) in enumerate(items):
+            if qi > 0:
+                yield ('wait', (cta, 'QEmpty'), qi - 1)
+            yield ('arrive', (lead, 'QFull'))
+            for j in range(nkv):
+                if pi == 0 and not own(pr, g0 + j):
+                    continue                 # the K ring carries this pair's tiles only
+                for _ in range(nkg if pi == 0 else 2):
+                    s = base + st
+                    yield ('wait', (cta, f'Empty{s}'), fills[s] - 1)
+                    fills[s] += 1
+                    yield ('arrive', (lead, f'Full{s}'))
+                    st = (st + 1) % n
+            g0 += nkv
+
+    def s_issuer(cta):
+        pr, pm = cta >> 1, (cta, cta + 1)
+        st, uses, gs, gt = 0, defaultdict(int), 0, 0
+        for qi, (_, nkv) in enumerate(items):
+            yield ('wait', (cta, 'QFull'), qi)
+            for _ in range(nkv):
+                g, gt = gt, gt + 1
+                if not own(pr, g):
+                    continue
+                buf, u = gs % NS, gs // NS
+                if mutation != 'no_sempty':
+                    yield ('wait', (cta, f'SEmpty{buf}'), u - 1)
+                yield ('use', ('S', cta, buf), 's_write', g)
+                for _ in range(nkg):
+                    yield ('wait', (cta, f'Full{st}'), uses[st])
+                    uses[st] += 1
+                    for c in pm:
+                        yield ('arrive', (c, f'Empty{st}'))
+                    st = (st + 1) % nk
+                for c in pm:
+                    yield ('arrive', (c, f'SFull{buf}'))
+                gs += 1
+            for c in pm:
+                yield ('arrive', (c, 'QEmpty'))
+
+    def o_issuer(cta):
+        pr, pm, xm = cta >> 1, (cta, cta + 1), (cta ^ 2, (cta ^ 2) + 1)
+        st, uses, gs, go, gt = 0, defaultdict(int), 0, 0, 0
+        for qi, (_, nkv) in enumerate(items):
+            if qi > 0 and mutation != 'no_odrained':
+                yield ('wait', (cta, 'ODrained'), qi - 1)
+            for j in range(nkv):
+                g, gt = gt, gt + 1
+                mine = own(pr, g)
+                if mine:
+                    buf = gs % NS
+                    yield ('wait', (cta, pfull(buf)), pfull_phase(gs))
+                    gs += 1
+                else:
+                    yield ('wait', (cta, 'PRx'), go)
+                    go += 1
+                got = []
+                for _ in range(2):
+                    s = nk + st
+                    yield ('wait', (cta, f'Full{s}'), uses[s])
+                    uses[s] += 1
+                    got.append(s)
+                    st = (st + 1) % nv
+                if j == 0:
+                    yield ('use', ('O', cta), 'write', None)
+                if mine:
+                    yield ('use', ('S', cta, buf), 'p_consume', g)
+                else:
+                    for c in pm:
+                        yield ('use', ('P', c), 'consume', g)
+                for s in got:
+                    for c in pm:
+                        yield ('arrive', (c, f'Empty{s}'))
+                for c in (pm if mine else xm):
+                    yield ('arrive', (c, f'SEmpty{buf}' if mine else 'PEmpty'))
+            for c in pm:
+                yield ('arrive', (c, 'OFull'))
+
+    def gating(cta, gw):
+        lead, pr, x = cta & ~1, cta >> 1, cta ^ 2
+        half = gw >> 2
+        gs, gt = 0, 0
+        for qi, (_, nkv) in enumerate(items):
+            partner_free = qi == 0
+            for j in range(0 if own(pr, gt) else 1, nkv, 2):
+                buf, u = gs % NS, gs // NS
+                yield ('wait', (cta, f'SFull{buf}'), u)
+                yield ('use', ('S', lead, buf), 'p_store', gt + j)
+                yield ('arrive', (lead, pfull(buf)))          # own P in TMEM
+                if not partner_free:
+                    if mutation != 'no_epidone':
+                        yield ('wait', (cta, 'EpiDone'), qi - 1)
+                    partner_free = True
+                if mutation != 'no_pempty':
+                    yield ('wait', (cta, 'PEmpty'), gs - 1)
+                yield ('use', ('P', x), 'write', gt + j)        # remote stores
+                yield ('arrive', (x & ~1, 'PRx'))
+                gs += 1
+            if not partner_free and mutation != 'no_idle_epidone':
+                yield ('wait', (cta, 'EpiDone'), qi - 1)
+            gt += nkv
+            yield ('nb', (cta, 'sums', qi), 8)
+            if half == 0:
+                yield ('arrive', (x, 'BxFull'))                  # row sums to the other pair
+            yield ('wait', (cta, 'OFull'), qi)
+            yield ('wait', (cta, 'BxFull'), qi)
+            yield ('nb', (cta, 'epi', qi), 8)
+            yield ('use', ('O', lead), 'read_begin', (cta, gw))
+            yield ('use', ('P', cta), 'stage_begin', gw)
+            yield ('use', ('P', cta), 'stage_end', gw)
+            yield ('use', ('O', lead), 'read_end', (cta, gw))
+            yield ('nb', (cta, 'end', qi), 8)
+            if gw == 5:
+                yield ('arrive', (lead, 'ODrained'))
+                yield ('arrive', (x, 'EpiDone'))
+
+    out = []
+    for cta in range(4):
+        out.append((f'producer K {cta}', producer(cta, 0)))
+        out.append((f'producer V {cta}', producer(cta, 1)))
+        if cta % 2 == 0:
+            out.append((f'S issuer {cta}', s_issuer(cta)))
+            out.append((f'O issuer {cta}', o_issuer(cta)))
+        for gw in range(8):
+            out.append((f'gating {cta}.{gw}', gating(cta, gw)))
+    return counts, out
+
+
+class _State:
+    def __init__(self, counts):
+        self.counts = counts
+        self.pending = {}
+        self.done = defaultdict(int)
+        self.named = defaultdict(set)
+        self.errors = []
+        self.o_readers = defaultdict(set)      # O accumulator (pair leader) -> open epilogue reads
+        self.stage = defaultdict(set)          # CTA -> warps staging through its P buffer
+        self.rx = {}                           # CTA -> [tile held, writes landed, consumed]
+        self.sbuf = {}                         # (pair leader, buffer) -> [tile, P stores, consumed]
+
+    def arrive(self, key):
+        c = self.counts[key]
+        p = self.pending.get(key, c) - 1
+        if p == 0:
+            self.done[key] += 1
+            p = c
+        self.pending[key] = p
+
+    def ready(self, key, k):
+        # the kernel's waits compare parities: phase k looks complete whenever
+        # the number of completed phases differs from k in parity
+        d = self.done[key]
+        if d >= k + 2:
+            self.errors.append(f'overrun: {key} wanted phase {k}, {d} completed')
+        elif d < k and (k - d) % 2 == 1:
+            self.errors.append(f'early pass: {key} wanted phase {k}, only {d} completed')
+        return d >= k + 1
+
+    def use(self, buf, op, x):
+        kind, cta = buf[0], buf[1]
+        if kind == 'S':
+            sb = self.sbuf.setdefault(buf, [None, 0, True])
+            if op == 's_write':
+                if not sb[2]:
+                    self.errors.append(f'hazard: S product of tile {x} overwrites unconsumed P of tile {sb[0]}')
+                self.sbuf[buf] = [x, 0, False]
+            elif op == 'p_store':
+                if sb[0] != x:
+                    self.errors.append(f'hazard: P of tile {x} stored over S of tile {sb[0]}')
+                sb[1] += 1
+            elif op == 'p_consume':
+                if sb[0] != x or sb[1] != 16:
+                    self.errors.append(f'hazard: O product reads P of tile {x} from {sb[:2]}')
+                sb[2] = True
+            return
+        if kind == 'O':
+            if op == 'write' and self.o_readers[cta]:
+                self.errors.append(f'hazard: O of pair {cta} overwritten while the epilogue reads it')
+            elif op == 'read_begin':
+                self.o_readers[cta].add(x)
+            elif op == 'read_end':
+                self.o_readers[cta].discard(x)
+            return
+        rx = self.rx.setdefault(cta, [None, 0, True])
+        if op == 'write':
+            if self.stage[cta]:
+                self.errors.append(f'hazard: P written into CTA {cta} while its epilogue stages there')
+            if rx[0] != x:
+                if not rx[2]:
+                    self.errors.append(f'hazard: P of tile {x} overwrites unconsumed tile {rx[0]} in CTA {cta}')
+                self.rx[cta] = [x, 1, False]
+            else:
+                rx[1] += 1
+        elif op == 'consume':
+            if rx[0] != x or rx[1] != 8:
+                self.errors.append(f'hazard: O product reads tile {x} in CTA {cta} holding {rx[:2]}')
+            rx[2] = True
+        elif op == 'stage_begin':
+            if not rx[2]:
+                self.errors.append(f'hazard: epilogue stages over unconsumed P in CTA {cta}')
+            self.stage[cta].add(x)
+        elif op == 'stage_end':
+            self.stage[cta].discard(x)
+            self.rx[cta] = [None, 0, True]
+
+
+def run(items, seed, **kw):
+    """Runs one random interleaving; returns (status, errors) with status
+    'ok' or 'deadlock'."""
+    counts, rl = roles(items, **kw)
+    st = _State(counts)
+    rng = random.Random(seed)
+    gens = dict(rl)
+    cur = {name: next(g, None) for name, g in rl}
+    while True:
+        live = [n for n in cur if cur[n] is not None]
+        if not live:
+            return 'ok', st.errors
+        rng.shuffle(live)
+        for n in live:
+            a = cur[n]
+            if a[0] == 'wait':
+                if a[2] >= 0 and not st.ready(a[1], a[2]):
+                    continue
+            elif a[0] == 'arrive':
+                st.arrive(a[1])
+            elif a[0] == 'nb':
+                st.named[a[1]].add(n)
+                if len(st.named[a[1]]) < a[2]:
+                    continue
+            elif a[0] == 'use':
+                st.use(a[1], a[2], a[3])
+            cur[n] = next(gens[n], None)
+            break
+        else:
+            return 'deadlock', st.errors + [f'blocked: {n} at {cur[n]}' for n in sorted(live)]
