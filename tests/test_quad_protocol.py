@@ -1,9 +1,13 @@
 """The synchronisation of the fused forward's four-CTA form (d_v = 512), on a
 model of its barriers and buffers (`quad_protocol_model.py`, CPU only): no
-deadlock, no wait that could take phase k + 2 for phase k, and no overlapping
-use of a pair's O accumulator or of a CTA's P buffer, over the work-item
-schedules of the GPU tests and of the bench's d = 512 layers and many random
-interleavings; and each planted mistake is caught."""
+deadlock, no parity wait that could be misread, and no overlapping use of a
+pair's O accumulator, an S buffer holding P or a CTA's P buffer, over the
+work-item schedules of the GPU tests and of the bench's d = 512 layers and
+many random interleavings; with waits that give up at random points, every
+warp still leaves (no group is stranded at a named barrier); and each planted
+mistake is caught."""
+import random
+
 import pytest
 
 import quad_protocol_model as Q
@@ -38,14 +42,14 @@ def test_schedule_runs_clean(shape, n_clusters):
             continue
         # interleavings per cluster, fewer where its schedule is long
         for seed in range(max(1, min(6, 600 // sum(n for _, n in items)))):
-            status, errors = Q.run(items, seed, nkg=nkg, nk=nk, nv=nv)
+            status, errors, _ = Q.run(items, seed, nkg=nkg, nk=nk, nv=nv)
             assert status == "ok" and not errors, (c, seed, status, errors[:3])
 
 
 def test_long_sequence_schedule_runs_clean():
     items = Q.cluster_items(36, 0, 1, 4, 16384)
     for seed in range(2):
-        status, errors = Q.run(items, seed)
+        status, errors, _ = Q.run(items, seed)
         assert status == "ok" and not errors, (seed, status, errors[:3])
 
 
@@ -73,6 +77,45 @@ def test_planted_mistake_is_caught(mutation):
         for c in range(min(n_clusters, 3)):
             items = Q.cluster_items(n_clusters, c, B, H, T)
             for seed in range(12):
-                status, errors = Q.run(items, seed, mutation=mutation)
+                status, errors, _ = Q.run(items, seed, mutation=mutation)
                 caught += status != "ok" or bool(errors)
     assert caught > 0, MUTATIONS[mutation]
+
+
+def _timeout_runs(items, n_runs, **kw):
+    """Runs with one wait giving up at a step drawn over the length of a clean
+    run (early, mid-item and at item ends alike)."""
+    _, _, length = Q.run(items, 0, **kw)
+    rng = random.Random(len(items) * 7919 + n_runs)
+    for seed in range(n_runs):
+        yield Q.run(items, seed, give_up_at=rng.randrange(1, length), **kw)
+
+
+@pytest.mark.parametrize("shape", [(8, 8, 640, 512), (1, 2, 500, 512), (2, 1, 384, 128)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_waits_that_give_up_leave_no_group_stranded(shape):
+    """A wait runs out of its budget (the kernel's spin limit) at a random
+    point: every role must still reach the end, through the reducing barriers
+    where the gating warps agree on their exit."""
+    B, H, T, dqk = shape
+    nkg, nk, nv = rings(dqk)
+    for n_clusters, n_runs in ((36, 40), (4, 6)):
+        items = Q.cluster_items(n_clusters, 0, B, H, T)
+        for status, errors, _ in _timeout_runs(items, n_runs, nkg=nkg, nk=nk, nv=nv):
+            assert status == "ok", (n_clusters, errors[-3:])
+
+
+EXIT_MUTATIONS = {
+    "exit_early": "a gating warp whose wait gave up leaves without meeting its group",
+    "exit_unreduced": "the gating warps meet before the epilogue without agreeing on the exit",
+}
+
+
+@pytest.mark.parametrize("mutation", sorted(EXIT_MUTATIONS))
+def test_planted_exit_mistake_strands_a_group(mutation):
+    stranded = 0
+    for shape in ((8, 8, 640), (4, 4, 2048)):
+        items = Q.cluster_items(36, 0, *shape)
+        for status, _, _ in _timeout_runs(items, 60, mutation=mutation):
+            stranded += status == "deadlock"
+    assert stranded > 0, EXIT_MUTATIONS[mutation]
