@@ -1,5 +1,6 @@
-"""Model of the synchronisation of the fused forward's four-CTA form (d_v = 512,
-`fwd_tc2.cu`, QUAD): test infrastructure, no arithmetic of the method.
+"""Model of the synchronisation of the fused forward on CTA pairs (`fwd_tc2.cu`):
+its four-CTA form (d_v = 512, QUAD) and its two-CTA form (`roles_pair`).  Test
+infrastructure, no arithmetic of the method.
 
 Every role of one cluster of four CTAs (two pairs over the same query rows) is
 a generator that yields the steps the kernel takes on its mbarriers and named
@@ -37,18 +38,19 @@ from collections import defaultdict
 BM = 128          # query rows per CTA, keys per tile
 
 
-def cluster_items(n_clusters, c, B, H, T):
+def cluster_items(n_clusters, c, B, H, T, nsplit=1):
     """Work items of cluster c in the kernel's serpentine longest-first order:
-    (head, number of key tiles)."""
-    BH = B * H
+    (head, number of key tiles); nsplit d_v slices per query block (two-CTA
+    form at d_v = 512 without the exchange)."""
+    per = B * H * nsplit
     npairs = ((T + BM - 1) // BM + 1) // 2
-    n_items = npairs * BH
+    n_items = npairs * per
     out, r = [], 0
     while r * n_clusters < n_items:
         w = r * n_clusters + ((n_clusters - 1 - c) if (r & 1) else c)
         if w < n_items:
-            pair = npairs - 1 - w // BH
-            out.append((w % BH, (min(T, (2 * pair + 2) * BM) - 1) // BM + 1))
+            pair = npairs - 1 - w // per
+            out.append(((w % per) // nsplit, (min(T, (2 * pair + 2) * BM) - 1) // BM + 1))
         r += 1
     return out
 
@@ -266,6 +268,156 @@ def roles(items, nkg=4, nk=2, nv=2, mutation=None):
     return counts, out
 
 
+def roles_pair(items, nsbuf=1, nkg=3, nk=3, nv=3, vpt=3, mutation=None):
+    """The two-CTA form's roles as (name, cta, generator): one pair, every key
+    tile its own; S in nsbuf TMEM buffers that the gating warps release once
+    they have read S; P through the CTA's shared-memory P buffer; vpt V
+    granules per tile."""
+    counts = {}
+    for cta in range(2):
+        counts[(cta, 'QFull')] = 4
+        counts[(cta, 'QEmpty')] = 1
+        for b in range(nsbuf):
+            counts[(cta, f'SFull{b}')] = 1
+            counts[(cta, f'SEmpty{b}')] = 8 if mutation == 'pair_sempty_count' else 16   # both CTAs' gating warps
+        counts[(cta, 'PFull')] = 16
+        counts[(cta, 'PEmpty')] = 1
+        counts[(cta, 'OFull')] = 1
+        for s in range(nk + nv):
+            counts[(cta, f'Full{s}')] = 2
+            counts[(cta, f'Empty{s}')] = 1
+
+    def producer(cta, pi):
+        base, n = (0, nk) if pi == 0 else (nk, nv)
+        st, fills = 0, defaultdict(int)
+        ok = True
+        for qi, (_, nkv) in enumerate(items):
+            if qi > 0:
+                ok = yield ('wait', (cta, 'QEmpty'), qi - 1)
+                if not ok:
+                    break
+            yield ('arrive', (0, 'QFull'))
+            for _ in range(nkv):
+                for _ in range(nkg if pi == 0 else vpt):
+                    s = base + st
+                    ok = yield ('wait', (cta, f'Empty{s}'), fills[s] - 1)
+                    if not ok:
+                        break
+                    fills[s] += 1
+                    yield ('arrive', (0, f'Full{s}'))
+                    st = (st + 1) % n
+                if not ok:
+                    break
+            if not ok:
+                break
+
+    def s_issuer():
+        st, uses, gt = 0, defaultdict(int), 0
+        for qi, (_, nkv) in enumerate(items):
+            ok = yield ('wait', (0, 'QFull'), qi)
+            for _ in range(nkv):
+                if not ok:
+                    break
+                g, gt = gt, gt + 1
+                buf, u = g % nsbuf, g // nsbuf
+                ok = yield ('wait', (0, f'SEmpty{buf}'), u - 1)
+                if not ok:
+                    break
+                yield ('use', ('S', 0, buf), 's_write', g)
+                for _ in range(nkg):
+                    ok = yield ('wait', (0, f'Full{st}'), uses[st])
+                    if not ok:
+                        break
+                    uses[st] += 1
+                    for c in (0, 1):
+                        yield ('arrive', (c, f'Empty{st}'))
+                    st = (st + 1) % nk
+                if not ok:
+                    break
+                for c in (0, 1):
+                    yield ('arrive', (c, f'SFull{buf}'))
+            if not ok:
+                break
+            for c in (0, 1):
+                yield ('arrive', (c, 'QEmpty'))
+
+    def o_issuer():
+        st, uses, gt = 0, defaultdict(int), 0
+        ok = True
+        for qi, (_, nkv) in enumerate(items):
+            for j in range(nkv):
+                g, gt = gt, gt + 1
+                ok = yield ('wait', (0, 'PFull'), g)
+                if not ok:
+                    break
+                got = []
+                for _ in range(vpt):
+                    s = nk + st
+                    ok = yield ('wait', (0, f'Full{s}'), uses[s])
+                    if not ok:
+                        break
+                    uses[s] += 1
+                    got.append(s)
+                    st = (st + 1) % nv
+                if not ok:
+                    break
+                if j == 0:
+                    yield ('use', ('O', 0), 'write', None)
+                for c in (0, 1):
+                    yield ('use', ('P', c), 'consume', g)
+                for s in got:
+                    for c in (0, 1):
+                        yield ('arrive', (c, f'Empty{s}'))
+                for c in (0, 1):
+                    yield ('arrive', (c, 'PEmpty'))
+            if not ok:
+                break
+            for c in (0, 1):
+                yield ('arrive', (c, 'OFull'))
+
+    def gating(cta, gw):
+        gt = 0
+        ok = True
+        for qi, (_, nkv) in enumerate(items):
+            for j in range(nkv):
+                g = gt + j
+                buf, u = g % nsbuf, g // nsbuf
+                ok = yield ('wait', (cta, f'SFull{buf}'), u)
+                if not ok:
+                    break
+                yield ('use', ('S', 0, buf), 's_read', g)
+                yield ('arrive', (0, f'SEmpty{buf}'))
+                ok = yield ('wait', (cta, 'PEmpty'), g - 1)
+                if not ok:
+                    break
+                yield ('use', ('P', cta), 'write', g)
+                yield ('arrive', (0, 'PFull'))
+            if not ok and mutation == 'pair_exit_early':
+                return
+            gt += nkv
+            if ok:
+                ok = yield ('wait', (cta, 'OFull'), qi)
+            ok = yield ('red', (cta, 'epi', qi), 8, ok)
+            if not ok:
+                break
+            yield ('use', ('O', 0), 'read_begin', (cta, gw))
+            yield ('use', ('P', cta), 'stage_begin', gw)
+            yield ('nb', (cta, 'half', gw >> 2, qi), 4)
+            yield ('use', ('P', cta), 'stage_end', gw)
+            yield ('use', ('O', 0), 'read_end', (cta, gw))
+            yield ('nb', (cta, 'end', qi), 8)
+
+    out = []
+    for cta in range(2):
+        out.append((f'producer K {cta}', cta, producer(cta, 0)))
+        out.append((f'producer V {cta}', cta, producer(cta, 1)))
+        for gw in range(8):
+            out.append((f'gating {cta}.{gw}', cta, gating(cta, gw)))
+    out.append(('S issuer', 0, s_issuer()))
+    out.append(('O issuer', 0, o_issuer()))
+    return counts, out
+
+
 class _State:
     def __init__(self, counts):
         self.counts = counts
@@ -318,6 +470,11 @@ class _State:
                 if sb[0] != x or sb[1] != 16:
                     self.hazard(f'O product reads P of tile {x} from {sb[:2]}')
                 sb[2] = True
+            elif op == 's_read':                       # two-CTA form: S read out, then released
+                if sb[0] != x:
+                    self.hazard(f'S of tile {x} read from a buffer holding tile {sb[0]}')
+                sb[1] += 1
+                sb[2] = sb[1] == 16
             return
         if kind == 'O':
             if op == 'write' and self.o_readers[cta]:
@@ -350,12 +507,12 @@ class _State:
             self.rx[cta] = [None, 0, True]
 
 
-def run(items, seed, give_up_at=None, **kw):
+def run(items, seed, give_up_at=None, form='quad', **kw):
     """Runs one random interleaving; returns (status, errors, steps) with
     status 'ok' or 'deadlock'.  A blocked wait gives up whenever nothing else
     can move, and (a spin budget running out) at the first step from
     `give_up_at` on where some wait is blocked."""
-    counts, rl = roles(items, **kw)
+    counts, rl = (roles_pair if form == 'pair' else roles)(items, **kw)
     st = _State(counts)
     rng = random.Random(seed)
     gens = {name: g for name, _, g in rl}

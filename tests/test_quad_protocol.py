@@ -1,5 +1,6 @@
-"""The synchronisation of the fused forward's four-CTA form (d_v = 512), on a
-model of its barriers and buffers (`quad_protocol_model.py`, CPU only): no
+"""The synchronisation of the fused forward on CTA pairs, its four-CTA form
+(d_v = 512) and its two-CTA form, on a model of their barriers and buffers
+(`quad_protocol_model.py`, CPU only): no
 deadlock, no parity wait that could be misread, and no overlapping use of a
 pair's O accumulator, an S buffer holding P or a CTA's P buffer, over the
 work-item schedules of the GPU tests and of the bench's d = 512 layers and
@@ -119,3 +120,45 @@ def test_planted_exit_mistake_strands_a_group(mutation):
         for status, _, _ in _timeout_runs(items, 60, mutation=mutation):
             stranded += status == "deadlock"
     assert stranded > 0, EXIT_MUTATIONS[mutation]
+
+
+# The two-CTA form: (B, H, T, nsplit, ring planner inputs) for the 125M-scale
+# layer (d = 384: one S buffer, 3 + 3 granules, three V granules a tile), the
+# split form at d_v = 512 (two slices, 2 + 2), d = 256 (two S buffers, 4 + 4)
+# and a one-token sequence.
+PAIR_FORMS = {
+    "d384": dict(nsbuf=1, nkg=3, nk=3, nv=3, vpt=3),
+    "d512split": dict(nsbuf=2, nkg=4, nk=2, nv=2, vpt=2),
+    "d256": dict(nsbuf=2, nkg=2, nk=4, nv=4, vpt=2),
+}
+PAIR_CASES = [("d384", (8, 4, 2048), 1), ("d384", (1, 1, 1), 1), ("d512split", (4, 4, 2048), 2),
+              ("d256", (2, 2, 300), 1)]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: c[0] + "-" + "x".join(map(str, c[1])))
+def test_pair_form_runs_clean_and_leaves_on_timeouts(case):
+    form, (B, H, T), nsplit = case
+    kw = dict(form="pair", **PAIR_FORMS[form])
+    for n_clusters, n_runs in ((76, 20), (4, 3)):
+        items = Q.cluster_items(n_clusters, 0, B, H, T, nsplit)
+        if not items:
+            continue
+        for seed in range(4):
+            status, errors, _ = Q.run(items, seed, **kw)
+            assert status == "ok" and not errors, (n_clusters, seed, errors[:3])
+        for status, errors, _ in _timeout_runs(items, n_runs, **kw):
+            assert status == "ok", (n_clusters, errors[-3:])
+
+
+@pytest.mark.parametrize("mutation", ["pair_exit_early", "pair_sempty_count"])
+def test_pair_form_planted_mistake_is_caught(mutation):
+    kw = dict(form="pair", mutation=mutation, **PAIR_FORMS["d384"])
+    caught = 0
+    for c in (0, 40, 75):
+        items = Q.cluster_items(76, c, 8, 4, 2048)
+        for status, errors, _ in _timeout_runs(items, 60, **kw):
+            caught += status != "ok"
+        for seed in range(4):
+            status, errors, _ = Q.run(items, seed, **kw)
+            caught += status != "ok" or bool(errors)
+    assert caught > 0, mutation
